@@ -1,0 +1,247 @@
+/*
+ * Paged verify-attention oracle: plain, slow, fp64, CPU only.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may build, load or call this file. It shares no code,
+ * header, table or constant with the CUDA library and must never be reached
+ * from the product path.
+ *
+ * What it computes (the definition, written out; no blocking, no fusion):
+ *
+ *   For sequence b with context length L and query length q, the q verify
+ *   tokens are the last q tokens of the context. Query row (token i, q head h)
+ *   of that sequence attends to keys t = 0 .. L - q + i of KV head
+ *   g = h / (Hq / Hkv):
+ *       K[t] = dec(k_cache[pg][g][t % 16][:]) * (FP8 ? k_scale[pg][g][t % 16] : 1)
+ *       V[t] = dec(v_cache[pg][g][t % 16][:]) * (FP8 ? v_scale[pg][g][t % 16] : 1)
+ *       pg   = block_table[b][t / 16]
+ *       z_t  = softmax_scale * sum_d Q[i, h, d] * K[t, d]
+ *       out  = sum_t exp(z_t - max z) V[t] / sum_t exp(z_t - max z)
+ *
+ * Sources, by page and section:
+ *   - rows = query length x GQA group, several q heads per KV head:
+ *     "fix(attention): keep MTP-5 decode on FlyDSL pa_decode past the gluon
+ *     query-length limit", Motivation.
+ *   - lengths + block table + per-token FP8 KV scales (trailing singleton
+ *     dimension) handed to the decode kernel: same page, Change and Tests.
+ *   - 16-token pages, head-major within a page: "[MiniMax-M3.1] P/D from a
+ *     PP4 prefill into a TP4 decode (2/2: DSpark)", description ("page-16
+ *     views", "head-major per page").
+ *   - causal mask inside the drafts, lengths that count the verify tokens,
+ *     contiguous GQA groups: readings where the pages are silent (the
+ *     repository's design notes list them).
+ *   - E4M3: OCP 8-bit floating point format (E4M3: 1 sign, 4 exponent bits
+ *     with bias 7, 3 mantissa bits, subnormals, no infinities, S.1111.111 = NaN).
+ *
+ * Parity pins: brute force on tiny inputs, the decode special case against a
+ * library attention routine, the causal-prefix identity, block-table
+ * permutation invariance, FP8 equal to attention on dequantised tensors,
+ * closed forms, and the E4M3 decoder against a library conversion; the
+ * tests under tests/test_oracle.py hold them.
+ *
+ * Compile-time ORACLE_MUTANT=k plants one known mistake (for the test that
+ * shows the pins catch it); it is 0 in every normal build.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+#define ORACLE_PAGE 16
+
+typedef struct {
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t kv_dtype; /* 0 = bf16 bits, 1 = OCP E4M3 bytes */
+  int32_t num_pages;
+  int32_t block_table_stride;
+  int32_t pad_;
+  const uint16_t* q;     /* [T][Hq][D] bf16 bits */
+  const void* k_cache;   /* [N_pg][Hkv][16][D] */
+  const void* v_cache;   /* [N_pg][Hkv][16][D] */
+  const float* k_scale;  /* [N_pg][Hkv][16] or NULL */
+  const float* v_scale;  /* [N_pg][Hkv][16] or NULL */
+  const int32_t* block_table; /* [B][stride] */
+  const int32_t* context_lens; /* [B] */
+  const int32_t* query_lens;   /* [B] */
+  double softmax_scale;
+} oracle_problem;
+
+/* bf16 -> fp64: a bf16 value is the top 16 bits of an IEEE binary32. */
+double oracle_decode_bf16(uint16_t bits) {
+  uint32_t w = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+/* OCP E4M3 -> fp64, from the format definition. */
+double oracle_decode_e4m3(uint8_t byte) {
+  int sign = (byte >> 7) & 1;
+  int e = (byte >> 3) & 0xF;
+  int m = byte & 0x7;
+  double mag;
+  if (e == 0xF && m == 0x7) return NAN;
+  if (e == 0)
+    mag = ldexp((double)m / 8.0, 1 - 7); /* subnormal: 2^(1-bias) * 0.m */
+  else
+    mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+
+static double load_kv(const oracle_problem* p, const void* cache, const float* scale,
+                      int32_t page, int g, int slot, int d) {
+  size_t idx = (((size_t)page * p->num_kv_heads + g) * ORACLE_PAGE + slot) * p->head_dim + d;
+  if (p->kv_dtype == 0) return oracle_decode_bf16(((const uint16_t*)cache)[idx]);
+  double s = scale[((size_t)page * p->num_kv_heads + g) * ORACLE_PAGE + slot];
+#if ORACLE_MUTANT == 4
+  s = 1.0; /* planted: scale dropped */
+#endif
+  return oracle_decode_e4m3(((const uint8_t*)cache)[idx]) * s;
+}
+
+/* One query row (token tau, q head h); out has head_dim entries.
+ * Returns 0, or -1 when the row does not exist. */
+static int row_attention(const oracle_problem* p, int64_t tau, int h, double* out, double* z) {
+  int64_t off = 0;
+  int b = -1;
+  for (int s = 0; s < p->num_seqs; ++s) {
+    if (tau < off + p->query_lens[s]) { b = s; break; }
+    off += p->query_lens[s];
+  }
+  if (b < 0 || h < 0 || h >= p->num_q_heads) return -1;
+  const int D = p->head_dim;
+  const int G = p->num_q_heads / p->num_kv_heads;
+  const int64_t i = tau - off;
+  const int64_t L = p->context_lens[b];
+  const int64_t q = p->query_lens[b];
+  int g = h / G;
+#if ORACLE_MUTANT == 2
+  g = h % p->num_kv_heads; /* planted: interleaved GQA groups */
+#endif
+  int64_t last = L - q + i; /* last visible key */
+#if ORACLE_MUTANT == 1
+  last = L - 1; /* planted: no causal mask inside the drafts */
+#endif
+  const uint16_t* qrow = p->q + ((size_t)tau * p->num_q_heads + h) * D;
+  const float* ks = p->k_scale;
+  const float* vs = p->v_scale;
+#if ORACLE_MUTANT == 5
+  ks = p->v_scale; vs = p->k_scale; /* planted: K and V scales swapped */
+#endif
+
+  /* pass 1: logits and their maximum */
+  double zmax = -INFINITY;
+  for (int64_t t = 0; t <= last; ++t) {
+    int32_t pg = p->block_table[(size_t)b * p->block_table_stride + t / ORACLE_PAGE];
+    int slot = (int)(t % ORACLE_PAGE);
+#if ORACLE_MUTANT == 3
+    slot = (int)((t + 1) % ORACLE_PAGE); /* planted: slot off by one */
+#endif
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d)
+      acc += oracle_decode_bf16(qrow[d]) * load_kv(p, p->k_cache, ks, pg, g, slot, d);
+    z[t] = p->softmax_scale * acc;
+    if (z[t] > zmax) zmax = z[t];
+  }
+  /* pass 2: weights and the weighted mean of V */
+  for (int d = 0; d < D; ++d) out[d] = 0.0;
+  double wsum = 0.0;
+  for (int64_t t = 0; t <= last; ++t) {
+    int32_t pg = p->block_table[(size_t)b * p->block_table_stride + t / ORACLE_PAGE];
+    int slot = (int)(t % ORACLE_PAGE);
+    double w = exp(z[t] - zmax);
+#if ORACLE_MUTANT == 6
+    w = exp(z[t]); /* planted: weights not normalised by the running max; fine
+                      numerically for small logits, so it must be caught by
+                      a pin with large logits */
+    if (z[t] - zmax < -700) w = 0.0;
+#endif
+    wsum += w;
+    for (int d = 0; d < D; ++d) out[d] += w * load_kv(p, p->v_cache, vs, pg, g, slot, d);
+  }
+  for (int d = 0; d < D; ++d) out[d] /= wsum;
+  return 0;
+}
+
+typedef struct {
+  const oracle_problem* p;
+  const int64_t* rows; /* pairs (tau, h) or NULL for all */
+  int64_t n_rows;
+  double* out;
+  int64_t next;
+  pthread_mutex_t lock;
+  int status;
+  int64_t max_ctx;
+} oracle_job;
+
+static void* worker(void* arg) {
+  oracle_job* job = (oracle_job*)arg;
+  double* z = (double*)malloc(sizeof(double) * (size_t)(job->max_ctx + 1));
+  if (!z) {
+    pthread_mutex_lock(&job->lock);
+    job->status = -5;
+    pthread_mutex_unlock(&job->lock);
+    return NULL;
+  }
+  for (;;) {
+    pthread_mutex_lock(&job->lock);
+    int64_t k = job->next++;
+    pthread_mutex_unlock(&job->lock);
+    if (k >= job->n_rows) break;
+    int64_t tau;
+    int h;
+    if (job->rows) {
+      tau = job->rows[2 * k];
+      h = (int)job->rows[2 * k + 1];
+    } else {
+      tau = k / job->p->num_q_heads;
+      h = (int)(k % job->p->num_q_heads);
+    }
+    if (row_attention(job->p, tau, h, job->out + (size_t)k * job->p->head_dim, z) != 0) {
+      pthread_mutex_lock(&job->lock);
+      job->status = -1;
+      pthread_mutex_unlock(&job->lock);
+    }
+  }
+  free(z);
+  return NULL;
+}
+
+/* Computes the selected rows (pairs (token, q head) in `rows`, or every row
+ * [T][Hq] when rows == NULL; n_rows is then T * Hq) into out[n_rows][D].
+ * n_threads <= 0 means one thread. Returns 0, -1 on a bad row or argument,
+ * -5 when out of host memory. */
+int oracle_verify_attention(const oracle_problem* p, const int64_t* rows, int64_t n_rows,
+                            double* out, int n_threads) {
+  if (!p || !out || n_rows < 0 || p->num_kv_heads <= 0 || p->num_q_heads % p->num_kv_heads)
+    return -1;
+  oracle_job job;
+  memset(&job, 0, sizeof job);
+  job.p = p;
+  job.rows = rows;
+  job.n_rows = n_rows;
+  job.out = out;
+  job.max_ctx = 1;
+  for (int s = 0; s < p->num_seqs; ++s)
+    if (p->context_lens[s] > job.max_ctx) job.max_ctx = p->context_lens[s];
+  pthread_mutex_init(&job.lock, NULL);
+  if (n_threads <= 1) {
+    worker(&job);
+  } else {
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)n_threads);
+    if (!th) return -5;
+    for (int k = 0; k < n_threads; ++k) pthread_create(&th[k], NULL, worker, &job);
+    for (int k = 0; k < n_threads; ++k) pthread_join(th[k], NULL);
+    free(th);
+  }
+  pthread_mutex_destroy(&job.lock);
+  return job.status;
+}
