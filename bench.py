@@ -1,0 +1,375 @@
+"""Benchmark of paged verify attention on GB300 (one JSON line on rank 0).
+
+A step is one call of the whole path (split-KV kernel + log-sum-exp combine)
+over one batch of the MTP-5 bf16 verify workload: 8 sequences, 6 verify
+tokens each, 32 q / 4 KV heads, head_dim 128, context lengths uniform in
+[4096, 32768], 16-token pages scattered in the pool, q/K/V ~ N(0, 1).
+`value` is KV GB/s (algorithmic K+V bytes read once, divided by the call
+time), `ms_per_step` the call time. Under torchrun each rank runs its own
+batch (weak scaling, no data exchange); rank 0 prints the job aggregate.
+
+`--impl reference` times the CPU fp64 oracle on the same workload instead
+(a bounded sample per step, on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_speculative_gb300 import synth  # noqa: E402
+
+METRIC = "verify-attention µs/call and KV GB/s vs GB300 HBM peak (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD_DESC = {
+    "tiny": "tiny: B=2 q=[1,6] ctx=[37,100] Hq=4 Hkv=1 D=64 bf16 KV, 32-page pool, seed 0",
+    "mtp5_bf16": "MTP-5 verify bf16 KV: B=8 q=6 Hq=32 Hkv=4 D=128 page 16, ctx U[4096,32768] (seed 2), scattered pages",
+    "mtp5_fp8": "MTP-5 verify FP8 E4M3 KV + per-token fp32 scales: B=4 q=6 Hq=32 Hkv=4 D=128, ctx 131072 each (seed 3)",
+    "mixed_fp8": "mixed FP8 batch: B=64 q U{1..8} Hq=16 Hkv=2 D=128, ctx lognormal(median 8192, sigma 1, cap 131072) (seed 4)",
+    "ctx1mi_bf16": "1Mi-token verify bf16 KV: B=1 q=6 Hq=8 Hkv=1 D=128, ctx 1048576, 65536-entry table, random page order (seed 5)",
+}
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "paged_kv_speculative_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                return json.load(f), "measured"
+        except Exception:
+            pass
+    return None, "fallback"
+
+
+def hbm_peak(peaks):
+    if peaks:
+        for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs", "hbm"):
+            v = peaks.get(k)
+            if isinstance(v, (int, float)) and v > 0:
+                return float(v), "of measured"
+            if isinstance(v, dict):
+                for kk in ("gbs", "value", "burst"):
+                    if isinstance(v.get(kk), (int, float)):
+                        return float(v[kk]), "of measured"
+    return FALLBACK_HBM_GBS, "of fallback"
+
+
+def traffic_for(workload: str):
+    """DRAM bytes per split-kernel launch from a committed ncu summary, if the
+    kernel sources still match the ones the counters were taken on."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_sample(prob, budget_s: float, sample_note_prefix: str):
+    """Times the oracle on whole sequences of `prob` (all their rows) until
+    about `budget_s` seconds of wall time have been spent."""
+    import oracle
+    threads = os.cpu_count() or 1
+    off = prob.q_offsets()
+    order = np.argsort(prob.context_lens)  # short sequences first keeps the first sample small
+    done_bytes, elapsed, seqs = 0, 0.0, 0
+    per_th = 2 * prob.head_dim * (2 if prob.kv_dtype == synth.KV_BF16 else 1) + (8 if prob.kv_dtype == synth.KV_FP8 else 0)
+    for b in order:
+        rows = np.array([(t, h) for t in range(off[b], off[b + 1]) for h in range(prob.num_q_heads)], dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.verify_attention(prob, rows=rows, threads=threads)
+        elapsed += time.perf_counter() - t0
+        done_bytes += int(prob.context_lens[b]) * prob.num_kv_heads * per_th
+        seqs += 1
+        if elapsed >= budget_s:
+            break
+    gbs = done_bytes / elapsed / 1e9
+    note = (f"{sample_note_prefix}: {seqs} of {prob.num_seqs} sequences (all rows), {done_bytes / 1e6:.1f} MB of KV, "
+            f"{elapsed:.2f} s, fp64 C oracle, {threads} threads")
+    return gbs, threads, note, elapsed
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    prob = synth.make_config(args.config, poison=False)
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        cpu_oracle_sample(prob, 0.0, "warmup")
+    vals, times = [], []
+    note, threads = "", 1
+    for _ in range(args.steps):
+        gbs, threads, note, el = cpu_oracle_sample(prob, args.ref_budget, "sample")
+        vals.append(gbs)
+        times.append(el)
+    value = float(statistics.median(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(statistics.median(times)),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD_DESC[args.config], "name": args.config},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": note},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mtp5_bf16", choices=list(synth.CONFIG_NAMES))
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=3.0, help="seconds of oracle time per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--also", default="", help="comma-separated extra workloads to report under 'other_configs'")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    from paged_kv_speculative_gb300 import _build, pa_verify as pv
+    from paged_kv_speculative_gb300.device_inputs import host_tensors
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MiB > 129 MB L2
+
+    def measure(name, steps, warmup, seed_offset):
+        ctx, ql, hq, hkv, d, kvd, seed = synth.config_lengths(name)
+        kw = {"pool_pages": 32} if name == "tiny" else {}
+        prob = synth.make_problem(ctx, ql, hq, hkv, d, kv_dtype=kvd, seed=seed + 1000 * seed_offset, poison=False,
+                                  name=name, **kw)
+        host = host_tensors(prob, pin=True)
+        dv = [None if x is None else x.to(dev) for x in host.args()]
+        va = pv.VerifyAttention(hq, hkv, d, kvd, prob.num_pages, prob.block_table.shape[1], ctx, ql,
+                                out_dtype=pv.OUT_BF16, device=dev)
+        out = va.new_out()
+        stream = torch.cuda.current_stream(dev)
+        for _ in range(warmup):
+            flush.zero_()
+            va(*dv, prob.softmax_scale, out=out)
+        torch.cuda.synchronize(dev)
+        pv.profile_enable(va.plan, True)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        split_ms, comb_ms = [], []
+        barrier()
+        torch.cuda.synchronize(dev)
+        wall0 = time.perf_counter()
+        for k in range(steps):
+            flush.zero_()
+            evs[k][0].record(stream)
+            va(*dv, prob.softmax_scale, out=out)
+            evs[k][1].record(stream)
+            a, c = pv.profile_read(va.plan)  # waits for this step; the next flush is enqueued after it
+            split_ms.append(a)
+            comb_ms.append(c)
+        torch.cuda.synchronize(dev)
+        barrier()
+        wall = time.perf_counter() - wall0
+        step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+        pv.profile_enable(va.plan, False)
+        errs = va.device_errors()
+        info = va.info
+        res = {"prob": prob, "host": host, "va": va, "dv": dv, "out": out, "step_ms": step_ms,
+               "split_ms": split_ms, "comb_ms": comb_ms, "wall": wall, "info": info, "errs": errs}
+        return res
+
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        r = measure(args.config, args.steps, args.warmup, rank)
+    clocks = clk.summary()
+    prob, info = r["prob"], r["info"]
+    total_ms = float(sum(r["step_ms"]))
+    mean_ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    kv_bytes_rank = int(info["kv_bytes"])
+    value = kv_bytes_rank * world * args.steps / (total_ms * 1e-3) / 1e9
+    split_avg = float(np.mean(r["split_ms"]))
+    comb_avg = float(np.mean(r["comb_ms"]))
+
+    # ---- end to end through the public API with host buffers
+    host, va = r["host"], r["va"]
+    out_host = torch.empty(r["out"].shape, dtype=r["out"].dtype, pin_memory=True)
+    dv = r["dv"]
+    h2d = sum(x.numel() * x.element_size() for x in host.args() if x is not None)
+    d2h = out_host.numel() * out_host.element_size()
+    stream = torch.cuda.current_stream(dev)
+    e2e_ms = []
+    for k in range(args.e2e_steps + 2):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for dst, src in zip(dv, host.args()):
+            if src is not None:
+                dst.copy_(src, non_blocking=True)
+        va(*dv, prob.softmax_scale, out=r["out"])
+        out_host.copy_(r["out"], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if k >= 2:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_val = kv_bytes_rank * world / (float(np.mean(e2e_ms)) * 1e-3) / 1e9
+
+    others = {}
+    for name in [x for x in args.also.split(",") if x]:
+        o = measure(name, max(10, args.steps // 2), args.warmup, rank)
+        oms = float(np.mean(o["step_ms"]))
+        osplit = float(np.mean(o["split_ms"]))
+        others[name] = {"us_per_call": 1e3 * oms, "kv_gbs": o["info"]["kv_bytes"] / (oms * 1e-3) / 1e9,
+                        "split_kernel_us": 1e3 * osplit,
+                        "split_kernel_gbs": o["info"]["kv_bytes"] / (osplit * 1e-3) / 1e9,
+                        "units": o["info"]["num_units"], "chunk": o["info"]["chunk_tokens"],
+                        "device_errors": o["errs"]}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, _ = load_peaks()
+    peak, peak_note = hbm_peak(peaks)
+    achieved = kv_bytes_rank / (split_avg * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        gbs, threads, note, _ = cpu_oracle_sample(prob, args.cpu_budget, "sample")
+        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": note}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "us_per_call": 1e3 * mean_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if prob.kv_dtype == 0 else "fp8-e4m3 KV, bf16 q",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.config], "name": args.config,
+                   "kv_bytes_per_call": kv_bytes_rank, "l2": "flushed between steps (256 MiB write, outside the events)",
+                   "units": info["num_units"], "chunk_tokens": info["chunk_tokens"], "splits_max": info["max_splits"],
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_note, "traffic": traffic_for(args.config),
+                     "kernel": "pa_split_kernel", "split_kernel_us": 1e3 * split_avg, "combine_kernel_us": 1e3 * comb_avg},
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": float(np.mean(e2e_ms))},
+        "gpu_launches": args.steps * (1 + int(info["needs_combine"])),
+        "clocks": clocks,
+        "device_errors": r["errs"],
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    if others:
+        line["other_configs"] = others
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

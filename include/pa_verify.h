@@ -1,0 +1,170 @@
+/*
+ * pa_verify — paged-KV attention for speculative-decoding verify steps on one
+ * GB300 GPU (sm_103a).
+ *
+ * The operation. Each sequence b of a batch brings q_b verify tokens
+ * (1 <= q_b <= 8; 6 for an MTP-5 / DSpark-5 verify step, 4 for MTP-3, 1 for a
+ * draft step). Those tokens are the last q_b tokens of the sequence's context of
+ * L_b cached tokens. Query row (token i, q head h) attends, with softmax scale
+ * `softmax_scale`, to keys 0 .. L_b - q_b + i of KV head h / (Hq / Hkv): the
+ * whole context, causal inside the drafts. The GQA group times the query length
+ * forms the rows that share one read of a KV head ("rows = query length x GQA
+ * group", e.g. qlen 6 x group 8 = 48 rows: "fix(attention): keep MTP-5 decode
+ * on FlyDSL pa_decode past the gluon query-length limit", Motivation). Keys and
+ * values live in a pool of 16-token pages, head-major within a page
+ * ("[MiniMax-M3.1] P/D from a PP4 prefill into a TP4 decode (2/2: DSpark)",
+ * page-16 views, head-major per page), reached through a per-sequence block
+ * table, and are bf16 or OCP FP8 E4M3 with per-token, per-head fp32 scales
+ * (the MTP-5 page, Motivation and Tests: per-token FP8 KV scales with a
+ * trailing singleton dimension).
+ *
+ * Calls. pa_verify_plan checks a batch description and its host-side lengths,
+ * refuses anything outside the supported envelope before any allocation, and
+ * picks the KV split (chunk length) from total context and SM count.
+ * pa_verify_run enqueues the attention on a stream: a split-KV kernel and, when
+ * some (sequence, KV head) was split, a log-sum-exp combine kernel.
+ *
+ * Conventions. All device pointers refer to memory of the current device.
+ * The caller owns every buffer; the library keeps no device memory and no
+ * pointer past a call. Nothing throws across this interface. Every function
+ * returns a status (PA_OK = 0 or a negative PA_ERR_*) and, on failure, leaves
+ * a message for pa_verify_last_error(). A refused call launches nothing and
+ * writes nothing.
+ */
+#ifndef PA_VERIFY_H
+#define PA_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without the CUDA headers. NULL = the legacy default stream. */
+typedef struct CUstream_st* pa_stream_t;
+
+/* Opaque plan: host memory only, owned by the library until pa_verify_free. */
+typedef struct pa_verify_plan_s* pa_verify_plan_t;
+
+enum {
+  PA_KV_BF16 = 0,     /* bf16 K/V */
+  PA_KV_FP8_E4M3 = 1  /* OCP E4M3 (max finite 448) K/V with fp32 scales */
+};
+
+enum { PA_OUT_BF16 = 0, PA_OUT_F32 = 1 };
+
+enum {
+  PA_OK = 0,
+  PA_ERR_INVALID = -1,     /* bad argument: null pointer, bad length, misalignment */
+  PA_ERR_UNSUPPORTED = -2, /* valid but outside the envelope (head_dim, group, batch) */
+  PA_ERR_WORKSPACE = -3,   /* workspace smaller than the plan needs */
+  PA_ERR_CUDA = -4,        /* a CUDA call failed (launch, tensor-map encode, device query) */
+  PA_ERR_NOMEM = -5        /* host allocation failed */
+};
+
+/* Bits of the device error word (pa_verify_device_errors). */
+enum {
+  PA_DEVERR_PAGE_RANGE = 1u,  /* a block-table entry outside [0, num_pages): zeros were read instead */
+  PA_DEVERR_LENGTHS = 2u,     /* device context_lens/query_lens differ from the planned ones */
+  PA_DEVERR_TIMEOUT = 4u      /* a wait for staged K/V timed out; the unit's output is invalid */
+};
+
+typedef struct {
+  int32_t num_seqs;           /* B, 0 .. 64 */
+  int32_t num_q_heads;        /* Hq >= 1 */
+  int32_t num_kv_heads;       /* Hkv >= 1, Hq % Hkv == 0, group G = Hq / Hkv */
+  int32_t head_dim;           /* D: 64 or 128 (bf16 KV); 128 (FP8 KV) */
+  int32_t page_size;          /* must be 16 */
+  int32_t kv_dtype;           /* PA_KV_* */
+  int32_t out_dtype;          /* PA_OUT_* */
+  int32_t num_pages;          /* pool size N_pg; block-table entries must lie in [0, N_pg) */
+  int32_t block_table_stride; /* int32 entries per block-table row, >= ceil(L_b / 16) */
+  int32_t split_override;     /* 0: the planner chooses; k > 0: chunk length
+                                 ceil(max_b L_b / k) rounded up to the staging tile */
+  int32_t sm_count;           /* 0: query the current device; > 0: plan for that many SMs */
+} pa_verify_desc;
+
+typedef struct {
+  int32_t num_units;       /* CTAs of the split kernel: sum_b Hkv * ceil(L_b / chunk) */
+  int32_t chunk_tokens;    /* context tokens per unit (a multiple of tile_tokens) */
+  int32_t tile_tokens;     /* tokens per shared-memory stage */
+  int32_t rows_max;        /* max_b q_b * G */
+  int32_t warps;           /* compute warps per CTA = ceil(rows_max / 16) */
+  int32_t max_splits;      /* max_b ceil(L_b / chunk) */
+  int32_t needs_combine;   /* 1 when some (sequence, KV head) has more than one unit */
+  int32_t num_tokens;      /* T = sum_b q_b */
+  int64_t kv_bytes;        /* algorithmic K/V(+scale) bytes one run reads */
+  size_t workspace_bytes;  /* bytes pa_verify_run needs in `workspace` */
+} pa_verify_plan_info;
+
+/*
+ * Checks the batch and builds a plan. Reads context_lens_host[num_seqs] and
+ * query_lens_host[num_seqs] (host memory, copied into the plan) and requires
+ * 1 <= q_b <= 8, q_b <= L_b, ceil(L_b / 16) <= block_table_stride, and
+ * (q_b * G) <= 128. On success *plan_out owns a host-side plan and
+ * *workspace_bytes_out is the device workspace a run needs (0 is possible only
+ * for an empty batch). On failure *plan_out is NULL; nothing is allocated and
+ * no CUDA call is made (with sm_count > 0 the function makes no CUDA call at all).
+ */
+int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
+                   const int32_t* query_lens_host, pa_verify_plan_t* plan_out,
+                   size_t* workspace_bytes_out);
+
+/* Copies the plan's figures into *info. */
+int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info);
+
+/*
+ * Enqueues verify attention on `stream` and returns without waiting.
+ *   q            [T, Hq, D] bf16, the q_b rows of each sequence packed in batch order
+ *   k_cache      [N_pg, Hkv, 16, D] bf16 or E4M3 bytes, 16-byte aligned base
+ *   v_cache      same layout as k_cache
+ *   k_scale      [N_pg, Hkv, 16] fp32 (a trailing [.., 1] is the same memory),
+ *                16-byte aligned; NULL for bf16 KV, required for FP8 KV
+ *   v_scale      same as k_scale
+ *   block_table  [B, block_table_stride] int32
+ *   context_lens [B] int32, device; must hold the planned values (a mismatch
+ *                sets PA_DEVERR_LENGTHS and leaves the output undefined)
+ *   query_lens   [B] int32, device; same rule
+ *   softmax_scale finite and > 0 (1/sqrt(D) is the usual choice)
+ *   out          [T, Hq, D] bf16 or fp32 (desc.out_dtype); every element is written
+ *   workspace    >= the planned workspace_bytes, 256-byte aligned; holds the
+ *                split partials and the device error word. Zero it once after
+ *                allocation; runs never clear the error word.
+ * All device buffers must stay valid until the enqueued work completes. Two
+ * runs that share a workspace must not overlap on the GPU.
+ */
+int pa_verify_run(pa_verify_plan_t plan, const void* q, const void* k_cache, const void* v_cache,
+                  const float* k_scale, const float* v_scale, const int32_t* block_table,
+                  const int32_t* context_lens, const int32_t* query_lens, float softmax_scale,
+                  void* out, void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Measurement hooks. After pa_verify_profile_enable(plan, 1), every
+ * pa_verify_run with this plan records CUDA events (owned by the plan) on its
+ * stream before the split kernel, between the kernels and after the combine.
+ * pa_verify_profile_read waits for the last profiled run and returns the
+ * device time of its split kernel and of its combine kernel (0 when there was
+ * none), in milliseconds. Enabling creates the events (needs a device);
+ * disabling keeps them until pa_verify_free.
+ */
+int pa_verify_profile_enable(pa_verify_plan_t plan, int enable);
+int pa_verify_profile_read(pa_verify_plan_t plan, float* split_ms, float* combine_ms);
+
+/* Frees a plan (NULL is allowed). */
+void pa_verify_free(pa_verify_plan_t plan);
+
+/*
+ * Reads the device error word of `workspace` (PA_DEVERR_* bits) after
+ * synchronising `stream`; clears it when `clear` is non-zero.
+ */
+int pa_verify_device_errors(void* workspace, uint32_t* flags_out, int clear, pa_stream_t stream);
+
+/* Message for the last failing call on this thread ("" when none). */
+const char* pa_verify_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_VERIFY_H */

@@ -1,0 +1,380 @@
+// C ABI of the paged verify-attention library: planner, validation, launch.
+//
+// The planner follows the pages' split-decode structure: a decode kernel
+// working over KV partitions plus a reducer, with the feasibility check done
+// before any plan or scratch exists ("check feasibility first", MTP-5 routing
+// page, review of base_attention.py) and a refusal instead of running outside
+// the envelope. The partition count is chosen from the total context and the
+// SM count so that one wave of CTAs covers the batch; a batch of one gets
+// the ceiling of splits it can use (the page's dense-decode split test).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "pa_internal.h"
+#include "../../include/pa_verify.h"
+
+namespace pav {
+cudaError_t launch_split_bf16(int head_dim, int warps, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                              const SplitParams* p, cudaStream_t stream);
+cudaError_t launch_split_fp8(int head_dim, int warps, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                             const SplitParams* p, cudaStream_t stream);
+}  // namespace pav
+
+using namespace pav;
+
+struct pa_verify_plan_s {
+  pa_verify_desc d;
+  int32_t tile = 0, chunk = 0, units = 0, rows_max = 0, warps = 0, max_splits = 0, needs_combine = 0;
+  int32_t num_tokens = 0, num_rows = 0;
+  int64_t kv_bytes = 0;
+  size_t ws_bytes = 0;
+  SeqInfo seq[kMaxSeqs];
+  // tensor maps, re-encoded only when the cache pointers change
+  const void* tm_k = nullptr;
+  const void* tm_v = nullptr;
+  CUtensorMap tmk, tmv;
+  // measurement events (pa_verify_profile_enable)
+  int profiling = 0;
+  int profiled_runs = 0;
+  int last_had_combine = 0;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+int encode_kv_map(CUtensorMap* map, const void* base, const pa_verify_desc& d) {
+  auto enc = get_encoder();
+  if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int esz = d.kv_dtype == PA_KV_FP8_E4M3 ? 1 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim),
+                        static_cast<cuuint64_t>(d.num_pages) * d.num_kv_heads * kPage};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(kPage)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
+  return PA_OK;
+}
+
+int supported_warps(int rows_max) {
+  const int w = (rows_max + 15) / 16;
+  return w <= 4 ? w : 8;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_verify_last_error(void) { return g_last_error.c_str(); }
+
+int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host, const int32_t* query_lens_host,
+                   pa_verify_plan_t* plan_out, size_t* workspace_bytes_out) {
+  g_last_error.clear();
+  if (plan_out) *plan_out = nullptr;
+  if (!desc || !plan_out || !workspace_bytes_out) return fail(PA_ERR_INVALID, "desc, plan_out and workspace_bytes_out must not be NULL");
+  const pa_verify_desc& d = *desc;
+  if (d.num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs < 0");
+  if (d.num_seqs > kMaxSeqs) return fail(PA_ERR_UNSUPPORTED, "num_seqs above " + std::to_string(kMaxSeqs));
+  if (d.num_seqs > 0 && (!context_lens_host || !query_lens_host))
+    return fail(PA_ERR_INVALID, "context_lens_host / query_lens_host must not be NULL");
+  if (d.num_q_heads < 1 || d.num_kv_heads < 1 || d.num_q_heads % d.num_kv_heads != 0)
+    return fail(PA_ERR_INVALID, "need num_q_heads >= 1, num_kv_heads >= 1 and num_q_heads % num_kv_heads == 0");
+  if (d.page_size != kPage) return fail(PA_ERR_UNSUPPORTED, "page_size must be 16");
+  if (d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_FP8_E4M3) return fail(PA_ERR_INVALID, "unknown kv_dtype");
+  if (d.out_dtype != PA_OUT_BF16 && d.out_dtype != PA_OUT_F32) return fail(PA_ERR_INVALID, "unknown out_dtype");
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  if (fp8 ? d.head_dim != 128 : (d.head_dim != 64 && d.head_dim != 128))
+    return fail(PA_ERR_UNSUPPORTED, fp8 ? "FP8 KV needs head_dim 128" : "bf16 KV needs head_dim 64 or 128");
+  if (d.num_seqs > 0 && (d.num_pages < 1 || d.block_table_stride < 1))
+    return fail(PA_ERR_INVALID, "num_pages and block_table_stride must be >= 1");
+  if (static_cast<int64_t>(d.num_pages) * d.num_kv_heads * kPage >= (int64_t(1) << 31))
+    return fail(PA_ERR_UNSUPPORTED, "num_pages * num_kv_heads * 16 must stay below 2^31");
+  if (d.split_override < 0 || d.sm_count < 0) return fail(PA_ERR_INVALID, "split_override and sm_count must be >= 0");
+
+  const int G = d.num_q_heads / d.num_kv_heads;
+  int rows_max = 0, max_len = 0;
+  int64_t total_tokens = 0, work = 0;
+  for (int b = 0; b < d.num_seqs; ++b) {
+    const int L = context_lens_host[b], q = query_lens_host[b];
+    if (q < 1 || q > kMaxQueryLen) return fail(PA_ERR_INVALID, "query_lens must lie in 1..8 (sequence " + std::to_string(b) + ")");
+    if (L < q) return fail(PA_ERR_INVALID, "context_len < query_len (sequence " + std::to_string(b) + ")");
+    if ((static_cast<int64_t>(L) + kPage - 1) / kPage > d.block_table_stride)
+      return fail(PA_ERR_INVALID, "context_len needs more pages than block_table_stride (sequence " + std::to_string(b) + ")");
+    if (q * G > kMaxRows) return fail(PA_ERR_UNSUPPORTED, "query_len * group above 128 rows");
+    rows_max = std::max(rows_max, q * G);
+    max_len = std::max(max_len, L);
+    total_tokens += q;
+    work += static_cast<int64_t>(L) * d.num_kv_heads;
+  }
+
+  int sms = d.sm_count;
+  if (sms == 0 && d.num_seqs > 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("SM count query failed: ") + cudaGetErrorString(e));
+  }
+
+  pa_verify_plan_s* P = new (std::nothrow) pa_verify_plan_s();
+  if (!P) return fail(PA_ERR_NOMEM, "out of host memory");
+  P->d = d;
+  P->d.sm_count = sms;
+  if (d.num_seqs == 0) {
+    P->ws_bytes = kWsHeader;
+    *plan_out = P;
+    *workspace_bytes_out = P->ws_bytes;
+    return PA_OK;
+  }
+  const int tile = tile_tokens(fp8 ? 1 : 0, d.head_dim);
+  const int warps = supported_warps(rows_max);
+  const int64_t slots = static_cast<int64_t>(sms) * split_ctas_per_sm(warps);
+  auto units_for = [&](int64_t c) {
+    int64_t u = 0;
+    for (int b = 0; b < d.num_seqs; ++b) u += (context_lens_host[b] + c - 1) / c;
+    return u * d.num_kv_heads;
+  };
+  const int64_t max_tile_len = align_up(static_cast<size_t>(max_len), static_cast<size_t>(tile));
+  int64_t chunk;
+  if (d.split_override > 0) {
+    chunk = align_up(static_cast<size_t>((max_len + d.split_override - 1) / d.split_override), static_cast<size_t>(tile));
+  } else {
+    // one wave: the smallest tile multiple whose unit count fits the resident CTA slots
+    chunk = align_up(static_cast<size_t>((work + slots - 1) / slots), static_cast<size_t>(tile));
+    chunk = std::max<int64_t>(chunk, tile);
+    while (chunk < max_tile_len && units_for(chunk) > slots) chunk += tile;
+  }
+  chunk = std::min<int64_t>(chunk, kMaxChunk);
+  chunk = std::min<int64_t>(chunk, std::max<int64_t>(max_tile_len, tile));
+  chunk = std::max<int64_t>(chunk, tile);
+
+  // sequences by decreasing context length: long units are scheduled first
+  std::vector<int> order(d.num_seqs);
+  for (int b = 0; b < d.num_seqs; ++b) order[b] = b;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int c) { return context_lens_host[a] > context_lens_host[c]; });
+  std::vector<int32_t> q_off(d.num_seqs);
+  int32_t acc = 0;
+  for (int b = 0; b < d.num_seqs; ++b) {
+    q_off[b] = acc;
+    acc += query_lens_host[b];
+  }
+  int64_t unit = 0, row = 0;
+  int max_splits = 0;
+  for (int k = 0; k < d.num_seqs; ++k) {
+    const int b = order[k];
+    SeqInfo& s = P->seq[k];
+    s.ctx_len = context_lens_host[b];
+    s.q_len = query_lens_host[b];
+    s.q_off = q_off[b];
+    s.unit_start = static_cast<int32_t>(unit);
+    s.row_start = static_cast<int32_t>(row);
+    s.n_chunks = static_cast<int32_t>((s.ctx_len + chunk - 1) / chunk);
+    s.b = b;
+    s.pad = 0;
+    unit += static_cast<int64_t>(s.n_chunks) * d.num_kv_heads;
+    row += static_cast<int64_t>(s.q_len) * d.num_q_heads;
+    max_splits = std::max(max_splits, s.n_chunks);
+  }
+  if (unit >= (int64_t(1) << 31) || row >= (int64_t(1) << 31)) {
+    delete P;
+    return fail(PA_ERR_UNSUPPORTED, "work too large for one call");
+  }
+  P->tile = tile;
+  P->chunk = static_cast<int32_t>(chunk);
+  P->units = static_cast<int32_t>(unit);
+  P->rows_max = rows_max;
+  P->warps = warps;
+  P->max_splits = max_splits;
+  P->needs_combine = max_splits > 1 ? 1 : 0;
+  P->num_tokens = static_cast<int32_t>(total_tokens);
+  P->num_rows = static_cast<int32_t>(row);
+  const int64_t per_th = fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim);
+  P->kv_bytes = work * per_th;
+  size_t ws = kWsHeader;
+  if (P->needs_combine) {
+    ws += align_up(static_cast<size_t>(unit) * rows_max * d.head_dim * 4, 256);
+    ws += align_up(static_cast<size_t>(unit) * rows_max * 4, 256);
+  }
+  P->ws_bytes = ws;
+  *plan_out = P;
+  *workspace_bytes_out = ws;
+  return PA_OK;
+}
+
+int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info) {
+  if (!plan || !info) return fail(PA_ERR_INVALID, "plan and info must not be NULL");
+  info->num_units = plan->units;
+  info->chunk_tokens = plan->chunk;
+  info->tile_tokens = plan->tile;
+  info->rows_max = plan->rows_max;
+  info->warps = plan->warps;
+  info->max_splits = plan->max_splits;
+  info->needs_combine = plan->needs_combine;
+  info->num_tokens = plan->num_tokens;
+  info->kv_bytes = plan->kv_bytes;
+  info->workspace_bytes = plan->ws_bytes;
+  return PA_OK;
+}
+
+int pa_verify_run(pa_verify_plan_t plan, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                  const float* v_scale, const int32_t* block_table, const int32_t* context_lens,
+                  const int32_t* query_lens, float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
+                  pa_stream_t stream) {
+  g_last_error.clear();
+  if (!plan) return fail(PA_ERR_INVALID, "plan must not be NULL");
+  const pa_verify_desc& d = plan->d;
+  if (d.num_seqs == 0) return PA_OK;
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !query_lens || !out || !workspace)
+    return fail(PA_ERR_INVALID, "a required pointer is NULL");
+  if (fp8 && (!k_scale || !v_scale)) return fail(PA_ERR_INVALID, "FP8 KV needs k_scale and v_scale");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return fail(PA_ERR_INVALID, "q, k_cache, v_cache and out must be 16-byte aligned");
+  if (fp8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16)))
+    return fail(PA_ERR_INVALID, "k_scale and v_scale must be 16-byte aligned");
+  if (!aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(query_lens, 4))
+    return fail(PA_ERR_INVALID, "int32 arrays must be 4-byte aligned");
+  if (!aligned(workspace, 256)) return fail(PA_ERR_INVALID, "workspace must be 256-byte aligned");
+  if (!(std::isfinite(softmax_scale) && softmax_scale > 0.f)) return fail(PA_ERR_INVALID, "softmax_scale must be finite and > 0");
+  if (workspace_bytes < plan->ws_bytes)
+    return fail(PA_ERR_WORKSPACE, "workspace of " + std::to_string(workspace_bytes) + " bytes, plan needs " +
+                                      std::to_string(plan->ws_bytes));
+
+  if (plan->tm_k != k_cache) {
+    int rc = encode_kv_map(&plan->tmk, k_cache, d);
+    if (rc) return rc;
+    plan->tm_k = k_cache;
+  }
+  if (plan->tm_v != v_cache) {
+    int rc = encode_kv_map(&plan->tmv, v_cache, d);
+    if (rc) return rc;
+    plan->tm_v = v_cache;
+  }
+
+  SplitParams* p = new (std::nothrow) SplitParams();
+  if (!p) return fail(PA_ERR_NOMEM, "out of host memory");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p->q = static_cast<const uint16_t*>(q);
+  p->block_table = block_table;
+  p->k_scale = fp8 ? k_scale : nullptr;
+  p->v_scale = fp8 ? v_scale : nullptr;
+  p->out = out;
+  p->err = reinterpret_cast<uint32_t*>(ws);
+  if (plan->needs_combine) {
+    p->part_o = reinterpret_cast<float*>(ws + kWsHeader);
+    p->part_lse = reinterpret_cast<float*>(
+        ws + kWsHeader + align_up(static_cast<size_t>(plan->units) * plan->rows_max * d.head_dim * 4, 256));
+  }
+  p->dev_ctx = context_lens;
+  p->dev_q = query_lens;
+  p->num_seqs = d.num_seqs;
+  p->num_q_heads = d.num_q_heads;
+  p->num_kv_heads = d.num_kv_heads;
+  p->group = d.num_q_heads / d.num_kv_heads;
+  p->bt_stride = d.block_table_stride;
+  p->num_pages = d.num_pages;
+  p->chunk = plan->chunk;
+  p->num_units = plan->units;
+  p->rows_max = plan->rows_max;
+  p->out_f32 = d.out_dtype == PA_OUT_F32 ? 1 : 0;
+  p->num_rows = plan->num_rows;
+  p->scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
+  std::memcpy(p->seq, plan->seq, sizeof(plan->seq));
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool prof = plan->profiling && plan->ev[0];
+  cudaError_t e = prof ? cudaEventRecord(plan->ev[0], s) : cudaSuccess;
+  if (e == cudaSuccess)
+    e = fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, p, s)
+                      : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, p, s);
+  if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[1], s);
+  if (e == cudaSuccess && plan->needs_combine) e = launch_combine(d.head_dim, p, s);
+  if (e == cudaSuccess && prof) {
+    e = cudaEventRecord(plan->ev[2], s);
+    plan->profiled_runs++;
+    plan->last_had_combine = plan->needs_combine;
+  }
+  delete p;
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
+  return PA_OK;
+}
+
+int pa_verify_profile_enable(pa_verify_plan_t plan, int enable) {
+  g_last_error.clear();
+  if (!plan) return fail(PA_ERR_INVALID, "plan must not be NULL");
+  if (enable && !plan->ev[0]) {
+    for (int k = 0; k < 3; ++k) {
+      cudaError_t e = cudaEventCreate(&plan->ev[k]);
+      if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("cudaEventCreate failed: ") + cudaGetErrorString(e));
+    }
+  }
+  plan->profiling = enable ? 1 : 0;
+  return PA_OK;
+}
+
+int pa_verify_profile_read(pa_verify_plan_t plan, float* split_ms, float* combine_ms) {
+  g_last_error.clear();
+  if (!plan || !split_ms || !combine_ms) return fail(PA_ERR_INVALID, "plan, split_ms and combine_ms must not be NULL");
+  if (!plan->ev[0] || plan->profiled_runs == 0) return fail(PA_ERR_INVALID, "no profiled run recorded");
+  cudaError_t e = cudaEventSynchronize(plan->ev[2]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(split_ms, plan->ev[0], plan->ev[1]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(combine_ms, plan->ev[1], plan->ev[2]);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("reading profile events failed: ") + cudaGetErrorString(e));
+  if (!plan->last_had_combine) *combine_ms = 0.f;
+  return PA_OK;
+}
+
+void pa_verify_free(pa_verify_plan_t plan) {
+  if (!plan) return;
+  for (auto& e : plan->ev)
+    if (e) cudaEventDestroy(e);
+  delete plan;
+}
+
+int pa_verify_device_errors(void* workspace, uint32_t* flags_out, int clear, pa_stream_t stream) {
+  g_last_error.clear();
+  if (!workspace || !flags_out) return fail(PA_ERR_INVALID, "workspace and flags_out must not be NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(flags_out, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(workspace, 0, sizeof(uint32_t));
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("reading the device error word failed: ") + cudaGetErrorString(e));
+  return PA_OK;
+}
+
+}  // extern "C"

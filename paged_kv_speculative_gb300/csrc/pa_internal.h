@@ -1,0 +1,73 @@
+// Internal declarations shared by the host planner / C ABI and the kernels.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the encoder is fetched at run time)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pav {
+
+constexpr int kPage = 16;         // tokens per KV page
+constexpr int kMaxSeqs = 64;      // sequences per call (the per-sequence table travels in kernel parameters)
+constexpr int kStages = 3;        // shared-memory ring depth of the split kernel
+constexpr int kMaxChunk = 16384;  // context tokens per work unit (bounds the page-id staging array)
+constexpr int kMaxRows = 128;     // q_len * group rows per (sequence, KV head)
+constexpr int kMaxQueryLen = 8;
+constexpr int kWsHeader = 256;    // workspace bytes before the partials (device error word at offset 0)
+
+// Per-sequence entry of the work description, sorted by decreasing context
+// length so that the longest units are scheduled first.
+struct SeqInfo {
+  int32_t ctx_len;     // L_b
+  int32_t q_len;       // q_b
+  int32_t q_off;       // first row of sequence b in q / out (batch order)
+  int32_t unit_start;  // first work unit of this sequence (units: kv head major, then chunk)
+  int32_t row_start;   // first combine row of this sequence (q_len * Hq rows)
+  int32_t n_chunks;    // ceil(L_b / chunk)
+  int32_t b;           // index of the sequence in the caller's batch
+  int32_t pad;
+};
+
+struct SplitParams {
+  const uint16_t* q;            // [T, Hq, D] bf16
+  const int32_t* block_table;   // [B, stride]
+  const float* k_scale;         // [N_pg, Hkv, 16] or null
+  const float* v_scale;
+  void* out;                    // [T, Hq, D] bf16 | f32
+  float* part_o;                // [U, rows_max, D]
+  float* part_lse;              // [U, rows_max], log2 domain
+  uint32_t* err;                // device error word
+  const int32_t* dev_ctx;       // device copies of the lengths (checked against the plan)
+  const int32_t* dev_q;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t group;
+  int32_t bt_stride;
+  int32_t num_pages;
+  int32_t chunk;
+  int32_t num_units;
+  int32_t rows_max;
+  int32_t out_f32;
+  int32_t num_rows;             // sum_b q_b * Hq (combine grid)
+  float scale_log2;             // softmax_scale * log2(e)
+  SeqInfo seq[kMaxSeqs];
+};
+
+// Tile geometry of the split kernel for a KV element size and head dim.
+__host__ __device__ constexpr int row_bytes(int kv_fp8, int d) { return d * (kv_fp8 ? 1 : 2); }
+__host__ __device__ constexpr int tile_tokens(int kv_fp8, int d) { return 16384 / row_bytes(kv_fp8, d); }
+__host__ __device__ constexpr int stage_bytes(int kv_fp8, int d) {
+  return 2 * 16384 + (kv_fp8 ? 2 * 4 * tile_tokens(kv_fp8, d) : 0);
+}
+__host__ __device__ constexpr int split_smem_bytes(int kv_fp8, int d) {
+  // stages + derived per-token scale terms (fp8) + page ids + barriers/flags + alignment slack
+  return kStages * stage_bytes(kv_fp8, d) + (kv_fp8 ? 16 * tile_tokens(kv_fp8, d) : 0) +
+         4 * (kMaxChunk / kPage) + 64 + 1024;
+}
+// CTAs of the split kernel resident per SM (shared memory bound), used by the planner.
+__host__ __device__ constexpr int split_ctas_per_sm(int warps) { return warps <= 4 ? 2 : 1; }
+
+cudaError_t launch_combine(int head_dim, const SplitParams* p, cudaStream_t stream);
+
+}  // namespace pav

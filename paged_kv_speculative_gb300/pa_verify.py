@@ -1,0 +1,237 @@
+"""Python binding of the C ABI in ``include/pa_verify.h``.
+
+Argument marshalling only: every step of the attention runs in the CUDA
+library ``_lib/libpa_verify.so``. There is no fallback; if the library is
+missing or fails to load, every entry point raises.
+
+Functions keep the C names without the ``pa_verify_`` prefix: ``plan``,
+``run``, ``free``, ``device_errors``, ``last_error``. ``VerifyAttention``
+bundles a plan with its device workspace.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import _build
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+OUT_BF16 = 0
+OUT_F32 = 1
+
+OK = 0
+ERR_INVALID = -1
+ERR_UNSUPPORTED = -2
+ERR_WORKSPACE = -3
+ERR_CUDA = -4
+ERR_NOMEM = -5
+
+DEVERR_PAGE_RANGE = 1
+DEVERR_LENGTHS = 2
+DEVERR_TIMEOUT = 4
+
+# every symbol include/pa_verify.h declares
+EXPORTED = ("pa_verify_plan", "pa_verify_plan_get_info", "pa_verify_run", "pa_verify_free",
+            "pa_verify_device_errors", "pa_verify_last_error", "pa_verify_profile_enable",
+            "pa_verify_profile_read")
+
+
+class PaVerifyError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"pa_verify status {status}: {message}")
+        self.status = status
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_seqs", "num_q_heads", "num_kv_heads", "head_dim", "page_size", "kv_dtype", "out_dtype",
+        "num_pages", "block_table_stride", "split_override", "sm_count")]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("num_units", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
+        ("rows_max", ctypes.c_int32), ("warps", ctypes.c_int32), ("max_splits", ctypes.c_int32),
+        ("needs_combine", ctypes.c_int32), ("num_tokens", ctypes.c_int32), ("kv_bytes", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_lib = None
+
+
+def lib(path: Optional[str] = None):
+    """Loads the library (it must have been built: ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library {p} is not built; run __graft_entry__.build() first")
+    L = ctypes.CDLL(p)
+    vp, sz, i32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int32)
+    L.pa_verify_plan.argtypes = [ctypes.POINTER(Desc), i32p, i32p, ctypes.POINTER(vp), ctypes.POINTER(sz)]
+    L.pa_verify_plan.restype = ctypes.c_int
+    L.pa_verify_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+    L.pa_verify_plan_get_info.restype = ctypes.c_int
+    L.pa_verify_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
+    L.pa_verify_run.restype = ctypes.c_int
+    L.pa_verify_free.argtypes = [vp]
+    L.pa_verify_free.restype = None
+    L.pa_verify_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, vp]
+    L.pa_verify_device_errors.restype = ctypes.c_int
+    L.pa_verify_profile_enable.argtypes = [vp, ctypes.c_int]
+    L.pa_verify_profile_enable.restype = ctypes.c_int
+    L.pa_verify_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
+    L.pa_verify_profile_read.restype = ctypes.c_int
+    L.pa_verify_last_error.argtypes = []
+    L.pa_verify_last_error.restype = ctypes.c_char_p
+    if path is None:
+        _lib = L
+    return L
+
+
+def last_error() -> str:
+    return lib().pa_verify_last_error().decode()
+
+
+def _check(status: int):
+    if status != OK:
+        raise PaVerifyError(status, last_error())
+
+
+class Plan:
+    """A host-side plan (owns the C handle)."""
+
+    def __init__(self, handle: int, desc: Desc, workspace_bytes: int):
+        self.handle = handle
+        self.desc = desc
+        self.workspace_bytes = workspace_bytes
+        info = PlanInfo()
+        _check(lib().pa_verify_plan_get_info(handle, ctypes.byref(info)))
+        self.info = info
+
+    def free(self):
+        if self.handle:
+            lib().pa_verify_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def plan(num_q_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: int, out_dtype: int, num_pages: int,
+         block_table_stride: int, context_lens: Sequence[int], query_lens: Sequence[int],
+         split_override: int = 0, sm_count: int = 0, page_size: int = 16) -> Plan:
+    """pa_verify_plan with host lengths; raises PaVerifyError on refusal."""
+    n = len(context_lens)
+    d = Desc(num_seqs=n, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+             page_size=page_size, kv_dtype=kv_dtype, out_dtype=out_dtype, num_pages=num_pages,
+             block_table_stride=block_table_stride, split_override=split_override, sm_count=sm_count)
+    arr = ctypes.c_int32 * max(1, n)
+    cl = arr(*[int(x) for x in context_lens])
+    ql = arr(*[int(x) for x in query_lens])
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    _check(lib().pa_verify_plan(ctypes.byref(d), cl, ql, ctypes.byref(h), ctypes.byref(ws)))
+    return Plan(h.value, d, ws.value)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def run(p: Plan, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional[torch.Tensor],
+        v_scale: Optional[torch.Tensor], block_table: torch.Tensor, context_lens: torch.Tensor,
+        query_lens: torch.Tensor, softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
+        stream: Optional[torch.cuda.Stream] = None):
+    """pa_verify_run on device tensors (enqueued on ``stream`` or torch's current stream)."""
+    _need(q, "q", torch.bfloat16)
+    for t, nm in ((k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out"), (workspace, "workspace")):
+        _need(t, nm)
+    for t, nm in ((block_table, "block_table"), (context_lens, "context_lens"), (query_lens, "query_lens")):
+        _need(t, nm, torch.int32)
+    for t, nm in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if t is not None:
+            _need(t, nm, torch.float32)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    _check(lib().pa_verify_run(p.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                               _ptr(block_table), _ptr(context_lens), _ptr(query_lens), float(softmax_scale),
+                               _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               s.cuda_stream))
+
+
+def device_errors(workspace: torch.Tensor, clear: bool = False, stream: Optional[torch.cuda.Stream] = None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    flags = ctypes.c_uint32()
+    _check(lib().pa_verify_device_errors(_ptr(workspace), ctypes.byref(flags), int(bool(clear)), s.cuda_stream))
+    return int(flags.value)
+
+
+def profile_enable(p: Plan, enable: bool = True):
+    _check(lib().pa_verify_profile_enable(p.handle, int(bool(enable))))
+
+
+def profile_read(p: Plan):
+    """(split kernel ms, combine kernel ms) of the last profiled run."""
+    a, b = ctypes.c_float(), ctypes.c_float()
+    _check(lib().pa_verify_profile_read(p.handle, ctypes.byref(a), ctypes.byref(b)))
+    return float(a.value), float(b.value)
+
+
+def free(p: Plan):
+    p.free()
+
+
+class VerifyAttention:
+    """A plan plus a zero-initialised device workspace for one batch shape."""
+
+    def __init__(self, num_q_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: int, num_pages: int,
+                 block_table_stride: int, context_lens: Sequence[int], query_lens: Sequence[int],
+                 out_dtype: int = OUT_F32, split_override: int = 0, device: Optional[torch.device] = None):
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        with torch.cuda.device(self.device):
+            self.plan = plan(num_q_heads, num_kv_heads, head_dim, kv_dtype, out_dtype, num_pages, block_table_stride,
+                             context_lens, query_lens, split_override=split_override)
+        self.out_dtype = out_dtype
+        self.num_q_heads = num_q_heads
+        self.head_dim = head_dim
+        self.workspace = torch.zeros(max(256, self.plan.workspace_bytes), dtype=torch.uint8, device=self.device)
+
+    @property
+    def info(self) -> dict:
+        return self.plan.info.as_dict()
+
+    def new_out(self) -> torch.Tensor:
+        T = self.plan.info.num_tokens
+        dt = torch.float32 if self.out_dtype == OUT_F32 else torch.bfloat16
+        return torch.empty((T, self.num_q_heads, self.head_dim), dtype=dt, device=self.device)
+
+    def __call__(self, q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens, query_lens,
+                 softmax_scale: float, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = self.new_out()
+        run(self.plan, q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens, query_lens,
+            softmax_scale, out, self.workspace, stream)
+        return out
+
+    def device_errors(self, clear: bool = False) -> int:
+        return device_errors(self.workspace, clear=clear)

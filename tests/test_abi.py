@@ -1,0 +1,149 @@
+"""The C ABI on the CPU: the library loads, exports what the header declares,
+plans and refuses without a GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_kv_speculative_gb300 import _build, pa_verify as pv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built():
+    _build.build()
+
+
+def header_symbols():
+    txt = open(os.path.join(ROOT, "include", "pa_verify.h")).read()
+    return sorted(set(re.findall(r"\b(pa_verify_\w+)\s*\(", txt)))
+
+
+def test_header_symbols_exported():
+    syms = header_symbols()
+    assert set(syms) == set(pv.EXPORTED)
+    lib = ctypes.CDLL(_build.LIB)
+    for s in syms:
+        assert hasattr(lib, s), s
+
+
+def mk(ctx, ql, hq=8, hkv=1, d=128, kv=pv.KV_BF16, sms=152, stride=None, pages=None, **kw):
+    stride = stride or max(1, max((c + 15) // 16 for c in ctx) if ctx else 1)
+    pages = pages or max(1, sum((c + 15) // 16 for c in ctx))
+    return pv.plan(hq, hkv, d, kv, pv.OUT_F32, pages, stride, ctx, ql, sm_count=sms, **kw)
+
+
+def test_rows_follow_the_pages_shape_facts():
+    with open(os.path.join(ROOT, "tests", "golden", "shape_facts.txt")) as f:
+        facts = [tuple(int(x) for x in ln.split("#")[0].split()) for ln in f if ln.split("#")[0].strip()]
+    assert facts
+    for qlen, group, rows in facts:
+        p = mk([4096], [qlen], hq=group, hkv=1)
+        assert p.info.rows_max == rows
+        assert p.info.warps == (rows + 15) // 16
+
+
+@pytest.mark.parametrize("ctx,ql,hkv", [([37, 100], [1, 6], 1), ([4096 + 7 * i for i in range(8)], [6] * 8, 4),
+                                         ([1 << 20], [6], 1), ([5, 9000, 131072, 64], [3, 8, 1, 2], 2)])
+def test_units_cover_every_token_once(ctx, ql, hkv):
+    p = mk(ctx, ql, hq=8 * hkv, hkv=hkv)
+    i = p.info
+    assert i.chunk_tokens % i.tile_tokens == 0
+    assert i.num_units == hkv * sum((c + i.chunk_tokens - 1) // i.chunk_tokens for c in ctx)
+    assert i.max_splits == max((c + i.chunk_tokens - 1) // i.chunk_tokens for c in ctx)
+    assert i.needs_combine == (i.max_splits > 1)
+    assert i.kv_bytes == sum(ctx) * hkv * 128 * 4
+
+
+def test_one_wave_when_possible():
+    ctx = [4096 + 997 * i for i in range(8)]
+    p = mk(ctx, [6] * 8, hq=32, hkv=4)
+    assert p.info.num_units <= 152 * 2
+
+
+def test_batch_one_gets_the_split_ceiling():
+    p1 = mk([1 << 20], [6])
+    assert p1.info.max_splits >= 152  # one sequence spreads over every SM
+    p2 = mk([1 << 20] * 4, [6] * 4)
+    assert p1.info.max_splits > p2.info.max_splits
+
+
+def test_split_count_monotone_in_context():
+    prev = 0
+    for L in (64, 1000, 10000, 100000, 1 << 20):
+        s = mk([L], [6]).info.max_splits
+        assert s >= prev
+        prev = s
+
+
+def test_split_override():
+    assert mk([10000], [6], split_override=1).info.max_splits == 1
+    assert mk([10000], [6], split_override=4).info.max_splits == 4
+    p = mk([10000], [6], split_override=100000)
+    assert p.info.chunk_tokens == p.info.tile_tokens
+
+
+def test_empty_batch_plans():
+    p = mk([], [])
+    assert p.info.num_units == 0 and p.workspace_bytes >= 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(ctx=[10], ql=[0]), pv.ERR_INVALID),
+    (dict(ctx=[10], ql=[9]), pv.ERR_INVALID),
+    (dict(ctx=[3], ql=[6]), pv.ERR_INVALID),
+    (dict(ctx=[10], ql=[1], d=96), pv.ERR_UNSUPPORTED),
+    (dict(ctx=[10], ql=[1], d=64, kv=pv.KV_FP8_E4M3), pv.ERR_UNSUPPORTED),
+    (dict(ctx=[100], ql=[8], hq=32, hkv=1), pv.ERR_UNSUPPORTED),
+    (dict(ctx=[100], ql=[2], hq=6, hkv=4), pv.ERR_INVALID),
+    (dict(ctx=[100], ql=[2], stride=3), pv.ERR_INVALID),
+    (dict(ctx=[10] * 65, ql=[1] * 65), pv.ERR_UNSUPPORTED),
+])
+def test_plan_refusals(kw, status):
+    with pytest.raises(pv.PaVerifyError) as e:
+        mk(**kw)
+    assert e.value.status == status
+    assert pv.last_error()
+
+
+def test_page_size_must_be_16():
+    with pytest.raises(pv.PaVerifyError) as e:
+        pv.plan(8, 1, 128, pv.KV_BF16, pv.OUT_F32, 10, 10, [100], [6], sm_count=152, page_size=32)
+    assert e.value.status == pv.ERR_UNSUPPORTED
+
+
+def test_run_refusals_launch_nothing():
+    """Argument checks of pa_verify_run happen before any CUDA call."""
+    L = pv.lib()
+    p = mk([100], [6])
+    fake = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: each call below is refused first
+    args = [p.handle] + [fake] * 8 + [ctypes.c_float(0.125), fake, fake, ctypes.c_size_t(p.workspace_bytes), None]
+    a = list(args); a[1] = None
+    assert L.pa_verify_run(*a) == pv.ERR_INVALID
+    a = list(args); a[9] = ctypes.c_float(float("nan"))
+    assert L.pa_verify_run(*a) == pv.ERR_INVALID
+    a = list(args); a[9] = ctypes.c_float(-1.0)
+    assert L.pa_verify_run(*a) == pv.ERR_INVALID
+    a = list(args); a[12] = ctypes.c_size_t(p.workspace_bytes - 1)
+    assert L.pa_verify_run(*a) == pv.ERR_WORKSPACE
+    a = list(args); a[11] = ctypes.c_void_p((1 << 20) + 16)
+    assert L.pa_verify_run(*a) == pv.ERR_INVALID  # workspace not 256-byte aligned
+    a = list(args); a[2] = ctypes.c_void_p((1 << 20) + 8)
+    assert L.pa_verify_run(*a) == pv.ERR_INVALID  # k_cache not 16-byte aligned
+    assert L.pa_verify_run(None, *args[1:]) == pv.ERR_INVALID
+
+
+def test_fp8_run_needs_scales():
+    L = pv.lib()
+    p = mk([100], [6], kv=pv.KV_FP8_E4M3)
+    fake = ctypes.c_void_p(1 << 20)
+    a = [p.handle, fake, fake, fake, None, None, fake, fake, fake, ctypes.c_float(0.1), fake, fake,
+         ctypes.c_size_t(p.workspace_bytes), None]
+    assert L.pa_verify_run(*a) == pv.ERR_INVALID
+
+
+def test_free_accepts_null():
+    pv.lib().pa_verify_free(None)

@@ -1,0 +1,158 @@
+"""CUDA path against the fp64 oracle, element by element, through the C ABI.
+
+Tolerances (max |GPU - oracle| on fp32 output): 1e-2 for bf16 KV and 2e-2 for
+FP8 KV, the bar the verify-attention workloads set. bf16 output adds its own
+rounding (2^-9 relative), so those comparisons allow 1e-2 on top.
+Full-size workloads are checked on sampled rows the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_speculative_gb300 import pa_verify as pv, synth
+from paged_kv_speculative_gb300.device_inputs import to_device
+from tests import oracle_pins
+
+pytestmark = pytest.mark.gpu
+
+TOL = {synth.KV_BF16: 1e-2, synth.KV_FP8: 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_speculative_gb300 import _build
+    _build.build()
+    yield
+
+
+def gpu_run(prob, out_dtype=pv.OUT_F32, split_override=0, dev=None, check_errors=True):
+    dev = dev or to_device(prob)
+    va = pv.VerifyAttention(prob.num_q_heads, prob.num_kv_heads, prob.head_dim, prob.kv_dtype, prob.num_pages,
+                            prob.block_table.shape[1], prob.context_lens.tolist(), prob.query_lens.tolist(),
+                            out_dtype=out_dtype, split_override=split_override)
+    out = va(*dev.args(), prob.softmax_scale)
+    torch.cuda.synchronize()
+    if check_errors:
+        assert va.device_errors() == 0
+    return out.float().cpu().numpy(), va
+
+
+def max_err(a, b):
+    d = np.abs(a.astype(np.float64) - b)
+    assert np.isfinite(d).all(), "non-finite output"
+    return float(d.max())
+
+
+SMALL = [
+    ("tiny", lambda: synth.make_config("tiny")),
+    ("gqa2_ragged", lambda: synth.make_problem([33, 70, 16, 1], [3, 8, 1, 1], 4, 2, 64, seed=11)),
+    ("d128_multi_tile", lambda: synth.make_problem([1000, 333, 2049], [6, 3, 8], 16, 2, 128, seed=31)),
+    ("d64_multi_tile", lambda: synth.make_problem([700, 129, 1500], [6, 1, 4], 8, 1, 64, seed=32)),
+    ("q_equals_ctx", lambda: synth.make_problem([6, 1, 8, 64], [6, 1, 8, 5], 8, 2, 128, seed=33)),
+    ("rows128", lambda: synth.make_problem([500, 77], [8, 5], 16, 1, 128, seed=34)),
+    ("fp8_small", lambda: synth.make_problem([45, 29, 300], [6, 2, 8], 8, 1, 128, kv_dtype=synth.KV_FP8, seed=12)),
+    ("fp8_multi_tile", lambda: synth.make_problem([1500, 257, 4099], [6, 1, 7], 16, 2, 128,
+                                                  kv_dtype=synth.KV_FP8, seed=35)),
+]
+
+
+@pytest.mark.parametrize("name,make", SMALL, ids=[s[0] for s in SMALL])
+@pytest.mark.parametrize("split", [0, 1, 3])
+def test_small_against_oracle(name, make, split):
+    prob = make()
+    ref = oracle.verify_attention(prob)
+    got, _ = gpu_run(prob, split_override=split)
+    assert max_err(got, ref) <= TOL[prob.kv_dtype], name
+
+
+@pytest.mark.parametrize("name,make", SMALL[:3] + SMALL[6:7], ids=[s[0] for s in SMALL[:3] + SMALL[6:7]])
+def test_bf16_output(name, make):
+    prob = make()
+    ref = oracle.verify_attention(prob)
+    got, _ = gpu_run(prob, out_dtype=pv.OUT_BF16)
+    assert max_err(got, ref) <= TOL[prob.kv_dtype] + 1e-2
+
+
+def test_split_count_does_not_change_the_result():
+    prob = synth.make_problem([3000, 1200], [6, 6], 16, 2, 128, seed=41)
+    outs = [gpu_run(prob, split_override=k)[0] for k in (1, 2, 5, 1000)]
+    for o in outs[1:]:
+        # P is rounded to bf16 against a split-dependent running max: 2^-8 relative per weight
+        assert max_err(o, outs[0]) <= 2e-3
+
+
+def test_repeat_runs_are_bit_identical():
+    prob = synth.make_problem([3000, 1200], [6, 6], 16, 2, 128, seed=42)
+    dev = to_device(prob)
+    a, va = gpu_run(prob, dev=dev)
+    b = va(*dev.args(), prob.softmax_scale).cpu().numpy()
+    assert np.array_equal(a, b)
+
+
+def test_page_relabelling_is_bit_identical():
+    prob = synth.make_problem([900, 400], [6, 3], 8, 1, 128, seed=43)
+    a, _ = gpu_run(prob)
+    b, _ = gpu_run(oracle_pins.permute_pool(prob, seed=5))
+    assert np.array_equal(a, b)
+
+
+def test_draft_row_matches_prefix_decode_on_gpu():
+    prob = synth.make_problem([777], [6], 8, 1, 128, seed=44)
+    full, _ = gpu_run(prob)
+    for i in range(6):
+        one = synth.Problem(**{**prob.__dict__, "q": prob.q[i:i + 1].copy(),
+                               "context_lens": np.array([777 - 6 + i + 1], dtype=np.int32),
+                               "query_lens": np.array([1], dtype=np.int32)})
+        row, _ = gpu_run(one)
+        assert max_err(full[i], row[0].astype(np.float64)) <= 2e-3
+
+
+def test_empty_batch_is_a_no_op():
+    va = pv.VerifyAttention(8, 1, 128, pv.KV_BF16, 4, 4, [], [], out_dtype=pv.OUT_F32)
+    z = torch.zeros(16, device="cuda")
+    t = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q = torch.zeros(1, 8, 128, dtype=torch.bfloat16, device="cuda")
+    pv.run(va.plan, q, z, z, None, None, t, t, t, 0.1, z, va.workspace)
+    torch.cuda.synchronize()
+
+
+def test_out_of_range_page_is_flagged_not_faulted():
+    prob = synth.make_problem([200], [6], 8, 1, 128, seed=45)
+    prob.block_table[0, 3] = prob.num_pages + 1000  # not a pool page
+    _, va = gpu_run(prob, check_errors=False)
+    assert va.device_errors(clear=True) & pv.DEVERR_PAGE_RANGE
+    assert va.device_errors() == 0
+
+
+def test_device_length_mismatch_is_flagged():
+    prob = synth.make_problem([200, 100], [6, 6], 8, 1, 128, seed=46)
+    dev = to_device(prob)
+    va = pv.VerifyAttention(8, 1, 128, pv.KV_BF16, prob.num_pages, prob.block_table.shape[1], [200, 100], [6, 6])
+    dev.context_lens[1] = 99  # differs from the planned 100 (still a valid length)
+    va(*dev.args(), prob.softmax_scale)
+    torch.cuda.synchronize()
+    assert va.device_errors() & pv.DEVERR_LENGTHS
+
+
+# --------------------------------------------------------------- full-size workloads
+def sample_rows(prob, n, seed):
+    rng = np.random.default_rng(seed)
+    T, H = prob.num_tokens, prob.num_q_heads
+    rows = {(int(t), int(h)) for t, h in zip(rng.integers(0, T, n), rng.integers(0, H, n))}
+    off = prob.q_offsets()
+    for b in range(prob.num_seqs):  # every sequence's first and last draft
+        rows.add((int(off[b]), 0))
+        rows.add((int(off[b + 1] - 1), H - 1))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["mtp5_bf16", "mtp5_fp8", "mixed_fp8", "ctx1mi_bf16"])
+def test_full_workload_sampled_rows(name):
+    prob = synth.make_config(name)
+    got, va = gpu_run(prob)
+    assert np.isfinite(got).all()
+    rows = sample_rows(prob, 48 if name != "mixed_fp8" else 200, seed=7)
+    ref = oracle.verify_attention(prob, rows=rows)
+    sel = got[rows[:, 0], rows[:, 1]]
+    assert max_err(sel, ref) <= TOL[prob.kv_dtype], name
