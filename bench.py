@@ -225,7 +225,7 @@ def main():
 
     import torch
     import torch.distributed as dist
-    from paged_kv_speculative_gb300 import _build, pa_verify as pv
+    from paged_kv_speculative_gb300 import _build, pa_verify as pv, replicas
     from paged_kv_speculative_gb300.device_inputs import host_tensors
 
     world, rank, local = dist_setup()
@@ -288,12 +288,10 @@ def main():
     prob, info = r["prob"], r["info"]
     total_ms = float(sum(r["step_ms"]))
     mean_ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = replicas.max_over_ranks(total_ms, device=dev)
     kv_bytes_rank = int(info["kv_bytes"])
-    value = kv_bytes_rank * world * args.steps / (total_ms * 1e-3) / 1e9
+    kv_bytes_all = replicas.sum_over_ranks(kv_bytes_rank, device=dev)
+    value = replicas.job_throughput(kv_bytes_all, args.steps, total_ms)
     split_avg = float(np.mean(r["split_ms"]))
     comb_avg = float(np.mean(r["comb_ms"]))
 
@@ -318,7 +316,7 @@ def main():
         torch.cuda.synchronize(dev)
         if k >= 2:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_val = kv_bytes_rank * world / (float(np.mean(e2e_ms)) * 1e-3) / 1e9
+    e2e_val = replicas.job_throughput(kv_bytes_all, 1, replicas.max_over_ranks(float(np.mean(e2e_ms)), device=dev))
 
     others = {}
     for name in [x for x in args.also.split(",") if x]:

@@ -160,6 +160,35 @@ void pa_verify_free(pa_verify_plan_t plan);
  */
 int pa_verify_device_errors(void* workspace, uint32_t* flags_out, int clear, pa_stream_t stream);
 
+/*
+ * Paged KV write (the step before verify attention): stores the K/V rows of
+ * num_tokens new tokens into their cache slots, in place.
+ *   k_new, v_new  [num_tokens, Hkv, D] bf16 (device), 4-byte aligned
+ *   slot_mapping  [num_tokens] int64 (device): slot = page * 16 + offset in the
+ *                 pool; -1 marks a padded or dead row, which writes nothing
+ *                 (in-place stores masked by row liveness: "[DeepSeek-V4.1]
+ *                 High-interactivity monokernel decode", description)
+ *   k_cache, v_cache  [N_pg, Hkv, 16, D] bf16 (copied as is) or E4M3
+ *   k_scale, v_scale  [N_pg, Hkv, 16] fp32, FP8 only (NULL for bf16)
+ *   error_flags   optional device uint32: PA_DEVERR_PAGE_RANGE is or-ed in
+ *                 when a slot lies outside the pool (that token is skipped)
+ * FP8 quantisation per (token, head): s = amax / 448 (1 when amax = 0),
+ * code = E4M3(x / s) with IEEE fp32 divisions, round to nearest even and
+ * saturation at +-448 (OCP E4M3). head_dim 64, 128 or 256. Slots of one
+ * call must be distinct. Asynchronous on `stream`; allocates nothing.
+ */
+typedef struct {
+  int32_t num_tokens;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t kv_dtype;  /* PA_KV_* */
+  int32_t num_pages;
+} pa_kv_write_desc;
+
+int pa_kv_write(const pa_kv_write_desc* desc, const void* k_new, const void* v_new,
+                const int64_t* slot_mapping, void* k_cache, void* v_cache, float* k_scale,
+                float* v_scale, uint32_t* error_flags, pa_stream_t stream);
+
 /* Message for the last failing call on this thread ("" when none). */
 const char* pa_verify_last_error(void);
 

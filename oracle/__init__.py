@@ -78,6 +78,11 @@ def _load(mutant: int = 0):
     lib.oracle_decode_e4m3.restype = ctypes.c_double
     lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
     lib.oracle_decode_bf16.restype = ctypes.c_double
+    lib.oracle_encode_e4m3.argtypes = [ctypes.c_float]
+    lib.oracle_encode_e4m3.restype = ctypes.c_uint8
+    vp = ctypes.c_void_p
+    lib.oracle_kv_write.argtypes = [ctypes.c_int32] * 5 + [vp] * 7
+    lib.oracle_kv_write.restype = ctypes.c_int
     _libs[mutant] = lib
     return lib
 
@@ -90,6 +95,29 @@ def decode_e4m3(codes) -> np.ndarray:
 def decode_bf16(bits) -> np.ndarray:
     lib = _load()
     return np.array([lib.oracle_decode_bf16(int(c)) for c in np.asarray(bits).ravel()], dtype=np.float64)
+
+
+def encode_e4m3(values) -> np.ndarray:
+    lib = _load()
+    return np.array([lib.oracle_encode_e4m3(float(v)) for v in np.asarray(values, dtype=np.float32).ravel()],
+                    dtype=np.uint8)
+
+
+def kv_write(k_new: np.ndarray, v_new: np.ndarray, slot_mapping: np.ndarray, k_cache: np.ndarray,
+             v_cache: np.ndarray, k_scale: Optional[np.ndarray], v_scale: Optional[np.ndarray],
+             kv_dtype: int) -> int:
+    """Paged KV write (in place on the given host arrays). k_new/v_new: uint16
+    bf16 bits [n, Hkv, D]; slot_mapping int64 [n] (-1 skips the token).
+    Returns the oracle's status (0, or -1 if a slot was out of range)."""
+    lib = _load()
+    n, hkv, d = k_new.shape
+    for a in (k_new, v_new, k_cache, v_cache):
+        assert a.flags.c_contiguous
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    return lib.oracle_kv_write(n, hkv, d, kv_dtype, k_cache.shape[0], k_new.ctypes.data, v_new.ctypes.data,
+                               sm.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
+                               None if k_scale is None else k_scale.ctypes.data,
+                               None if v_scale is None else v_scale.ctypes.data)
 
 
 def _ptr(a: Optional[np.ndarray]) -> Optional[int]:

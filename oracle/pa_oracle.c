@@ -245,3 +245,90 @@ int oracle_verify_attention(const oracle_problem* p, const int64_t* rows, int64_
   pthread_mutex_destroy(&job.lock);
   return job.status;
 }
+
+/* ---------------------------------------------------------------------------
+ * Paged KV write with per-token FP8 quantisation (the step that fills the
+ * cache the verify step reads): the new tokens' K/V rows are stored into
+ * their slots (slot = page * 16 + offset, from a slot mapping), and a slot of
+ * -1 (a padded or dead row) stores nothing ("every store masked by its row's
+ * liveness": DeepSeek-V4.1 page, description of the in-place KV writes).
+ * FP8: per (token, head), s = amax / 448 (s = 1 when amax = 0) and
+ * code = E4M3(x / s), round to nearest even, saturating at +-448. The
+ * division and the scale are single-precision IEEE operations: the codes are
+ * integers decided by floating point, and the CUDA kernel takes the same
+ * decision in the same precision.
+ * ------------------------------------------------------------------------- */
+
+/* fp32 -> OCP E4M3, round to nearest (ties to even), saturating to +-448;
+ * NaN -> 0x7F. Written from the format: values are (-1)^s 2^(e-7) (1 + m/8)
+ * for e = 1..15 (except S.1111.111), subnormals 2^-6 (m/8). */
+uint8_t oracle_encode_e4m3(float x) {
+  if (x != x) return 0x7F;
+  uint8_t sign = (x < 0.0f || (x == 0.0f && 1.0f / x < 0.0f)) ? 0x80 : 0x00;
+  double a = fabs((double)x);
+  if (a >= 448.0) return sign | 0x7E;
+  /* scale to units of the smallest subnormal step 2^-9 within the binade */
+  int e;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: value = m * 2^-9, m = 0..7 (8 rounds up to the min normal) */
+    double m = a / ldexp(1.0, -9);
+    double fl = floor(m);
+    double frac = m - fl;
+    int mi = (int)fl;
+    if (frac > 0.5 || (frac == 0.5 && (mi & 1))) mi += 1;
+    if (mi >= 8) return sign | 0x08; /* rounds to 2^-6 */
+    return sign | (uint8_t)mi;
+  }
+  frexp(a, &e); /* a = f * 2^e, f in [0.5, 1) -> a in [2^(e-1), 2^e) */
+  int ue = e - 1; /* unbiased exponent: a in [2^ue, 2^(ue+1)) */
+  double m = (a / ldexp(1.0, ue) - 1.0) * 8.0; /* mantissa in [0, 8) */
+  double fl = floor(m);
+  double frac = m - fl;
+  int mi = (int)fl;
+  if (frac > 0.5 || (frac == 0.5 && (mi & 1))) mi += 1;
+  if (mi == 8) { mi = 0; ue += 1; }
+  int be = ue + 7;
+  if (be > 15 || (be == 15 && mi == 7)) return sign | 0x7E; /* above 448 saturates */
+  return sign | (uint8_t)((be << 3) | mi);
+}
+
+/* Writes n_tokens new rows. k_new/v_new: [n][Hkv][D] bf16 bits; slot: [n]
+ * (-1 = skip); caches/scales as in the attention problem. kv_dtype 0 stores
+ * the bf16 bits unchanged. Returns 0, or -1 when a slot is out of range (that
+ * token is skipped, the others are written). */
+int oracle_kv_write(int32_t n_tokens, int32_t num_kv_heads, int32_t head_dim, int32_t kv_dtype,
+                    int32_t num_pages, const uint16_t* k_new, const uint16_t* v_new, const int64_t* slot,
+                    void* k_cache, void* v_cache, float* k_scale, float* v_scale) {
+  int status = 0;
+  for (int32_t t = 0; t < n_tokens; ++t) {
+    const int64_t sl = slot[t];
+    if (sl < 0) continue;
+    if (sl >= (int64_t)num_pages * ORACLE_PAGE) { status = -1; continue; }
+    const int64_t page = sl / ORACLE_PAGE, off = sl % ORACLE_PAGE;
+    for (int g = 0; g < num_kv_heads; ++g) {
+      const size_t src = ((size_t)t * num_kv_heads + g) * head_dim;
+      const size_t dst = (((size_t)page * num_kv_heads + g) * ORACLE_PAGE + off) * head_dim;
+      const size_t sdst = ((size_t)page * num_kv_heads + g) * ORACLE_PAGE + off;
+      for (int which = 0; which < 2; ++which) {
+        const uint16_t* x = (which ? v_new : k_new) + src;
+        void* cache = which ? v_cache : k_cache;
+        if (kv_dtype == 0) {
+          memcpy((uint16_t*)cache + dst, x, sizeof(uint16_t) * (size_t)head_dim);
+          continue;
+        }
+        float amax = 0.0f;
+        for (int d = 0; d < head_dim; ++d) {
+          float v = (float)oracle_decode_bf16(x[d]);
+          if (fabsf(v) > amax) amax = fabsf(v);
+        }
+        volatile float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+        for (int d = 0; d < head_dim; ++d) {
+          volatile float y = (float)oracle_decode_bf16(x[d]) / s;
+          ((uint8_t*)cache)[dst + d] = oracle_encode_e4m3(y);
+        }
+        (which ? v_scale : k_scale)[sdst] = s;
+      }
+    }
+  }
+  return status;
+}

@@ -26,6 +26,9 @@ cudaError_t launch_split_bf16(int head_dim, int warps, int units, const CUtensor
                               const SplitParams* p, cudaStream_t stream);
 cudaError_t launch_split_fp8(int head_dim, int warps, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
                              const SplitParams* p, cudaStream_t stream);
+cudaError_t launch_kv_write(int head_dim, int fp8, int n_tokens, int num_kv_heads, int num_pages, const void* k_new,
+                            const void* v_new, const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                            float* k_scale, float* v_scale, uint32_t* err, cudaStream_t stream);
 }  // namespace pav
 
 using namespace pav;
@@ -356,6 +359,33 @@ int pa_verify_profile_read(pa_verify_plan_t plan, float* split_ms, float* combin
   if (e == cudaSuccess) e = cudaEventElapsedTime(combine_ms, plan->ev[1], plan->ev[2]);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("reading profile events failed: ") + cudaGetErrorString(e));
   if (!plan->last_had_combine) *combine_ms = 0.f;
+  return PA_OK;
+}
+
+int pa_kv_write(const pa_kv_write_desc* desc, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                void* k_cache, void* v_cache, float* k_scale, float* v_scale, uint32_t* error_flags,
+                pa_stream_t stream) {
+  g_last_error.clear();
+  if (!desc) return fail(PA_ERR_INVALID, "desc must not be NULL");
+  const pa_kv_write_desc& d = *desc;
+  if (d.num_tokens < 0 || d.num_kv_heads < 1 || d.num_pages < 0)
+    return fail(PA_ERR_INVALID, "need num_tokens >= 0, num_kv_heads >= 1, num_pages >= 0");
+  if (d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_FP8_E4M3) return fail(PA_ERR_INVALID, "unknown kv_dtype");
+  if (d.head_dim != 64 && d.head_dim != 128 && d.head_dim != 256)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+  if (static_cast<int64_t>(d.num_tokens) * d.num_kv_heads * 32 >= (int64_t(1) << 31))
+    return fail(PA_ERR_UNSUPPORTED, "too many tokens for one call");
+  if (d.num_tokens == 0) return PA_OK;
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return fail(PA_ERR_INVALID, "a required pointer is NULL");
+  if (fp8 && (!k_scale || !v_scale)) return fail(PA_ERR_INVALID, "FP8 KV needs k_scale and v_scale");
+  if (!aligned(k_new, 4) || !aligned(v_new, 4) || !aligned(k_cache, 4) || !aligned(v_cache, 4) ||
+      !aligned(slot_mapping, 8))
+    return fail(PA_ERR_INVALID, "k_new/v_new/caches must be 4-byte and slot_mapping 8-byte aligned");
+  cudaError_t e = launch_kv_write(d.head_dim, fp8 ? 1 : 0, d.num_tokens, d.num_kv_heads, d.num_pages, k_new, v_new,
+                                  slot_mapping, k_cache, v_cache, fp8 ? k_scale : nullptr, fp8 ? v_scale : nullptr,
+                                  error_flags, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("kv write launch failed: ") + cudaGetErrorString(e));
   return PA_OK;
 }
 

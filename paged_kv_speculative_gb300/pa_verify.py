@@ -37,7 +37,7 @@ DEVERR_TIMEOUT = 4
 # every symbol include/pa_verify.h declares
 EXPORTED = ("pa_verify_plan", "pa_verify_plan_get_info", "pa_verify_run", "pa_verify_free",
             "pa_verify_device_errors", "pa_verify_last_error", "pa_verify_profile_enable",
-            "pa_verify_profile_read")
+            "pa_verify_profile_read", "pa_kv_write")
 
 
 class PaVerifyError(RuntimeError):
@@ -50,6 +50,10 @@ class Desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_seqs", "num_q_heads", "num_kv_heads", "head_dim", "page_size", "kv_dtype", "out_dtype",
         "num_pages", "block_table_stride", "split_override", "sm_count")]
+
+
+class KvWriteDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_tokens", "num_kv_heads", "head_dim", "kv_dtype", "num_pages")]
 
 
 class PlanInfo(ctypes.Structure):
@@ -90,6 +94,8 @@ def lib(path: Optional[str] = None):
     L.pa_verify_profile_enable.restype = ctypes.c_int
     L.pa_verify_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
     L.pa_verify_profile_read.restype = ctypes.c_int
+    L.pa_kv_write.argtypes = [ctypes.POINTER(KvWriteDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.pa_kv_write.restype = ctypes.c_int
     L.pa_verify_last_error.argtypes = []
     L.pa_verify_last_error.restype = ctypes.c_char_p
     if path is None:
@@ -199,6 +205,22 @@ def profile_read(p: Plan):
 
 def free(p: Plan):
     p.free()
+
+
+def kv_write(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+             v_cache: torch.Tensor, k_scale: Optional[torch.Tensor], v_scale: Optional[torch.Tensor],
+             kv_dtype: int, error_flags: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """pa_kv_write: stores new tokens' K/V rows [n, Hkv, D] into their slots."""
+    _need(k_new, "k_new", torch.bfloat16)
+    _need(v_new, "v_new", torch.bfloat16)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache")
+    n, hkv, d = k_new.shape
+    desc = KvWriteDesc(num_tokens=n, num_kv_heads=hkv, head_dim=d, kv_dtype=kv_dtype, num_pages=k_cache.shape[0])
+    s = stream if stream is not None else torch.cuda.current_stream(k_new.device)
+    _check(lib().pa_kv_write(ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache),
+                             _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(error_flags), s.cuda_stream))
 
 
 class VerifyAttention:
