@@ -189,6 +189,31 @@ int pa_kv_write(const pa_kv_write_desc* desc, const void* k_new, const void* v_n
                 const int64_t* slot_mapping, void* k_cache, void* v_cache, float* k_scale,
                 float* v_scale, uint32_t* error_flags, pa_stream_t stream);
 
+/*
+ * Greedy verify verdict (the step after verify attention): from the target
+ * model's logits at the verify positions, the number of accepted drafts per
+ * sequence and the next token ("ids + verdict" kept on the device:
+ * "[DeepSeek-V4.1] High-interactivity monokernel decode", in-graph head).
+ *   logits      [T, vocab] bf16 (device), rows packed by sequence like q
+ *   input_ids   [T] int32 (device): per sequence the token fed at each verify
+ *               position: the last committed token, then the q_b - 1 drafts
+ *   query_lens  [num_seqs] int32 (device), 1 .. 32, summing to T
+ *   target_ids  [T] int32 out: first index of each row's maximum (a NaN
+ *               counts as the maximum; -0 equals +0)
+ *   accepted    [num_seqs] int32 out: the longest prefix of drafts equal to
+ *               the target's picks, 0 .. q_b - 1
+ *   next_token  [num_seqs] int32 out: the target's pick after the accepted prefix
+ *   workspace   >= pa_greedy_verdict_workspace_bytes(T, vocab), 256-byte
+ *               aligned; its first word is a device error word (PA_DEVERR_LENGTHS
+ *               when query_lens are out of range; pa_verify_device_errors reads it)
+ * Asynchronous on `stream`; allocates nothing.
+ */
+size_t pa_greedy_verdict_workspace_bytes(int32_t num_tokens, int32_t vocab);
+int pa_greedy_verdict(int32_t num_seqs, int32_t num_tokens, int32_t vocab, const void* logits,
+                      const int32_t* input_ids, const int32_t* query_lens, int32_t* target_ids,
+                      int32_t* accepted, int32_t* next_token, void* workspace, size_t workspace_bytes,
+                      pa_stream_t stream);
+
 /* Message for the last failing call on this thread ("" when none). */
 const char* pa_verify_last_error(void);
 

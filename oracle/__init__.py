@@ -83,6 +83,8 @@ def _load(mutant: int = 0):
     vp = ctypes.c_void_p
     lib.oracle_kv_write.argtypes = [ctypes.c_int32] * 5 + [vp] * 7
     lib.oracle_kv_write.restype = ctypes.c_int
+    lib.oracle_greedy_verdict.argtypes = [ctypes.c_int32, vp, ctypes.c_int32, vp, vp, vp, vp, vp]
+    lib.oracle_greedy_verdict.restype = ctypes.c_int
     _libs[mutant] = lib
     return lib
 
@@ -118,6 +120,25 @@ def kv_write(k_new: np.ndarray, v_new: np.ndarray, slot_mapping: np.ndarray, k_c
                                sm.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
                                None if k_scale is None else k_scale.ctypes.data,
                                None if v_scale is None else v_scale.ctypes.data)
+
+
+def greedy_verdict(query_lens: np.ndarray, logits_bf16: np.ndarray, input_ids: np.ndarray):
+    """(target_ids [T], accepted [B], next_token [B]) of a greedy verify step.
+    logits_bf16: uint16 [T, V]; input_ids: int32 [T] (per sequence: last
+    committed token, then the drafts)."""
+    lib = _load()
+    ql = np.ascontiguousarray(query_lens, dtype=np.int32)
+    lg = np.ascontiguousarray(logits_bf16, dtype=np.uint16)
+    ids = np.ascontiguousarray(input_ids, dtype=np.int32)
+    T, V = lg.shape
+    tgt = np.empty(T, dtype=np.int32)
+    acc = np.empty(ql.shape[0], dtype=np.int32)
+    nxt = np.empty(ql.shape[0], dtype=np.int32)
+    rc = lib.oracle_greedy_verdict(ql.shape[0], ql.ctypes.data, V, lg.ctypes.data, ids.ctypes.data,
+                                   tgt.ctypes.data, acc.ctypes.data, nxt.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"oracle_greedy_verdict failed with status {rc}")
+    return tgt, acc, nxt
 
 
 def _ptr(a: Optional[np.ndarray]) -> Optional[int]:

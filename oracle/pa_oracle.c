@@ -332,3 +332,42 @@ int oracle_kv_write(int32_t n_tokens, int32_t num_kv_heads, int32_t head_dim, in
   }
   return status;
 }
+
+/* ---------------------------------------------------------------------------
+ * Greedy verify verdict (the step after verify attention: the target model's
+ * picks at the q_b verify positions decide how many drafts are accepted; the
+ * DeepSeek-V4.1 page keeps "ids + verdict" on the device, in the graph).
+ * Position i of sequence b was fed token x_i (x_0 the last committed token,
+ * x_1 .. x_{q-1} the drafts). The target's pick t_i is the first index of
+ * the maximum of logits[i] (a NaN counts as the maximum). The accepted count
+ * a is the largest k <= q - 1 with x_{j+1} == t_j for every j < k; the next
+ * token is t_a.
+ * ------------------------------------------------------------------------- */
+int oracle_greedy_verdict(int32_t num_seqs, const int32_t* query_lens, int32_t vocab,
+                          const uint16_t* logits, /* [T][vocab] bf16 bits */
+                          const int32_t* input_ids, /* [T] */
+                          int32_t* target_ids, /* [T] out */
+                          int32_t* accepted, int32_t* next_token /* [B] out */) {
+  int64_t row = 0;
+  for (int b = 0; b < num_seqs; ++b) {
+    const int q = query_lens[b];
+    if (q < 1) return -1;
+    for (int i = 0; i < q; ++i) {
+      const uint16_t* lr = logits + (size_t)(row + i) * vocab;
+      int best = 0;
+      double bv = oracle_decode_bf16(lr[0]);
+      for (int v = 1; v < vocab; ++v) {
+        if (bv != bv) break; /* a NaN is already the maximum */
+        double x = oracle_decode_bf16(lr[v]);
+        if (x != x || x > bv) { bv = x; best = v; }
+      }
+      target_ids[row + i] = best;
+    }
+    int a = 0;
+    while (a < q - 1 && input_ids[row + a + 1] == target_ids[row + a]) ++a;
+    accepted[b] = a;
+    next_token[b] = target_ids[row + a];
+    row += q;
+  }
+  return 0;
+}

@@ -29,6 +29,10 @@ cudaError_t launch_split_fp8(int head_dim, int warps, int units, const CUtensorM
 cudaError_t launch_kv_write(int head_dim, int fp8, int n_tokens, int num_kv_heads, int num_pages, const void* k_new,
                             const void* v_new, const int64_t* slot_mapping, void* k_cache, void* v_cache,
                             float* k_scale, float* v_scale, uint32_t* err, cudaStream_t stream);
+size_t verdict_workspace_bytes(int num_tokens, int vocab);
+cudaError_t launch_verdict(int num_seqs, int num_tokens, int vocab, const void* logits, const int32_t* input_ids,
+                           const int32_t* query_lens, int32_t* target_ids, int32_t* accepted, int32_t* next_token,
+                           void* workspace, cudaStream_t stream);
 }  // namespace pav
 
 using namespace pav;
@@ -386,6 +390,32 @@ int pa_kv_write(const pa_kv_write_desc* desc, const void* k_new, const void* v_n
                                   slot_mapping, k_cache, v_cache, fp8 ? k_scale : nullptr, fp8 ? v_scale : nullptr,
                                   error_flags, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("kv write launch failed: ") + cudaGetErrorString(e));
+  return PA_OK;
+}
+
+size_t pa_greedy_verdict_workspace_bytes(int32_t num_tokens, int32_t vocab) {
+  if (num_tokens < 0 || vocab < 1) return 0;
+  return verdict_workspace_bytes(num_tokens, vocab);
+}
+
+int pa_greedy_verdict(int32_t num_seqs, int32_t num_tokens, int32_t vocab, const void* logits,
+                      const int32_t* input_ids, const int32_t* query_lens, int32_t* target_ids, int32_t* accepted,
+                      int32_t* next_token, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  g_last_error.clear();
+  if (num_seqs < 0 || num_tokens < 0 || vocab < 1) return fail(PA_ERR_INVALID, "need num_seqs >= 0, num_tokens >= 0, vocab >= 1");
+  if (num_tokens < num_seqs || (num_seqs == 0) != (num_tokens == 0))
+    return fail(PA_ERR_INVALID, "every sequence needs at least one verify position");
+  if (static_cast<int64_t>(num_tokens) * ((vocab + 8191) / 8192) >= (int64_t(1) << 31))
+    return fail(PA_ERR_UNSUPPORTED, "logits too large for one call");
+  if (num_seqs == 0) return PA_OK;
+  if (!logits || !input_ids || !query_lens || !target_ids || !accepted || !next_token || !workspace)
+    return fail(PA_ERR_INVALID, "a required pointer is NULL");
+  if (!aligned(logits, 2) || !aligned(workspace, 256)) return fail(PA_ERR_INVALID, "logits must be 2-byte and workspace 256-byte aligned");
+  if (workspace_bytes < verdict_workspace_bytes(num_tokens, vocab))
+    return fail(PA_ERR_WORKSPACE, "workspace smaller than pa_greedy_verdict_workspace_bytes");
+  cudaError_t e = launch_verdict(num_seqs, num_tokens, vocab, logits, input_ids, query_lens, target_ids, accepted,
+                                 next_token, workspace, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("verdict launch failed: ") + cudaGetErrorString(e));
   return PA_OK;
 }
 

@@ -37,7 +37,8 @@ DEVERR_TIMEOUT = 4
 # every symbol include/pa_verify.h declares
 EXPORTED = ("pa_verify_plan", "pa_verify_plan_get_info", "pa_verify_run", "pa_verify_free",
             "pa_verify_device_errors", "pa_verify_last_error", "pa_verify_profile_enable",
-            "pa_verify_profile_read", "pa_kv_write")
+            "pa_verify_profile_read", "pa_kv_write", "pa_greedy_verdict_workspace_bytes",
+            "pa_greedy_verdict")
 
 
 class PaVerifyError(RuntimeError):
@@ -96,6 +97,10 @@ def lib(path: Optional[str] = None):
     L.pa_verify_profile_read.restype = ctypes.c_int
     L.pa_kv_write.argtypes = [ctypes.POINTER(KvWriteDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.pa_kv_write.restype = ctypes.c_int
+    L.pa_greedy_verdict_workspace_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    L.pa_greedy_verdict_workspace_bytes.restype = ctypes.c_size_t
+    L.pa_greedy_verdict.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32] + [vp] * 7 + [sz, vp]
+    L.pa_greedy_verdict.restype = ctypes.c_int
     L.pa_verify_last_error.argtypes = []
     L.pa_verify_last_error.restype = ctypes.c_char_p
     if path is None:
@@ -257,3 +262,24 @@ class VerifyAttention:
 
     def device_errors(self, clear: bool = False) -> int:
         return device_errors(self.workspace, clear=clear)
+
+
+def greedy_verdict(logits: torch.Tensor, input_ids: torch.Tensor, query_lens: torch.Tensor,
+                   workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """pa_greedy_verdict: (target_ids [T], accepted [B], next_token [B]) int32 device tensors."""
+    _need(logits, "logits", torch.bfloat16)
+    _need(input_ids, "input_ids", torch.int32)
+    _need(query_lens, "query_lens", torch.int32)
+    T, V = logits.shape
+    B = query_lens.shape[0]
+    dev = logits.device
+    need = lib().pa_greedy_verdict_workspace_bytes(T, V)
+    if workspace is None:
+        workspace = torch.zeros(max(256, need), dtype=torch.uint8, device=dev)
+    tgt = torch.empty(T, dtype=torch.int32, device=dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    _check(lib().pa_greedy_verdict(B, T, V, _ptr(logits), _ptr(input_ids), _ptr(query_lens), _ptr(tgt), _ptr(acc),
+                                   _ptr(nxt), _ptr(workspace), workspace.numel(), s.cuda_stream))
+    return tgt, acc, nxt

@@ -19,7 +19,7 @@ def built():
 
 def header_symbols():
     txt = open(os.path.join(ROOT, "include", "pa_verify.h")).read()
-    return sorted(set(re.findall(r"^(?:int|void|const char\*)\s+(pa_\w+)\s*\(", txt, flags=re.M)))
+    return sorted(set(re.findall(r"^(?:int|void|size_t|const char\*)\s+(pa_\w+)\s*\(", txt, flags=re.M)))
 
 
 def test_header_symbols_exported():
