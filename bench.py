@@ -205,6 +205,78 @@ def run_reference(args):
     return 0
 
 
+def _timed(fn, steps, warmup, flush, dev):
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return ms
+
+
+def run_side_op(args):
+    """Measures the paged KV write (FP8 quantising) or the greedy verdict."""
+    import torch
+    from paged_kv_speculative_gb300 import _build, pa_verify as pv
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build.build()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    peaks, _ = load_peaks()
+    peak, peak_note = hbm_peak(peaks)
+    if args.op == "kv_write":
+        # bulk write: 8192 new tokens x 8 KV heads x head_dim 128, bf16 in -> E4M3 + fp32 scales
+        n, hkv, d, n_pg = 8192, 8, 128, 8192 // 16 + 64
+        k_new = torch.randn((n, hkv, d), generator=g).to(torch.bfloat16).to(dev)
+        v_new = torch.randn((n, hkv, d), generator=g).to(torch.bfloat16).to(dev)
+        slots = torch.randperm(n_pg * 16, generator=g)[:n].to(torch.int64).to(dev)
+        kc = torch.zeros((n_pg, hkv, 16, d), dtype=torch.uint8, device=dev)
+        vc = torch.zeros_like(kc)
+        ks = torch.zeros((n_pg, hkv, 16), dtype=torch.float32, device=dev)
+        vs = torch.zeros_like(ks)
+        fn = lambda: pv.kv_write(k_new, v_new, slots, kc, vc, ks, vs, pv.KV_FP8_E4M3)
+        nbytes = 2 * n * hkv * d * 2 + n * 8 + 2 * n * hkv * (d + 4)
+        workload = "paged KV write, FP8 per-token quantisation: 8192 tokens x 8 KV heads x D=128, random slots"
+        metric, launches = "paged KV write GB/s (bf16 in, E4M3 + fp32 scales out)", 1
+    else:
+        # greedy verdict over the MTP-5 verify positions of 8 sequences, vocab 151936
+        B, q, V = 8, 6, 151936
+        T = B * q
+        logits = (torch.randn((T, V), generator=g) * 3).to(torch.bfloat16).to(dev)
+        ids = torch.randint(0, V, (T,), generator=g, dtype=torch.int32).to(dev)
+        ql = torch.full((B,), q, dtype=torch.int32, device=dev)
+        ws = torch.zeros(pv.lib().pa_greedy_verdict_workspace_bytes(T, V), dtype=torch.uint8, device=dev)
+        fn = lambda: pv.greedy_verdict(logits, ids, ql, workspace=ws)
+        nbytes = T * V * 2
+        workload = "greedy verify verdict: 8 sequences x 6 verify positions, vocab 151936, bf16 logits"
+        metric, launches = "greedy verdict GB/s (logits read once)", 2
+    ms = _timed(fn, args.steps, args.warmup, flush, dev)
+    mean = float(np.mean(ms))
+    gbs = nbytes / (mean * 1e-3) / 1e9
+    line = {"op": args.op, "metric": metric, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean, "us_per_call": 1e3 * mean, "higher_is_better": True,
+            "dtype": "bf16 in", "data": "synthetic",
+            "config": {"workload": workload, "bytes_per_call": nbytes,
+                       "l2": "flushed between steps (256 MiB write, outside the events)"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "peak_source": peak_note},
+            "gpu_launches": args.steps * launches}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -217,11 +289,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--also", default="", help="comma-separated extra workloads to report under 'other_configs'")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "tc"],
+                    help="split kernel: automatic choice, warp-MMA, or tcgen05")
+    ap.add_argument("--op", default="verify", choices=["verify", "kv_write", "verdict"],
+                    help="verify attention (the path), or the paged KV write / greedy verdict steps around it")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.op != "verify":
+        return run_side_op(args)
 
     import torch
     import torch.distributed as dist
@@ -249,8 +327,9 @@ def main():
                                   name=name, **kw)
         host = host_tensors(prob, pin=True)
         dv = [None if x is None else x.to(dev) for x in host.args()]
+        kern = {"auto": pv.KERNEL_AUTO, "mma": pv.KERNEL_WARP_MMA, "tc": pv.KERNEL_TCGEN05}[args.kernel]
         va = pv.VerifyAttention(hq, hkv, d, kvd, prob.num_pages, prob.block_table.shape[1], ctx, ql,
-                                out_dtype=pv.OUT_BF16, device=dev)
+                                out_dtype=pv.OUT_BF16, device=dev, kernel=kern)
         out = va.new_out()
         stream = torch.cuda.current_stream(dev)
         for _ in range(warmup):
@@ -327,6 +406,7 @@ def main():
                         "split_kernel_us": 1e3 * osplit,
                         "split_kernel_gbs": o["info"]["kv_bytes"] / (osplit * 1e-3) / 1e9,
                         "units": o["info"]["num_units"], "chunk": o["info"]["chunk_tokens"],
+                        "kernel": "tcgen05" if o["info"]["kernel"] == pv.KERNEL_TCGEN05 else "warp-mma",
                         "device_errors": o["errs"]}
 
     if rank != 0:
@@ -349,10 +429,12 @@ def main():
         "config": {"workload": WORKLOAD_DESC[args.config], "name": args.config,
                    "kv_bytes_per_call": kv_bytes_rank, "l2": "flushed between steps (256 MiB write, outside the events)",
                    "units": info["num_units"], "chunk_tokens": info["chunk_tokens"], "splits_max": info["max_splits"],
+                   "kernel": "tcgen05" if info["kernel"] == pv.KERNEL_TCGEN05 else "warp-mma",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_note, "traffic": traffic_for(args.config),
-                     "kernel": "pa_split_kernel", "split_kernel_us": 1e3 * split_avg, "combine_kernel_us": 1e3 * comb_avg},
+                     "kernel": "pa_tc_split_kernel" if info["kernel"] == pv.KERNEL_TCGEN05 else "pa_split_kernel",
+                     "split_kernel_us": 1e3 * split_avg, "combine_kernel_us": 1e3 * comb_avg},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": float(np.mean(e2e_ms))},
         "gpu_launches": args.steps * (1 + int(info["needs_combine"])),

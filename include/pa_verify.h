@@ -83,7 +83,11 @@ typedef struct {
   int32_t split_override;     /* 0: the planner chooses; k > 0: chunk length
                                  ceil(max_b L_b / k) rounded up to the staging tile */
   int32_t sm_count;           /* 0: query the current device; > 0: plan for that many SMs */
+  int32_t kernel;             /* PA_KERNEL_*: 0 picks the tensor-core (tcgen05) kernel where it
+                                 applies (head_dim 128, q_b * G <= 64), else the warp-MMA kernel */
 } pa_verify_desc;
+
+enum { PA_KERNEL_AUTO = 0, PA_KERNEL_WARP_MMA = 1, PA_KERNEL_TCGEN05 = 2 };
 
 typedef struct {
   int32_t num_units;       /* CTAs of the split kernel: sum_b Hkv * ceil(L_b / chunk) */
@@ -96,6 +100,7 @@ typedef struct {
   int32_t num_tokens;      /* T = sum_b q_b */
   int64_t kv_bytes;        /* algorithmic K/V(+scale) bytes one run reads */
   size_t workspace_bytes;  /* bytes pa_verify_run needs in `workspace` */
+  int32_t kernel;          /* PA_KERNEL_WARP_MMA or PA_KERNEL_TCGEN05 */
 } pa_verify_plan_info;
 
 /*

@@ -26,6 +26,8 @@ cudaError_t launch_split_bf16(int head_dim, int warps, int units, const CUtensor
                               const SplitParams* p, cudaStream_t stream);
 cudaError_t launch_split_fp8(int head_dim, int warps, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
                              const SplitParams* p, cudaStream_t stream);
+cudaError_t launch_tc_split(int kv_fp8, int rows_max, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                            const SplitParams* p, cudaStream_t stream);
 cudaError_t launch_kv_write(int head_dim, int fp8, int n_tokens, int num_kv_heads, int num_pages, const void* k_new,
                             const void* v_new, const int64_t* slot_mapping, void* k_cache, void* v_cache,
                             float* k_scale, float* v_scale, uint32_t* err, cudaStream_t stream);
@@ -41,6 +43,7 @@ struct pa_verify_plan_s {
   pa_verify_desc d;
   int32_t tile = 0, chunk = 0, units = 0, rows_max = 0, warps = 0, max_splits = 0, needs_combine = 0;
   int32_t num_tokens = 0, num_rows = 0;
+  int32_t kernel = PA_KERNEL_WARP_MMA;
   int64_t kv_bytes = 0;
   size_t ws_bytes = 0;
   SeqInfo seq[kMaxSeqs];
@@ -132,6 +135,7 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
   if (static_cast<int64_t>(d.num_pages) * d.num_kv_heads * kPage >= (int64_t(1) << 31))
     return fail(PA_ERR_UNSUPPORTED, "num_pages * num_kv_heads * 16 must stay below 2^31");
   if (d.split_override < 0 || d.sm_count < 0) return fail(PA_ERR_INVALID, "split_override and sm_count must be >= 0");
+  if (d.kernel < PA_KERNEL_AUTO || d.kernel > PA_KERNEL_TCGEN05) return fail(PA_ERR_INVALID, "unknown kernel");
 
   const int G = d.num_q_heads / d.num_kv_heads;
   int rows_max = 0, max_len = 0;
@@ -167,9 +171,15 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
     *workspace_bytes_out = P->ws_bytes;
     return PA_OK;
   }
-  const int tile = tile_tokens(fp8 ? 1 : 0, d.head_dim);
+  const bool tc_ok = d.head_dim == 128 && rows_max <= 64;
+  if (d.kernel == PA_KERNEL_TCGEN05 && !tc_ok) {
+    delete P;
+    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs head_dim 128 and q_len * group <= 64");
+  }
+  const bool use_tc = d.kernel == PA_KERNEL_TCGEN05 || (d.kernel == PA_KERNEL_AUTO && tc_ok);
+  const int tile = use_tc ? 128 : tile_tokens(fp8 ? 1 : 0, d.head_dim);
   const int warps = supported_warps(rows_max);
-  const int64_t slots = static_cast<int64_t>(sms) * split_ctas_per_sm(warps);
+  const int64_t slots = static_cast<int64_t>(sms) * (use_tc ? 1 : split_ctas_per_sm(warps));
   auto units_for = [&](int64_t c) {
     int64_t u = 0;
     for (int b = 0; b < d.num_seqs; ++b) u += (context_lens_host[b] + c - 1) / c;
@@ -221,6 +231,7 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
     delete P;
     return fail(PA_ERR_UNSUPPORTED, "work too large for one call");
   }
+  P->kernel = use_tc ? PA_KERNEL_TCGEN05 : PA_KERNEL_WARP_MMA;
   P->tile = tile;
   P->chunk = static_cast<int32_t>(chunk);
   P->units = static_cast<int32_t>(unit);
@@ -255,6 +266,7 @@ int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info) {
   info->num_tokens = plan->num_tokens;
   info->kv_bytes = plan->kv_bytes;
   info->workspace_bytes = plan->ws_bytes;
+  info->kernel = plan->kernel;
   return PA_OK;
 }
 
@@ -327,8 +339,10 @@ int pa_verify_run(pa_verify_plan_t plan, const void* q, const void* k_cache, con
   const bool prof = plan->profiling && plan->ev[0];
   cudaError_t e = prof ? cudaEventRecord(plan->ev[0], s) : cudaSuccess;
   if (e == cudaSuccess)
-    e = fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, p, s)
-                      : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, p, s);
+    e = plan->kernel == PA_KERNEL_TCGEN05
+            ? launch_tc_split(fp8 ? 1 : 0, plan->rows_max, plan->units, &plan->tmk, &plan->tmv, p, s)
+        : fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, p, s)
+              : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, p, s);
   if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[1], s);
   if (e == cudaSuccess && plan->needs_combine) e = launch_combine(d.head_dim, p, s);
   if (e == cudaSuccess && prof) {

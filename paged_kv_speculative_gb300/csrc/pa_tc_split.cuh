@@ -1,0 +1,563 @@
+// Split-KV paged verify attention on 5th-generation tensor cores (tcgen05).
+//
+// One CTA per work unit (sequence b, KV head g, context chunk [t0, t1)). The
+// unit's q_b * G query rows ("rows = query length x GQA group", MTP-5 routing
+// page, Motivation) are the N dimension of the MMAs, padded to NP; the 128
+// tokens of a K/V tile are the M dimension, so every K/V byte reaches the
+// tensor core straight from the TMA-staged shared memory, once:
+//   S^T[tok, r]  = K[tok, :] . Q[r, :]           (A = K tile, K-major; B = Q, K-major)
+//   O^T[d, r]   += V[:, d]^T . P^T[:, r]          (A = V tile, MN-major; B = P, MN-major)
+// with both accumulators in tensor memory.
+//
+// Warp roles (192 threads): warp 0 gathers pages through the block table with
+// 2-D TMA boxes (lane 0 feeds a KS-deep K ring, lane 1 a VS-deep V ring that
+// also carries the FP8 scales); warp 1 allocates tensor memory and issues the
+// MMAs (one thread); warps 2-5 are the softmax warpgroup, one thread per
+// token of the tile. Stages hand over on mbarriers; every wait is bounded.
+//
+// Softmax. Row r keeps a reference maximum M_r, uniform across the CTA. A
+// tile whose scores stay below M_r + 8 (log2 units) uses M_r as is, so P <= 2^8
+// and no cross-thread row maximum is needed. Otherwise (the first tile, or a
+// score that rose by more than 2^8) the warpgroup takes the exact tile row
+// maxima, raises M_r and rescales l_r and the O accumulator. The final O / l is
+// the same softmax whatever reference was used.
+//
+// FP8 E4M3 K/V stay 8-bit all the way (kind::f8f6f4). Q and P are each split
+// into two E4M3 terms, x = hi + lo, and both terms go through the tensor core
+// into the same accumulator: Q row r is scaled by a power of two 2^e_r first,
+// and P (<= 2^8) has its mantissa cut to 3 bits for hi. The per-token scales
+// are constant along the head dimension, so s_k multiplies score column t and
+// log2 s_v enters the exponent, with l accumulating P / s_v.
+#pragma once
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_tc.cuh"
+
+namespace pav {
+
+template <int KV_FP8, int NP>
+struct TcCfg {
+  static constexpr int kD = 128;
+  static constexpr int kTile = 128;                          // tokens per K/V tile = MMA M
+  static constexpr int kRowB = KV_FP8 ? 128 : 256;           // bytes per token row
+  static constexpr int kTileB = kTile * kRowB;               // 16 KB (fp8) / 32 KB (bf16)
+  static constexpr int KS = KV_FP8 ? 4 : 3;                  // K ring depth
+  static constexpr int VS = KV_FP8 ? 3 : 2;                  // V ring depth
+  static constexpr int kVStage = kTileB + (KV_FP8 ? 2 * 4 * kTile : 0);  // V data + k/v scales
+  static constexpr int kQPlane = 64 * 128;                   // one 128-byte-wide plane of 64 rows
+  static constexpr int kQB = 2 * kQPlane;                    // bf16: two 64-column halves; fp8: hi and lo
+  static constexpr int kPPlane = KV_FP8 ? kTile * 64 : kTile * 128;  // bytes of one P plane
+  static constexpr int kPBuf = KV_FP8 ? 2 * kPPlane : kPPlane;       // fp8: hi and lo planes
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + KS * kTileB;
+  static constexpr int kOffQ = kOffV + ((VS * kVStage + 1023) / 1024) * 1024;
+  static constexpr int kOffP = kOffQ + kQB;
+  static constexpr int kOffPid = kOffP + 2 * kPBuf;
+  static constexpr int kOffRow = kOffPid + 4 * (kMaxChunk / kPage);  // per-row constants
+  static constexpr int kOffRed = kOffRow + 4 * 64 * 4;               // tile maxima of the 4 softmax warps
+  static constexpr int kOffBar = kOffRed + 4 * 64 * 4;
+  static constexpr int kSmem = kOffBar + 256 + 1024;                 // barriers, tmem base, alignment slack
+  static_assert(NP % 16 == 0 && NP >= 16 && NP <= 64, "N must be 16..64 in steps of 16");
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kTile * NP * 4 <= KS * kTileB, "epilogue l-sum scratch fits the K ring");
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+// OR of `pred` over the `nthreads` threads of named barrier `id`.
+__device__ __forceinline__ bool named_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %3, 0;\n barrier.red.or.pred po, %1, %2, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"(id), "r"(nthreads), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
+// Two fp32 -> E4M3 bytes, round to nearest even, saturating (lo -> low byte).
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int KV_FP8, int NP>
+__global__ void __launch_bounds__(192, 1)
+    pa_tc_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                       const __grid_constant__ SplitParams p) {
+  using C = TcCfg<KV_FP8, NP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = sm + C::kOffK;
+  uint8_t* sV = sm + C::kOffV;
+  uint8_t* sQ = sm + C::kOffQ;
+  uint8_t* sP = sm + C::kOffP;
+  int32_t* pids = reinterpret_cast<int32_t*>(sm + C::kOffPid);
+  float* rowM = reinterpret_cast<float*>(sm + C::kOffRow);      // reference maxima (log2 units)
+  float* rowC = rowM + 64;                                       // score multiplier per row
+  int* rowLim = reinterpret_cast<int*>(rowC + 64);               // last visible key per row (-1: padding)
+  float* red = reinterpret_cast<float*>(sm + C::kOffRed);        // [4 warps][64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  uint64_t* kfull = bars;
+  uint64_t* kempty = kfull + C::KS;
+  uint64_t* vfull = kempty + C::KS;
+  uint64_t* vempty = vfull + C::VS;
+  uint64_t* sfull = vempty + C::VS;
+  uint64_t* sfree = sfull + 2;
+  uint64_t* pfull = sfree + 2;
+  uint64_t* pfree = pfull + 2;
+  uint64_t* qready = pfree + 2;
+  uint32_t* tbase_slot = reinterpret_cast<uint32_t*>(qready + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tbase_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ------------------------------------------------------------ the unit
+  const int u = blockIdx.x;
+  int lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.seq[mid].unit_start <= u) lo = mid; else hi = mid - 1;
+  }
+  const SeqInfo& si = p.seq[lo];
+  const int local = u - si.unit_start;
+  const int kvh = local / si.n_chunks;
+  const int chunk_idx = local - kvh * si.n_chunks;
+  const int L = si.ctx_len, QL = si.q_len, b = si.b, G = p.group;
+  const int rows = QL * G;
+  const int t0 = chunk_idx * p.chunk;
+  const int t_end = min(L, t0 + p.chunk);
+  const int n_tiles = (t_end - t0 + C::kTile - 1) / C::kTile;
+  const int n_pages = (t_end - t0 + kPage - 1) / kPage;
+  const bool split = si.n_chunks > 1;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::KS; ++s) { mbar_init(smem_addr(&kfull[s]), 1); mbar_init(smem_addr(&kempty[s]), 1); }
+    for (int s = 0; s < C::VS; ++s) { mbar_init(smem_addr(&vfull[s]), 1); mbar_init(smem_addr(&vempty[s]), 1); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&sfull[s]), 1);
+      mbar_init(smem_addr(&sfree[s]), 4);
+      mbar_init(smem_addr(&pfull[s]), 4);
+      mbar_init(smem_addr(&pfree[s]), 1);
+    }
+    mbar_init(smem_addr(qready), 4);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    if (chunk_idx == 0 && kvh == 0 && (p.dev_ctx[b] != L || p.dev_q[b] != QL)) atomicOr(p.err, 2u);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tbase_slot, 256);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0) {
+    const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.bt_stride + t0 / kPage;
+    for (int i = lane; i < n_pages; i += 32) {
+      int pg = __ldg(bt + i);
+      if (static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages)) {
+        atomicOr(p.err, 1u);
+        pg = -1;
+      }
+      pids[i] = pg;
+    }
+  }
+  if (tid >= 64 && tid < 128) {  // per-row constants for the softmax warpgroup
+    const int r = tid - 64;
+    rowM[r] = -INFINITY;
+    rowC[r] = p.scale_log2;
+    rowLim[r] = r < rows ? L - QL + r / G : -1;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tbase_slot;
+  const uint32_t tS[2] = {tmem, tmem + 64};
+  const uint32_t tO = tmem + 128;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicOr(p.err, 4u);
+  };
+
+  if (warp == 0) {
+    // ============================================================ producer
+    if (lane < 2) {
+      const bool is_k = lane == 0;
+      const int depth = is_k ? C::KS : C::VS;
+      const CUtensorMap* map = is_k ? &tmk : &tmv;
+      uint64_t* full = is_k ? kfull : vfull;
+      uint64_t* empty = is_k ? kempty : vempty;
+      int issued = 0;
+      for (int k = 0; k < n_tiles && !*abort_flag; ++k) {
+        const int s = k % depth;
+        if (k >= depth && !mbar_wait_bounded(smem_addr(&empty[s]), static_cast<uint32_t>(k / depth - 1) & 1u)) {
+          fail();
+          break;
+        }
+        ++issued;
+        uint8_t* dst = is_k ? sK + s * C::kTileB : sV + s * C::kVStage;
+        const int tok0 = t0 + k * C::kTile;
+        const int npg = (min(t_end, tok0 + C::kTile) - tok0 + kPage - 1) / kPage;
+        uint32_t bytes = npg * (kPage * C::kRowB);
+        if (KV_FP8 && !is_k)
+          for (int j = 0; j < npg; ++j)
+            if (pids[(tok0 - t0) / kPage + j] >= 0) bytes += 2 * kPage * 4;
+        const uint32_t bar = smem_addr(&full[s]);
+        mbar_arrive_expect_tx(bar, bytes);
+        for (int j = 0; j < npg; ++j) {
+          const int pg = pids[(tok0 - t0) / kPage + j];
+          const int row = (pg >= 0 ? pg : p.num_pages) * p.num_kv_heads * kPage + kvh * kPage;
+#pragma unroll
+          for (int hf = 0; hf < C::kRowB / 128; ++hf)
+            tma_load_2d(smem_addr(dst + hf * (C::kTile * 128) + j * kPage * 128), map, bar,
+                        hf * (KV_FP8 ? 128 : 64), row);
+          if (KV_FP8 && !is_k && pg >= 0) {
+            const size_t so = (static_cast<size_t>(pg) * p.num_kv_heads + kvh) * kPage;
+            bulk_load(smem_addr(dst + C::kTileB + j * kPage * 4), p.k_scale + so, kPage * 4, bar);
+            bulk_load(smem_addr(dst + C::kTileB + C::kTile * 4 + j * kPage * 4), p.v_scale + so, kPage * 4, bar);
+          }
+        }
+      }
+      // No copy may land after the CTA exits: wait (bounded) for the last
+      // copies of each ring slot; only this lane arms these barriers, so the
+      // parity of tile k's phase is exact.
+      for (int k = max(0, issued - depth); k < issued; ++k)
+        (void)mbar_wait_bounded(smem_addr(&full[k % depth]), static_cast<uint32_t>(k / depth) & 1u);
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t fa = KV_FP8 ? tc::kE4M3 : tc::kBF16;
+      constexpr uint32_t idS = tc::idesc(fa, fa, tc::kKMajor, tc::kKMajor, 128, NP);
+      constexpr uint32_t idPV = tc::idesc(fa, fa, tc::kMNMajor, tc::kMNMajor, 128, NP);
+      const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aP = smem_addr(sP);
+      bool ok = mbar_wait_bounded(smem_addr(qready), 0);
+      auto issue_pv = [&](int j) -> bool {
+        const int vs = j % C::VS, pb = j & 1;
+        if (!mbar_wait_bounded(smem_addr(&vfull[vs]), static_cast<uint32_t>(j / C::VS) & 1u)) return false;
+        if (!mbar_wait_bounded(smem_addr(&pfull[pb]), static_cast<uint32_t>(j >> 1) & 1u)) return false;
+        tc::fence_after_sync();
+        const uint32_t v0 = aV + vs * C::kVStage;
+        const uint32_t p0 = aP + pb * C::kPBuf;
+        if (KV_FP8) {
+          // 4 k-steps of 32 tokens; hi then lo plane of P into the same accumulator
+#pragma unroll
+          for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc::mma_f8(tO, tc::sdesc(v0 + ks * 4096, 16384, 1024, tc::kSwizzle128B),
+                         tc::sdesc(p0 + pl * C::kPPlane + ks * 2048, 16384, 512, tc::kSwizzle64B), idPV,
+                         (j > 0 || pl > 0 || ks > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_f16(tO, tc::sdesc(v0 + ks * 2048, C::kTile * 128, 1024, tc::kSwizzle128B),
+                        tc::sdesc(p0 + ks * 2048, 16384, 1024, tc::kSwizzle128B), idPV, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc::commit(&vempty[vs]);
+        tc::commit(&pfree[pb]);  // also tells the softmax warpgroup that O holds tiles 0..j
+        return true;
+      };
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int ks_ = i % C::KS, sb = i & 1;
+        if (!mbar_wait_bounded(smem_addr(&kfull[ks_]), static_cast<uint32_t>(i / C::KS) & 1u)) { ok = false; break; }
+        if (i >= 2 && !mbar_wait_bounded(smem_addr(&sfree[sb]), static_cast<uint32_t>((i >> 1) - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t k0 = aK + ks_ * C::kTileB;
+        if (KV_FP8) {
+#pragma unroll
+          for (int pl = 0; pl < 2; ++pl)  // Q hi then Q lo
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc::mma_f8(tS[sb], tc::sdesc(k0 + ks * 32, 16, 1024, tc::kSwizzle128B),
+                         tc::sdesc(aQ + pl * C::kQPlane + ks * 32, 16, 1024, tc::kSwizzle128B), idS,
+                         (pl > 0 || ks > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_f16(tS[sb], tc::sdesc(k0 + (ks >> 2) * (C::kTile * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
+                        tc::sdesc(aQ + (ks >> 2) * C::kQPlane + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B), idS,
+                        ks > 0 ? 1u : 0u);
+        }
+        tc::commit(&sfull[sb]);
+        tc::commit(&kempty[ks_]);
+        if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
+      }
+      if (ok && n_tiles > 0) ok = issue_pv(n_tiles - 1);
+      if (!ok) fail();
+    }
+  } else {
+    // ============================================================ softmax warpgroup
+    const int wt = tid - 64;           // 0..127
+    const int q4 = warp & 3;           // tensor-memory lane quarter of this warp
+    const int tok = q4 * 32 + lane;    // token of the tile this thread owns (= TMEM lane)
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+
+    // ---- Q staging: rows r < NP, K-major, 128B swizzle (fp8: hi / lo planes)
+    for (int r = wt >> 5; r < NP; r += 4) {
+      // warp-per-row: lane owns 4 consecutive head-dim entries
+      const uint16_t* qp = nullptr;
+      if (r < rows) {
+        const int i = r / G;
+        qp = p.q + (static_cast<size_t>(si.q_off + i) * p.num_q_heads + kvh * G + (r - i * G)) * C::kD;
+      }
+      uint2 w = qp ? *reinterpret_cast<const uint2*>(qp + 4 * lane) : make_uint2(0, 0);
+      if (!KV_FP8) {
+        // 4 bf16 = 8 bytes at byte 8*lane of the 256-byte row: half lane/16, chunk (lane%16)/2
+        const int hf = lane >> 4, ch = (lane & 15) >> 1;
+        uint8_t* dst = sQ + hf * C::kQPlane + r * 128 + ((ch ^ (r & 7)) << 4) + (lane & 1) * 8;
+        *reinterpret_cast<uint2*>(dst) = w;
+      } else {
+        float x[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
+        float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        int ex = 0;
+        if (mx > 0.f) {
+          int e2;
+          frexpf(mx, &e2);  // mx in [2^(e2-1), 2^e2)
+          ex = 8 - e2;      // scaled row max in [128, 256)
+        }
+        uint32_t hw = 0, lw = 0;
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          const float a = ldexpf(x[e], ex), c = ldexpf(x[e + 1], ex);
+          const float ah = __uint_as_float(__float_as_uint(a) & 0xFFF00000u);  // 3 mantissa bits
+          const float ch2 = __uint_as_float(__float_as_uint(c) & 0xFFF00000u);
+          hw |= e4m3x2(ah, ch2) << (8 * e);
+          lw |= e4m3x2(a - ah, c - ch2) << (8 * e);
+        }
+        // 4 bytes at byte 4*lane of the 128-byte row: chunk lane/4
+        const uint32_t off = r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4;
+        *reinterpret_cast<uint32_t*>(sQ + off) = hw;
+        *reinterpret_cast<uint32_t*>(sQ + C::kQPlane + off) = lw;
+        if (lane == 0) rowC[r] = ldexpf(p.scale_log2, -ex);
+      }
+    }
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(qready);
+    named_sync(1, 128);  // rowC written
+
+    float l[NP];
+#pragma unroll
+    for (int c = 0; c < NP; ++c) l[c] = 0.f;
+    const int lim_first = L - QL;  // last key every real row sees
+
+    // A failed wait marks this thread and skips its later waits, but every
+    // named barrier below is still reached in order: no thread of the
+    // warpgroup can be left behind at one.
+    bool ok_sm = true;
+    auto wait = [&](uint64_t* bar, uint32_t par) {
+      if (ok_sm && !mbar_wait_bounded(smem_addr(bar), par)) {
+        ok_sm = false;
+        fail();
+      }
+    };
+    for (int i = 0; i < n_tiles; ++i) {
+      const int sb = i & 1;
+      wait(&sfull[sb], static_cast<uint32_t>(i >> 1) & 1u);
+      tc::fence_after_sync();
+      float y[NP];
+#pragma unroll
+      for (int c0 = 0; c0 < NP; c0 += 16) {
+        uint32_t r16[16];
+        tc::ld16(tS[sb] + lane_off + c0, r16);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) y[c0 + j] = __uint_as_float(r16[j]);
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfree[sb]);
+
+      const int tabs = t0 + i * C::kTile + tok;
+      float inv_sv = 1.f;
+      // every tile's V phase is observed in order (a skipped phase would make a later parity wait ambiguous)
+      const int vs = i % C::VS;
+      wait(&vfull[vs], static_cast<uint32_t>(i / C::VS) & 1u);
+      if (tabs >= t_end) {
+        // this token lies past the unit: its V row holds stale ring data or a last page's unused slots
+        // (possibly NaN), and P = 0 times NaN would still poison O, so the row becomes zeros
+#pragma unroll
+        for (int hf = 0; hf < C::kRowB / 128; ++hf) {
+          uint4* z = reinterpret_cast<uint4*>(sV + vs * C::kVStage + hf * (C::kTile * 128) + tok * 128);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) z[k] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (KV_FP8) {
+        const float* sc = reinterpret_cast<const float*>(sV + vs * C::kVStage + C::kTileB);
+        float sk = sc[tok], sv = sc[C::kTile + tok];
+        if (tabs >= t_end) { sk = 0.f; sv = 1.f; }
+        sv = fmaxf(sv, 7.888609052210118e-31f);  // 2^-100 floor keeps log2 and 1/x finite
+        const float ls = __log2f(sv);
+        inv_sv = __frcp_rn(sv);
+#pragma unroll
+        for (int c = 0; c < NP; ++c) y[c] = fmaf(y[c] * sk, rowC[c], ls);
+      } else {
+#pragma unroll
+        for (int c = 0; c < NP; ++c) y[c] *= p.scale_log2;
+      }
+      // causal mask inside the drafts / unit end / padding rows
+      if (tabs >= t_end) {
+#pragma unroll
+        for (int c = 0; c < NP; ++c) y[c] = -INFINITY;
+      } else if (tabs > lim_first) {
+#pragma unroll
+        for (int c = 0; c < NP; ++c)
+          if (tabs > rowLim[c]) y[c] = -INFINITY;
+      }
+      bool exceed = false;
+#pragma unroll
+      for (int c = 0; c < NP; ++c) exceed |= y[c] > rowM[c] + 8.f;
+      if (named_or(2, 128, exceed)) {
+        // ---- exact tile row maxima, raise the references, rescale l and O
+#pragma unroll
+        for (int c = 0; c < NP; ++c) {
+          float m = y[c];
+#pragma unroll
+          for (int k = 16; k >= 1; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
+          if (lane == 0) red[(warp - 2) * 64 + c] = m;
+        }
+        named_sync(1, 128);
+        // alpha_c = 2^(M_old - M_new) for each column, recomputed where needed
+        auto alpha_of = [&](int c) {
+          const float tm = fmaxf(fmaxf(red[c], red[64 + c]), fmaxf(red[128 + c], red[192 + c]));
+          const float mo = rowM[c];
+          const float mn = fmaxf(mo, tm);
+          return (mn == -INFINITY || mo == mn) ? 1.f : fast_exp2(mo - mn);
+        };
+        bool any_scale = false;
+        for (int c = 0; c < NP; ++c) any_scale |= alpha_of(c) != 1.f;
+        if (any_scale && i > 0) {
+          wait(&pfree[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u);  // PV of tile i-1 done
+          tc::fence_after_sync();
+#pragma unroll 1
+          for (int c0 = 0; c0 < NP; c0 += 16) {
+            uint32_t r16[16];
+            tc::ld16(tO + lane_off + c0, r16);
+            tc::wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r16[j] = __float_as_uint(__uint_as_float(r16[j]) * alpha_of(c0 + j));
+            tc::st16(tO + lane_off + c0, r16);
+          }
+          tc::wait_st();
+        }
+#pragma unroll
+        for (int c = 0; c < NP; ++c) l[c] *= alpha_of(c);
+        named_sync(1, 128);  // every thread has read the old references
+        if (wt < NP) {
+          const float tm = fmaxf(fmaxf(red[wt], red[64 + wt]), fmaxf(red[128 + wt], red[192 + wt]));
+          rowM[wt] = fmaxf(rowM[wt], tm);
+        }
+        named_sync(1, 128);
+      }
+      // ---- P = 2^(y - M) (<= 2^8), row sums, P into shared memory as the MMA's B operand
+      const int pb = i & 1;
+      if (i >= 2) wait(&pfree[pb], static_cast<uint32_t>((i >> 1) - 1) & 1u);
+      uint8_t* prow = sP + pb * C::kPBuf;
+#pragma unroll
+      for (int c0 = 0; c0 < NP; c0 += 8) {
+        float pv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float m = rowM[c0 + j];
+          pv[j] = (y[c0 + j] == -INFINITY) ? 0.f : fast_exp2(y[c0 + j] - m);
+          l[c0 + j] = fmaf(pv[j], inv_sv, l[c0 + j]);
+        }
+        if (!KV_FP8) {
+          uint4 w;
+          w.x = pack_bf16(pv[0], pv[1]);
+          w.y = pack_bf16(pv[2], pv[3]);
+          w.z = pack_bf16(pv[4], pv[5]);
+          w.w = pack_bf16(pv[6], pv[7]);
+          const int ch = c0 >> 3;  // 16-byte chunk of the 128-byte token row
+          *reinterpret_cast<uint4*>(prow + tok * 128 + ((ch ^ (tok & 7)) << 4)) = w;
+        } else {
+          uint32_t hw0 = 0, hw1 = 0, lw0 = 0, lw1 = 0;
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            const float a = pv[j], c = pv[j + 1];
+            const float ah = __uint_as_float(__float_as_uint(a) & 0xFFF00000u);
+            const float ch2 = __uint_as_float(__float_as_uint(c) & 0xFFF00000u);
+            const uint32_t hb = e4m3x2(ah, ch2), lb = e4m3x2(a - ah, c - ch2);
+            if (j < 4) { hw0 |= hb << (8 * j); lw0 |= lb << (8 * j); }
+            else { hw1 |= hb << (8 * (j - 4)); lw1 |= lb << (8 * (j - 4)); }
+          }
+          // 8 bytes at byte c0 of the 64-byte token row (64B swizzle: chunk ^= (tok/2)%4)
+          const int ch = c0 >> 4;
+          const uint32_t off = tok * 64 + ((ch ^ ((tok >> 1) & 3)) << 4) + (c0 & 8);
+          *reinterpret_cast<uint2*>(prow + off) = make_uint2(hw0, hw1);
+          *reinterpret_cast<uint2*>(prow + C::kPPlane + off) = make_uint2(lw0, lw1);
+        }
+      }
+      fence_proxy_async();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pfull[pb]);
+    }
+
+    // ---- epilogue: O / l
+    if (n_tiles > 0) wait(&pfree[(n_tiles - 1) & 1], static_cast<uint32_t>((n_tiles - 1) >> 1) & 1u);
+    const bool ok = ok_sm;
+    // l partial sums of every token -> per-row totals (scratch: the K ring, idle now)
+    float* lred = reinterpret_cast<float*>(sK);
+#pragma unroll
+    for (int c = 0; c < NP; ++c) lred[c * 128 + tok] = l[c];
+    named_sync(1, 128);
+    if (wt < NP) {
+      float s = 0.f;
+      for (int t = 0; t < 128; ++t) s += lred[wt * 128 + t];
+      red[wt] = s;  // row total
+    }
+    named_sync(1, 128);
+    if (ok) {
+      tc::fence_after_sync();
+      const int d = tok;  // O^T lanes are head-dim entries
+#pragma unroll
+      for (int c0 = 0; c0 < NP; c0 += 16) {
+        uint32_t r16[16];
+        tc::ld16(tO + lane_off + c0, r16);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = c0 + j;
+          if (r >= rows) continue;
+          const float lt = red[r];
+          const float val = lt > 0.f ? __uint_as_float(r16[j]) / lt : 0.f;
+          if (split) {
+            p.part_o[(static_cast<size_t>(u) * p.rows_max + r) * C::kD + d] = val;
+          } else {
+            const int qi = r / G;
+            const size_t o = (static_cast<size_t>(si.q_off + qi) * p.num_q_heads + kvh * G + (r - qi * G)) * C::kD + d;
+            if (p.out_f32) reinterpret_cast<float*>(p.out)[o] = val;
+            else reinterpret_cast<uint16_t*>(p.out)[o] = static_cast<uint16_t>(pack_bf16(val, 0.f) & 0xFFFFu);
+          }
+        }
+      }
+      if (split && wt < rows) {
+        const float lt = red[wt];
+        p.part_lse[static_cast<size_t>(u) * p.rows_max + wt] = lt > 0.f ? rowM[wt] + __log2f(lt) : -INFINITY;
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 256);
+  }
+}
+
+}  // namespace pav

@@ -30,6 +30,10 @@ ERR_WORKSPACE = -3
 ERR_CUDA = -4
 ERR_NOMEM = -5
 
+KERNEL_AUTO = 0
+KERNEL_WARP_MMA = 1
+KERNEL_TCGEN05 = 2
+
 DEVERR_PAGE_RANGE = 1
 DEVERR_LENGTHS = 2
 DEVERR_TIMEOUT = 4
@@ -50,7 +54,7 @@ class PaVerifyError(RuntimeError):
 class Desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_seqs", "num_q_heads", "num_kv_heads", "head_dim", "page_size", "kv_dtype", "out_dtype",
-        "num_pages", "block_table_stride", "split_override", "sm_count")]
+        "num_pages", "block_table_stride", "split_override", "sm_count", "kernel")]
 
 
 class KvWriteDesc(ctypes.Structure):
@@ -62,7 +66,7 @@ class PlanInfo(ctypes.Structure):
         ("num_units", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
         ("rows_max", ctypes.c_int32), ("warps", ctypes.c_int32), ("max_splits", ctypes.c_int32),
         ("needs_combine", ctypes.c_int32), ("num_tokens", ctypes.c_int32), ("kv_bytes", ctypes.c_int64),
-        ("workspace_bytes", ctypes.c_size_t)]
+        ("workspace_bytes", ctypes.c_size_t), ("kernel", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -142,12 +146,13 @@ class Plan:
 
 def plan(num_q_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: int, out_dtype: int, num_pages: int,
          block_table_stride: int, context_lens: Sequence[int], query_lens: Sequence[int],
-         split_override: int = 0, sm_count: int = 0, page_size: int = 16) -> Plan:
+         split_override: int = 0, sm_count: int = 0, page_size: int = 16, kernel: int = KERNEL_AUTO) -> Plan:
     """pa_verify_plan with host lengths; raises PaVerifyError on refusal."""
     n = len(context_lens)
     d = Desc(num_seqs=n, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
              page_size=page_size, kv_dtype=kv_dtype, out_dtype=out_dtype, num_pages=num_pages,
-             block_table_stride=block_table_stride, split_override=split_override, sm_count=sm_count)
+             block_table_stride=block_table_stride, split_override=split_override, sm_count=sm_count,
+             kernel=kernel)
     arr = ctypes.c_int32 * max(1, n)
     cl = arr(*[int(x) for x in context_lens])
     ql = arr(*[int(x) for x in query_lens])
@@ -233,11 +238,12 @@ class VerifyAttention:
 
     def __init__(self, num_q_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: int, num_pages: int,
                  block_table_stride: int, context_lens: Sequence[int], query_lens: Sequence[int],
-                 out_dtype: int = OUT_F32, split_override: int = 0, device: Optional[torch.device] = None):
+                 out_dtype: int = OUT_F32, split_override: int = 0, device: Optional[torch.device] = None,
+                 kernel: int = KERNEL_AUTO):
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         with torch.cuda.device(self.device):
             self.plan = plan(num_q_heads, num_kv_heads, head_dim, kv_dtype, out_dtype, num_pages, block_table_stride,
-                             context_lens, query_lens, split_override=split_override)
+                             context_lens, query_lens, split_override=split_override, kernel=kernel)
         self.out_dtype = out_dtype
         self.num_q_heads = num_q_heads
         self.head_dim = head_dim

@@ -26,11 +26,19 @@ def built():
     yield
 
 
-def gpu_run(prob, out_dtype=pv.OUT_F32, split_override=0, dev=None, check_errors=True):
+def tc_applies(prob):
+    return prob.head_dim == 128 and int(prob.query_lens.max()) * prob.group <= 64
+
+
+KERNELS = [pv.KERNEL_WARP_MMA, pv.KERNEL_TCGEN05]
+KID = {pv.KERNEL_WARP_MMA: "mma", pv.KERNEL_TCGEN05: "tc"}
+
+
+def gpu_run(prob, out_dtype=pv.OUT_F32, split_override=0, dev=None, check_errors=True, kernel=pv.KERNEL_AUTO):
     dev = dev or to_device(prob)
     va = pv.VerifyAttention(prob.num_q_heads, prob.num_kv_heads, prob.head_dim, prob.kv_dtype, prob.num_pages,
                             prob.block_table.shape[1], prob.context_lens.tolist(), prob.query_lens.tolist(),
-                            out_dtype=out_dtype, split_override=split_override)
+                            out_dtype=out_dtype, split_override=split_override, kernel=kernel)
     out = va(*dev.args(), prob.softmax_scale)
     torch.cuda.synchronize()
     if check_errors:
@@ -59,10 +67,14 @@ SMALL = [
 
 @pytest.mark.parametrize("name,make", SMALL, ids=[s[0] for s in SMALL])
 @pytest.mark.parametrize("split", [0, 1, 3])
-def test_small_against_oracle(name, make, split):
+@pytest.mark.parametrize("kernel", KERNELS, ids=[KID[k] for k in KERNELS])
+def test_small_against_oracle(name, make, split, kernel):
     prob = make()
+    if kernel == pv.KERNEL_TCGEN05 and not tc_applies(prob):
+        pytest.skip("outside the tcgen05 kernel's envelope")
     ref = oracle.verify_attention(prob)
-    got, _ = gpu_run(prob, split_override=split)
+    got, va = gpu_run(prob, split_override=split, kernel=kernel)
+    assert va.info["kernel"] == kernel
     assert max_err(got, ref) <= TOL[prob.kv_dtype], name
 
 
@@ -74,18 +86,20 @@ def test_bf16_output(name, make):
     assert max_err(got, ref) <= TOL[prob.kv_dtype] + 1e-2
 
 
-def test_split_count_does_not_change_the_result():
+@pytest.mark.parametrize("kernel", KERNELS, ids=[KID[k] for k in KERNELS])
+def test_split_count_does_not_change_the_result(kernel):
     prob = synth.make_problem([3000, 1200], [6, 6], 16, 2, 128, seed=41)
-    outs = [gpu_run(prob, split_override=k)[0] for k in (1, 2, 5, 1000)]
+    outs = [gpu_run(prob, split_override=k, kernel=kernel)[0] for k in (1, 2, 5, 1000)]
     for o in outs[1:]:
         # P is rounded to bf16 against a split-dependent running max: 2^-8 relative per weight
         assert max_err(o, outs[0]) <= 2e-3
 
 
-def test_repeat_runs_are_bit_identical():
+@pytest.mark.parametrize("kernel", KERNELS, ids=[KID[k] for k in KERNELS])
+def test_repeat_runs_are_bit_identical(kernel):
     prob = synth.make_problem([3000, 1200], [6, 6], 16, 2, 128, seed=42)
     dev = to_device(prob)
-    a, va = gpu_run(prob, dev=dev)
+    a, va = gpu_run(prob, dev=dev, kernel=kernel)
     b = va(*dev.args(), prob.softmax_scale).cpu().numpy()
     assert np.array_equal(a, b)
 
@@ -136,6 +150,22 @@ def test_device_length_mismatch_is_flagged():
 
 
 # --------------------------------------------------------------- full-size workloads
+_cache = {}
+
+
+def _workload(name):
+    if name not in _cache:
+        _cache[name] = synth.make_config(name)
+    return _cache[name]
+
+
+def _workload_dev(name):
+    key = name + ":dev"
+    if key not in _cache:
+        _cache[key] = to_device(_workload(name))
+    return _cache[key]
+
+
 def sample_rows(prob, n, seed):
     rng = np.random.default_rng(seed)
     T, H = prob.num_tokens, prob.num_q_heads
@@ -148,9 +178,10 @@ def sample_rows(prob, n, seed):
 
 
 @pytest.mark.parametrize("name", ["mtp5_bf16", "mtp5_fp8", "mixed_fp8", "ctx1mi_bf16"])
-def test_full_workload_sampled_rows(name):
-    prob = synth.make_config(name)
-    got, va = gpu_run(prob)
+@pytest.mark.parametrize("kernel", KERNELS, ids=[KID[k] for k in KERNELS])
+def test_full_workload_sampled_rows(name, kernel):
+    prob = _workload(name)
+    got, va = gpu_run(prob, dev=_workload_dev(name), kernel=kernel)
     assert np.isfinite(got).all()
     rows = sample_rows(prob, 48 if name != "mixed_fp8" else 200, seed=7)
     ref = oracle.verify_attention(prob, rows=rows)
