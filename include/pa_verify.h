@@ -156,6 +156,33 @@ int pa_verify_run(pa_verify_plan_t plan, const void* q, const void* k_cache, con
 int pa_verify_profile_enable(pa_verify_plan_t plan, int enable);
 int pa_verify_profile_read(pa_verify_plan_t plan, float* split_ms, float* combine_ms);
 
+/*
+ * pa_verify_run_static: pa_verify_run without a workspace argument, for
+ * callers that cannot allocate device memory. Examples: a serving loop that
+ * has reserved nearly all HBM for its KV cache up front, a host application
+ * that owns every device allocation and gives plug-ins none, or code that must
+ * not call cudaMalloc because it would synchronise the device or break a
+ * memory-pool policy. (The pages this library follows have no counterpart.)
+ *
+ * The scratch this call needs (its device error word and the split partials)
+ * is a single file-scope device array of PA_STATIC_SCRATCH_BYTES, which every
+ * GPU that loads the library holds until the process exits. The first call on
+ * a device looks up that array's device address there (cudaGetSymbolAddress,
+ * with the device current); make that first call before any stream capture.
+ * A plan that needs more scratch than the array holds is refused with
+ * PA_ERR_WORKSPACE before anything is enqueued. The call allocates nothing and
+ * calls neither cudaMalloc nor cudaFree. Every call shares the one array, which
+ * keeps the last call's contents; the error word at its start is cleared on
+ * the stream at the start of each call. Calls that overlap on the GPU (two
+ * streams, two threads) race on the shared scratch: serialise them. Other
+ * arguments, checks and return codes are those of pa_verify_run.
+ */
+#define PA_STATIC_SCRATCH_BYTES (16u << 20)
+int pa_verify_run_static(pa_verify_plan_t plan, const void* q, const void* k_cache, const void* v_cache,
+                         const float* k_scale, const float* v_scale, const int32_t* block_table,
+                         const int32_t* context_lens, const int32_t* query_lens, float softmax_scale,
+                         void* out, pa_stream_t stream);
+
 /* Frees a plan (NULL is allowed). */
 void pa_verify_free(pa_verify_plan_t plan);
 

@@ -355,6 +355,90 @@ int pa_verify_run(pa_verify_plan_t plan, const void* q, const void* k_cache, con
   return PA_OK;
 }
 
+}  // extern "C"
+
+namespace pav {
+
+// Enqueue for callers that bring their own scratch and cannot have anything
+// allocated on their behalf: the same checks and launches as pa_verify_run,
+// with the kernel parameters on the stack and no profiling events.
+int enqueue_with_scratch(pa_verify_plan_t plan, const void* q, const void* k_cache, const void* v_cache,
+                         const float* k_scale, const float* v_scale, const int32_t* block_table,
+                         const int32_t* context_lens, const int32_t* query_lens, float softmax_scale, void* out,
+                         uint8_t* scratch, size_t scratch_bytes, cudaStream_t s) {
+  g_last_error.clear();
+  if (!plan) return fail(PA_ERR_INVALID, "plan must not be NULL");
+  const pa_verify_desc& d = plan->d;
+  if (d.num_seqs == 0) return PA_OK;
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !query_lens || !out || !scratch)
+    return fail(PA_ERR_INVALID, "a required pointer is NULL");
+  if (fp8 && (!k_scale || !v_scale)) return fail(PA_ERR_INVALID, "FP8 KV needs k_scale and v_scale");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return fail(PA_ERR_INVALID, "q, k_cache, v_cache and out must be 16-byte aligned");
+  if (fp8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16)))
+    return fail(PA_ERR_INVALID, "k_scale and v_scale must be 16-byte aligned");
+  if (!aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(query_lens, 4))
+    return fail(PA_ERR_INVALID, "int32 arrays must be 4-byte aligned");
+  if (!(std::isfinite(softmax_scale) && softmax_scale > 0.f)) return fail(PA_ERR_INVALID, "softmax_scale must be finite and > 0");
+  if (scratch_bytes < plan->ws_bytes)
+    return fail(PA_ERR_WORKSPACE, "this plan needs " + std::to_string(plan->ws_bytes) +
+                                      " bytes of scratch; the fixed scratch holds " + std::to_string(scratch_bytes));
+  if (plan->tm_k != k_cache) {
+    int rc = encode_kv_map(&plan->tmk, k_cache, d);
+    if (rc) return rc;
+    plan->tm_k = k_cache;
+  }
+  if (plan->tm_v != v_cache) {
+    int rc = encode_kv_map(&plan->tmv, v_cache, d);
+    if (rc) return rc;
+    plan->tm_v = v_cache;
+  }
+  SplitParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.block_table = block_table;
+  p.k_scale = fp8 ? k_scale : nullptr;
+  p.v_scale = fp8 ? v_scale : nullptr;
+  p.out = out;
+  p.err = reinterpret_cast<uint32_t*>(scratch);
+  if (plan->needs_combine) {
+    p.part_o = reinterpret_cast<float*>(scratch + kWsHeader);
+    p.part_lse = reinterpret_cast<float*>(
+        scratch + kWsHeader + align_up(static_cast<size_t>(plan->units) * plan->rows_max * d.head_dim * 4, 256));
+  }
+  p.dev_ctx = context_lens;
+  p.dev_q = query_lens;
+  p.num_seqs = d.num_seqs;
+  p.num_q_heads = d.num_q_heads;
+  p.num_kv_heads = d.num_kv_heads;
+  p.group = d.num_q_heads / d.num_kv_heads;
+  p.bt_stride = d.block_table_stride;
+  p.num_pages = d.num_pages;
+  p.chunk = plan->chunk;
+  p.num_units = plan->units;
+  p.rows_max = plan->rows_max;
+  p.out_f32 = d.out_dtype == PA_OUT_F32 ? 1 : 0;
+  p.num_rows = plan->num_rows;
+  p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
+  std::memcpy(p.seq, plan->seq, sizeof(plan->seq));
+  // the error word starts each call at zero (the scratch keeps the last call's contents)
+  cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess)
+    e = plan->kernel == PA_KERNEL_TCGEN05
+            ? launch_tc_split(fp8 ? 1 : 0, plan->rows_max, plan->units, &plan->tmk, &plan->tmv, &p, s)
+        : fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s)
+              : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s);
+  if (e == cudaSuccess && plan->needs_combine) e = launch_combine(d.head_dim, &p, s);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
+  return PA_OK;
+}
+
+int report_error(int code, const char* msg) { return fail(code, msg); }
+
+}  // namespace pav
+
+extern "C" {
+
 int pa_verify_profile_enable(pa_verify_plan_t plan, int enable) {
   g_last_error.clear();
   if (!plan) return fail(PA_ERR_INVALID, "plan must not be NULL");

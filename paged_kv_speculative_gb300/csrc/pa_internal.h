@@ -71,3 +71,18 @@ __host__ __device__ constexpr int split_ctas_per_sm(int warps) { return warps <=
 cudaError_t launch_combine(int head_dim, const SplitParams* p, cudaStream_t stream);
 
 }  // namespace pav
+
+typedef struct pa_verify_plan_s* pa_verify_plan_t;
+
+namespace pav {
+
+// pa_verify_run's checks and launches with caller-provided scratch, kernel
+// parameters on the stack, nothing allocated (host or device).
+int enqueue_with_scratch(pa_verify_plan_t plan, const void* q, const void* k_cache, const void* v_cache,
+                         const float* k_scale, const float* v_scale, const int32_t* block_table,
+                         const int32_t* context_lens, const int32_t* query_lens, float softmax_scale, void* out,
+                         uint8_t* scratch, size_t scratch_bytes, cudaStream_t stream);
+// Records `msg` as this thread's last error and returns `code`.
+int report_error(int code, const char* msg);
+
+}  // namespace pav

@@ -42,7 +42,7 @@ DEVERR_TIMEOUT = 4
 EXPORTED = ("pa_verify_plan", "pa_verify_plan_get_info", "pa_verify_run", "pa_verify_free",
             "pa_verify_device_errors", "pa_verify_last_error", "pa_verify_profile_enable",
             "pa_verify_profile_read", "pa_kv_write", "pa_greedy_verdict_workspace_bytes",
-            "pa_greedy_verdict")
+            "pa_greedy_verdict", "pa_verify_run_static")
 
 
 class PaVerifyError(RuntimeError):
@@ -91,6 +91,8 @@ def lib(path: Optional[str] = None):
     L.pa_verify_plan_get_info.restype = ctypes.c_int
     L.pa_verify_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     L.pa_verify_run.restype = ctypes.c_int
+    L.pa_verify_run_static.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
+    L.pa_verify_run_static.restype = ctypes.c_int
     L.pa_verify_free.argtypes = [vp]
     L.pa_verify_free.restype = None
     L.pa_verify_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, vp]
@@ -193,6 +195,21 @@ def run(p: Plan, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, 
                                _ptr(block_table), _ptr(context_lens), _ptr(query_lens), float(softmax_scale),
                                _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                s.cuda_stream))
+
+
+def run_static(p: Plan, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+               k_scale: Optional[torch.Tensor], v_scale: Optional[torch.Tensor], block_table: torch.Tensor,
+               context_lens: torch.Tensor, query_lens: torch.Tensor, softmax_scale: float, out: torch.Tensor,
+               stream: Optional[torch.cuda.Stream] = None):
+    """pa_verify_run_static: like ``run`` but with the library's fixed device
+    scratch instead of a workspace, for callers that cannot allocate."""
+    _need(q, "q", torch.bfloat16)
+    for t, nm in ((k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
+        _need(t, nm)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    _check(lib().pa_verify_run_static(p.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                      _ptr(v_scale), _ptr(block_table), _ptr(context_lens), _ptr(query_lens),
+                                      float(softmax_scale), _ptr(out), s.cuda_stream))
 
 
 def device_errors(workspace: torch.Tensor, clear: bool = False, stream: Optional[torch.cuda.Stream] = None) -> int:
