@@ -9,13 +9,14 @@
 //   O^T[d, r]   += V[:, d]^T . P^T[:, r]          (A = V tile, MN-major; B = P, MN-major)
 // with both accumulators in tensor memory.
 //
-// Warp roles (192 threads): warp 0 gathers pages through the block table with
+// Warp roles (320 threads): warp 0 gathers pages through the block table with
 // 2-D TMA boxes (lane 0 feeds a KS-deep K ring, lane 1 a VS-deep V ring that
 // also carries the FP8 scales); warp 1 allocates tensor memory and issues the
-// MMAs (one thread); warps 2-5 are the softmax warpgroup, one thread per
-// token of the tile. Stages hand over on mbarriers; every wait is bounded.
+// MMAs (one thread); warps 2-9 are two softmax warpgroups, one thread per
+// token of the tile, each group owning half of the row columns. Stages hand
+// over on mbarriers; every wait is bounded.
 //
-// Softmax. Row r keeps a reference maximum M_r, uniform across the CTA. A
+// Softmax. Row r keeps a reference maximum M_r, uniform across its group. A
 // tile whose scores stay below M_r + 8 (log2 units) uses M_r as is, so P <= 2^8
 // and no cross-thread row maximum is needed. Otherwise (the first tile, or a
 // score that rose by more than 2^8) the warpgroup takes the exact tile row
@@ -55,10 +56,11 @@ struct TcCfg {
   static constexpr int kOffP = kOffQ + kQB;
   static constexpr int kOffPid = kOffP + 2 * kPBuf;
   static constexpr int kOffRow = kOffPid + 4 * (kMaxChunk / kPage);  // per-row constants
-  static constexpr int kOffRed = kOffRow + 4 * 64 * 4;               // tile maxima of the 4 softmax warps
-  static constexpr int kOffBar = kOffRed + 4 * 64 * 4;
+  static constexpr int kOffRed = kOffRow + 4 * 64 * 4;               // tile maxima of the 8 softmax warps + row totals
+  static constexpr int kOffBar = kOffRed + 9 * 64 * 4;
   static constexpr int kSmem = kOffBar + 256 + 1024;                 // barriers, tmem base, alignment slack
   static_assert(NP % 16 == 0 && NP >= 16 && NP <= 64, "N must be 16..64 in steps of 16");
+  static_assert((NP / 2) % 8 == 0, "each softmax warpgroup owns a multiple of 8 columns");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kTile * NP * 4 <= KS * kTileB, "epilogue l-sum scratch fits the K ring");
 };
@@ -87,7 +89,7 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 }
 
 template <int KV_FP8, int NP>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     pa_tc_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ SplitParams p) {
   using C = TcCfg<KV_FP8, NP>;
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(192, 1)
   float* rowM = reinterpret_cast<float*>(sm + C::kOffRow);      // reference maxima (log2 units)
   float* rowC = rowM + 64;                                       // score multiplier per row
   int* rowLim = reinterpret_cast<int*>(rowC + 64);               // last visible key per row (-1: padding)
-  float* red = reinterpret_cast<float*>(sm + C::kOffRed);        // [4 warps][64]
+  float* red = reinterpret_cast<float*>(sm + C::kOffRed);        // [8 warps][64] maxima, then [64] row totals
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   uint64_t* kfull = bars;
   uint64_t* kempty = kfull + C::KS;
@@ -141,11 +143,11 @@ __global__ void __launch_bounds__(192, 1)
     for (int s = 0; s < C::VS; ++s) { mbar_init(smem_addr(&vfull[s]), 1); mbar_init(smem_addr(&vempty[s]), 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_addr(&sfull[s]), 1);
-      mbar_init(smem_addr(&sfree[s]), 4);
-      mbar_init(smem_addr(&pfull[s]), 4);
+      mbar_init(smem_addr(&sfree[s]), 8);
+      mbar_init(smem_addr(&pfull[s]), 8);
       mbar_init(smem_addr(&pfree[s]), 1);
     }
-    mbar_init(smem_addr(qready), 4);
+    mbar_init(smem_addr(qready), 8);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmk);
@@ -296,15 +298,21 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok) fail();
     }
   } else {
-    // ============================================================ softmax warpgroup
-    const int wt = tid - 64;           // 0..127
-    const int q4 = warp & 3;           // tensor-memory lane quarter of this warp
-    const int tok = q4 * 32 + lane;    // token of the tile this thread owns (= TMEM lane)
+    // ============================================================ softmax warpgroups
+    // Two warpgroups (warps 2-5 and 6-9). Each covers the 128 tokens of a tile
+    // (one per thread, = tensor-memory lane) for its own NH = NP/2 columns
+    // (rows of the unit); the groups never wait on each other inside the loop.
+    constexpr int NH = NP / 2;
+    const int wg = (warp - 2) >> 2;               // 0 or 1
+    const int gt = tid - 64 - wg * 128;           // 0..127 inside the group
+    const int q4 = warp & 3;                      // tensor-memory lane quarter of this warp
+    const int tok = q4 * 32 + lane;               // token of the tile this thread owns
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const int col0 = wg * NH;                     // first column this group owns
+    const int bar_sync = 1 + 2 * wg, bar_or = 2 + 2 * wg;
 
-    // ---- Q staging: rows r < NP, K-major, 128B swizzle (fp8: hi / lo planes)
-    for (int r = wt >> 5; r < NP; r += 4) {
-      // warp-per-row: lane owns 4 consecutive head-dim entries
+    // ---- Q staging by all 8 softmax warps: row r is one warp's job
+    for (int r = warp - 2; r < NP; r += 8) {
       const uint16_t* qp = nullptr;
       if (r < rows) {
         const int i = r / G;
@@ -346,16 +354,20 @@ __global__ void __launch_bounds__(192, 1)
     fence_proxy_async();
     __syncwarp();
     if (lane == 0) mbar_arrive(qready);
-    named_sync(1, 128);  // rowC written
+    named_sync(5, 256);  // both groups' rows staged (rowC complete)
 
-    float l[NP];
+    float mref[NH], crow[NH], l[NH];  // reference max, score multiplier, row-sum partial per owned column
 #pragma unroll
-    for (int c = 0; c < NP; ++c) l[c] = 0.f;
+    for (int c = 0; c < NH; ++c) {
+      mref[c] = -INFINITY;
+      crow[c] = rowC[col0 + c];
+      l[c] = 0.f;
+    }
     const int lim_first = L - QL;  // last key every real row sees
 
     // A failed wait marks this thread and skips its later waits, but every
     // named barrier below is still reached in order: no thread of the
-    // warpgroup can be left behind at one.
+    // group can be left behind at one.
     bool ok_sm = true;
     auto wait = [&](uint64_t* bar, uint32_t par) {
       if (ok_sm && !mbar_wait_bounded(smem_addr(bar), par)) {
@@ -367,14 +379,14 @@ __global__ void __launch_bounds__(192, 1)
       const int sb = i & 1;
       wait(&sfull[sb], static_cast<uint32_t>(i >> 1) & 1u);
       tc::fence_after_sync();
-      float y[NP];
+      float y[NH];
 #pragma unroll
-      for (int c0 = 0; c0 < NP; c0 += 16) {
-        uint32_t r16[16];
-        tc::ld16(tS[sb] + lane_off + c0, r16);
+      for (int c0 = 0; c0 < NH; c0 += 8) {
+        uint32_t r8[8];
+        tc::ld8(tS[sb] + lane_off + col0 + c0, r8);
         tc::wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) y[c0 + j] = __uint_as_float(r16[j]);
+        for (int j = 0; j < 8; ++j) y[c0 + j] = __uint_as_float(r8[j]);
       }
       tc::fence_before_sync();
       __syncwarp();
@@ -385,7 +397,7 @@ __global__ void __launch_bounds__(192, 1)
       // every tile's V phase is observed in order (a skipped phase would make a later parity wait ambiguous)
       const int vs = i % C::VS;
       wait(&vfull[vs], static_cast<uint32_t>(i / C::VS) & 1u);
-      if (tabs >= t_end) {
+      if (wg == 0 && tabs >= t_end) {
         // this token lies past the unit: its V row holds stale ring data or a last page's unused slots
         // (possibly NaN), and P = 0 times NaN would still poison O, so the row becomes zeros
 #pragma unroll
@@ -403,85 +415,91 @@ __global__ void __launch_bounds__(192, 1)
         const float ls = __log2f(sv);
         inv_sv = __frcp_rn(sv);
 #pragma unroll
-        for (int c = 0; c < NP; ++c) y[c] = fmaf(y[c] * sk, rowC[c], ls);
+        for (int c = 0; c < NH; ++c) y[c] = fmaf(y[c] * sk, crow[c], ls);
       } else {
 #pragma unroll
-        for (int c = 0; c < NP; ++c) y[c] *= p.scale_log2;
+        for (int c = 0; c < NH; ++c) y[c] *= p.scale_log2;
       }
       // causal mask inside the drafts / unit end / padding rows
       if (tabs >= t_end) {
 #pragma unroll
-        for (int c = 0; c < NP; ++c) y[c] = -INFINITY;
+        for (int c = 0; c < NH; ++c) y[c] = -INFINITY;
       } else if (tabs > lim_first) {
 #pragma unroll
-        for (int c = 0; c < NP; ++c)
-          if (tabs > rowLim[c]) y[c] = -INFINITY;
+        for (int c = 0; c < NH; ++c)
+          if (tabs > rowLim[col0 + c]) y[c] = -INFINITY;
       }
       bool exceed = false;
 #pragma unroll
-      for (int c = 0; c < NP; ++c) exceed |= y[c] > rowM[c] + 8.f;
-      if (named_or(2, 128, exceed)) {
-        // ---- exact tile row maxima, raise the references, rescale l and O
+      for (int c = 0; c < NH; ++c) exceed |= y[c] > mref[c] + 8.f;
+      if (named_or(bar_or, 128, exceed)) {
+        // ---- exact tile maxima of the owned columns, raise the references, rescale l and O
 #pragma unroll
-        for (int c = 0; c < NP; ++c) {
+        for (int c = 0; c < NH; ++c) {
           float m = y[c];
 #pragma unroll
           for (int k = 16; k >= 1; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
-          if (lane == 0) red[(warp - 2) * 64 + c] = m;
+          if (lane == 0) red[(warp - 2) * 64 + col0 + c] = m;
         }
-        named_sync(1, 128);
-        // alpha_c = 2^(M_old - M_new) for each column, recomputed where needed
-        auto alpha_of = [&](int c) {
-          const float tm = fmaxf(fmaxf(red[c], red[64 + c]), fmaxf(red[128 + c], red[192 + c]));
-          const float mo = rowM[c];
-          const float mn = fmaxf(mo, tm);
-          return (mn == -INFINITY || mo == mn) ? 1.f : fast_exp2(mo - mn);
+        named_sync(bar_sync, 128);
+        const float* rg = red + wg * 4 * 64 + col0;  // this group's 4 warp rows
+        auto new_max = [&](int c) {
+          return fmaxf(mref[c], fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
         };
         bool any_scale = false;
-        for (int c = 0; c < NP; ++c) any_scale |= alpha_of(c) != 1.f;
+#pragma unroll
+        for (int c = 0; c < NH; ++c) {
+          const float mn = new_max(c);
+          any_scale |= (mn != -INFINITY && mn != mref[c]);
+        }
         if (any_scale && i > 0) {
           wait(&pfree[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u);  // PV of tile i-1 done
           tc::fence_after_sync();
-#pragma unroll 1
-          for (int c0 = 0; c0 < NP; c0 += 16) {
-            uint32_t r16[16];
-            tc::ld16(tO + lane_off + c0, r16);
+#pragma unroll
+          for (int c0 = 0; c0 < NH; c0 += 8) {
+            uint32_t r8[8];
+            tc::ld8(tO + lane_off + col0 + c0, r8);
             tc::wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) r16[j] = __float_as_uint(__uint_as_float(r16[j]) * alpha_of(c0 + j));
-            tc::st16(tO + lane_off + c0, r16);
+            for (int j = 0; j < 8; ++j) {
+              const float mn = new_max(c0 + j);
+              const float a = (mn == -INFINITY || mn == mref[c0 + j]) ? 1.f : fast_exp2(mref[c0 + j] - mn);
+              r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+            }
+            tc::st8(tO + lane_off + col0 + c0, r8);
           }
           tc::wait_st();
         }
 #pragma unroll
-        for (int c = 0; c < NP; ++c) l[c] *= alpha_of(c);
-        named_sync(1, 128);  // every thread has read the old references
-        if (wt < NP) {
-          const float tm = fmaxf(fmaxf(red[wt], red[64 + wt]), fmaxf(red[128 + wt], red[192 + wt]));
-          rowM[wt] = fmaxf(rowM[wt], tm);
+        for (int c = 0; c < NH; ++c) {
+          const float mn = new_max(c);
+          if (mn != -INFINITY && mn != mref[c]) {
+            l[c] *= fast_exp2(mref[c] - mn);
+            mref[c] = mn;
+          }
         }
-        named_sync(1, 128);
+        // red is rewritten only after the next vote (a barrier of this group), when every read here is done
       }
       // ---- P = 2^(y - M) (<= 2^8), row sums, P into shared memory as the MMA's B operand
       const int pb = i & 1;
       if (i >= 2) wait(&pfree[pb], static_cast<uint32_t>((i >> 1) - 1) & 1u);
       uint8_t* prow = sP + pb * C::kPBuf;
 #pragma unroll
-      for (int c0 = 0; c0 < NP; c0 += 8) {
+      for (int c0 = 0; c0 < NH; c0 += 8) {
         float pv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float m = rowM[c0 + j];
-          pv[j] = (y[c0 + j] == -INFINITY) ? 0.f : fast_exp2(y[c0 + j] - m);
+          pv[j] = (y[c0 + j] == -INFINITY) ? 0.f : fast_exp2(y[c0 + j] - mref[c0 + j]);
           l[c0 + j] = fmaf(pv[j], inv_sv, l[c0 + j]);
         }
+        const int cg = col0 + c0;  // first global column of these 8
         if (!KV_FP8) {
           uint4 w;
           w.x = pack_bf16(pv[0], pv[1]);
           w.y = pack_bf16(pv[2], pv[3]);
           w.z = pack_bf16(pv[4], pv[5]);
           w.w = pack_bf16(pv[6], pv[7]);
-          const int ch = c0 >> 3;  // 16-byte chunk of the 128-byte token row
+          const int ch = cg >> 3;  // 16-byte chunk of the 128-byte token row
           *reinterpret_cast<uint4*>(prow + tok * 128 + ((ch ^ (tok & 7)) << 4)) = w;
         } else {
           uint32_t hw0 = 0, hw1 = 0, lw0 = 0, lw1 = 0;
@@ -494,9 +512,9 @@ __global__ void __launch_bounds__(192, 1)
             if (j < 4) { hw0 |= hb << (8 * j); lw0 |= lb << (8 * j); }
             else { hw1 |= hb << (8 * (j - 4)); lw1 |= lb << (8 * (j - 4)); }
           }
-          // 8 bytes at byte c0 of the 64-byte token row (64B swizzle: chunk ^= (tok/2)%4)
-          const int ch = c0 >> 4;
-          const uint32_t off = tok * 64 + ((ch ^ ((tok >> 1) & 3)) << 4) + (c0 & 8);
+          // 8 bytes at byte cg of the 64-byte token row (64B swizzle: chunk ^= (tok/2)%4)
+          const int ch = cg >> 4;
+          const uint32_t off = tok * 64 + ((ch ^ ((tok >> 1) & 3)) << 4) + (cg & 8);
           *reinterpret_cast<uint2*>(prow + off) = make_uint2(hw0, hw1);
           *reinterpret_cast<uint2*>(prow + C::kPPlane + off) = make_uint2(lw0, lw1);
         }
@@ -507,34 +525,41 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) mbar_arrive(&pfull[pb]);
     }
 
-    // ---- epilogue: O / l
+    // ---- epilogue: O / l for the owned columns
     if (n_tiles > 0) wait(&pfree[(n_tiles - 1) & 1], static_cast<uint32_t>((n_tiles - 1) >> 1) & 1u);
     const bool ok = ok_sm;
-    // l partial sums of every token -> per-row totals (scratch: the K ring, idle now)
+    // l partial sums of every token -> per-row totals (scratch: the K ring, idle once every MMA is done)
     float* lred = reinterpret_cast<float*>(sK);
+    float* rtot = red + 8 * 64;  // row totals, after the 8 warp rows of maxima
 #pragma unroll
-    for (int c = 0; c < NP; ++c) lred[c * 128 + tok] = l[c];
-    named_sync(1, 128);
-    if (wt < NP) {
-      float s = 0.f;
-      for (int t = 0; t < 128; ++t) s += lred[wt * 128 + t];
-      red[wt] = s;  // row total
+    for (int c = 0; c < NH; ++c) lred[(col0 + c) * 128 + tok] = l[c];
+    named_sync(bar_sync, 128);
+    if (gt < NH) {
+      float s2 = 0.f;
+      for (int t = 0; t < 128; ++t) s2 += lred[(col0 + gt) * 128 + t];
+      rtot[col0 + gt] = s2;
+      float mg = -INFINITY;  // this column's reference max (registers hold every column's)
+#pragma unroll
+      for (int c = 0; c < NH; ++c)
+        if (c == gt) mg = mref[c];
+      if (ok && split && col0 + gt < rows)
+        p.part_lse[static_cast<size_t>(u) * p.rows_max + col0 + gt] = s2 > 0.f ? mg + __log2f(s2) : -INFINITY;
     }
-    named_sync(1, 128);
+    named_sync(bar_sync, 128);
     if (ok) {
       tc::fence_after_sync();
       const int d = tok;  // O^T lanes are head-dim entries
 #pragma unroll
-      for (int c0 = 0; c0 < NP; c0 += 16) {
-        uint32_t r16[16];
-        tc::ld16(tO + lane_off + c0, r16);
+      for (int c0 = 0; c0 < NH; c0 += 8) {
+        uint32_t r8[8];
+        tc::ld8(tO + lane_off + col0 + c0, r8);
         tc::wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = c0 + j;
+        for (int j = 0; j < 8; ++j) {
+          const int r = col0 + c0 + j;
           if (r >= rows) continue;
-          const float lt = red[r];
-          const float val = lt > 0.f ? __uint_as_float(r16[j]) / lt : 0.f;
+          const float lt = rtot[r];
+          const float val = lt > 0.f ? __uint_as_float(r8[j]) / lt : 0.f;
           if (split) {
             p.part_o[(static_cast<size_t>(u) * p.rows_max + r) * C::kD + d] = val;
           } else {
@@ -544,10 +569,6 @@ __global__ void __launch_bounds__(192, 1)
             else reinterpret_cast<uint16_t*>(p.out)[o] = static_cast<uint16_t>(pack_bf16(val, 0.f) & 0xFFFFu);
           }
         }
-      }
-      if (split && wt < rows) {
-        const float lt = red[wt];
-        p.part_lse[static_cast<size_t>(u) * p.rows_max + wt] = lt > 0.f ? rowM[wt] + __log2f(lt) : -INFINITY;
       }
     }
   }
