@@ -101,6 +101,7 @@ typedef struct {
   int64_t kv_bytes;        /* algorithmic K/V(+scale) bytes one run reads */
   size_t workspace_bytes;  /* bytes pa_verify_run needs in `workspace` */
   int32_t kernel;          /* PA_KERNEL_WARP_MMA or PA_KERNEL_TCGEN05 */
+  int32_t dynamic;         /* 1 for pa_verify_plan_dynamic plans (figures above are capacities) */
 } pa_verify_plan_info;
 
 /*
@@ -115,6 +116,26 @@ typedef struct {
 int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
                    const int32_t* query_lens_host, pa_verify_plan_t* plan_out,
                    size_t* workspace_bytes_out);
+
+/*
+ * Capacity plan for CUDA-graph replay of padded batches: the lengths are read
+ * on the device at every run, so one plan (and one captured graph) serves any
+ * batch that fits. desc->num_seqs is the batch capacity (the capture width);
+ * at run time sequence b may have query_lens[b] = 0 (a padded slot: no output
+ * row, nothing written) or 1 <= query_lens[b] <= max_query_len with
+ * query_lens[b] <= context_lens[b] <= max_context_len. Out-of-range lengths set
+ * PA_DEVERR_LENGTHS and that sequence is treated as padding. q and out hold the
+ * live sequences' rows packed in batch order, capacity num_seqs * max_query_len
+ * rows. A run enqueues a one-CTA planner kernel (the split of the context and
+ * the schedule, by the same rules as pa_verify_plan), the split kernel with a
+ * grid sized for the capacity and the combine. Workspace is sized for the
+ * capacity. split_override must be 0. Lengths and padding follow the pages'
+ * CUDA-graph capture of fixed batch sizes and stores masked by row liveness
+ * ("[DeepSeek-V4.1] High-interactivity monokernel decode", launch flags and
+ * description).
+ */
+int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, int32_t max_query_len,
+                           pa_verify_plan_t* plan_out, size_t* workspace_bytes_out);
 
 /* Copies the plan's figures into *info. */
 int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info);

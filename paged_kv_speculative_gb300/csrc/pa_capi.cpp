@@ -26,6 +26,9 @@ cudaError_t launch_split_bf16(int head_dim, int warps, int units, const CUtensor
                               const SplitParams* p, cudaStream_t stream);
 cudaError_t launch_split_fp8(int head_dim, int warps, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
                              const SplitParams* p, cudaStream_t stream);
+cudaError_t launch_dyn_plan(const int32_t* ctx, const int32_t* ql, DynWork* out, uint32_t* err, int num_seqs,
+                            int num_q_heads, int num_kv_heads, int bt_stride, int max_len, int max_q, int slots, int tile,
+                            int max_chunk, cudaStream_t stream);
 cudaError_t launch_tc_split(int kv_fp8, int rows_max, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
                             const SplitParams* p, cudaStream_t stream);
 cudaError_t launch_kv_write(int head_dim, int fp8, int n_tokens, int num_kv_heads, int num_pages, const void* k_new,
@@ -44,6 +47,9 @@ struct pa_verify_plan_s {
   int32_t tile = 0, chunk = 0, units = 0, rows_max = 0, warps = 0, max_splits = 0, needs_combine = 0;
   int32_t num_tokens = 0, num_rows = 0;
   int32_t kernel = PA_KERNEL_WARP_MMA;
+  int32_t dynamic = 0;           // capacity plan: the work table is built on the device each run
+  int32_t max_len = 0, max_q = 0, slots = 0;
+  size_t off_dyn = 0, off_part = kWsHeader, off_lse = kWsHeader;  // workspace layout
   int64_t kv_bytes = 0;
   size_t ws_bytes = 0;
   SeqInfo seq[kMaxSeqs];
@@ -104,6 +110,97 @@ int encode_kv_map(CUtensorMap* map, const void* base, const pa_verify_desc& d) {
 int supported_warps(int rows_max) {
   const int w = (rows_max + 15) / 16;
   return w <= 4 ? w : 8;
+}
+
+int check_run_args(pa_verify_plan_t plan, const void* q, const void* k_cache, const void* v_cache,
+                   const float* k_scale, const float* v_scale, const int32_t* block_table,
+                   const int32_t* context_lens, const int32_t* query_lens, float softmax_scale, const void* out) {
+  const bool fp8 = plan->d.kv_dtype == PA_KV_FP8_E4M3;
+  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !query_lens || !out)
+    return fail(PA_ERR_INVALID, "a required pointer is NULL");
+  if (fp8 && (!k_scale || !v_scale)) return fail(PA_ERR_INVALID, "FP8 KV needs k_scale and v_scale");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return fail(PA_ERR_INVALID, "q, k_cache, v_cache and out must be 16-byte aligned");
+  if (fp8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16)))
+    return fail(PA_ERR_INVALID, "k_scale and v_scale must be 16-byte aligned");
+  if (!aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(query_lens, 4))
+    return fail(PA_ERR_INVALID, "int32 arrays must be 4-byte aligned");
+  if (!(std::isfinite(softmax_scale) && softmax_scale > 0.f)) return fail(PA_ERR_INVALID, "softmax_scale must be finite and > 0");
+  return PA_OK;
+}
+
+int encode_maps(pa_verify_plan_t plan, const void* k_cache, const void* v_cache) {
+  if (plan->tm_k != k_cache) {
+    int rc = encode_kv_map(&plan->tmk, k_cache, plan->d);
+    if (rc) return rc;
+    plan->tm_k = k_cache;
+  }
+  if (plan->tm_v != v_cache) {
+    int rc = encode_kv_map(&plan->tmv, v_cache, plan->d);
+    if (rc) return rc;
+    plan->tm_v = v_cache;
+  }
+  return PA_OK;
+}
+
+void fill_params(SplitParams& p, pa_verify_plan_t plan, const void* q, const float* k_scale, const float* v_scale,
+                 const int32_t* block_table, const int32_t* context_lens, const int32_t* query_lens,
+                 float softmax_scale, void* out, uint8_t* ws) {
+  const pa_verify_desc& d = plan->d;
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  p.q = static_cast<const uint16_t*>(q);
+  p.block_table = block_table;
+  p.k_scale = fp8 ? k_scale : nullptr;
+  p.v_scale = fp8 ? v_scale : nullptr;
+  p.out = out;
+  p.err = reinterpret_cast<uint32_t*>(ws);
+  if (plan->needs_combine) {
+    p.part_o = reinterpret_cast<float*>(ws + plan->off_part);
+    p.part_lse = reinterpret_cast<float*>(ws + plan->off_lse);
+  }
+  p.dyn = plan->dynamic ? reinterpret_cast<const DynWork*>(ws + plan->off_dyn) : nullptr;
+  p.dev_ctx = context_lens;
+  p.dev_q = query_lens;
+  p.num_seqs = d.num_seqs;
+  p.num_q_heads = d.num_q_heads;
+  p.num_kv_heads = d.num_kv_heads;
+  p.group = d.num_q_heads / d.num_kv_heads;
+  p.bt_stride = d.block_table_stride;
+  p.num_pages = d.num_pages;
+  p.chunk = plan->chunk;
+  p.num_units = plan->units;
+  p.rows_max = plan->rows_max;
+  p.out_f32 = d.out_dtype == PA_OUT_F32 ? 1 : 0;
+  p.num_rows = plan->num_rows;
+  p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
+  std::memcpy(p.seq, plan->seq, sizeof(plan->seq));
+}
+
+// Enqueues (dynamic plans: the device planner, then) the split kernel and the
+// combine; with `prof`, the plan's events bracket the two kernels.
+cudaError_t launch_all(pa_verify_plan_t plan, SplitParams& p, cudaStream_t s, bool prof) {
+  const pa_verify_desc& d = plan->d;
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  cudaError_t e = cudaSuccess;
+  if (plan->dynamic)
+    e = launch_dyn_plan(p.dev_ctx, p.dev_q, const_cast<DynWork*>(p.dyn), p.err, d.num_seqs, d.num_q_heads,
+                        d.num_kv_heads, d.block_table_stride, plan->max_len, plan->max_q, plan->slots, plan->tile,
+                        kMaxChunk, s);
+  prof = prof && plan->profiling && plan->ev[0];
+  if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[0], s);
+  if (e == cudaSuccess)
+    e = plan->kernel == PA_KERNEL_TCGEN05
+            ? launch_tc_split(fp8 ? 1 : 0, plan->rows_max, plan->units, &plan->tmk, &plan->tmv, &p, s)
+        : fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s)
+              : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s);
+  if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[1], s);
+  if (e == cudaSuccess && plan->needs_combine) e = launch_combine(d.head_dim, &p, s);
+  if (e == cudaSuccess && prof) {
+    e = cudaEventRecord(plan->ev[2], s);
+    plan->profiled_runs++;
+    plan->last_had_combine = plan->needs_combine;
+  }
+  return e;
 }
 
 }  // namespace
@@ -245,7 +342,9 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
   P->kv_bytes = work * per_th;
   size_t ws = kWsHeader;
   if (P->needs_combine) {
+    P->off_part = ws;
     ws += align_up(static_cast<size_t>(unit) * rows_max * d.head_dim * 4, 256);
+    P->off_lse = ws;
     ws += align_up(static_cast<size_t>(unit) * rows_max * 4, 256);
   }
   P->ws_bytes = ws;
@@ -267,6 +366,7 @@ int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info) {
   info->kv_bytes = plan->kv_bytes;
   info->workspace_bytes = plan->ws_bytes;
   info->kernel = plan->kernel;
+  info->dynamic = plan->dynamic;
   return PA_OK;
 }
 
@@ -276,81 +376,21 @@ int pa_verify_run(pa_verify_plan_t plan, const void* q, const void* k_cache, con
                   pa_stream_t stream) {
   g_last_error.clear();
   if (!plan) return fail(PA_ERR_INVALID, "plan must not be NULL");
-  const pa_verify_desc& d = plan->d;
-  if (d.num_seqs == 0) return PA_OK;
-  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
-  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !query_lens || !out || !workspace)
-    return fail(PA_ERR_INVALID, "a required pointer is NULL");
-  if (fp8 && (!k_scale || !v_scale)) return fail(PA_ERR_INVALID, "FP8 KV needs k_scale and v_scale");
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
-    return fail(PA_ERR_INVALID, "q, k_cache, v_cache and out must be 16-byte aligned");
-  if (fp8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16)))
-    return fail(PA_ERR_INVALID, "k_scale and v_scale must be 16-byte aligned");
-  if (!aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(query_lens, 4))
-    return fail(PA_ERR_INVALID, "int32 arrays must be 4-byte aligned");
+  if (plan->d.num_seqs == 0) return PA_OK;
+  int rc = check_run_args(plan, q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens, query_lens,
+                          softmax_scale, out);
+  if (rc) return rc;
+  if (!workspace) return fail(PA_ERR_INVALID, "a required pointer is NULL");
   if (!aligned(workspace, 256)) return fail(PA_ERR_INVALID, "workspace must be 256-byte aligned");
-  if (!(std::isfinite(softmax_scale) && softmax_scale > 0.f)) return fail(PA_ERR_INVALID, "softmax_scale must be finite and > 0");
   if (workspace_bytes < plan->ws_bytes)
     return fail(PA_ERR_WORKSPACE, "workspace of " + std::to_string(workspace_bytes) + " bytes, plan needs " +
                                       std::to_string(plan->ws_bytes));
-
-  if (plan->tm_k != k_cache) {
-    int rc = encode_kv_map(&plan->tmk, k_cache, d);
-    if (rc) return rc;
-    plan->tm_k = k_cache;
-  }
-  if (plan->tm_v != v_cache) {
-    int rc = encode_kv_map(&plan->tmv, v_cache, d);
-    if (rc) return rc;
-    plan->tm_v = v_cache;
-  }
-
-  SplitParams* p = new (std::nothrow) SplitParams();
-  if (!p) return fail(PA_ERR_NOMEM, "out of host memory");
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p->q = static_cast<const uint16_t*>(q);
-  p->block_table = block_table;
-  p->k_scale = fp8 ? k_scale : nullptr;
-  p->v_scale = fp8 ? v_scale : nullptr;
-  p->out = out;
-  p->err = reinterpret_cast<uint32_t*>(ws);
-  if (plan->needs_combine) {
-    p->part_o = reinterpret_cast<float*>(ws + kWsHeader);
-    p->part_lse = reinterpret_cast<float*>(
-        ws + kWsHeader + align_up(static_cast<size_t>(plan->units) * plan->rows_max * d.head_dim * 4, 256));
-  }
-  p->dev_ctx = context_lens;
-  p->dev_q = query_lens;
-  p->num_seqs = d.num_seqs;
-  p->num_q_heads = d.num_q_heads;
-  p->num_kv_heads = d.num_kv_heads;
-  p->group = d.num_q_heads / d.num_kv_heads;
-  p->bt_stride = d.block_table_stride;
-  p->num_pages = d.num_pages;
-  p->chunk = plan->chunk;
-  p->num_units = plan->units;
-  p->rows_max = plan->rows_max;
-  p->out_f32 = d.out_dtype == PA_OUT_F32 ? 1 : 0;
-  p->num_rows = plan->num_rows;
-  p->scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
-  std::memcpy(p->seq, plan->seq, sizeof(plan->seq));
-
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool prof = plan->profiling && plan->ev[0];
-  cudaError_t e = prof ? cudaEventRecord(plan->ev[0], s) : cudaSuccess;
-  if (e == cudaSuccess)
-    e = plan->kernel == PA_KERNEL_TCGEN05
-            ? launch_tc_split(fp8 ? 1 : 0, plan->rows_max, plan->units, &plan->tmk, &plan->tmv, p, s)
-        : fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, p, s)
-              : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, p, s);
-  if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[1], s);
-  if (e == cudaSuccess && plan->needs_combine) e = launch_combine(d.head_dim, p, s);
-  if (e == cudaSuccess && prof) {
-    e = cudaEventRecord(plan->ev[2], s);
-    plan->profiled_runs++;
-    plan->last_had_combine = plan->needs_combine;
-  }
-  delete p;
+  rc = encode_maps(plan, k_cache, v_cache);
+  if (rc) return rc;
+  SplitParams p{};
+  fill_params(p, plan, q, k_scale, v_scale, block_table, context_lens, query_lens, softmax_scale, out,
+              static_cast<uint8_t*>(workspace));
+  cudaError_t e = launch_all(plan, p, reinterpret_cast<cudaStream_t>(stream), true);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
   return PA_OK;
 }
@@ -368,67 +408,21 @@ int enqueue_with_scratch(pa_verify_plan_t plan, const void* q, const void* k_cac
                          uint8_t* scratch, size_t scratch_bytes, cudaStream_t s) {
   g_last_error.clear();
   if (!plan) return fail(PA_ERR_INVALID, "plan must not be NULL");
-  const pa_verify_desc& d = plan->d;
-  if (d.num_seqs == 0) return PA_OK;
-  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
-  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !query_lens || !out || !scratch)
-    return fail(PA_ERR_INVALID, "a required pointer is NULL");
-  if (fp8 && (!k_scale || !v_scale)) return fail(PA_ERR_INVALID, "FP8 KV needs k_scale and v_scale");
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
-    return fail(PA_ERR_INVALID, "q, k_cache, v_cache and out must be 16-byte aligned");
-  if (fp8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16)))
-    return fail(PA_ERR_INVALID, "k_scale and v_scale must be 16-byte aligned");
-  if (!aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(query_lens, 4))
-    return fail(PA_ERR_INVALID, "int32 arrays must be 4-byte aligned");
-  if (!(std::isfinite(softmax_scale) && softmax_scale > 0.f)) return fail(PA_ERR_INVALID, "softmax_scale must be finite and > 0");
+  if (plan->d.num_seqs == 0) return PA_OK;
+  int rc = check_run_args(plan, q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens, query_lens,
+                          softmax_scale, out);
+  if (rc) return rc;
+  if (!scratch) return fail(PA_ERR_INVALID, "a required pointer is NULL");
   if (scratch_bytes < plan->ws_bytes)
     return fail(PA_ERR_WORKSPACE, "this plan needs " + std::to_string(plan->ws_bytes) +
                                       " bytes of scratch; the fixed scratch holds " + std::to_string(scratch_bytes));
-  if (plan->tm_k != k_cache) {
-    int rc = encode_kv_map(&plan->tmk, k_cache, d);
-    if (rc) return rc;
-    plan->tm_k = k_cache;
-  }
-  if (plan->tm_v != v_cache) {
-    int rc = encode_kv_map(&plan->tmv, v_cache, d);
-    if (rc) return rc;
-    plan->tm_v = v_cache;
-  }
+  rc = encode_maps(plan, k_cache, v_cache);
+  if (rc) return rc;
   SplitParams p{};
-  p.q = static_cast<const uint16_t*>(q);
-  p.block_table = block_table;
-  p.k_scale = fp8 ? k_scale : nullptr;
-  p.v_scale = fp8 ? v_scale : nullptr;
-  p.out = out;
-  p.err = reinterpret_cast<uint32_t*>(scratch);
-  if (plan->needs_combine) {
-    p.part_o = reinterpret_cast<float*>(scratch + kWsHeader);
-    p.part_lse = reinterpret_cast<float*>(
-        scratch + kWsHeader + align_up(static_cast<size_t>(plan->units) * plan->rows_max * d.head_dim * 4, 256));
-  }
-  p.dev_ctx = context_lens;
-  p.dev_q = query_lens;
-  p.num_seqs = d.num_seqs;
-  p.num_q_heads = d.num_q_heads;
-  p.num_kv_heads = d.num_kv_heads;
-  p.group = d.num_q_heads / d.num_kv_heads;
-  p.bt_stride = d.block_table_stride;
-  p.num_pages = d.num_pages;
-  p.chunk = plan->chunk;
-  p.num_units = plan->units;
-  p.rows_max = plan->rows_max;
-  p.out_f32 = d.out_dtype == PA_OUT_F32 ? 1 : 0;
-  p.num_rows = plan->num_rows;
-  p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
-  std::memcpy(p.seq, plan->seq, sizeof(plan->seq));
+  fill_params(p, plan, q, k_scale, v_scale, block_table, context_lens, query_lens, softmax_scale, out, scratch);
   // the error word starts each call at zero (the scratch keeps the last call's contents)
   cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);
-  if (e == cudaSuccess)
-    e = plan->kernel == PA_KERNEL_TCGEN05
-            ? launch_tc_split(fp8 ? 1 : 0, plan->rows_max, plan->units, &plan->tmk, &plan->tmv, &p, s)
-        : fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s)
-              : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s);
-  if (e == cudaSuccess && plan->needs_combine) e = launch_combine(d.head_dim, &p, s);
+  if (e == cudaSuccess) e = launch_all(plan, p, s, false);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
   return PA_OK;
 }
@@ -514,6 +508,88 @@ int pa_greedy_verdict(int32_t num_seqs, int32_t num_tokens, int32_t vocab, const
   cudaError_t e = launch_verdict(num_seqs, num_tokens, vocab, logits, input_ids, query_lens, target_ids, accepted,
                                  next_token, workspace, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("verdict launch failed: ") + cudaGetErrorString(e));
+  return PA_OK;
+}
+
+int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, int32_t max_query_len,
+                           pa_verify_plan_t* plan_out, size_t* workspace_bytes_out) {
+  g_last_error.clear();
+  if (plan_out) *plan_out = nullptr;
+  if (!desc || !plan_out || !workspace_bytes_out)
+    return fail(PA_ERR_INVALID, "desc, plan_out and workspace_bytes_out must not be NULL");
+  const pa_verify_desc& d = *desc;
+  if (d.num_seqs < 1) return fail(PA_ERR_INVALID, "a dynamic plan needs num_seqs (the batch capacity) >= 1");
+  if (d.num_seqs > kMaxSeqs) return fail(PA_ERR_UNSUPPORTED, "num_seqs above " + std::to_string(kMaxSeqs));
+  if (d.num_q_heads < 1 || d.num_kv_heads < 1 || d.num_q_heads % d.num_kv_heads != 0)
+    return fail(PA_ERR_INVALID, "need num_q_heads >= 1, num_kv_heads >= 1 and num_q_heads % num_kv_heads == 0");
+  if (d.page_size != kPage) return fail(PA_ERR_UNSUPPORTED, "page_size must be 16");
+  if (d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_FP8_E4M3) return fail(PA_ERR_INVALID, "unknown kv_dtype");
+  if (d.out_dtype != PA_OUT_BF16 && d.out_dtype != PA_OUT_F32) return fail(PA_ERR_INVALID, "unknown out_dtype");
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  if (fp8 ? d.head_dim != 128 : (d.head_dim != 64 && d.head_dim != 128))
+    return fail(PA_ERR_UNSUPPORTED, fp8 ? "FP8 KV needs head_dim 128" : "bf16 KV needs head_dim 64 or 128");
+  if (d.num_pages < 1 || d.block_table_stride < 1) return fail(PA_ERR_INVALID, "num_pages and block_table_stride must be >= 1");
+  if (static_cast<int64_t>(d.num_pages) * d.num_kv_heads * kPage >= (int64_t(1) << 31))
+    return fail(PA_ERR_UNSUPPORTED, "num_pages * num_kv_heads * 16 must stay below 2^31");
+  if (d.split_override != 0) return fail(PA_ERR_INVALID, "split_override is not available for dynamic plans");
+  if (d.sm_count < 0) return fail(PA_ERR_INVALID, "sm_count must be >= 0");
+  if (d.kernel < PA_KERNEL_AUTO || d.kernel > PA_KERNEL_TCGEN05) return fail(PA_ERR_INVALID, "unknown kernel");
+  if (max_query_len < 1 || max_query_len > kMaxQueryLen) return fail(PA_ERR_INVALID, "max_query_len must lie in 1..8");
+  if (max_context_len < max_query_len) return fail(PA_ERR_INVALID, "max_context_len < max_query_len");
+  if ((static_cast<int64_t>(max_context_len) + kPage - 1) / kPage > d.block_table_stride)
+    return fail(PA_ERR_INVALID, "max_context_len needs more pages than block_table_stride");
+  const int G = d.num_q_heads / d.num_kv_heads;
+  const int rows_max = max_query_len * G;
+  if (rows_max > kMaxRows) return fail(PA_ERR_UNSUPPORTED, "max_query_len * group above 128 rows");
+  int sms = d.sm_count;
+  if (sms == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("SM count query failed: ") + cudaGetErrorString(e));
+  }
+  const bool tc_ok = d.head_dim == 128 && rows_max <= 64;
+  if (d.kernel == PA_KERNEL_TCGEN05 && !tc_ok)
+    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs head_dim 128 and q_len * group <= 64");
+  const bool use_tc = d.kernel == PA_KERNEL_TCGEN05 || (d.kernel == PA_KERNEL_AUTO && tc_ok);
+  const int warps = supported_warps(rows_max);
+  const int64_t slots = static_cast<int64_t>(sms) * (use_tc ? 1 : split_ctas_per_sm(warps));
+  const int64_t per_pair = (static_cast<int64_t>(max_context_len) + kMaxChunk - 1) / kMaxChunk;
+  const int64_t units_cap = std::max<int64_t>(slots, static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * per_pair);
+  const int64_t rows_cap = static_cast<int64_t>(d.num_seqs) * max_query_len * d.num_q_heads;
+  if (units_cap >= (int64_t(1) << 31) || rows_cap >= (int64_t(1) << 31))
+    return fail(PA_ERR_UNSUPPORTED, "capacity too large for one call");
+
+  pa_verify_plan_s* P = new (std::nothrow) pa_verify_plan_s();
+  if (!P) return fail(PA_ERR_NOMEM, "out of host memory");
+  P->d = d;
+  P->d.sm_count = sms;
+  P->dynamic = 1;
+  P->max_len = max_context_len;
+  P->max_q = max_query_len;
+  P->slots = static_cast<int32_t>(slots);
+  P->kernel = use_tc ? PA_KERNEL_TCGEN05 : PA_KERNEL_WARP_MMA;
+  P->tile = use_tc ? 128 : tile_tokens(fp8 ? 1 : 0, d.head_dim);
+  P->chunk = 0;  // chosen on the device each run
+  P->units = static_cast<int32_t>(units_cap);
+  P->rows_max = rows_max;
+  P->warps = warps;
+  P->max_splits = static_cast<int32_t>(std::min<int64_t>(units_cap, (max_context_len + P->tile - 1) / P->tile));
+  P->needs_combine = 1;
+  P->num_tokens = d.num_seqs * max_query_len;
+  P->num_rows = static_cast<int32_t>(rows_cap);
+  const int64_t per_th = fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim);
+  P->kv_bytes = static_cast<int64_t>(d.num_seqs) * max_context_len * d.num_kv_heads * per_th;  // at capacity
+  size_t ws = kWsHeader;
+  P->off_dyn = ws;
+  ws += align_up(sizeof(DynWork), 256);
+  P->off_part = ws;
+  ws += align_up(static_cast<size_t>(units_cap) * rows_max * d.head_dim * 4, 256);
+  P->off_lse = ws;
+  ws += align_up(static_cast<size_t>(units_cap) * rows_max * 4, 256);
+  P->ws_bytes = ws;
+  *plan_out = P;
+  *workspace_bytes_out = ws;
   return PA_OK;
 }
 

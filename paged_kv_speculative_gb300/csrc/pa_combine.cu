@@ -23,12 +23,14 @@ __global__ void __launch_bounds__(256) pa_combine_kernel(const __grid_constant__
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
   const int rho = blockIdx.x;
-  int lo = 0, hi = p.num_seqs - 1;
+  const WorkView wv = work_view(p);
+  if (rho >= wv.num_rows) return;  // a dynamic plan's grid covers its capacity
+  int lo = 0, hi = wv.num_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.seq[mid].row_start <= rho) lo = mid; else hi = mid - 1;
+    if (wv.seq[mid].row_start <= rho) lo = mid; else hi = mid - 1;
   }
-  const SeqInfo& si = p.seq[lo];
+  const SeqInfo si = wv.seq[lo];
   const int n = si.n_chunks;
   if (n <= 1) return;
   const int local = rho - si.row_start;

@@ -28,6 +28,16 @@ struct SeqInfo {
   int32_t pad;
 };
 
+// Work description written on the device by the planner kernel of a
+// dynamic (capacity) plan, from the device lengths of the call.
+struct DynWork {
+  int32_t num_units;  // split units of this call
+  int32_t chunk;      // context tokens per unit
+  int32_t num_rows;   // combine rows of this call (sum of q_b * Hq)
+  int32_t num_tokens; // sum of q_b
+  SeqInfo seq[kMaxSeqs];  // live sequences by decreasing length, then padded ones
+};
+
 struct SplitParams {
   const uint16_t* q;            // [T, Hq, D] bf16
   const int32_t* block_table;   // [B, stride]
@@ -51,8 +61,23 @@ struct SplitParams {
   int32_t out_f32;
   int32_t num_rows;             // sum_b q_b * Hq (combine grid)
   float scale_log2;             // softmax_scale * log2(e)
+  const DynWork* dyn;           // dynamic plans: the device-written work table; else null
   SeqInfo seq[kMaxSeqs];
 };
+
+#ifdef __CUDACC__
+// The work table a kernel follows: kernel parameters (plans built from host
+// lengths) or the device planner's output (dynamic plans; grids are sized for
+// the plan's capacity and CTAs past the call's work return at once).
+struct WorkView {
+  const SeqInfo* seq;
+  int num_seqs, chunk, num_units, num_rows;
+};
+__device__ __forceinline__ WorkView work_view(const SplitParams& p) {
+  if (p.dyn) return WorkView{p.dyn->seq, p.num_seqs, p.dyn->chunk, p.dyn->num_units, p.dyn->num_rows};
+  return WorkView{p.seq, p.num_seqs, p.chunk, p.num_units, p.num_rows};
+}
+#endif
 
 // Tile geometry of the split kernel for a KV element size and head dim.
 __host__ __device__ constexpr int row_bytes(int kv_fp8, int d) { return d * (kv_fp8 ? 1 : 2); }

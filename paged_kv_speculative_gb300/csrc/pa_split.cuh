@@ -75,12 +75,14 @@ __global__ void __launch_bounds__(NW * 32)
 
   // ------------------------------------------------------------ the unit
   const int u = blockIdx.x;
-  int lo = 0, hi = p.num_seqs - 1;
+  const WorkView wv = work_view(p);
+  if (u >= wv.num_units) return;  // a dynamic plan's grid covers its capacity
+  int lo = 0, hi = wv.num_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.seq[mid].unit_start <= u) lo = mid; else hi = mid - 1;
+    if (wv.seq[mid].unit_start <= u) lo = mid; else hi = mid - 1;
   }
-  const SeqInfo& si = p.seq[lo];
+  const SeqInfo si = wv.seq[lo];
   const int local = u - si.unit_start;
   const int kvh = local / si.n_chunks;
   const int chunk_idx = local - kvh * si.n_chunks;
@@ -89,8 +91,8 @@ __global__ void __launch_bounds__(NW * 32)
   const int b = si.b;
   const int G = p.group;
   const int rows = QL * G;
-  const int t0 = chunk_idx * p.chunk;
-  const int t_end = min(L, t0 + p.chunk);
+  const int t0 = chunk_idx * wv.chunk;
+  const int t_end = min(L, t0 + wv.chunk);
   const int n_stages = (t_end - t0 + C::kTile - 1) / C::kTile;
   const int n_pages = (t_end - t0 + kPage - 1) / kPage;
   const bool split = si.n_chunks > 1;

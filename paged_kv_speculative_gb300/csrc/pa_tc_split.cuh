@@ -10,9 +10,9 @@
 // with both accumulators in tensor memory.
 //
 // Warp roles (320 threads): warp 0 gathers pages through the block table with
-// 2-D TMA boxes (lane 0 feeds a KS-deep K ring, lane 1 a VS-deep V ring that
-// also carries the FP8 scales); warp 1 allocates tensor memory and issues the
-// MMAs (one thread); warps 2-9 are two softmax warpgroups, one thread per
+// 2-D TMA boxes (one thread feeds a KS-deep K ring and a VS-deep V ring that
+// also carries the FP8 scales, whichever frees first); warp 1 allocates tensor
+// memory and issues the MMAs (one thread, S and PV each as soon as ready); warps 2-9 are two softmax warpgroups, one thread per
 // token of the tile, each group owning half of the row columns. Stages hand
 // over on mbarriers; every wait is bounded.
 //
@@ -43,8 +43,8 @@ struct TcCfg {
   static constexpr int kTile = 128;                          // tokens per K/V tile = MMA M
   static constexpr int kRowB = KV_FP8 ? 128 : 256;           // bytes per token row
   static constexpr int kTileB = kTile * kRowB;               // 16 KB (fp8) / 32 KB (bf16)
-  static constexpr int KS = KV_FP8 ? 4 : 3;                  // K ring depth
-  static constexpr int VS = KV_FP8 ? 3 : 2;                  // V ring depth
+  static constexpr int KS = KV_FP8 ? 5 : 2;                  // K ring depth (a K slot frees once S is done)
+  static constexpr int VS = KV_FP8 ? 5 : 3;                  // V ring depth (a V slot frees only after PV)
   static constexpr int kVStage = kTileB + (KV_FP8 ? 2 * 4 * kTile : 0);  // V data + k/v scales
   static constexpr int kQPlane = 64 * 128;                   // one 128-byte-wide plane of 64 rows
   static constexpr int kQB = 2 * kQPlane;                    // bf16: two 64-column halves; fp8: hi and lo
@@ -121,19 +121,21 @@ __global__ void __launch_bounds__(320, 1)
 
   // ------------------------------------------------------------ the unit
   const int u = blockIdx.x;
-  int lo = 0, hi = p.num_seqs - 1;
+  const WorkView wv = work_view(p);
+  if (u >= wv.num_units) return;  // a dynamic plan's grid covers its capacity
+  int lo = 0, hi = wv.num_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.seq[mid].unit_start <= u) lo = mid; else hi = mid - 1;
+    if (wv.seq[mid].unit_start <= u) lo = mid; else hi = mid - 1;
   }
-  const SeqInfo& si = p.seq[lo];
+  const SeqInfo si = wv.seq[lo];
   const int local = u - si.unit_start;
   const int kvh = local / si.n_chunks;
   const int chunk_idx = local - kvh * si.n_chunks;
   const int L = si.ctx_len, QL = si.q_len, b = si.b, G = p.group;
   const int rows = QL * G;
-  const int t0 = chunk_idx * p.chunk;
-  const int t_end = min(L, t0 + p.chunk);
+  const int t0 = chunk_idx * wv.chunk;
+  const int t_end = min(L, t0 + wv.chunk);
   const int n_tiles = (t_end - t0 + C::kTile - 1) / C::kTile;
   const int n_pages = (t_end - t0 + kPage - 1) / kPage;
   const bool split = si.n_chunks > 1;
@@ -189,31 +191,23 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 0) {
     // ============================================================ producer
-    if (lane < 2) {
-      const bool is_k = lane == 0;
-      const int depth = is_k ? C::KS : C::VS;
-      const CUtensorMap* map = is_k ? &tmk : &tmv;
-      uint64_t* full = is_k ? kfull : vfull;
-      uint64_t* empty = is_k ? kempty : vempty;
-      int issued = 0;
-      for (int k = 0; k < n_tiles && !*abort_flag; ++k) {
-        const int s = k % depth;
-        if (k >= depth && !mbar_wait_bounded(smem_addr(&empty[s]), static_cast<uint32_t>(k / depth - 1) & 1u)) {
-          fail();
-          break;
-        }
-        ++issued;
+    // One thread feeds both rings, issuing whichever slot frees first.
+    if (lane == 0) {
+      auto issue = [&](bool is_k, int k) {
+        const int s = k % (is_k ? C::KS : C::VS);
         uint8_t* dst = is_k ? sK + s * C::kTileB : sV + s * C::kVStage;
+        const CUtensorMap* map = is_k ? &tmk : &tmv;
+        const uint32_t bar = smem_addr(is_k ? &kfull[s] : &vfull[s]);
         const int tok0 = t0 + k * C::kTile;
         const int npg = (min(t_end, tok0 + C::kTile) - tok0 + kPage - 1) / kPage;
         uint32_t bytes = npg * (kPage * C::kRowB);
         if (KV_FP8 && !is_k)
           for (int j = 0; j < npg; ++j)
             if (pids[(tok0 - t0) / kPage + j] >= 0) bytes += 2 * kPage * 4;
-        const uint32_t bar = smem_addr(&full[s]);
         mbar_arrive_expect_tx(bar, bytes);
         for (int j = 0; j < npg; ++j) {
           const int pg = pids[(tok0 - t0) / kPage + j];
+          // an invalid page reads past the tensor's end: TMA fills zeros
           const int row = (pg >= 0 ? pg : p.num_pages) * p.num_kv_heads * kPage + kvh * kPage;
 #pragma unroll
           for (int hf = 0; hf < C::kRowB / 128; ++hf)
@@ -225,77 +219,121 @@ __global__ void __launch_bounds__(320, 1)
             bulk_load(smem_addr(dst + C::kTileB + C::kTile * 4 + j * kPage * 4), p.v_scale + so, kPage * 4, bar);
           }
         }
+      };
+      int kn = 0, vn = 0;
+      uint64_t idle_since = 0;
+      while ((kn < n_tiles || vn < n_tiles) && !*abort_flag) {
+        bool progressed = false;
+        // V first: its slots are held until the tile's PV product completes, so they turn over last
+        if (vn < n_tiles &&
+            (vn < C::VS || mbar_test_wait(smem_addr(&vempty[vn % C::VS]), static_cast<uint32_t>(vn / C::VS - 1) & 1u))) {
+          issue(false, vn++);
+          progressed = true;
+        }
+        if (kn < n_tiles &&
+            (kn < C::KS || mbar_test_wait(smem_addr(&kempty[kn % C::KS]), static_cast<uint32_t>(kn / C::KS - 1) & 1u))) {
+          issue(true, kn++);
+          progressed = true;
+        }
+        if (progressed) {
+          idle_since = 0;
+        } else if (idle_since == 0) {
+          idle_since = global_ns();
+        } else if (global_ns() - idle_since > 1000000000ull) {
+          fail();
+          break;
+        }
       }
-      // No copy may land after the CTA exits: wait (bounded) for the last
-      // copies of each ring slot; only this lane arms these barriers, so the
-      // parity of tile k's phase is exact.
-      for (int k = max(0, issued - depth); k < issued; ++k)
-        (void)mbar_wait_bounded(smem_addr(&full[k % depth]), static_cast<uint32_t>(k / depth) & 1u);
+      // No copy may land after the CTA exits: wait (bounded) for the last copies
+      // of each ring slot; only this thread arms these barriers, so the parity
+      // of tile k's phase is exact.
+      for (int k = max(0, kn - C::KS); k < kn; ++k)
+        (void)mbar_wait_bounded(smem_addr(&kfull[k % C::KS]), static_cast<uint32_t>(k / C::KS) & 1u);
+      for (int k = max(0, vn - C::VS); k < vn; ++k)
+        (void)mbar_wait_bounded(smem_addr(&vfull[k % C::VS]), static_cast<uint32_t>(k / C::VS) & 1u);
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
+    // One thread issues S^T = K Q^T of tile i and O^T += V^T P^T of tile j as
+    // soon as each one's inputs are ready (S runs at most two tiles ahead of
+    // the softmax through the double-buffered score tile).
     if (lane == 0) {
       constexpr uint32_t fa = KV_FP8 ? tc::kE4M3 : tc::kBF16;
       constexpr uint32_t idS = tc::idesc(fa, fa, tc::kKMajor, tc::kKMajor, 128, NP);
       constexpr uint32_t idPV = tc::idesc(fa, fa, tc::kMNMajor, tc::kMNMajor, 128, NP);
       const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aP = smem_addr(sP);
       bool ok = mbar_wait_bounded(smem_addr(qready), 0);
-      auto issue_pv = [&](int j) -> bool {
-        const int vs = j % C::VS, pb = j & 1;
-        if (!mbar_wait_bounded(smem_addr(&vfull[vs]), static_cast<uint32_t>(j / C::VS) & 1u)) return false;
-        if (!mbar_wait_bounded(smem_addr(&pfull[pb]), static_cast<uint32_t>(j >> 1) & 1u)) return false;
-        tc::fence_after_sync();
-        const uint32_t v0 = aV + vs * C::kVStage;
-        const uint32_t p0 = aP + pb * C::kPBuf;
-        if (KV_FP8) {
-          // 4 k-steps of 32 tokens; hi then lo plane of P into the same accumulator
+      if (!ok) fail();
+      int si_ = 0, pj = 0;
+      uint64_t idle_since = 0;
+      while (ok && pj < n_tiles && !*abort_flag) {
+        bool progressed = false;
+        if (pj < si_) {  // PV of tile pj: V tile and P tile in shared memory
+          const int vs = pj % C::VS, pb = pj & 1;
+          if (mbar_test_wait(smem_addr(&vfull[vs]), static_cast<uint32_t>(pj / C::VS) & 1u) &&
+              mbar_test_wait(smem_addr(&pfull[pb]), static_cast<uint32_t>(pj >> 1) & 1u)) {
+            tc::fence_after_sync();
+            const uint32_t v0 = aV + vs * C::kVStage;
+            const uint32_t p0 = aP + pb * C::kPBuf;
+            if (KV_FP8) {
+              // 4 k-steps of 32 tokens; hi then lo plane of P into the same accumulator
 #pragma unroll
-          for (int pl = 0; pl < 2; ++pl)
+              for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc::mma_f8(tO, tc::sdesc(v0 + ks * 4096, 16384, 1024, tc::kSwizzle128B),
-                         tc::sdesc(p0 + pl * C::kPPlane + ks * 2048, 16384, 512, tc::kSwizzle64B), idPV,
-                         (j > 0 || pl > 0 || ks > 0) ? 1u : 0u);
-        } else {
+                for (int ks = 0; ks < 4; ++ks)
+                  tc::mma_f8(tO, tc::sdesc(v0 + ks * 4096, 16384, 1024, tc::kSwizzle128B),
+                             tc::sdesc(p0 + pl * C::kPPlane + ks * 2048, 16384, 512, tc::kSwizzle64B), idPV,
+                             (pj > 0 || pl > 0 || ks > 0) ? 1u : 0u);
+            } else {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc::mma_f16(tO, tc::sdesc(v0 + ks * 2048, C::kTile * 128, 1024, tc::kSwizzle128B),
-                        tc::sdesc(p0 + ks * 2048, 16384, 1024, tc::kSwizzle128B), idPV, (j > 0 || ks > 0) ? 1u : 0u);
+              for (int ks = 0; ks < 8; ++ks)
+                tc::mma_f16(tO, tc::sdesc(v0 + ks * 2048, C::kTile * 128, 1024, tc::kSwizzle128B),
+                            tc::sdesc(p0 + ks * 2048, 16384, 1024, tc::kSwizzle128B), idPV,
+                            (pj > 0 || ks > 0) ? 1u : 0u);
+            }
+            tc::commit(&vempty[vs]);
+            tc::commit(&pfree[pb]);  // also tells the softmax warpgroups that O holds tiles 0..pj
+            ++pj;
+            progressed = true;
+          }
         }
-        tc::commit(&vempty[vs]);
-        tc::commit(&pfree[pb]);  // also tells the softmax warpgroup that O holds tiles 0..j
-        return true;
-      };
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int ks_ = i % C::KS, sb = i & 1;
-        if (!mbar_wait_bounded(smem_addr(&kfull[ks_]), static_cast<uint32_t>(i / C::KS) & 1u)) { ok = false; break; }
-        if (i >= 2 && !mbar_wait_bounded(smem_addr(&sfree[sb]), static_cast<uint32_t>((i >> 1) - 1) & 1u)) {
-          ok = false;
+        if (si_ < n_tiles) {  // S of tile si_: K tile landed, score buffer free
+          const int ks_ = si_ % C::KS, sb = si_ & 1;
+          if (mbar_test_wait(smem_addr(&kfull[ks_]), static_cast<uint32_t>(si_ / C::KS) & 1u) &&
+              (si_ < 2 || mbar_test_wait(smem_addr(&sfree[sb]), static_cast<uint32_t>((si_ >> 1) - 1) & 1u))) {
+            tc::fence_after_sync();
+            const uint32_t k0 = aK + ks_ * C::kTileB;
+            if (KV_FP8) {
+#pragma unroll
+              for (int pl = 0; pl < 2; ++pl)  // Q hi then Q lo
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                  tc::mma_f8(tS[sb], tc::sdesc(k0 + ks * 32, 16, 1024, tc::kSwizzle128B),
+                             tc::sdesc(aQ + pl * C::kQPlane + ks * 32, 16, 1024, tc::kSwizzle128B), idS,
+                             (pl > 0 || ks > 0) ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks)
+                tc::mma_f16(tS[sb],
+                            tc::sdesc(k0 + (ks >> 2) * (C::kTile * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
+                            tc::sdesc(aQ + (ks >> 2) * C::kQPlane + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B), idS,
+                            ks > 0 ? 1u : 0u);
+            }
+            tc::commit(&sfull[sb]);
+            tc::commit(&kempty[ks_]);
+            ++si_;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          idle_since = 0;
+        } else if (idle_since == 0) {
+          idle_since = global_ns();
+        } else if (global_ns() - idle_since > 1000000000ull) {
+          fail();
           break;
         }
-        tc::fence_after_sync();
-        const uint32_t k0 = aK + ks_ * C::kTileB;
-        if (KV_FP8) {
-#pragma unroll
-          for (int pl = 0; pl < 2; ++pl)  // Q hi then Q lo
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc::mma_f8(tS[sb], tc::sdesc(k0 + ks * 32, 16, 1024, tc::kSwizzle128B),
-                         tc::sdesc(aQ + pl * C::kQPlane + ks * 32, 16, 1024, tc::kSwizzle128B), idS,
-                         (pl > 0 || ks > 0) ? 1u : 0u);
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc::mma_f16(tS[sb], tc::sdesc(k0 + (ks >> 2) * (C::kTile * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
-                        tc::sdesc(aQ + (ks >> 2) * C::kQPlane + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B), idS,
-                        ks > 0 ? 1u : 0u);
-        }
-        tc::commit(&sfull[sb]);
-        tc::commit(&kempty[ks_]);
-        if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
       }
-      if (ok && n_tiles > 0) ok = issue_pv(n_tiles - 1);
-      if (!ok) fail();
     }
   } else {
     // ============================================================ softmax warpgroups

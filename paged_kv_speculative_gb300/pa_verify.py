@@ -42,7 +42,7 @@ DEVERR_TIMEOUT = 4
 EXPORTED = ("pa_verify_plan", "pa_verify_plan_get_info", "pa_verify_run", "pa_verify_free",
             "pa_verify_device_errors", "pa_verify_last_error", "pa_verify_profile_enable",
             "pa_verify_profile_read", "pa_kv_write", "pa_greedy_verdict_workspace_bytes",
-            "pa_greedy_verdict", "pa_verify_run_static")
+            "pa_greedy_verdict", "pa_verify_run_static", "pa_verify_plan_dynamic")
 
 
 class PaVerifyError(RuntimeError):
@@ -66,7 +66,7 @@ class PlanInfo(ctypes.Structure):
         ("num_units", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
         ("rows_max", ctypes.c_int32), ("warps", ctypes.c_int32), ("max_splits", ctypes.c_int32),
         ("needs_combine", ctypes.c_int32), ("num_tokens", ctypes.c_int32), ("kv_bytes", ctypes.c_int64),
-        ("workspace_bytes", ctypes.c_size_t), ("kernel", ctypes.c_int32)]
+        ("workspace_bytes", ctypes.c_size_t), ("kernel", ctypes.c_int32), ("dynamic", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -87,6 +87,9 @@ def lib(path: Optional[str] = None):
     vp, sz, i32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int32)
     L.pa_verify_plan.argtypes = [ctypes.POINTER(Desc), i32p, i32p, ctypes.POINTER(vp), ctypes.POINTER(sz)]
     L.pa_verify_plan.restype = ctypes.c_int
+    L.pa_verify_plan_dynamic.argtypes = [ctypes.POINTER(Desc), ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(vp),
+                                         ctypes.POINTER(sz)]
+    L.pa_verify_plan_dynamic.restype = ctypes.c_int
     L.pa_verify_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
     L.pa_verify_plan_get_info.restype = ctypes.c_int
     L.pa_verify_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
@@ -161,6 +164,20 @@ def plan(num_q_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: int, out_
     h = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     _check(lib().pa_verify_plan(ctypes.byref(d), cl, ql, ctypes.byref(h), ctypes.byref(ws)))
+    return Plan(h.value, d, ws.value)
+
+
+def plan_dynamic(num_q_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: int, out_dtype: int, num_pages: int,
+                 block_table_stride: int, capacity: int, max_context_len: int, max_query_len: int,
+                 sm_count: int = 0, kernel: int = KERNEL_AUTO) -> Plan:
+    """pa_verify_plan_dynamic: a capacity plan whose lengths are read on the device each run."""
+    d = Desc(num_seqs=capacity, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim, page_size=16,
+             kv_dtype=kv_dtype, out_dtype=out_dtype, num_pages=num_pages, block_table_stride=block_table_stride,
+             split_override=0, sm_count=sm_count, kernel=kernel)
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    _check(lib().pa_verify_plan_dynamic(ctypes.byref(d), int(max_context_len), int(max_query_len), ctypes.byref(h),
+                                        ctypes.byref(ws)))
     return Plan(h.value, d, ws.value)
 
 
