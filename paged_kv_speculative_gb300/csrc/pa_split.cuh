@@ -120,36 +120,43 @@ __global__ void __launch_bounds__(NW * 32)
   }
   __syncthreads();
 
-  // Stage issue (thread 0 only): pages of tile `k` into ring slot `s`.
+  // Stage issue (warp 0): pages of tile `k` into ring slot `s`. A TMA issue
+  // costs its thread about one memory latency, so each page box and scale
+  // copy gets its own lane: K boxes on lanes 0-7, V boxes on 8-15, FP8 k/v
+  // scales on 16-23 / 24-31 (every tile has at most 8 boxes per tensor).
   auto issue = [&](int k, int s) {
     uint8_t* st = stage_base + s * C::kStage;
     const uint32_t bar = smem_addr(&bars[s]);
     const int tok0 = t0 + k * C::kTile;
-    int npg = (min(t_end, tok0 + C::kTile) - tok0 + kPage - 1) / kPage;
-    uint32_t bytes = npg * (2 * kPage * C::kRowBytes);
-    if (KV_FP8) {
-      for (int j = 0; j < npg; ++j)
-        if (pids[(tok0 - t0) / kPage + j] >= 0) bytes += 2 * kPage * 4;
+    const int pg0 = (tok0 - t0) / kPage;
+    const int npg = (min(t_end, tok0 + C::kTile) - tok0 + kPage - 1) / kPage;
+    if (lane == 0) {
+      uint32_t bytes = npg * (2 * kPage * C::kRowBytes);
+      if (KV_FP8)
+        for (int j = 0; j < npg; ++j)
+          if (pids[pg0 + j] >= 0) bytes += 2 * kPage * 4;
+      mbar_arrive_expect_tx(bar, bytes);
     }
-    mbar_arrive_expect_tx(bar, bytes);
-    for (int j = 0; j < npg; ++j) {
-      const int pg = pids[(tok0 - t0) / kPage + j];
+    __syncwarp();
+    const int grp = lane >> 3, idx = lane & 7;  // grp 0: K, 1: V, 2: k scales, 3: v scales
+    if (grp < 2 && idx < npg * C::kHalves) {
+      const int j = idx / C::kHalves, hf = idx % C::kHalves;
+      const int pg = pids[pg0 + j];
       // an invalid page reads past the tensor's end: TMA fills zeros
       const int row = (pg >= 0 ? pg : p.num_pages) * p.num_kv_heads * kPage + kvh * kPage;
-#pragma unroll
-      for (int hf = 0; hf < C::kHalves; ++hf) {
-        const uint32_t off = hf * (C::kTile * 128) + j * kPage * 128;
-        tma_load_2d(smem_addr(st + off), &tmk, bar, hf * (128 / (KV_FP8 ? 1 : 2)), row);
-        tma_load_2d(smem_addr(st + C::kKBytes + off), &tmv, bar, hf * (128 / (KV_FP8 ? 1 : 2)), row);
-      }
-      if (KV_FP8 && pg >= 0) {
+      const uint32_t off = hf * (C::kTile * 128) + j * kPage * 128 + (grp ? C::kKBytes : 0);
+      tma_load_2d(smem_addr(st + off), grp ? &tmv : &tmk, bar, hf * (128 / (KV_FP8 ? 1 : 2)), row);
+    }
+    if (KV_FP8 && grp >= 2 && idx < npg) {
+      const int pg = pids[pg0 + idx];
+      if (pg >= 0) {
         const size_t so = (static_cast<size_t>(pg) * p.num_kv_heads + kvh) * kPage;
-        bulk_load(smem_addr(st + 2 * C::kKBytes + j * kPage * 4), p.k_scale + so, kPage * 4, bar);
-        bulk_load(smem_addr(st + 2 * C::kKBytes + C::kTile * 4 + j * kPage * 4), p.v_scale + so, kPage * 4, bar);
+        bulk_load(smem_addr(st + 2 * C::kKBytes + (grp == 3 ? C::kTile * 4 : 0) + idx * kPage * 4),
+                  (grp == 2 ? p.k_scale : p.v_scale) + so, kPage * 4, bar);
       }
     }
   };
-  if (tid == 0) {
+  if (warp == 0) {
     for (int s = 0; s < min(kStages, n_stages); ++s) issue(s, s);
   }
 
@@ -455,7 +462,7 @@ __global__ void __launch_bounds__(NW * 32)
       aborted = true;
       break;
     }
-    if (tid == 0 && it + kStages < n_stages) {
+    if (warp == 0 && it + kStages < n_stages) {
       fence_proxy_async();
       issue(it + kStages, s);
     }

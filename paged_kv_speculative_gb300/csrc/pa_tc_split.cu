@@ -15,7 +15,7 @@ static cudaError_t run_tc(int units, const CUtensorMap* tmk, const CUtensorMap* 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<units, 320, smem, stream>>>(*tmk, *tmv, *p);
+  kern<<<units, 352, smem, stream>>>(*tmk, *tmv, *p);
   return cudaGetLastError();
 }
 

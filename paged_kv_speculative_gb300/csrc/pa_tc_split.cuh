@@ -9,9 +9,9 @@
 //   O^T[d, r]   += V[:, d]^T . P^T[:, r]          (A = V tile, MN-major; B = P, MN-major)
 // with both accumulators in tensor memory.
 //
-// Warp roles (320 threads): warp 0 gathers pages through the block table with
-// 2-D TMA boxes (one thread feeds a KS-deep K ring and a VS-deep V ring that
-// also carries the FP8 scales, whichever frees first); warp 1 allocates tensor
+// Warp roles (352 threads): warps 0 and 10 gather pages through the block
+// table with 2-D TMA boxes into a KS-deep K ring and a VS-deep V ring (which
+// also carries the FP8 scales), one lane per box; warp 1 allocates tensor
 // memory and issues the MMAs (one thread, S and PV each as soon as ready); warps 2-9 are two softmax warpgroups, one thread per
 // token of the tile, each group owning half of the row columns. Stages hand
 // over on mbarriers; every wait is bounded.
@@ -89,7 +89,7 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 }
 
 template <int KV_FP8, int NP>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     pa_tc_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ SplitParams p) {
   using C = TcCfg<KV_FP8, NP>;
@@ -189,69 +189,69 @@ __global__ void __launch_bounds__(320, 1)
     atomicOr(p.err, 4u);
   };
 
-  if (warp == 0) {
-    // ============================================================ producer
-    // One thread feeds both rings, issuing whichever slot frees first.
-    if (lane == 0) {
-      auto issue = [&](bool is_k, int k) {
-        const int s = k % (is_k ? C::KS : C::VS);
-        uint8_t* dst = is_k ? sK + s * C::kTileB : sV + s * C::kVStage;
-        const CUtensorMap* map = is_k ? &tmk : &tmv;
-        const uint32_t bar = smem_addr(is_k ? &kfull[s] : &vfull[s]);
-        const int tok0 = t0 + k * C::kTile;
-        const int npg = (min(t_end, tok0 + C::kTile) - tok0 + kPage - 1) / kPage;
-        uint32_t bytes = npg * (kPage * C::kRowB);
-        if (KV_FP8 && !is_k)
-          for (int j = 0; j < npg; ++j)
-            if (pids[(tok0 - t0) / kPage + j] >= 0) bytes += 2 * kPage * 4;
-        mbar_arrive_expect_tx(bar, bytes);
-        for (int j = 0; j < npg; ++j) {
-          const int pg = pids[(tok0 - t0) / kPage + j];
-          // an invalid page reads past the tensor's end: TMA fills zeros
-          const int row = (pg >= 0 ? pg : p.num_pages) * p.num_kv_heads * kPage + kvh * kPage;
-#pragma unroll
-          for (int hf = 0; hf < C::kRowB / 128; ++hf)
-            tma_load_2d(smem_addr(dst + hf * (C::kTile * 128) + j * kPage * 128), map, bar,
-                        hf * (KV_FP8 ? 128 : 64), row);
-          if (KV_FP8 && !is_k && pg >= 0) {
-            const size_t so = (static_cast<size_t>(pg) * p.num_kv_heads + kvh) * kPage;
-            bulk_load(smem_addr(dst + C::kTileB + j * kPage * 4), p.k_scale + so, kPage * 4, bar);
-            bulk_load(smem_addr(dst + C::kTileB + C::kTile * 4 + j * kPage * 4), p.v_scale + so, kPage * 4, bar);
-          }
-        }
-      };
-      int kn = 0, vn = 0;
-      uint64_t idle_since = 0;
-      while ((kn < n_tiles || vn < n_tiles) && !*abort_flag) {
-        bool progressed = false;
-        // V first: its slots are held until the tile's PV product completes, so they turn over last
-        if (vn < n_tiles &&
-            (vn < C::VS || mbar_test_wait(smem_addr(&vempty[vn % C::VS]), static_cast<uint32_t>(vn / C::VS - 1) & 1u))) {
-          issue(false, vn++);
-          progressed = true;
-        }
-        if (kn < n_tiles &&
-            (kn < C::KS || mbar_test_wait(smem_addr(&kempty[kn % C::KS]), static_cast<uint32_t>(kn / C::KS - 1) & 1u))) {
-          issue(true, kn++);
-          progressed = true;
-        }
-        if (progressed) {
-          idle_since = 0;
-        } else if (idle_since == 0) {
-          idle_since = global_ns();
-        } else if (global_ns() - idle_since > 1000000000ull) {
-          fail();
+  if (warp == 0 || warp == 10) {
+    // ============================================================ producers
+    // Warp 0 feeds the K ring, warp 10 the V ring (with the FP8 scales). A
+    // TMA issue costs its thread about one memory latency, so every page box
+    // (and scale copy) of a tile gets its own lane: lane 0 arms the stage's
+    // byte count, then the lanes issue together.
+    const bool is_k = warp == 0;
+    const int depth = is_k ? C::KS : C::VS;
+    const CUtensorMap* map = is_k ? &tmk : &tmv;
+    uint64_t* full = is_k ? kfull : vfull;
+    uint64_t* empty = is_k ? kempty : vempty;
+    constexpr int kHalves = C::kRowB / 128;
+    int issued = 0;
+    for (int k = 0; k < n_tiles && !*abort_flag; ++k) {
+      const int s = k % depth;
+      if (k >= depth) {
+        // lane 0 waits; the verdict is the same for every lane (no lane is left at a warp sync)
+        bool ok = lane != 0 || mbar_wait_bounded(smem_addr(&empty[s]), static_cast<uint32_t>(k / depth - 1) & 1u);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          if (lane == 0) fail();
           break;
         }
       }
-      // No copy may land after the CTA exits: wait (bounded) for the last copies
-      // of each ring slot; only this thread arms these barriers, so the parity
-      // of tile k's phase is exact.
-      for (int k = max(0, kn - C::KS); k < kn; ++k)
-        (void)mbar_wait_bounded(smem_addr(&kfull[k % C::KS]), static_cast<uint32_t>(k / C::KS) & 1u);
-      for (int k = max(0, vn - C::VS); k < vn; ++k)
-        (void)mbar_wait_bounded(smem_addr(&vfull[k % C::VS]), static_cast<uint32_t>(k / C::VS) & 1u);
+      uint8_t* dst = is_k ? sK + s * C::kTileB : sV + s * C::kVStage;
+      const uint32_t bar = smem_addr(&full[s]);
+      const int tok0 = t0 + k * C::kTile;
+      const int pg0 = (tok0 - t0) / kPage;
+      const int npg = (min(t_end, tok0 + C::kTile) - tok0 + kPage - 1) / kPage;
+      if (lane == 0) {
+        uint32_t bytes = npg * (kPage * C::kRowB);
+        if (KV_FP8 && !is_k)
+          for (int j = 0; j < npg; ++j)
+            if (pids[pg0 + j] >= 0) bytes += 2 * kPage * 4;
+        mbar_arrive_expect_tx(bar, bytes);
+      }
+      __syncwarp();
+      // lanes [0, npg * halves): page boxes; FP8 V: lanes 16 + j (k scales), 24 + j (v scales)
+      if (lane < npg * kHalves) {
+        const int j = lane / kHalves, hf = lane % kHalves;
+        const int pg = pids[pg0 + j];
+        // an invalid page reads past the tensor's end: TMA fills zeros
+        const int row = (pg >= 0 ? pg : p.num_pages) * p.num_kv_heads * kPage + kvh * kPage;
+        tma_load_2d(smem_addr(dst + hf * (C::kTile * 128) + j * kPage * 128), map, bar, hf * (KV_FP8 ? 128 : 64), row);
+      }
+      if (KV_FP8 && !is_k && lane >= 16 && (lane & 7) < npg) {
+        const int j = lane & 7;
+        const int pg = pids[pg0 + j];
+        if (pg >= 0) {
+          const size_t so = (static_cast<size_t>(pg) * p.num_kv_heads + kvh) * kPage;
+          const bool ksc = lane < 24;
+          bulk_load(smem_addr(dst + C::kTileB + (ksc ? 0 : C::kTile * 4) + j * kPage * 4),
+                    (ksc ? p.k_scale : p.v_scale) + so, kPage * 4, bar);
+        }
+      }
+      ++issued;
     }
+    // No copy may land after the CTA exits: wait (bounded) for the last
+    // copies of each ring slot; only this warp arms these barriers, so the
+    // parity of tile k's phase is exact.
+    if (lane == 0)
+      for (int k = max(0, issued - depth); k < issued; ++k)
+        (void)mbar_wait_bounded(smem_addr(&full[k % depth]), static_cast<uint32_t>(k / depth) & 1u);
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     // One thread issues S^T = K Q^T of tile i and O^T += V^T P^T of tile j as
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-  } else {
+  } else if (warp >= 2 && warp <= 9) {
     // ============================================================ softmax warpgroups
     // Two warpgroups (warps 2-5 and 6-9). Each covers the 128 tokens of a tile
     // (one per thread, = tensor-memory lane) for its own NH = NP/2 columns
