@@ -205,16 +205,33 @@ def run_reference(args):
     return 0
 
 
+class L2Flush:
+    """Evicts the call's inputs from L2 between steps, outside the timed events:
+    writes one 256 MiB buffer (> 129 MB L2), then reads another, so the timed
+    call starts with L2 holding clean lines only, as under ncu's cache control
+    (with dirty lines left behind, their write-back would compete with the
+    call's reads)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
 def _timed(fn, steps, warmup, flush, dev):
     import torch
     stream = torch.cuda.current_stream(dev)
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         fn()
     torch.cuda.synchronize(dev)
     ms = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         fn()
@@ -232,7 +249,7 @@ def run_side_op(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     _build.build()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     g = torch.Generator(device="cpu").manual_seed(7)
     peaks, _ = load_peaks()
     peak, peak_note = hbm_peak(peaks)
@@ -269,7 +286,7 @@ def run_side_op(args):
             "warmup": args.warmup, "ms_per_step": mean, "us_per_call": 1e3 * mean, "higher_is_better": True,
             "dtype": "bf16 in", "data": "synthetic",
             "config": {"workload": workload, "bytes_per_call": nbytes,
-                       "l2": "flushed between steps (256 MiB write, outside the events)"},
+                       "l2": "flushed between steps (256 MiB write, then 256 MiB read: L2 left clean; outside the events)"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "peak_source": peak_note},
             "gpu_launches": args.steps * launches}
@@ -318,7 +335,7 @@ def main():
         if world > 1:
             dist.barrier()
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MiB > 129 MB L2
+    flush = L2Flush(dev)
 
     def measure(name, steps, warmup, seed_offset):
         ctx, ql, hq, hkv, d, kvd, seed = synth.config_lengths(name)
@@ -333,7 +350,7 @@ def main():
         out = va.new_out()
         stream = torch.cuda.current_stream(dev)
         for _ in range(warmup):
-            flush.zero_()
+            flush()
             va(*dv, prob.softmax_scale, out=out)
         torch.cuda.synchronize(dev)
         # timed steps: events only around the call, nothing recorded inside it
@@ -342,7 +359,7 @@ def main():
         torch.cuda.synchronize(dev)
         wall0 = time.perf_counter()
         for k in range(steps):
-            flush.zero_()
+            flush()
             evs[k][0].record(stream)
             va(*dv, prob.softmax_scale, out=out)
             evs[k][1].record(stream)
@@ -354,7 +371,7 @@ def main():
         pv.profile_enable(va.plan, True)
         split_ms, comb_ms = [], []
         for k in range(steps):
-            flush.zero_()
+            flush()
             va(*dv, prob.softmax_scale, out=out)
             a, c = pv.profile_read(va.plan)
             split_ms.append(a)
@@ -388,7 +405,7 @@ def main():
     stream = torch.cuda.current_stream(dev)
     e2e_ms = []
     for k in range(args.e2e_steps + 2):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for dst, src in zip(dv, host.args()):
@@ -432,7 +449,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if prob.kv_dtype == 0 else "fp8-e4m3 KV, bf16 q",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC[args.config], "name": args.config,
-                   "kv_bytes_per_call": kv_bytes_rank, "l2": "flushed between steps (256 MiB write, outside the events)",
+                   "kv_bytes_per_call": kv_bytes_rank, "l2": "flushed between steps (256 MiB write, then 256 MiB read: L2 left clean; outside the events)",
                    "units": info["num_units"], "chunk_tokens": info["chunk_tokens"], "splits_max": info["max_splits"],
                    "kernel": "tcgen05" if info["kernel"] == pv.KERNEL_TCGEN05 else "warp-mma",
                    "parallelism": f"replicas x{world}"},

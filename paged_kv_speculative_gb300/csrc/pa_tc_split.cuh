@@ -254,86 +254,80 @@ __global__ void __launch_bounds__(352, 1)
         (void)mbar_wait_bounded(smem_addr(&full[k % depth]), static_cast<uint32_t>(k / depth) & 1u);
   } else if (warp == 1) {
     // ============================================================ MMA issuer
-    // One thread issues S^T = K Q^T of tile i and O^T += V^T P^T of tile j as
-    // soon as each one's inputs are ready (S runs at most two tiles ahead of
-    // the softmax through the double-buffered score tile).
+    // One thread issues S^T = K Q^T of tile i and O^T += V^T P^T of tile j in
+    // the fixed order S0 S1 | S2 PV0 | S3 PV1 | ...: S(j+2) needs only that the
+    // softmax has read S(j) (early in its tile) while PV(j) needs its finished
+    // P, so each wait is on the event due first and the thread sleeps in
+    // hardware (try_wait) instead of polling.
     if (lane == 0) {
       constexpr uint32_t fa = KV_FP8 ? tc::kE4M3 : tc::kBF16;
       constexpr uint32_t idS = tc::idesc(fa, fa, tc::kKMajor, tc::kKMajor, 128, NP);
       constexpr uint32_t idPV = tc::idesc(fa, fa, tc::kMNMajor, tc::kMNMajor, 128, NP);
       const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aP = smem_addr(sP);
+      auto issue_s = [&](int i) -> bool {
+        const int ks_ = i % C::KS, sb = i & 1;
+        if (!mbar_wait_bounded(smem_addr(&kfull[ks_]), static_cast<uint32_t>(i / C::KS) & 1u)) return false;
+        if (i >= 2 && !mbar_wait_bounded(smem_addr(&sfree[sb]), static_cast<uint32_t>((i >> 1) - 1) & 1u))
+          return false;
+        tc::fence_after_sync();
+        const uint32_t k0 = aK + ks_ * C::kTileB;
+        if (KV_FP8) {
+#pragma unroll
+          for (int pl = 0; pl < 2; ++pl)  // Q hi then Q lo
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc::mma_f8(tS[sb], tc::sdesc(k0 + ks * 32, 16, 1024, tc::kSwizzle128B),
+                         tc::sdesc(aQ + pl * C::kQPlane + ks * 32, 16, 1024, tc::kSwizzle128B), idS,
+                         (pl > 0 || ks > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_f16(tS[sb], tc::sdesc(k0 + (ks >> 2) * (C::kTile * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
+                        tc::sdesc(aQ + (ks >> 2) * C::kQPlane + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B), idS,
+                        ks > 0 ? 1u : 0u);
+        }
+        tc::commit(&sfull[sb]);
+        tc::commit(&kempty[ks_]);
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int vs = j % C::VS, pb = j & 1;
+        if (!mbar_wait_bounded(smem_addr(&vfull[vs]), static_cast<uint32_t>(j / C::VS) & 1u)) return false;
+        if (!mbar_wait_bounded(smem_addr(&pfull[pb]), static_cast<uint32_t>(j >> 1) & 1u)) return false;
+        tc::fence_after_sync();
+        const uint32_t v0 = aV + vs * C::kVStage;
+        const uint32_t p0 = aP + pb * C::kPBuf;
+        // only the k-steps holding tokens of the unit: rows past them may be stale or never loaded
+        const int nv = min(C::kTile, t_end - (t0 + j * C::kTile));
+        if (KV_FP8) {
+          const int nks = (nv + 31) >> 5;  // 32 tokens per k-step; hi then lo plane of P
+#pragma unroll
+          for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              if (ks < nks)
+                tc::mma_f8(tO, tc::sdesc(v0 + ks * 4096, 16384, 1024, tc::kSwizzle128B),
+                           tc::sdesc(p0 + pl * C::kPPlane + ks * 2048, 16384, 512, tc::kSwizzle64B), idPV,
+                           (j > 0 || pl > 0 || ks > 0) ? 1u : 0u);
+        } else {
+          const int nks = (nv + 15) >> 4;  // 16 tokens per k-step
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            if (ks < nks)
+              tc::mma_f16(tO, tc::sdesc(v0 + ks * 2048, C::kTile * 128, 1024, tc::kSwizzle128B),
+                          tc::sdesc(p0 + ks * 2048, 16384, 1024, tc::kSwizzle128B), idPV, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc::commit(&vempty[vs]);
+        tc::commit(&pfree[pb]);  // also tells the softmax warpgroups that O holds tiles 0..j
+        return true;
+      };
       bool ok = mbar_wait_bounded(smem_addr(qready), 0);
-      if (!ok) fail();
-      int si_ = 0, pj = 0;
-      uint64_t idle_since = 0;
-      while (ok && pj < n_tiles && !*abort_flag) {
-        bool progressed = false;
-        if (pj < si_) {  // PV of tile pj: V tile and P tile in shared memory
-          const int vs = pj % C::VS, pb = pj & 1;
-          if (mbar_test_wait(smem_addr(&vfull[vs]), static_cast<uint32_t>(pj / C::VS) & 1u) &&
-              mbar_test_wait(smem_addr(&pfull[pb]), static_cast<uint32_t>(pj >> 1) & 1u)) {
-            tc::fence_after_sync();
-            const uint32_t v0 = aV + vs * C::kVStage;
-            const uint32_t p0 = aP + pb * C::kPBuf;
-            if (KV_FP8) {
-              // 4 k-steps of 32 tokens; hi then lo plane of P into the same accumulator
-#pragma unroll
-              for (int pl = 0; pl < 2; ++pl)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                  tc::mma_f8(tO, tc::sdesc(v0 + ks * 4096, 16384, 1024, tc::kSwizzle128B),
-                             tc::sdesc(p0 + pl * C::kPPlane + ks * 2048, 16384, 512, tc::kSwizzle64B), idPV,
-                             (pj > 0 || pl > 0 || ks > 0) ? 1u : 0u);
-            } else {
-#pragma unroll
-              for (int ks = 0; ks < 8; ++ks)
-                tc::mma_f16(tO, tc::sdesc(v0 + ks * 2048, C::kTile * 128, 1024, tc::kSwizzle128B),
-                            tc::sdesc(p0 + ks * 2048, 16384, 1024, tc::kSwizzle128B), idPV,
-                            (pj > 0 || ks > 0) ? 1u : 0u);
-            }
-            tc::commit(&vempty[vs]);
-            tc::commit(&pfree[pb]);  // also tells the softmax warpgroups that O holds tiles 0..pj
-            ++pj;
-            progressed = true;
-          }
-        }
-        if (si_ < n_tiles) {  // S of tile si_: K tile landed, score buffer free
-          const int ks_ = si_ % C::KS, sb = si_ & 1;
-          if (mbar_test_wait(smem_addr(&kfull[ks_]), static_cast<uint32_t>(si_ / C::KS) & 1u) &&
-              (si_ < 2 || mbar_test_wait(smem_addr(&sfree[sb]), static_cast<uint32_t>((si_ >> 1) - 1) & 1u))) {
-            tc::fence_after_sync();
-            const uint32_t k0 = aK + ks_ * C::kTileB;
-            if (KV_FP8) {
-#pragma unroll
-              for (int pl = 0; pl < 2; ++pl)  // Q hi then Q lo
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                  tc::mma_f8(tS[sb], tc::sdesc(k0 + ks * 32, 16, 1024, tc::kSwizzle128B),
-                             tc::sdesc(aQ + pl * C::kQPlane + ks * 32, 16, 1024, tc::kSwizzle128B), idS,
-                             (pl > 0 || ks > 0) ? 1u : 0u);
-            } else {
-#pragma unroll
-              for (int ks = 0; ks < 8; ++ks)
-                tc::mma_f16(tS[sb],
-                            tc::sdesc(k0 + (ks >> 2) * (C::kTile * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
-                            tc::sdesc(aQ + (ks >> 2) * C::kQPlane + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B), idS,
-                            ks > 0 ? 1u : 0u);
-            }
-            tc::commit(&sfull[sb]);
-            tc::commit(&kempty[ks_]);
-            ++si_;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          idle_since = 0;
-        } else if (idle_since == 0) {
-          idle_since = global_ns();
-        } else if (global_ns() - idle_since > 1000000000ull) {
-          fail();
-          break;
-        }
+      for (int i = 0; ok && i < min(2, n_tiles); ++i) ok = issue_s(i);
+      for (int j = 0; ok && j < n_tiles && !*abort_flag; ++j) {
+        if (j + 2 < n_tiles) ok = issue_s(j + 2);
+        if (ok) ok = issue_pv(j);
       }
+      if (!ok) fail();
     }
   } else if (warp >= 2 && warp <= 9) {
     // ============================================================ softmax warpgroups
@@ -394,12 +388,13 @@ __global__ void __launch_bounds__(352, 1)
     if (lane == 0) mbar_arrive(qready);
     named_sync(5, 256);  // both groups' rows staged (rowC complete)
 
-    float mref[NH], crow[NH], l[NH];  // reference max, score multiplier, row-sum partial per owned column
+    // per owned column pair: minus the reference max, score multiplier (FP8), row-sum partial
+    float2 negm[NH / 2], crow2[NH / 2], l[NH / 2];
 #pragma unroll
-    for (int c = 0; c < NH; ++c) {
-      mref[c] = -INFINITY;
-      crow[c] = rowC[col0 + c];
-      l[c] = 0.f;
+    for (int c = 0; c < NH / 2; ++c) {
+      negm[c] = make_float2(INFINITY, INFINITY);
+      crow2[c] = make_float2(rowC[col0 + 2 * c], rowC[col0 + 2 * c + 1]);
+      l[c] = make_float2(0.f, 0.f);
     }
     const int lim_first = L - QL;  // last key every real row sees
 
@@ -415,66 +410,66 @@ __global__ void __launch_bounds__(352, 1)
     };
     for (int i = 0; i < n_tiles; ++i) {
       const int sb = i & 1;
+      const bool last = i == n_tiles - 1;
       wait(&sfull[sb], static_cast<uint32_t>(i >> 1) & 1u);
       tc::fence_after_sync();
-      float y[NH];
+      float2 y[NH / 2];  // scores of the owned columns, in pairs (packed f32x2 arithmetic)
+      {
+        uint32_t r[NH];
 #pragma unroll
-      for (int c0 = 0; c0 < NH; c0 += 8) {
-        uint32_t r8[8];
-        tc::ld8(tS[sb] + lane_off + col0 + c0, r8);
+        for (int c0 = 0; c0 < NH; c0 += 8) tc::ld8(tS[sb] + lane_off + col0 + c0, *reinterpret_cast<uint32_t(*)[8]>(r + c0));
         tc::wait_ld();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) y[c0 + j] = __uint_as_float(r8[j]);
+        for (int c = 0; c < NH / 2; ++c) y[c] = make_float2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
       }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[sb]);
 
       const int tabs = t0 + i * C::kTile + tok;
-      float inv_sv = 1.f;
-      // every tile's V phase is observed in order (a skipped phase would make a later parity wait ambiguous)
       const int vs = i % C::VS;
-      wait(&vfull[vs], static_cast<uint32_t>(i / C::VS) & 1u);
-      if (wg == 0 && tabs >= t_end) {
-        // this token lies past the unit: its V row holds stale ring data or a last page's unused slots
-        // (possibly NaN), and P = 0 times NaN would still poison O, so the row becomes zeros
-#pragma unroll
-        for (int hf = 0; hf < C::kRowB / 128; ++hf) {
-          uint4* z = reinterpret_cast<uint4*>(sV + vs * C::kVStage + hf * (C::kTile * 128) + tok * 128);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) z[k] = make_uint4(0, 0, 0, 0);
-        }
-      }
+      float inv_sv = 1.f;
       if (KV_FP8) {
+        // the tile's scales ride in its V stage: every tile's V phase is observed in order
+        wait(&vfull[vs], static_cast<uint32_t>(i / C::VS) & 1u);
         const float* sc = reinterpret_cast<const float*>(sV + vs * C::kVStage + C::kTileB);
         float sk = sc[tok], sv = sc[C::kTile + tok];
         if (tabs >= t_end) { sk = 0.f; sv = 1.f; }
         sv = fmaxf(sv, 7.888609052210118e-31f);  // 2^-100 floor keeps log2 and 1/x finite
-        const float ls = __log2f(sv);
+        const float2 ls = make_float2(__log2f(sv), __log2f(sv));
         inv_sv = __frcp_rn(sv);
+        const float2 sk2 = make_float2(sk, sk);
 #pragma unroll
-        for (int c = 0; c < NH; ++c) y[c] = fmaf(y[c] * sk, crow[c], ls);
+        for (int c = 0; c < NH / 2; ++c) y[c] = __ffma2_rn(__fmul2_rn(y[c], sk2), crow2[c], ls);
       } else {
+        const float2 s2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-        for (int c = 0; c < NH; ++c) y[c] *= p.scale_log2;
+        for (int c = 0; c < NH / 2; ++c) y[c] = __fmul2_rn(y[c], s2);
       }
       // causal mask inside the drafts / unit end / padding rows
       if (tabs >= t_end) {
 #pragma unroll
-        for (int c = 0; c < NH; ++c) y[c] = -INFINITY;
+        for (int c = 0; c < NH / 2; ++c) y[c] = make_float2(-INFINITY, -INFINITY);
       } else if (tabs > lim_first) {
 #pragma unroll
-        for (int c = 0; c < NH; ++c)
-          if (tabs > rowLim[col0 + c]) y[c] = -INFINITY;
+        for (int c = 0; c < NH / 2; ++c) {
+          if (tabs > rowLim[col0 + 2 * c]) y[c].x = -INFINITY;
+          if (tabs > rowLim[col0 + 2 * c + 1]) y[c].y = -INFINITY;
+        }
       }
-      bool exceed = false;
+      // d = y - M (log2 units); with M = -inf a finite score gives +inf (and a masked one NaN, dropped below)
+      float2 dl[NH / 2];
+      float dmax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < NH; ++c) exceed |= y[c] > mref[c] + 8.f;
-      if (named_or(bar_or, 128, exceed)) {
+      for (int c = 0; c < NH / 2; ++c) {
+        dl[c] = __fadd2_rn(y[c], negm[c]);
+        dmax = fmaxf(dmax, fmaxf(dl[c].x, dl[c].y));
+      }
+      if (named_or(bar_or, 128, dmax > 8.f)) {
         // ---- exact tile maxima of the owned columns, raise the references, rescale l and O
 #pragma unroll
         for (int c = 0; c < NH; ++c) {
-          float m = y[c];
+          float m = (c & 1) ? y[c >> 1].y : y[c >> 1].x;
 #pragma unroll
           for (int k = 16; k >= 1; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
           if (lane == 0) red[(warp - 2) * 64 + col0 + c] = m;
@@ -482,13 +477,15 @@ __global__ void __launch_bounds__(352, 1)
         named_sync(bar_sync, 128);
         const float* rg = red + wg * 4 * 64 + col0;  // this group's 4 warp rows
         auto new_max = [&](int c) {
-          return fmaxf(mref[c], fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
+          const float mo = (c & 1) ? -negm[c >> 1].y : -negm[c >> 1].x;
+          return fmaxf(mo, fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
         };
+        auto old_max = [&](int c) { return (c & 1) ? -negm[c >> 1].y : -negm[c >> 1].x; };
         bool any_scale = false;
 #pragma unroll
         for (int c = 0; c < NH; ++c) {
           const float mn = new_max(c);
-          any_scale |= (mn != -INFINITY && mn != mref[c]);
+          any_scale |= (mn != -INFINITY && mn != old_max(c));
         }
         if (any_scale && i > 0) {
           wait(&pfree[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u);  // PV of tile i-1 done
@@ -500,8 +497,8 @@ __global__ void __launch_bounds__(352, 1)
             tc::wait_ld();
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float mn = new_max(c0 + j);
-              const float a = (mn == -INFINITY || mn == mref[c0 + j]) ? 1.f : fast_exp2(mref[c0 + j] - mn);
+              const float mn = new_max(c0 + j), mo = old_max(c0 + j);
+              const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
               r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
             }
             tc::st8(tO + lane_off + col0 + c0, r8);
@@ -510,45 +507,68 @@ __global__ void __launch_bounds__(352, 1)
         }
 #pragma unroll
         for (int c = 0; c < NH; ++c) {
-          const float mn = new_max(c);
-          if (mn != -INFINITY && mn != mref[c]) {
-            l[c] *= fast_exp2(mref[c] - mn);
-            mref[c] = mn;
+          const float mn = new_max(c), mo = old_max(c);
+          if (mn != -INFINITY && mn != mo) {
+            float& lc = (c & 1) ? l[c >> 1].y : l[c >> 1].x;
+            lc *= fast_exp2(mo - mn);
+            if (c & 1) negm[c >> 1].y = -mn; else negm[c >> 1].x = -mn;
           }
         }
+#pragma unroll
+        for (int c = 0; c < NH / 2; ++c) dl[c] = __fadd2_rn(y[c], negm[c]);
         // red is rewritten only after the next vote (a barrier of this group), when every read here is done
       }
       // ---- P = 2^(y - M) (<= 2^8), row sums, P into shared memory as the MMA's B operand
       const int pb = i & 1;
       if (i >= 2) wait(&pfree[pb], static_cast<uint32_t>((i >> 1) - 1) & 1u);
+      if (last) {
+        // Rows past the unit inside the last MMA k-step (a page's unused slots, or a page never loaded)
+        // may hold anything, and P = 0 times NaN would still poison O: they become zeros. bf16 looks at
+        // its V ring only here; PV(i-2) done implies every earlier phase of this slot completed.
+        if (!KV_FP8) wait(&vfull[vs], static_cast<uint32_t>(i / C::VS) & 1u);
+        const int nv = t_end - (t0 + i * C::kTile);
+        const int kend = KV_FP8 ? ((nv + 31) & ~31) : ((nv + 15) & ~15);
+        if (wg == 0 && tok >= nv && tok < kend) {
+#pragma unroll
+          for (int hf = 0; hf < C::kRowB / 128; ++hf) {
+            uint4* z = reinterpret_cast<uint4*>(sV + vs * C::kVStage + hf * (C::kTile * 128) + tok * 128);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) z[k] = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
       uint8_t* prow = sP + pb * C::kPBuf;
+      const float2 iv2 = make_float2(inv_sv, inv_sv);
 #pragma unroll
       for (int c0 = 0; c0 < NH; c0 += 8) {
-        float pv[8];
+        float2 pv[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          pv[j] = (y[c0 + j] == -INFINITY) ? 0.f : fast_exp2(y[c0 + j] - mref[c0 + j]);
-          l[c0 + j] = fmaf(pv[j], inv_sv, l[c0 + j]);
+        for (int j = 0; j < 4; ++j) {
+          const float2 d = dl[c0 / 2 + j];
+          // exp2 of max(d, -200): a masked score (-inf, or NaN against M = -inf) gives 0 after flush-to-zero
+          pv[j] = make_float2(fast_exp2(fmaxf(d.x, -200.f)), fast_exp2(fmaxf(d.y, -200.f)));
+          l[c0 / 2 + j] = __ffma2_rn(pv[j], iv2, l[c0 / 2 + j]);
         }
         const int cg = col0 + c0;  // first global column of these 8
         if (!KV_FP8) {
           uint4 w;
-          w.x = pack_bf16(pv[0], pv[1]);
-          w.y = pack_bf16(pv[2], pv[3]);
-          w.z = pack_bf16(pv[4], pv[5]);
-          w.w = pack_bf16(pv[6], pv[7]);
+          w.x = pack_bf16(pv[0].x, pv[0].y);
+          w.y = pack_bf16(pv[1].x, pv[1].y);
+          w.z = pack_bf16(pv[2].x, pv[2].y);
+          w.w = pack_bf16(pv[3].x, pv[3].y);
           const int ch = cg >> 3;  // 16-byte chunk of the 128-byte token row
           *reinterpret_cast<uint4*>(prow + tok * 128 + ((ch ^ (tok & 7)) << 4)) = w;
         } else {
           uint32_t hw0 = 0, hw1 = 0, lw0 = 0, lw1 = 0;
 #pragma unroll
-          for (int j = 0; j < 8; j += 2) {
-            const float a = pv[j], c = pv[j + 1];
-            const float ah = __uint_as_float(__float_as_uint(a) & 0xFFF00000u);
-            const float ch2 = __uint_as_float(__float_as_uint(c) & 0xFFF00000u);
-            const uint32_t hb = e4m3x2(ah, ch2), lb = e4m3x2(a - ah, c - ch2);
-            if (j < 4) { hw0 |= hb << (8 * j); lw0 |= lb << (8 * j); }
-            else { hw1 |= hb << (8 * (j - 4)); lw1 |= lb << (8 * (j - 4)); }
+          for (int j = 0; j < 4; ++j) {
+            const float2 a = pv[j];
+            const float2 ah = make_float2(__uint_as_float(__float_as_uint(a.x) & 0xFFF00000u),
+                                          __uint_as_float(__float_as_uint(a.y) & 0xFFF00000u));  // 3 mantissa bits
+            const float2 al = __ffma2_rn(ah, make_float2(-1.f, -1.f), a);                      // exact remainder
+            const uint32_t hb = e4m3x2(ah.x, ah.y), lb = e4m3x2(al.x, al.y);
+            if (j < 2) { hw0 |= hb << (16 * j); lw0 |= lb << (16 * j); }
+            else { hw1 |= hb << (16 * (j - 2)); lw1 |= lb << (16 * (j - 2)); }
           }
           // 8 bytes at byte cg of the 64-byte token row (64B swizzle: chunk ^= (tok/2)%4)
           const int ch = cg >> 4;
@@ -570,7 +590,10 @@ __global__ void __launch_bounds__(352, 1)
     float* lred = reinterpret_cast<float*>(sK);
     float* rtot = red + 8 * 64;  // row totals, after the 8 warp rows of maxima
 #pragma unroll
-    for (int c = 0; c < NH; ++c) lred[(col0 + c) * 128 + tok] = l[c];
+    for (int c = 0; c < NH / 2; ++c) {
+      lred[(col0 + 2 * c) * 128 + tok] = l[c].x;
+      lred[(col0 + 2 * c + 1) * 128 + tok] = l[c].y;
+    }
     named_sync(bar_sync, 128);
     if (gt < NH) {
       float s2 = 0.f;
@@ -578,8 +601,10 @@ __global__ void __launch_bounds__(352, 1)
       rtot[col0 + gt] = s2;
       float mg = -INFINITY;  // this column's reference max (registers hold every column's)
 #pragma unroll
-      for (int c = 0; c < NH; ++c)
-        if (c == gt) mg = mref[c];
+      for (int c = 0; c < NH / 2; ++c) {
+        if (2 * c == gt) mg = -negm[c].x;
+        if (2 * c + 1 == gt) mg = -negm[c].y;
+      }
       if (ok && split && col0 + gt < rows)
         p.part_lse[static_cast<size_t>(u) * p.rows_max + col0 + gt] = s2 > 0.f ? mg + __log2f(s2) : -INFINITY;
     }
