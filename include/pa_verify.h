@@ -89,19 +89,29 @@ typedef struct {
 
 enum { PA_KERNEL_AUTO = 0, PA_KERNEL_WARP_MMA = 1, PA_KERNEL_TCGEN05 = 2 };
 
+/*
+ * Two plan kinds. Chunk plans (warp-MMA kernel): one CTA per (sequence, KV
+ * head, chunk of chunk_tokens). Flat plans (tcgen05 kernel): the (sequence,
+ * KV head) pairs laid end to end as 128-token tiles and every CTA given the
+ * same number of consecutive tiles (chunk_tokens / 128 of them), so one
+ * wave ends together whatever the length mix.
+ */
 typedef struct {
-  int32_t num_units;       /* CTAs of the split kernel: sum_b Hkv * ceil(L_b / chunk) */
+  int32_t num_units;       /* CTAs of the split kernel: chunk plans sum_b Hkv * ceil(L_b / chunk),
+                              flat plans ceil(total_tiles / (chunk_tokens / 128)) */
   int32_t chunk_tokens;    /* context tokens per unit (a multiple of tile_tokens) */
-  int32_t tile_tokens;     /* tokens per shared-memory stage */
+  int32_t tile_tokens;     /* tokens per shared-memory stage (flat plans: 128) */
   int32_t rows_max;        /* max_b q_b * G */
-  int32_t warps;           /* compute warps per CTA = ceil(rows_max / 16) */
-  int32_t max_splits;      /* max_b ceil(L_b / chunk) */
+  int32_t warps;           /* compute warps per CTA = ceil(rows_max / 16) (warp-MMA kernel) */
+  int32_t max_splits;      /* most units one (sequence, KV head) is spread over */
   int32_t needs_combine;   /* 1 when some (sequence, KV head) has more than one unit */
   int32_t num_tokens;      /* T = sum_b q_b */
   int64_t kv_bytes;        /* algorithmic K/V(+scale) bytes one run reads */
   size_t workspace_bytes;  /* bytes pa_verify_run needs in `workspace` */
   int32_t kernel;          /* PA_KERNEL_WARP_MMA or PA_KERNEL_TCGEN05 */
   int32_t dynamic;         /* 1 for pa_verify_plan_dynamic plans (figures above are capacities) */
+  int32_t flat;            /* 1 for flat plans */
+  int32_t total_tiles;     /* flat plans: sum_b Hkv * ceil(L_b / 128) (dynamic plans: chosen per run, 0 here) */
 } pa_verify_plan_info;
 
 /*

@@ -26,7 +26,7 @@ cudaError_t launch_split_bf16(int head_dim, int warps, int units, const CUtensor
                               const SplitParams* p, cudaStream_t stream);
 cudaError_t launch_split_fp8(int head_dim, int warps, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
                              const SplitParams* p, cudaStream_t stream);
-cudaError_t launch_dyn_plan(const int32_t* ctx, const int32_t* ql, DynWork* out, uint32_t* err, int num_seqs,
+cudaError_t launch_dyn_plan(const int32_t* ctx, const int32_t* ql, DynWork* out, uint32_t* err, int flat, int num_seqs,
                             int num_q_heads, int num_kv_heads, int bt_stride, int max_len, int max_q, int slots, int tile,
                             int max_chunk, cudaStream_t stream);
 cudaError_t launch_tc_split(int kv_fp8, int rows_max, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
@@ -48,6 +48,8 @@ struct pa_verify_plan_s {
   int32_t num_tokens = 0, num_rows = 0;
   int32_t kernel = PA_KERNEL_WARP_MMA;
   int32_t dynamic = 0;           // capacity plan: the work table is built on the device each run
+  int32_t flat = 0, per = 0, total_tiles = 0;  // flat plans (tcgen05 kernel): tiles per CTA, tiles in all
+  int64_t part_units = 0;        // partial slots in the workspace
   int32_t max_len = 0, max_q = 0, slots = 0;
   size_t off_dyn = 0, off_part = kWsHeader, off_lse = kWsHeader;  // workspace layout
   int64_t kv_bytes = 0;
@@ -172,6 +174,9 @@ void fill_params(SplitParams& p, pa_verify_plan_t plan, const void* q, const flo
   p.rows_max = plan->rows_max;
   p.out_f32 = d.out_dtype == PA_OUT_F32 ? 1 : 0;
   p.num_rows = plan->num_rows;
+  p.flat = plan->flat;
+  p.per = plan->per;
+  p.total_tiles = plan->total_tiles;
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
   std::memcpy(p.seq, plan->seq, sizeof(plan->seq));
 }
@@ -183,7 +188,7 @@ cudaError_t launch_all(pa_verify_plan_t plan, SplitParams& p, cudaStream_t s, bo
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
   cudaError_t e = cudaSuccess;
   if (plan->dynamic)
-    e = launch_dyn_plan(p.dev_ctx, p.dev_q, const_cast<DynWork*>(p.dyn), p.err, d.num_seqs, d.num_q_heads,
+    e = launch_dyn_plan(p.dev_ctx, p.dev_q, const_cast<DynWork*>(p.dyn), p.err, plan->flat, d.num_seqs, d.num_q_heads,
                         d.num_kv_heads, d.block_table_stride, plan->max_len, plan->max_q, plan->slots, plan->tile,
                         kMaxChunk, s);
   prof = prof && plan->profiling && plan->ev[0];
@@ -201,6 +206,88 @@ cudaError_t launch_all(pa_verify_plan_t plan, SplitParams& p, cudaStream_t s, bo
     plan->last_had_combine = plan->needs_combine;
   }
   return e;
+}
+
+// Flat plan of the tcgen05 kernel: the (sequence, KV head) pairs laid end to
+// end as 128-token tiles, longest sequences first, and every CTA the same
+// number of consecutive tiles, so one wave of CTAs finishes together whatever
+// the length mix. (`split_override` = n asks for ceil(longest pair / n) tiles
+// per CTA instead.)
+int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, const int32_t* ql, int sms,
+              pa_verify_plan_t* plan_out, size_t* workspace_bytes_out) {
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  const int G = d.num_q_heads / d.num_kv_heads, Hkv = d.num_kv_heads;
+  std::vector<int> order(d.num_seqs);
+  for (int b = 0; b < d.num_seqs; ++b) order[b] = b;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int c) { return ctx[a] > ctx[c]; });
+  std::vector<int32_t> q_off(d.num_seqs);
+  int32_t acc = 0;
+  for (int b = 0; b < d.num_seqs; ++b) {
+    q_off[b] = acc;
+    acc += ql[b];
+  }
+  int64_t tiles = 0, row = 0, work = 0, max_nt = 0, total_tokens = 0;
+  int rows_max = 0;
+  for (int k = 0; k < d.num_seqs; ++k) {
+    const int b = order[k];
+    SeqInfo& s = P->seq[k];
+    s.ctx_len = ctx[b];
+    s.q_len = ql[b];
+    s.q_off = q_off[b];
+    s.unit_start = 0;
+    s.row_start = static_cast<int32_t>(row);
+    s.n_chunks = 0;
+    s.b = b;
+    s.tile_start = static_cast<int32_t>(std::min<int64_t>(tiles, INT32_MAX));
+    s.n_tiles = (s.ctx_len + kFlatTile - 1) / kFlatTile;
+    s.pad = 0;
+    tiles += static_cast<int64_t>(s.n_tiles) * Hkv;
+    row += static_cast<int64_t>(s.q_len) * d.num_q_heads;
+    work += static_cast<int64_t>(s.ctx_len) * Hkv;
+    max_nt = std::max<int64_t>(max_nt, s.n_tiles);
+    rows_max = std::max(rows_max, s.q_len * G);
+    total_tokens += s.q_len;
+  }
+  if (tiles >= (int64_t(1) << 31) || row >= (int64_t(1) << 31)) {
+    delete P;
+    return fail(PA_ERR_UNSUPPORTED, "work too large for one call");
+  }
+  int64_t per = d.split_override > 0 ? (max_nt + d.split_override - 1) / d.split_override : (tiles + sms - 1) / sms;
+  per = std::max<int64_t>(per, 1);
+  const int64_t n_cta = (tiles + per - 1) / per;
+  int max_splits = 0;
+  for (int k = 0; k < d.num_seqs; ++k)
+    for (int g = 0; g < Hkv; ++g) {
+      const int64_t t0 = P->seq[k].tile_start + static_cast<int64_t>(g) * P->seq[k].n_tiles;
+      const int64_t t1 = t0 + P->seq[k].n_tiles - 1;
+      max_splits = std::max<int>(max_splits, static_cast<int>(t1 / per - t0 / per + 1));
+    }
+  P->kernel = PA_KERNEL_TCGEN05;
+  P->flat = 1;
+  P->tile = kFlatTile;
+  P->per = static_cast<int32_t>(per);
+  P->total_tiles = static_cast<int32_t>(tiles);
+  P->chunk = static_cast<int32_t>(std::min<int64_t>(per * kFlatTile, INT32_MAX));
+  P->units = static_cast<int32_t>(n_cta);
+  P->rows_max = rows_max;
+  P->warps = supported_warps(rows_max);
+  P->max_splits = max_splits;
+  P->needs_combine = max_splits > 1 ? 1 : 0;
+  P->num_tokens = static_cast<int32_t>(total_tokens);
+  P->num_rows = static_cast<int32_t>(row);
+  P->part_units = n_cta + static_cast<int64_t>(d.num_seqs) * Hkv;  // slot c + p < CTAs + pairs
+  P->kv_bytes = work * (fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim));
+  size_t ws = kWsHeader;
+  if (P->needs_combine) {
+    P->off_part = ws;
+    ws += align_up(static_cast<size_t>(P->part_units) * rows_max * d.head_dim * 4, 256);
+    P->off_lse = ws;
+    ws += align_up(static_cast<size_t>(P->part_units) * rows_max * 4, 256);
+  }
+  P->ws_bytes = ws;
+  *plan_out = P;
+  *workspace_bytes_out = ws;
+  return PA_OK;
 }
 
 }  // namespace
@@ -282,6 +369,7 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
     for (int b = 0; b < d.num_seqs; ++b) u += (context_lens_host[b] + c - 1) / c;
     return u * d.num_kv_heads;
   };
+  if (use_tc) return plan_flat(P, d, context_lens_host, query_lens_host, sms, plan_out, workspace_bytes_out);
   const int64_t max_tile_len = align_up(static_cast<size_t>(max_len), static_cast<size_t>(tile));
   int64_t chunk;
   if (d.split_override > 0) {
@@ -338,6 +426,7 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
   P->needs_combine = max_splits > 1 ? 1 : 0;
   P->num_tokens = static_cast<int32_t>(total_tokens);
   P->num_rows = static_cast<int32_t>(row);
+  P->part_units = unit;
   const int64_t per_th = fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim);
   P->kv_bytes = work * per_th;
   size_t ws = kWsHeader;
@@ -367,6 +456,8 @@ int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info) {
   info->workspace_bytes = plan->ws_bytes;
   info->kernel = plan->kernel;
   info->dynamic = plan->dynamic;
+  info->flat = plan->flat;
+  info->total_tiles = plan->dynamic ? 0 : plan->total_tiles;
   return PA_OK;
 }
 
@@ -555,7 +646,10 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
   const int warps = supported_warps(rows_max);
   const int64_t slots = static_cast<int64_t>(sms) * (use_tc ? 1 : split_ctas_per_sm(warps));
   const int64_t per_pair = (static_cast<int64_t>(max_context_len) + kMaxChunk - 1) / kMaxChunk;
-  const int64_t units_cap = std::max<int64_t>(slots, static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * per_pair);
+  const int64_t units_cap =
+      use_tc ? slots : std::max<int64_t>(slots, static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * per_pair);
+  // partial slots: a flat plan's CTA c writes pair p's partial at c + p
+  const int64_t part_cap = use_tc ? units_cap + static_cast<int64_t>(d.num_seqs) * d.num_kv_heads : units_cap;
   const int64_t rows_cap = static_cast<int64_t>(d.num_seqs) * max_query_len * d.num_q_heads;
   if (units_cap >= (int64_t(1) << 31) || rows_cap >= (int64_t(1) << 31))
     return fail(PA_ERR_UNSUPPORTED, "capacity too large for one call");
@@ -569,7 +663,8 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
   P->max_q = max_query_len;
   P->slots = static_cast<int32_t>(slots);
   P->kernel = use_tc ? PA_KERNEL_TCGEN05 : PA_KERNEL_WARP_MMA;
-  P->tile = use_tc ? 128 : tile_tokens(fp8 ? 1 : 0, d.head_dim);
+  P->flat = use_tc ? 1 : 0;  // flat: one CTA per SM, the tiles per CTA chosen on the device
+  P->tile = use_tc ? kFlatTile : tile_tokens(fp8 ? 1 : 0, d.head_dim);
   P->chunk = 0;  // chosen on the device each run
   P->units = static_cast<int32_t>(units_cap);
   P->rows_max = rows_max;
@@ -580,13 +675,14 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
   P->num_rows = static_cast<int32_t>(rows_cap);
   const int64_t per_th = fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim);
   P->kv_bytes = static_cast<int64_t>(d.num_seqs) * max_context_len * d.num_kv_heads * per_th;  // at capacity
+  P->part_units = part_cap;
   size_t ws = kWsHeader;
   P->off_dyn = ws;
   ws += align_up(sizeof(DynWork), 256);
   P->off_part = ws;
-  ws += align_up(static_cast<size_t>(units_cap) * rows_max * d.head_dim * 4, 256);
+  ws += align_up(static_cast<size_t>(part_cap) * rows_max * d.head_dim * 4, 256);
   P->off_lse = ws;
-  ws += align_up(static_cast<size_t>(units_cap) * rows_max * 4, 256);
+  ws += align_up(static_cast<size_t>(part_cap) * rows_max * 4, 256);
   P->ws_bytes = ws;
   *plan_out = P;
   *workspace_bytes_out = ws;

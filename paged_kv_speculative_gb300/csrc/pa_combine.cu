@@ -31,15 +31,26 @@ __global__ void __launch_bounds__(256) pa_combine_kernel(const __grid_constant__
     if (wv.seq[mid].row_start <= rho) lo = mid; else hi = mid - 1;
   }
   const SeqInfo si = wv.seq[lo];
-  const int n = si.n_chunks;
-  if (n <= 1) return;
   const int local = rho - si.row_start;
   const int i = local / p.num_q_heads;
   const int h = local - i * p.num_q_heads;
   const int G = p.group;
   const int kvh = h / G;
   const int r = i * G + (h - kvh * G);
-  const size_t u0 = static_cast<size_t>(si.unit_start) + static_cast<size_t>(kvh) * n;
+  int n;
+  size_t u0;
+  if (p.flat) {
+    // pair (lo, kvh) covers tiles [t0, t0 + n_tiles); CTA c wrote its piece at slot c + pair
+    const int pair = lo * p.num_kv_heads + kvh;
+    const int t0 = si.tile_start + kvh * si.n_tiles;
+    const int c0 = t0 / wv.per;
+    n = (t0 + si.n_tiles - 1) / wv.per - c0 + 1;
+    u0 = static_cast<size_t>(c0) + pair;
+  } else {
+    n = si.n_chunks;
+    u0 = static_cast<size_t>(si.unit_start) + static_cast<size_t>(kvh) * n;
+  }
+  if (n <= 1) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float* lse_base = p.part_lse + u0 * p.rows_max + r;
   const float* o_base = p.part_o + (u0 * p.rows_max + r) * D + lane * kPer;

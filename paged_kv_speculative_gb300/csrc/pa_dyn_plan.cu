@@ -5,9 +5,11 @@
 // unit and no output row, so they write nothing (stores masked by row
 // liveness: DeepSeek-V4.1 page, description of the in-place KV stores).
 //
-// Same rules as the host planner: the chunk is the smallest multiple of the
-// staging tile whose unit count fits `slots` (one wave), capped at the
-// page-id staging limit; sequences are scheduled longest first.
+// Same rules as the host planner. Chunk plans: the chunk is the smallest
+// multiple of the staging tile whose unit count fits `slots` (one wave),
+// capped at the page-id staging limit. Flat plans: the pairs' 128-token tiles
+// end to end, ceil(tiles / slots) of them per CTA. Sequences are scheduled
+// longest first.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,11 +22,12 @@ struct DynPlanArgs {
   const int32_t* ql;   // [B] device query lengths (0 = padding)
   DynWork* out;
   uint32_t* err;
+  int32_t flat;
   int32_t num_seqs, num_q_heads, num_kv_heads, bt_stride, max_len, max_q, slots, tile, max_chunk;
 };
 
 __global__ void __launch_bounds__(64) pa_dyn_plan_kernel(DynPlanArgs a) {
-  __shared__ int s_len[kMaxSeqs], s_q[kMaxSeqs], s_rank_units[kMaxSeqs], s_rank_rows[kMaxSeqs];
+  __shared__ int s_len[kMaxSeqs], s_q[kMaxSeqs], s_rank_units[kMaxSeqs], s_rank_rows[kMaxSeqs], s_rank_tiles[kMaxSeqs];
   __shared__ int s_red[2];
   __shared__ long long s_red64[2];
   const int b = threadIdx.x;
@@ -64,7 +67,7 @@ __global__ void __launch_bounds__(64) pa_dyn_plan_kernel(DynPlanArgs a) {
   auto units_for = [&](long long c) { return sum64(L > 0 ? (L + c - 1) / c : 0) * a.num_kv_heads; };
 
   int chunk = a.tile;
-  if (max_l > 0) {
+  if (max_l > 0 && !a.flat) {
     const long long m_hi = (max_l + a.tile - 1) / a.tile;
     long long m_lo = (work + static_cast<long long>(a.slots) * a.tile - 1) / (static_cast<long long>(a.slots) * a.tile);
     m_lo = max(1LL, min(m_lo, m_hi));
@@ -76,7 +79,8 @@ __global__ void __launch_bounds__(64) pa_dyn_plan_kernel(DynPlanArgs a) {
     }
     chunk = static_cast<int>(min(lo * a.tile, static_cast<long long>(a.max_chunk)));
   }
-  const int n_chunks = L > 0 ? (L + chunk - 1) / chunk : 0;
+  const int n_chunks = a.flat ? 0 : (L > 0 ? (L + chunk - 1) / chunk : 0);
+  const int n_tiles = (L + kFlatTile - 1) / kFlatTile;  // 0 for padding
 
   // rank: live sequences by decreasing length (ties by index), then padding by index
   int rank = 0;
@@ -96,13 +100,15 @@ __global__ void __launch_bounds__(64) pa_dyn_plan_kernel(DynPlanArgs a) {
   if (live) {
     s_rank_units[rank] = n_chunks * a.num_kv_heads;
     s_rank_rows[rank] = q * a.num_q_heads;
+    s_rank_tiles[rank] = n_tiles * a.num_kv_heads;
   }
   __syncthreads();
   if (live) {
-    int us = 0, rs = 0;
+    int us = 0, rs = 0, ts = 0;
     for (int r = 0; r < rank; ++r) {
       us += s_rank_units[r];
       rs += s_rank_rows[r];
+      ts += s_rank_tiles[r];
     }
     SeqInfo si;
     si.ctx_len = L;
@@ -112,25 +118,36 @@ __global__ void __launch_bounds__(64) pa_dyn_plan_kernel(DynPlanArgs a) {
     si.row_start = rs;
     si.n_chunks = n_chunks;
     si.b = b;
+    si.tile_start = ts;
+    si.n_tiles = n_tiles;
     si.pad = 0;
     a.out->seq[rank] = si;
   }
   const long long total_units = sum64(static_cast<long long>(n_chunks) * a.num_kv_heads);
   const long long total_rows = sum64(static_cast<long long>(q) * a.num_q_heads);
   const long long total_tokens = sum64(q);
+  const long long total_tiles = sum64(static_cast<long long>(n_tiles) * a.num_kv_heads);
   if (b == 0) {
-    a.out->num_units = static_cast<int>(total_units);
-    a.out->chunk = chunk;
+    long long per = 1, n_cta = 0;
+    if (total_tiles > 0) {
+      per = (total_tiles + a.slots - 1) / a.slots;
+      n_cta = (total_tiles + per - 1) / per;  // <= slots, the grid of a flat plan
+    }
+    a.out->num_units = a.flat ? static_cast<int>(n_cta) : static_cast<int>(total_units);
+    a.out->per = static_cast<int>(per);
+    a.out->total_tiles = static_cast<int>(total_tiles);
+    a.out->chunk = a.flat ? kFlatTile : chunk;
     a.out->num_rows = static_cast<int>(total_rows);
     a.out->num_tokens = static_cast<int>(total_tokens);
   }
   (void)n_live;
 }
 
-cudaError_t launch_dyn_plan(const int32_t* ctx, const int32_t* ql, DynWork* out, uint32_t* err, int num_seqs,
+cudaError_t launch_dyn_plan(const int32_t* ctx, const int32_t* ql, DynWork* out, uint32_t* err, int flat, int num_seqs,
                             int num_q_heads, int num_kv_heads, int bt_stride, int max_len, int max_q, int slots, int tile,
                             int max_chunk, cudaStream_t stream) {
-  DynPlanArgs a{ctx, ql, out, err, num_seqs, num_q_heads, num_kv_heads, bt_stride, max_len, max_q, slots, tile, max_chunk};
+  DynPlanArgs a{ctx, ql, out, err, flat, num_seqs, num_q_heads, num_kv_heads, bt_stride, max_len, max_q, slots, tile,
+                max_chunk};
   pa_dyn_plan_kernel<<<1, 64, 0, stream>>>(a);
   return cudaGetLastError();
 }

@@ -15,26 +15,42 @@ constexpr int kMaxRows = 128;     // q_len * group rows per (sequence, KV head)
 constexpr int kMaxQueryLen = 8;
 constexpr int kWsHeader = 256;    // workspace bytes before the partials (device error word at offset 0)
 
+constexpr int kFlatTile = 128;   // tokens per tile of a flat plan
+
 // Per-sequence entry of the work description, sorted by decreasing context
 // length so that the longest units are scheduled first.
+//
+// Two kinds of plan share it. A chunk plan (warp-MMA kernel) gives every
+// (sequence, KV head, chunk) its own CTA. A flat plan (tcgen05 kernel) lays
+// the (sequence, KV head) pairs end to end as 128-token tiles, pair p =
+// k * Hkv + g for the k-th entry and head g, and hands every CTA the same
+// number of consecutive tiles (`per`): CTA c works through the pieces
+// ("segments") of the pairs its range [c * per, (c + 1) * per) touches. The
+// partial of pair p made by CTA c sits at slot c + p, which is unique and
+// increases along the tiles, so the slots of one pair are consecutive.
 struct SeqInfo {
   int32_t ctx_len;     // L_b
   int32_t q_len;       // q_b
   int32_t q_off;       // first row of sequence b in q / out (batch order)
-  int32_t unit_start;  // first work unit of this sequence (units: kv head major, then chunk)
+  int32_t unit_start;  // chunk plans: first work unit of this sequence (units: kv head major, then chunk)
   int32_t row_start;   // first combine row of this sequence (q_len * Hq rows)
-  int32_t n_chunks;    // ceil(L_b / chunk)
+  int32_t n_chunks;    // chunk plans: ceil(L_b / chunk)
   int32_t b;           // index of the sequence in the caller's batch
+  int32_t tile_start;  // flat plans: first tile of head 0 (head g starts at tile_start + g * n_tiles)
+  int32_t n_tiles;     // flat plans: ceil(L_b / 128) tiles per KV head (0 for a padded sequence)
   int32_t pad;
 };
 
 // Work description written on the device by the planner kernel of a
 // dynamic (capacity) plan, from the device lengths of the call.
 struct DynWork {
-  int32_t num_units;  // split units of this call
-  int32_t chunk;      // context tokens per unit
+  int32_t num_units;  // split units (flat plans: CTAs with work) of this call
+  int32_t chunk;      // context tokens per unit (flat plans: 128)
   int32_t num_rows;   // combine rows of this call (sum of q_b * Hq)
   int32_t num_tokens; // sum of q_b
+  int32_t per;        // flat plans: tiles per CTA
+  int32_t total_tiles;
+  int32_t pad[2];
   SeqInfo seq[kMaxSeqs];  // live sequences by decreasing length, then padded ones
 };
 
@@ -60,6 +76,9 @@ struct SplitParams {
   int32_t rows_max;
   int32_t out_f32;
   int32_t num_rows;             // sum_b q_b * Hq (combine grid)
+  int32_t flat;                 // 1: flat plan (tiles per CTA), 0: chunk plan
+  int32_t per;                  // flat plans: tiles per CTA
+  int32_t total_tiles;          // flat plans: tiles of every pair
   float scale_log2;             // softmax_scale * log2(e)
   const DynWork* dyn;           // dynamic plans: the device-written work table; else null
   SeqInfo seq[kMaxSeqs];
@@ -71,11 +90,22 @@ struct SplitParams {
 // the plan's capacity and CTAs past the call's work return at once).
 struct WorkView {
   const SeqInfo* seq;
-  int num_seqs, chunk, num_units, num_rows;
+  int num_seqs, chunk, num_units, num_rows, per, total_tiles;
 };
 __device__ __forceinline__ WorkView work_view(const SplitParams& p) {
-  if (p.dyn) return WorkView{p.dyn->seq, p.num_seqs, p.dyn->chunk, p.dyn->num_units, p.dyn->num_rows};
-  return WorkView{p.seq, p.num_seqs, p.chunk, p.num_units, p.num_rows};
+  if (p.dyn)
+    return WorkView{p.dyn->seq, p.num_seqs, p.dyn->chunk, p.dyn->num_units, p.dyn->num_rows, p.dyn->per,
+                    p.dyn->total_tiles};
+  return WorkView{p.seq, p.num_seqs, p.chunk, p.num_units, p.num_rows, p.per, p.total_tiles};
+}
+// Index of the entry whose tiles contain flat tile f (the last entry with tile_start <= f).
+__device__ __forceinline__ int flat_seq_of(const WorkView& wv, int f) {
+  int lo = 0, hi = wv.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (wv.seq[mid].tile_start <= f) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 #endif
 

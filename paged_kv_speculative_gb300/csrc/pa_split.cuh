@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(NW * 32)
       pids[i] = pg;
     }
   }
+  __syncwarp();  // thread 0 ran the set-up alone: its warp reconverges before the CTA barrier
   __syncthreads();
 
   // Stage issue (warp 0): pages of tile `k` into ring slot `s`. A TMA issue
@@ -475,6 +476,7 @@ __global__ void __launch_bounds__(NW * 32)
       for (int k = it; k < min(n_stages, it + kStages); ++k)
         (void)mbar_wait_bounded(smem_addr(&bars[k % kStages]), static_cast<uint32_t>(k / kStages) & 1u);
     }
+    __syncwarp();
     __syncthreads();
     return;
   }

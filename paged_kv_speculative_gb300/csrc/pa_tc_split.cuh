@@ -1,27 +1,37 @@
 // Split-KV paged verify attention on 5th-generation tensor cores (tcgen05).
 //
-// One CTA per work unit (sequence b, KV head g, context chunk [t0, t1)). The
-// unit's q_b * G query rows ("rows = query length x GQA group", MTP-5 routing
-// page, Motivation) are the N dimension of the MMAs, padded to NP; the 128
-// tokens of a K/V tile are the M dimension, so every K/V byte reaches the
-// tensor core straight from the TMA-staged shared memory, once:
+// Work. The (sequence, KV head) pairs are laid end to end as 128-token tiles
+// and CTA c takes the consecutive tiles [c * per, (c + 1) * per), so every SM
+// gets the same amount of K/V whatever the length mix. A CTA walks its range
+// as segments, one per pair the range touches. A segment covering a whole
+// pair writes the output; otherwise it writes a normalised partial and its
+// log2-sum-exp at slot c + pair for the combine kernel (the "reducer" of a
+// split decode: MTP-5 routing page, Motivation).
+//
+// A pair's q_b * G query rows ("rows = query length x GQA group", same page)
+// are the N dimension of the MMAs, padded to NP; the 128 tokens of a K/V
+// tile are the M dimension, so every K/V byte reaches the tensor core
+// straight from the TMA-staged shared memory, once:
 //   S^T[tok, r]  = K[tok, :] . Q[r, :]           (A = K tile, K-major; B = Q, K-major)
 //   O^T[d, r]   += V[:, d]^T . P^T[:, r]          (A = V tile, MN-major; B = P, MN-major)
 // with both accumulators in tensor memory.
 //
 // Warp roles (352 threads): warps 0 and 10 gather pages through the block
 // table with 2-D TMA boxes into a KS-deep K ring and a VS-deep V ring (which
-// also carries the FP8 scales), one lane per box; warp 1 allocates tensor
-// memory and issues the MMAs (one thread, S and PV each as soon as ready); warps 2-9 are two softmax warpgroups, one thread per
-// token of the tile, each group owning half of the row columns. Stages hand
-// over on mbarriers; every wait is bounded.
+// also carries the FP8 scales), one lane per box, reading the next tile's
+// page ids while the current tile is issued; warp 1 allocates tensor memory
+// and issues the MMAs (one thread); warps 2-9 are two softmax warpgroups, one
+// thread per token of the tile, each group owning half of the row columns and
+// staging its own rows of Q. Stages hand over on mbarriers; every wait is
+// bounded. The rings run on across segment boundaries; Q is restaged once the
+// last S of a segment is done.
 //
 // Softmax. Row r keeps a reference maximum M_r, uniform across its group. A
 // tile whose scores stay below M_r + 8 (log2 units) uses M_r as is, so P <= 2^8
-// and no cross-thread row maximum is needed. Otherwise (the first tile, or a
-// score that rose by more than 2^8) the warpgroup takes the exact tile row
-// maxima, raises M_r and rescales l_r and the O accumulator. The final O / l is
-// the same softmax whatever reference was used.
+// and no cross-thread row maximum is needed. Otherwise (a segment's first
+// tile, or a score that rose by more than 2^8) the warpgroup takes the exact
+// tile row maxima, raises M_r and rescales l_r and the O accumulator. The final
+// O / l is the same softmax whatever reference was used.
 //
 // FP8 E4M3 K/V stay 8-bit all the way (kind::f8f6f4). Q and P are each split
 // into two E4M3 terms, x = hi + lo, and both terms go through the tensor core
@@ -40,7 +50,7 @@ namespace pav {
 template <int KV_FP8, int NP>
 struct TcCfg {
   static constexpr int kD = 128;
-  static constexpr int kTile = 128;                          // tokens per K/V tile = MMA M
+  static constexpr int kTile = kFlatTile;                    // tokens per K/V tile = MMA M
   static constexpr int kRowB = KV_FP8 ? 128 : 256;           // bytes per token row
   static constexpr int kTileB = kTile * kRowB;               // 16 KB (fp8) / 32 KB (bf16)
   static constexpr int KS = KV_FP8 ? 5 : 2;                  // K ring depth (a K slot frees once S is done)
@@ -54,15 +64,15 @@ struct TcCfg {
   static constexpr int kOffV = kOffK + KS * kTileB;
   static constexpr int kOffQ = kOffV + ((VS * kVStage + 1023) / 1024) * 1024;
   static constexpr int kOffP = kOffQ + kQB;
-  static constexpr int kOffPid = kOffP + 2 * kPBuf;
-  static constexpr int kOffRow = kOffPid + 4 * (kMaxChunk / kPage);  // per-row constants
-  static constexpr int kOffRed = kOffRow + 4 * 64 * 4;               // tile maxima of the 8 softmax warps + row totals
-  static constexpr int kOffBar = kOffRed + 9 * 64 * 4;
-  static constexpr int kSmem = kOffBar + 256 + 1024;                 // barriers, tmem base, alignment slack
+  static constexpr int kOffRow = kOffP + 2 * kPBuf;          // rowC[2][64] f32, rowLim[2][64] i32 (by segment parity)
+  static constexpr int kOffRed = kOffRow + 4 * 64 * 4;       // tile maxima [8 warps][64], then row totals [64]
+  static constexpr int kOffRedL = kOffRed + 9 * 64 * 4;      // row-sum partials [8 warps][64]
+  static constexpr int kOffBar = kOffRedL + 8 * 64 * 4;
+  static constexpr int kSmem = kOffBar + 256 + 1024;         // barriers, tmem base, alignment slack
   static_assert(NP % 16 == 0 && NP >= 16 && NP <= 64, "N must be 16..64 in steps of 16");
   static_assert((NP / 2) % 8 == 0, "each softmax warpgroup owns a multiple of 8 columns");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
-  static_assert(kTile * NP * 4 <= KS * kTileB, "epilogue l-sum scratch fits the K ring");
+  static_assert(2 * KS + 2 * VS + 9 <= 30, "barriers fit their 256 bytes with the tmem slot and abort flag");
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -81,12 +91,50 @@ __device__ __forceinline__ bool named_or(int id, int nthreads, bool pred) {
       : "memory");
   return r != 0;
 }
+// Maximum of v over the 32 lanes of the warp, in one instruction.
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(v));
+  return r;
+}
 // Two fp32 -> E4M3 bytes, round to nearest even, saturating (lo -> low byte).
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+
+// Position in a CTA's tile range: entry k of the work table (plan order), KV
+// head g, tile t of the pair, with the entry's figures.
+struct TileCursor {
+  int k, g, t;
+  int L, QL, q_off, b, n_t;
+  __device__ __forceinline__ void load_seq(const WorkView& wv) {
+    const SeqInfo& s = wv.seq[k];
+    L = s.ctx_len;
+    QL = s.q_len;
+    q_off = s.q_off;
+    b = s.b;
+    n_t = s.n_tiles;
+  }
+  __device__ __forceinline__ void seek(const WorkView& wv, int f) {
+    k = flat_seq_of(wv, f);
+    load_seq(wv);
+    const int off = f - wv.seq[k].tile_start;
+    g = off / n_t;
+    t = off - g * n_t;
+  }
+  // to the next tile; the caller guarantees the range has one
+  __device__ __forceinline__ void advance(const WorkView& wv, int hkv) {
+    if (++t < n_t) return;
+    t = 0;
+    if (++g < hkv) return;
+    g = 0;
+    ++k;
+    load_seq(wv);
+  }
+  __device__ __forceinline__ int pair(int hkv) const { return k * hkv + g; }
+};
 
 template <int KV_FP8, int NP>
 __global__ void __launch_bounds__(352, 1)
@@ -99,11 +147,10 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* sV = sm + C::kOffV;
   uint8_t* sQ = sm + C::kOffQ;
   uint8_t* sP = sm + C::kOffP;
-  int32_t* pids = reinterpret_cast<int32_t*>(sm + C::kOffPid);
-  float* rowM = reinterpret_cast<float*>(sm + C::kOffRow);      // reference maxima (log2 units)
-  float* rowC = rowM + 64;                                       // score multiplier per row
-  int* rowLim = reinterpret_cast<int*>(rowC + 64);               // last visible key per row (-1: padding)
-  float* red = reinterpret_cast<float*>(sm + C::kOffRed);        // [8 warps][64] maxima, then [64] row totals
+  float* rowC = reinterpret_cast<float*>(sm + C::kOffRow);     // [2][64] score multiplier per row
+  int* rowLim = reinterpret_cast<int*>(rowC + 128);             // [2][64] last visible key per row (-1: padding)
+  float* red = reinterpret_cast<float*>(sm + C::kOffRed);       // [8 warps][64] maxima, then [64] row totals
+  float* redl = reinterpret_cast<float*>(sm + C::kOffRedL);     // [8 warps][64] row-sum partials
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   uint64_t* kfull = bars;
   uint64_t* kempty = kfull + C::KS;
@@ -119,26 +166,55 @@ __global__ void __launch_bounds__(352, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ------------------------------------------------------------ the unit
-  const int u = blockIdx.x;
+  // ------------------------------------------------------------ the CTA's tiles
+  const int cta = blockIdx.x;
   const WorkView wv = work_view(p);
-  if (u >= wv.num_units) return;  // a dynamic plan's grid covers its capacity
-  int lo = 0, hi = wv.num_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (wv.seq[mid].unit_start <= u) lo = mid; else hi = mid - 1;
-  }
-  const SeqInfo si = wv.seq[lo];
-  const int local = u - si.unit_start;
-  const int kvh = local / si.n_chunks;
-  const int chunk_idx = local - kvh * si.n_chunks;
-  const int L = si.ctx_len, QL = si.q_len, b = si.b, G = p.group;
-  const int rows = QL * G;
-  const int t0 = chunk_idx * wv.chunk;
-  const int t_end = min(L, t0 + wv.chunk);
-  const int n_tiles = (t_end - t0 + C::kTile - 1) / C::kTile;
-  const int n_pages = (t_end - t0 + kPage - 1) / kPage;
-  const bool split = si.n_chunks > 1;
+  if (cta >= wv.num_units) return;  // a dynamic plan's grid covers its capacity
+  const int f_lo = cta * wv.per;
+  const int n_tiles = min(wv.per, wv.total_tiles - f_lo);
+  const int Hkv = p.num_kv_heads, G = p.group;
+
+  // Work that needs neither the barriers nor tensor memory starts before the
+  // set-up, so that its memory reads are ahead of the rings' first TMA traffic:
+  // the producers find their first tile and read its page ids, the softmax
+  // warps find their first segment and load its Q rows.
+  constexpr int NH = NP / 2;                    // columns per softmax warpgroup
+  constexpr int kRowsPerWarp = NH / 4;          // Q rows each softmax warp stages
+  const bool is_prod = warp == 0 || warp == 10, is_sm = warp >= 2 && warp <= 9;
+  const int wg = is_sm ? (warp - 2) >> 2 : 0;   // softmax warpgroup 0 or 1
+  const int col0 = wg * NH;                     // first column this group owns
+  constexpr int kHalves = C::kRowB / 128;
+  const bool is_k = warp == 0;
+  // producer lanes: page (within the tile) of this lane's copy: boxes on lanes [0, 8 * halves), FP8 scales on 16-31
+  const int jl = lane < 8 * kHalves ? lane / kHalves : ((KV_FP8 && warp == 10 && lane >= 16) ? (lane & 7) : 8);
+  auto npages = [&](const TileCursor& cq) {
+    return min(C::kTile / kPage, (cq.L - cq.t * C::kTile + kPage - 1) / kPage);
+  };
+  // this lane's raw page id for a tile (-1: no copy); checked against the pool when issued
+  auto fetch = [&](const TileCursor& cq) {
+    return jl < npages(cq) ? __ldg(p.block_table + static_cast<size_t>(cq.b) * p.bt_stride + cq.t * (C::kTile / kPage) + jl)
+                           : -1;
+  };
+  // a softmax warp's Q rows of a segment: row r = col0 + (warp - 2) % 4 + 4 m, 8 bytes per lane
+  auto q_load = [&](const TileCursor& cq, uint2 (&wq)[kRowsPerWarp]) {
+    const int rows = cq.QL * G;
+#pragma unroll
+    for (int m = 0; m < kRowsPerWarp; ++m) {
+      const int r = col0 + ((warp - 2) & 3) + 4 * m;
+      wq[m] = make_uint2(0, 0);
+      if (r < rows) {
+        const int i = r / G;
+        wq[m] = *reinterpret_cast<const uint2*>(
+            p.q + (static_cast<size_t>(cq.q_off + i) * p.num_q_heads + cq.g * G + (r - i * G)) * C::kD + 4 * lane);
+      }
+    }
+  };
+  TileCursor cu0;  // producers: the first tile; softmax warps: the first segment
+  int pg0 = -1;
+  uint2 wq0[kRowsPerWarp];
+  if (is_prod || is_sm) cu0.seek(wv, f_lo);
+  if (is_prod) pg0 = fetch(cu0);
+  if (is_sm) q_load(cu0, wq0);
 
   if (tid == 0) {
     for (int s = 0; s < C::KS; ++s) { mbar_init(smem_addr(&kfull[s]), 1); mbar_init(smem_addr(&kempty[s]), 1); }
@@ -149,35 +225,20 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(smem_addr(&pfull[s]), 8);
       mbar_init(smem_addr(&pfree[s]), 1);
     }
-    mbar_init(smem_addr(qready), 8);
+    mbar_init(smem_addr(qready), 8);  // one phase per segment: each softmax warp staged its rows
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-    if (chunk_idx == 0 && kvh == 0 && (p.dev_ctx[b] != L || p.dev_q[b] != QL)) atomicOr(p.err, 2u);
   }
   if (warp == 1) {
     tc::tmem_alloc(tbase_slot, 256);
     tc::tmem_relinquish();
   }
-  if (warp == 0) {
-    const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.bt_stride + t0 / kPage;
-    for (int i = lane; i < n_pages; i += 32) {
-      int pg = __ldg(bt + i);
-      if (static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages)) {
-        atomicOr(p.err, 1u);
-        pg = -1;
-      }
-      pids[i] = pg;
-    }
-  }
-  if (tid >= 64 && tid < 128) {  // per-row constants for the softmax warpgroup
-    const int r = tid - 64;
-    rowM[r] = -INFINITY;
-    rowC[r] = p.scale_log2;
-    rowLim[r] = r < rows ? L - QL + r / G : -1;
-  }
+  // Each warp reconverges first: lanes that took different paths must reach the
+  // CTA barrier together, or it can release before thread 0's set-up is done.
+  __syncwarp();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -195,14 +256,22 @@ __global__ void __launch_bounds__(352, 1)
     // TMA issue costs its thread about one memory latency, so every page box
     // (and scale copy) of a tile gets its own lane: lane 0 arms the stage's
     // byte count, then the lanes issue together.
-    const bool is_k = warp == 0;
     const int depth = is_k ? C::KS : C::VS;
     const CUtensorMap* map = is_k ? &tmk : &tmv;
     uint64_t* full = is_k ? kfull : vfull;
     uint64_t* empty = is_k ? kempty : vempty;
-    constexpr int kHalves = C::kRowB / 128;
+    TileCursor cu = cu0;
+    int pg_raw = pg0;
     int issued = 0;
     for (int k = 0; k < n_tiles && !*abort_flag; ++k) {
+      // the next tile's page ids are read now; their latency hides behind this tile's wait and issue
+      TileCursor nx = cu;
+      int pg_next = -1;
+      if (k + 1 < n_tiles) {
+        nx.advance(wv, Hkv);
+        pg_next = fetch(nx);
+      }
+
       const int s = k % depth;
       if (k >= depth) {
         // lane 0 waits; the verdict is the same for every lane (no lane is left at a warp sync)
@@ -215,36 +284,36 @@ __global__ void __launch_bounds__(352, 1)
       }
       uint8_t* dst = is_k ? sK + s * C::kTileB : sV + s * C::kVStage;
       const uint32_t bar = smem_addr(&full[s]);
-      const int tok0 = t0 + k * C::kTile;
-      const int pg0 = (tok0 - t0) / kPage;
-      const int npg = (min(t_end, tok0 + C::kTile) - tok0 + kPage - 1) / kPage;
-      if (lane == 0) {
-        uint32_t bytes = npg * (kPage * C::kRowB);
-        if (KV_FP8 && !is_k)
-          for (int j = 0; j < npg; ++j)
-            if (pids[pg0 + j] >= 0) bytes += 2 * kPage * 4;
-        mbar_arrive_expect_tx(bar, bytes);
+      const int npg = npages(cu);
+      // an id outside the pool is flagged and read past the tensor's end, where TMA fills zeros
+      int pg = pg_raw;
+      if (jl < npg && static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages)) {
+        atomicOr(p.err, 1u);
+        pg = -1;
       }
+      // FP8 V: one k and one v scale copy per page inside the pool (lanes 16-23 hold the ids)
+      const uint32_t nsc =
+          (KV_FP8 && !is_k) ? __popc(__ballot_sync(0xffffffffu, lane >= 16 && lane < 24 && pg >= 0)) : 0u;
+      if (lane == 0) mbar_arrive_expect_tx(bar, npg * (kPage * C::kRowB) + nsc * (2 * kPage * 4));
       __syncwarp();
-      // lanes [0, npg * halves): page boxes; FP8 V: lanes 16 + j (k scales), 24 + j (v scales)
       if (lane < npg * kHalves) {
-        const int j = lane / kHalves, hf = lane % kHalves;
-        const int pg = pids[pg0 + j];
-        // an invalid page reads past the tensor's end: TMA fills zeros
-        const int row = (pg >= 0 ? pg : p.num_pages) * p.num_kv_heads * kPage + kvh * kPage;
-        tma_load_2d(smem_addr(dst + hf * (C::kTile * 128) + j * kPage * 128), map, bar, hf * (KV_FP8 ? 128 : 64), row);
+        const int hf = lane % kHalves;
+        // an id outside the pool reads past the tensor's end: TMA fills zeros
+        const int row = (pg >= 0 ? pg : p.num_pages) * Hkv * kPage + cu.g * kPage;
+        tma_load_2d(smem_addr(dst + hf * (C::kTile * 128) + jl * kPage * 128), map, bar, hf * (KV_FP8 ? 128 : 64), row);
       }
-      if (KV_FP8 && !is_k && lane >= 16 && (lane & 7) < npg) {
-        const int j = lane & 7;
-        const int pg = pids[pg0 + j];
-        if (pg >= 0) {
-          const size_t so = (static_cast<size_t>(pg) * p.num_kv_heads + kvh) * kPage;
-          const bool ksc = lane < 24;
-          bulk_load(smem_addr(dst + C::kTileB + (ksc ? 0 : C::kTile * 4) + j * kPage * 4),
-                    (ksc ? p.k_scale : p.v_scale) + so, kPage * 4, bar);
-        }
+      if (KV_FP8 && !is_k && lane >= 16 && jl < npg && pg >= 0) {
+        const size_t so = (static_cast<size_t>(pg) * Hkv + cu.g) * kPage;
+        const bool ksc = lane < 24;
+        bulk_load(smem_addr(dst + C::kTileB + (ksc ? 0 : C::kTile * 4) + jl * kPage * 4),
+                  (ksc ? p.k_scale : p.v_scale) + so, kPage * 4, bar);
       }
+      // (after the issue, off its path) the device lengths must be the planned ones
+      if (is_k && lane == 0 && cu.t == 0 && cu.g == 0 && (p.dev_ctx[cu.b] != cu.L || p.dev_q[cu.b] != cu.QL))
+        atomicOr(p.err, 2u);
       ++issued;
+      cu = nx;
+      pg_raw = pg_next;
     }
     // No copy may land after the CTA exits: wait (bounded) for the last
     // copies of each ring slot; only this warp arms these barriers, so the
@@ -258,14 +327,24 @@ __global__ void __launch_bounds__(352, 1)
     // the fixed order S0 S1 | S2 PV0 | S3 PV1 | ...: S(j+2) needs only that the
     // softmax has read S(j) (early in its tile) while PV(j) needs its finished
     // P, so each wait is on the event due first and the thread sleeps in
-    // hardware (try_wait) instead of polling.
+    // hardware (try_wait) instead of polling. A segment's first S needs that
+    // segment's Q, staged by the softmax at the start of the previous tile,
+    // after the segment before it may have waited for PV(j) in its epilogue:
+    // such an S goes after PV(j) instead.
     if (lane == 0) {
       constexpr uint32_t fa = KV_FP8 ? tc::kE4M3 : tc::kBF16;
       constexpr uint32_t idS = tc::idesc(fa, fa, tc::kKMajor, tc::kKMajor, 128, NP);
       constexpr uint32_t idPV = tc::idesc(fa, fa, tc::kMNMajor, tc::kMNMajor, 128, NP);
       const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aP = smem_addr(sP);
+      TileCursor cs, cv;  // the next S tile, the next PV tile
+      cs.seek(wv, f_lo);
+      cv = cs;
+      int seg_s = 0;      // segment of the next S tile
       auto issue_s = [&](int i) -> bool {
         const int ks_ = i % C::KS, sb = i & 1;
+        if (i > 0 && cs.t == 0) ++seg_s;
+        if ((i == 0 || cs.t == 0) && !mbar_wait_bounded(smem_addr(qready), static_cast<uint32_t>(seg_s) & 1u))
+          return false;
         if (!mbar_wait_bounded(smem_addr(&kfull[ks_]), static_cast<uint32_t>(i / C::KS) & 1u)) return false;
         if (i >= 2 && !mbar_wait_bounded(smem_addr(&sfree[sb]), static_cast<uint32_t>((i >> 1) - 1) & 1u))
           return false;
@@ -288,17 +367,19 @@ __global__ void __launch_bounds__(352, 1)
         }
         tc::commit(&sfull[sb]);
         tc::commit(&kempty[ks_]);
+        if (i + 1 < n_tiles) cs.advance(wv, Hkv);
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
         const int vs = j % C::VS, pb = j & 1;
+        const bool first = j == 0 || cv.t == 0;  // the segment's first PV starts its accumulator
         if (!mbar_wait_bounded(smem_addr(&vfull[vs]), static_cast<uint32_t>(j / C::VS) & 1u)) return false;
         if (!mbar_wait_bounded(smem_addr(&pfull[pb]), static_cast<uint32_t>(j >> 1) & 1u)) return false;
         tc::fence_after_sync();
         const uint32_t v0 = aV + vs * C::kVStage;
         const uint32_t p0 = aP + pb * C::kPBuf;
-        // only the k-steps holding tokens of the unit: rows past them may be stale or never loaded
-        const int nv = min(C::kTile, t_end - (t0 + j * C::kTile));
+        // only the k-steps holding tokens of the pair: rows past them may be stale or never loaded
+        const int nv = min(C::kTile, cv.L - cv.t * C::kTile);
         if (KV_FP8) {
           const int nks = (nv + 31) >> 5;  // 32 tokens per k-step; hi then lo plane of P
 #pragma unroll
@@ -308,24 +389,28 @@ __global__ void __launch_bounds__(352, 1)
               if (ks < nks)
                 tc::mma_f8(tO, tc::sdesc(v0 + ks * 4096, 16384, 1024, tc::kSwizzle128B),
                            tc::sdesc(p0 + pl * C::kPPlane + ks * 2048, 16384, 512, tc::kSwizzle64B), idPV,
-                           (j > 0 || pl > 0 || ks > 0) ? 1u : 0u);
+                           (!first || pl > 0 || ks > 0) ? 1u : 0u);
         } else {
           const int nks = (nv + 15) >> 4;  // 16 tokens per k-step
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             if (ks < nks)
               tc::mma_f16(tO, tc::sdesc(v0 + ks * 2048, C::kTile * 128, 1024, tc::kSwizzle128B),
-                          tc::sdesc(p0 + ks * 2048, 16384, 1024, tc::kSwizzle128B), idPV, (j > 0 || ks > 0) ? 1u : 0u);
+                          tc::sdesc(p0 + ks * 2048, 16384, 1024, tc::kSwizzle128B), idPV, (!first || ks > 0) ? 1u : 0u);
         }
         tc::commit(&vempty[vs]);
-        tc::commit(&pfree[pb]);  // also tells the softmax warpgroups that O holds tiles 0..j
+        tc::commit(&pfree[pb]);  // also tells the softmax warpgroups that O holds the segment's tiles up to j
+        if (j + 1 < n_tiles) cv.advance(wv, Hkv);
         return true;
       };
-      bool ok = mbar_wait_bounded(smem_addr(qready), 0);
+      bool ok = true;
       for (int i = 0; ok && i < min(2, n_tiles); ++i) ok = issue_s(i);
       for (int j = 0; ok && j < n_tiles && !*abort_flag; ++j) {
-        if (j + 2 < n_tiles) ok = issue_s(j + 2);
+        const bool s_next = j + 2 < n_tiles;
+        const bool s_new_seg = s_next && cs.t == 0;  // cs stands at tile j + 2
+        if (s_next && !s_new_seg) ok = issue_s(j + 2);
         if (ok) ok = issue_pv(j);
+        if (ok && s_new_seg) ok = issue_s(j + 2);
       }
       if (!ok) fail();
     }
@@ -333,70 +418,70 @@ __global__ void __launch_bounds__(352, 1)
     // ============================================================ softmax warpgroups
     // Two warpgroups (warps 2-5 and 6-9). Each covers the 128 tokens of a tile
     // (one per thread, = tensor-memory lane) for its own NH = NP/2 columns
-    // (rows of the unit); the groups never wait on each other inside the loop.
-    constexpr int NH = NP / 2;
-    const int wg = (warp - 2) >> 2;               // 0 or 1
+    // (rows of the pair); the groups never wait on each other inside the loop.
     const int gt = tid - 64 - wg * 128;           // 0..127 inside the group
     const int q4 = warp & 3;                      // tensor-memory lane quarter of this warp
     const int tok = q4 * 32 + lane;               // token of the tile this thread owns
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    const int col0 = wg * NH;                     // first column this group owns
     const int bar_sync = 1 + 2 * wg, bar_or = 2 + 2 * wg;
 
-    // ---- Q staging by all 8 softmax warps: row r is one warp's job
-    for (int r = warp - 2; r < NP; r += 8) {
-      const uint16_t* qp = nullptr;
-      if (r < rows) {
-        const int i = r / G;
-        qp = p.q + (static_cast<size_t>(si.q_off + i) * p.num_q_heads + kvh * G + (r - i * G)) * C::kD;
-      }
-      uint2 w = qp ? *reinterpret_cast<const uint2*>(qp + 4 * lane) : make_uint2(0, 0);
-      if (!KV_FP8) {
-        // 4 bf16 = 8 bytes at byte 8*lane of the 256-byte row: half lane/16, chunk (lane%16)/2
-        const int hf = lane >> 4, ch = (lane & 15) >> 1;
-        uint8_t* dst = sQ + hf * C::kQPlane + r * 128 + ((ch ^ (r & 7)) << 4) + (lane & 1) * 8;
-        *reinterpret_cast<uint2*>(dst) = w;
-      } else {
-        float x[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
-        float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    // ---- Q rows [col0, col0 + NH) of a segment into the Q buffer (one warp a row), their
+    // constants into slot `sl`; then this warp's arrival on qready
+    auto stage_q = [&](const TileCursor& cq, const uint2 (&wq)[kRowsPerWarp], int sl) {
+      const int rows = cq.QL * G;
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-        int ex = 0;
-        if (mx > 0.f) {
-          int e2;
-          frexpf(mx, &e2);  // mx in [2^(e2-1), 2^e2)
-          ex = 8 - e2;      // scaled row max in [128, 256)
-        }
-        uint32_t hw = 0, lw = 0;
+      for (int m = 0; m < kRowsPerWarp; ++m) {
+        const int r = col0 + ((warp - 2) & 3) + 4 * m;
+        const uint2 w = wq[m];
+        float cr = p.scale_log2;
+        if (!KV_FP8) {
+          // 4 bf16 = 8 bytes at byte 8*lane of the 256-byte row: half lane/16, chunk (lane%16)/2
+          const int hf = lane >> 4, ch = (lane & 15) >> 1;
+          uint8_t* dst = sQ + hf * C::kQPlane + r * 128 + ((ch ^ (r & 7)) << 4) + (lane & 1) * 8;
+          *reinterpret_cast<uint2*>(dst) = w;
+        } else {
+          float x[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
+          float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          const float a = ldexpf(x[e], ex), c = ldexpf(x[e + 1], ex);
-          const float ah = __uint_as_float(__float_as_uint(a) & 0xFFF00000u);  // 3 mantissa bits
-          const float ch2 = __uint_as_float(__float_as_uint(c) & 0xFFF00000u);
-          hw |= e4m3x2(ah, ch2) << (8 * e);
-          lw |= e4m3x2(a - ah, c - ch2) << (8 * e);
+          for (int k = 16; k >= 1; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
+          int ex = 0;
+          if (mx > 0.f) {
+            int e2;
+            frexpf(mx, &e2);  // mx in [2^(e2-1), 2^e2)
+            ex = 8 - e2;      // scaled row max in [128, 256)
+          }
+          uint32_t hw = 0, lw = 0;
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const float a = ldexpf(x[e], ex), c = ldexpf(x[e + 1], ex);
+            const float ah = __uint_as_float(__float_as_uint(a) & 0xFFF00000u);  // 3 mantissa bits
+            const float ch2 = __uint_as_float(__float_as_uint(c) & 0xFFF00000u);
+            hw |= e4m3x2(ah, ch2) << (8 * e);
+            lw |= e4m3x2(a - ah, c - ch2) << (8 * e);
+          }
+          // 4 bytes at byte 4*lane of the 128-byte row: chunk lane/4
+          const uint32_t off = r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4;
+          *reinterpret_cast<uint32_t*>(sQ + off) = hw;
+          *reinterpret_cast<uint32_t*>(sQ + C::kQPlane + off) = lw;
+          cr = ldexpf(p.scale_log2, -ex);
         }
-        // 4 bytes at byte 4*lane of the 128-byte row: chunk lane/4
-        const uint32_t off = r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4;
-        *reinterpret_cast<uint32_t*>(sQ + off) = hw;
-        *reinterpret_cast<uint32_t*>(sQ + C::kQPlane + off) = lw;
-        if (lane == 0) rowC[r] = ldexpf(p.scale_log2, -ex);
+        if (lane == 0) {
+          rowC[sl * 64 + r] = cr;
+          rowLim[sl * 64 + r] = r < rows ? cq.L - cq.QL + r / G : -1;
+        }
       }
-    }
-    fence_proxy_async();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(qready);
-    named_sync(5, 256);  // both groups' rows staged (rowC complete)
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qready);
+    };
+
+    TileCursor cu = cu0;
+    stage_q(cu, wq0, 0);
+    named_sync(bar_sync, 128);  // the group's row constants are visible to the group
 
     // per owned column pair: minus the reference max, score multiplier (FP8), row-sum partial
     float2 negm[NH / 2], crow2[NH / 2], l[NH / 2];
-#pragma unroll
-    for (int c = 0; c < NH / 2; ++c) {
-      negm[c] = make_float2(INFINITY, INFINITY);
-      crow2[c] = make_float2(rowC[col0 + 2 * c], rowC[col0 + 2 * c + 1]);
-      l[c] = make_float2(0.f, 0.f);
-    }
-    const int lim_first = L - QL;  // last key every real row sees
+    int seg = 0, seg_t0 = 0;
 
     // A failed wait marks this thread and skips its later waits, but every
     // named barrier below is still reached in order: no thread of the
@@ -409,8 +494,33 @@ __global__ void __launch_bounds__(352, 1)
       }
     };
     for (int i = 0; i < n_tiles; ++i) {
-      const int sb = i & 1;
-      const bool last = i == n_tiles - 1;
+      const int sb = i & 1, sl = seg & 1;
+      const bool seg_first = i == 0 || cu.t == 0;
+      const bool pair_last = cu.t == cu.n_t - 1;
+      const bool seg_last = i == n_tiles - 1 || pair_last;
+      if (seg_first) {
+        seg_t0 = cu.t;
+#pragma unroll
+        for (int c = 0; c < NH / 2; ++c) {
+          negm[c] = make_float2(INFINITY, INFINITY);
+          crow2[c] = make_float2(rowC[sl * 64 + col0 + 2 * c], rowC[sl * 64 + col0 + 2 * c + 1]);
+          l[c] = make_float2(0.f, 0.f);
+        }
+        // the next segment's Q rows (the pair after this one, if the range reaches it) into L2
+        if (cu.n_t - cu.t < n_tiles - i && gt < NH) {
+          TileCursor nx = cu;
+          nx.t = cu.n_t - 1;
+          nx.advance(wv, Hkv);
+          const int r = col0 + gt;
+          if (r < nx.QL * G) {
+            const int qi = r / G;
+            const uint16_t* qp =
+                p.q + (static_cast<size_t>(nx.q_off + qi) * p.num_q_heads + nx.g * G + (r - qi * G)) * C::kD;
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(qp));
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(qp + 64));
+          }
+        }
+      }
       wait(&sfull[sb], static_cast<uint32_t>(i >> 1) & 1u);
       tc::fence_after_sync();
       float2 y[NH / 2];  // scores of the owned columns, in pairs (packed f32x2 arithmetic)
@@ -425,8 +535,17 @@ __global__ void __launch_bounds__(352, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[sb]);
+      if (seg_last && i + 1 < n_tiles) {
+        // S(i), the last reader of this segment's Q, is done: stage the next segment's rows
+        TileCursor nx = cu;
+        nx.advance(wv, Hkv);
+        uint2 wq[kRowsPerWarp];
+        q_load(nx, wq);  // every row's load first: one memory latency for the warp's rows
+        stage_q(nx, wq, sl ^ 1);
+      }
 
-      const int tabs = t0 + i * C::kTile + tok;
+      const int L = cu.L;
+      const int tabs = cu.t * C::kTile + tok;
       const int vs = i % C::VS;
       float inv_sv = 1.f;
       if (KV_FP8) {
@@ -434,7 +553,7 @@ __global__ void __launch_bounds__(352, 1)
         wait(&vfull[vs], static_cast<uint32_t>(i / C::VS) & 1u);
         const float* sc = reinterpret_cast<const float*>(sV + vs * C::kVStage + C::kTileB);
         float sk = sc[tok], sv = sc[C::kTile + tok];
-        if (tabs >= t_end) { sk = 0.f; sv = 1.f; }
+        if (tabs >= L) { sk = 0.f; sv = 1.f; }
         sv = fmaxf(sv, 7.888609052210118e-31f);  // 2^-100 floor keeps log2 and 1/x finite
         const float2 ls = make_float2(__log2f(sv), __log2f(sv));
         inv_sv = __frcp_rn(sv);
@@ -446,15 +565,16 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int c = 0; c < NH / 2; ++c) y[c] = __fmul2_rn(y[c], s2);
       }
-      // causal mask inside the drafts / unit end / padding rows
-      if (tabs >= t_end) {
+      // causal mask inside the drafts / pair end / padding rows
+      if (tabs >= L) {
 #pragma unroll
         for (int c = 0; c < NH / 2; ++c) y[c] = make_float2(-INFINITY, -INFINITY);
-      } else if (tabs > lim_first) {
+      } else if (tabs > L - cu.QL) {
+        const int* lim = rowLim + sl * 64 + col0;
 #pragma unroll
         for (int c = 0; c < NH / 2; ++c) {
-          if (tabs > rowLim[col0 + 2 * c]) y[c].x = -INFINITY;
-          if (tabs > rowLim[col0 + 2 * c + 1]) y[c].y = -INFINITY;
+          if (tabs > lim[2 * c]) y[c].x = -INFINITY;
+          if (tabs > lim[2 * c + 1]) y[c].y = -INFINITY;
         }
       }
       // d = y - M (log2 units); with M = -inf a finite score gives +inf (and a masked one NaN, dropped below)
@@ -469,25 +589,22 @@ __global__ void __launch_bounds__(352, 1)
         // ---- exact tile maxima of the owned columns, raise the references, rescale l and O
 #pragma unroll
         for (int c = 0; c < NH; ++c) {
-          float m = (c & 1) ? y[c >> 1].y : y[c >> 1].x;
-#pragma unroll
-          for (int k = 16; k >= 1; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
+          const float m = warp_max((c & 1) ? y[c >> 1].y : y[c >> 1].x);
           if (lane == 0) red[(warp - 2) * 64 + col0 + c] = m;
         }
         named_sync(bar_sync, 128);
         const float* rg = red + wg * 4 * 64 + col0;  // this group's 4 warp rows
-        auto new_max = [&](int c) {
-          const float mo = (c & 1) ? -negm[c >> 1].y : -negm[c >> 1].x;
-          return fmaxf(mo, fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
-        };
         auto old_max = [&](int c) { return (c & 1) ? -negm[c >> 1].y : -negm[c >> 1].x; };
+        auto new_max = [&](int c) {
+          return fmaxf(old_max(c), fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
+        };
         bool any_scale = false;
 #pragma unroll
         for (int c = 0; c < NH; ++c) {
           const float mn = new_max(c);
           any_scale |= (mn != -INFINITY && mn != old_max(c));
         }
-        if (any_scale && i > 0) {
+        if (any_scale && !seg_first) {
           wait(&pfree[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u);  // PV of tile i-1 done
           tc::fence_after_sync();
 #pragma unroll
@@ -521,12 +638,12 @@ __global__ void __launch_bounds__(352, 1)
       // ---- P = 2^(y - M) (<= 2^8), row sums, P into shared memory as the MMA's B operand
       const int pb = i & 1;
       if (i >= 2) wait(&pfree[pb], static_cast<uint32_t>((i >> 1) - 1) & 1u);
-      if (last) {
-        // Rows past the unit inside the last MMA k-step (a page's unused slots, or a page never loaded)
+      const int nv = L - cu.t * C::kTile;
+      if (nv < C::kTile) {
+        // Rows past the pair inside the last MMA k-step (a page's unused slots, or a page never loaded)
         // may hold anything, and P = 0 times NaN would still poison O: they become zeros. bf16 looks at
         // its V ring only here; PV(i-2) done implies every earlier phase of this slot completed.
         if (!KV_FP8) wait(&vfull[vs], static_cast<uint32_t>(i / C::VS) & 1u);
-        const int nv = t_end - (t0 + i * C::kTile);
         const int kend = KV_FP8 ? ((nv + 31) & ~31) : ((nv + 15) & ~15);
         if (wg == 0 && tok >= nv && tok < kend) {
 #pragma unroll
@@ -581,61 +698,91 @@ __global__ void __launch_bounds__(352, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pfull[pb]);
-    }
 
-    // ---- epilogue: O / l for the owned columns
-    if (n_tiles > 0) wait(&pfree[(n_tiles - 1) & 1], static_cast<uint32_t>((n_tiles - 1) >> 1) & 1u);
-    const bool ok = ok_sm;
-    // l partial sums of every token -> per-row totals (scratch: the K ring, idle once every MMA is done)
-    float* lred = reinterpret_cast<float*>(sK);
-    float* rtot = red + 8 * 64;  // row totals, after the 8 warp rows of maxima
+      if (seg_last) {
+        // ---- segment epilogue: O / l for the owned columns (PV(i) done: O holds the segment)
+        wait(&pfree[pb], static_cast<uint32_t>(i >> 1) & 1u);
+        tc::fence_after_sync();
+        // Row sums over the group's 128 tokens. Within a warp, a halving butterfly: at each step a lane
+        // keeps half of its columns, sends the other half to its partner and adds what it receives, so
+        // the NH columns cost about NH shuffles in all and lane L ends with column L >> (5 - log2 W).
+        // Then the group's 4 warps meet in shared memory. (This code runs once per segment: it is kept
+        // short, as it usually runs cold in the instruction cache while HBM traffic is at its peak.)
+        {
+          constexpr int W = NH <= 8 ? 8 : NH <= 16 ? 16 : 32;  // columns padded to a power of two
+          float v[W];
 #pragma unroll
-    for (int c = 0; c < NH / 2; ++c) {
-      lred[(col0 + 2 * c) * 128 + tok] = l[c].x;
-      lred[(col0 + 2 * c + 1) * 128 + tok] = l[c].y;
-    }
-    named_sync(bar_sync, 128);
-    if (gt < NH) {
-      float s2 = 0.f;
-      for (int t = 0; t < 128; ++t) s2 += lred[(col0 + gt) * 128 + t];
-      rtot[col0 + gt] = s2;
-      float mg = -INFINITY;  // this column's reference max (registers hold every column's)
+          for (int c = 0; c < W; ++c) v[c] = c < NH ? ((c & 1) ? l[c >> 1].y : l[c >> 1].x) : 0.f;
 #pragma unroll
-      for (int c = 0; c < NH / 2; ++c) {
-        if (2 * c == gt) mg = -negm[c].x;
-        if (2 * c + 1 == gt) mg = -negm[c].y;
-      }
-      if (ok && split && col0 + gt < rows)
-        p.part_lse[static_cast<size_t>(u) * p.rows_max + col0 + gt] = s2 > 0.f ? mg + __log2f(s2) : -INFINITY;
-    }
-    named_sync(bar_sync, 128);
-    if (ok) {
-      tc::fence_after_sync();
-      const int d = tok;  // O^T lanes are head-dim entries
+          for (int w = W, k = 16; w > 1; w >>= 1, k >>= 1) {
+            const bool up = (lane & k) != 0;
 #pragma unroll
-      for (int c0 = 0; c0 < NH; c0 += 8) {
-        uint32_t r8[8];
-        tc::ld8(tO + lane_off + col0 + c0, r8);
-        tc::wait_ld();
+            for (int i = 0; i < w / 2; ++i) {
+              const float send = up ? v[i] : v[i + w / 2];
+              const float keep = up ? v[i + w / 2] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+            }
+          }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = col0 + c0 + j;
-          if (r >= rows) continue;
-          const float lt = rtot[r];
-          const float val = lt > 0.f ? __uint_as_float(r8[j]) / lt : 0.f;
-          if (split) {
-            p.part_o[(static_cast<size_t>(u) * p.rows_max + r) * C::kD + d] = val;
-          } else {
-            const int qi = r / G;
-            const size_t o = (static_cast<size_t>(si.q_off + qi) * p.num_q_heads + kvh * G + (r - qi * G)) * C::kD + d;
-            if (p.out_f32) reinterpret_cast<float*>(p.out)[o] = val;
-            else reinterpret_cast<uint16_t*>(p.out)[o] = static_cast<uint16_t>(pack_bf16(val, 0.f) & 0xFFFFu);
+          for (int k = 32 / W / 2; k >= 1; k >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], k);
+          constexpr int kShift = W == 32 ? 0 : W == 16 ? 1 : 2;
+          const int col = lane >> kShift;
+          if ((lane & ((1 << kShift) - 1)) == 0 && col < NH) redl[(warp - 2) * 64 + col0 + col] = v[0];
+        }
+        named_sync(bar_sync, 128);
+        const int rows = cu.QL * G;
+        const bool whole = seg_t0 == 0 && pair_last;  // the segment is the whole pair: no combine
+        const size_t u = static_cast<size_t>(cta) + cu.pair(Hkv);
+        float* rinv = red + 8 * 64;  // 1 / row total (0 for an empty row)
+        if (gt < NH) {
+          const int cc = col0 + gt;
+          const float* rl = redl + wg * 4 * 64 + cc;
+          const float s2 = (rl[0] + rl[64]) + (rl[128] + rl[192]);
+          rinv[cc] = s2 > 0.f ? __frcp_rn(s2) : 0.f;
+          float mg = -INFINITY;  // this column's reference max (registers hold every column's)
+#pragma unroll
+          for (int c = 0; c < NH / 2; ++c) {
+            if (2 * c == gt) mg = -negm[c].x;
+            if (2 * c + 1 == gt) mg = -negm[c].y;
+          }
+          if (ok_sm && !whole && cc < rows)
+            p.part_lse[u * p.rows_max + cc] = s2 > 0.f ? mg + __log2f(s2) : -INFINITY;
+        }
+        named_sync(bar_sync, 128);
+        if (ok_sm) {
+          const int d = tok;  // O^T lanes are head-dim entries
+#pragma unroll 1
+          for (int c0 = 0; c0 < NH; c0 += 8) {
+            uint32_t r8[8];
+            tc::ld8(tO + lane_off + col0 + c0, r8);
+            tc::wait_ld();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int r = col0 + c0 + j;
+              if (r >= rows) break;
+              const float val = __uint_as_float(r8[j]) * rinv[r];
+              if (!whole) {
+                p.part_o[(u * p.rows_max + r) * C::kD + d] = val;
+              } else {
+                const int qi = r / G;
+                const size_t o =
+                    (static_cast<size_t>(cu.q_off + qi) * p.num_q_heads + cu.g * G + (r - qi * G)) * C::kD + d;
+                if (p.out_f32) reinterpret_cast<float*>(p.out)[o] = val;
+                else reinterpret_cast<uint16_t*>(p.out)[o] = static_cast<uint16_t>(pack_bf16(val, 0.f) & 0xFFFFu);
+              }
+            }
           }
         }
+        tc::fence_before_sync();  // the O reads above come before the next segment's first PV
+        ++seg;
       }
+      if (i + 1 < n_tiles) cu.advance(wv, Hkv);
     }
   }
 
+  // Lane 0 of the MMA warp and of the producers ran alone until here: reconverge
+  // before the CTA barrier, so that the TMEM release below follows every role's last use.
+  __syncwarp();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) {

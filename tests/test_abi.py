@@ -46,11 +46,55 @@ def test_rows_follow_the_pages_shape_facts():
         assert p.info.warps == (rows + 15) // 16
 
 
-@pytest.mark.parametrize("ctx,ql,hkv", [([37, 100], [1, 6], 1), ([4096 + 7 * i for i in range(8)], [6] * 8, 4),
-                                         ([1 << 20], [6], 1), ([5, 9000, 131072, 64], [3, 8, 1, 2], 2)])
-def test_units_cover_every_token_once(ctx, ql, hkv):
-    p = mk(ctx, ql, hq=8 * hkv, hkv=hkv)
+CASES = [([37, 100], [1, 6], 1), ([4096 + 7 * i for i in range(8)], [6] * 8, 4),
+         ([1 << 20], [6], 1), ([5, 9000, 131072, 64], [3, 8, 1, 2], 2)]
+
+
+def flat_model(ctx, hkv, sms, split_override=0):
+    """Independent model of a flat plan: pairs (longest sequence first, then
+    KV head) end to end as 128-token tiles, the same tile count per CTA.
+    Returns (tiles per CTA, CTAs, every pair's (first CTA, last CTA))."""
+    order = sorted(range(len(ctx)), key=lambda b: -ctx[b])  # stable: ties keep batch order
+    nt = [(c + 127) // 128 for c in ctx]
+    total = hkv * sum(nt)
+    if split_override:
+        per = max(1, -(-max(nt) // split_override))
+    else:
+        per = max(1, -(-total // sms))
+    spans, t = [], 0
+    for b in order:
+        for _ in range(hkv):
+            spans.append((t // per, (t + nt[b] - 1) // per))
+            t += nt[b]
+    return per, -(-total // per), spans
+
+
+@pytest.mark.parametrize("ctx,ql,hkv", CASES)
+@pytest.mark.parametrize("split", [0, 1, 4, 1000])
+def test_flat_plan_gives_every_cta_the_same_tiles(ctx, ql, hkv, split):
+    p = mk(ctx, ql, hq=8 * hkv, hkv=hkv, split_override=split)
     i = p.info
+    assert i.flat == 1 and i.kernel == pv.KERNEL_TCGEN05 and i.tile_tokens == 128
+    per, n_cta, spans = flat_model(ctx, hkv, 152, split)
+    assert i.total_tiles == hkv * sum((c + 127) // 128 for c in ctx)
+    assert i.chunk_tokens == 128 * per and i.num_units == n_cta
+    # every CTA but the last holds exactly `per` tiles: the tiles are covered once
+    assert (n_cta - 1) * per < i.total_tiles <= n_cta * per
+    assert i.max_splits == max(b - a + 1 for a, b in spans)
+    assert i.needs_combine == (i.max_splits > 1)
+    assert i.kv_bytes == sum(ctx) * hkv * 128 * 4
+    # slot c + pair of each CTA's piece of a pair is unique, and below CTAs + pairs (the workspace's slots)
+    slots = [c + k for k, (a, b) in enumerate(spans) for c in range(a, b + 1)]
+    assert len(slots) == len(set(slots)) and max(slots) < n_cta + len(spans)
+    if split == 0:
+        assert n_cta <= 152
+
+
+@pytest.mark.parametrize("ctx,ql,hkv", CASES)
+def test_chunk_plan_units_cover_every_token_once(ctx, ql, hkv):
+    p = mk(ctx, ql, hq=8 * hkv, hkv=hkv, kernel=pv.KERNEL_WARP_MMA)
+    i = p.info
+    assert i.flat == 0
     assert i.chunk_tokens % i.tile_tokens == 0
     assert i.num_units == hkv * sum((c + i.chunk_tokens - 1) // i.chunk_tokens for c in ctx)
     assert i.max_splits == max((c + i.chunk_tokens - 1) // i.chunk_tokens for c in ctx)

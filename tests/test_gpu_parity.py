@@ -78,6 +78,22 @@ def test_small_against_oracle(name, make, split, kernel):
     assert max_err(got, ref) <= TOL[prob.kv_dtype], name
 
 
+# Flat plans: tiles per CTA of 1, 2, 3 and 5 (split_override = ceil(17 / per)) put segment
+# boundaries everywhere, one-tile segments and CTAs spanning several sequences included.
+SEG_CTX = [1, 17, 128, 129, 255, 300, 640, 1000, 5, 2049, 16, 383]
+SEG_Q = [1, 6, 8, 2, 3, 6, 7, 1, 4, 6, 5, 8]
+
+
+@pytest.mark.parametrize("split", [17, 9, 6, 4, 0])
+@pytest.mark.parametrize("kv", [synth.KV_BF16, synth.KV_FP8], ids=["bf16", "fp8"])
+def test_flat_segments_against_oracle(kv, split):
+    prob = synth.make_problem(SEG_CTX, SEG_Q, 16, 2, 128, kv_dtype=kv, seed=36)
+    ref = oracle.verify_attention(prob)
+    got, va = gpu_run(prob, split_override=split, kernel=pv.KERNEL_TCGEN05)
+    assert va.info["flat"] == 1
+    assert max_err(got, ref) <= TOL[kv]
+
+
 @pytest.mark.parametrize("name,make", SMALL[:3] + SMALL[6:7], ids=[s[0] for s in SMALL[:3] + SMALL[6:7]])
 def test_bf16_output(name, make):
     prob = make()
