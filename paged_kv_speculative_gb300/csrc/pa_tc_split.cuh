@@ -65,8 +65,8 @@ struct TcCfg {
   static constexpr int kOffQ = kOffV + ((VS * kVStage + 1023) / 1024) * 1024;
   static constexpr int kOffP = kOffQ + kQB;
   static constexpr int kOffRow = kOffP + 2 * kPBuf;          // rowC[2][64] f32, rowLim[2][64] i32 (by segment parity)
-  static constexpr int kOffRed = kOffRow + 4 * 64 * 4;       // tile maxima [8 warps][64], then row totals [64]
-  static constexpr int kOffRedL = kOffRed + 9 * 64 * 4;      // row-sum partials [8 warps][64]
+  static constexpr int kOffRed = kOffRow + 4 * 64 * 4;       // tile maxima [8 warps][64], 1 / row totals [64], reference maxima [64]
+  static constexpr int kOffRedL = kOffRed + 10 * 64 * 4;     // row-sum partials [8 warps][64]
   static constexpr int kOffBar = kOffRedL + 8 * 64 * 4;
   static constexpr int kSmem = kOffBar + 256 + 1024;         // barriers, tmem base, alignment slack
   static_assert(NP % 16 == 0 && NP >= 16 && NP <= 64, "N must be 16..64 in steps of 16");
@@ -149,7 +149,8 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* sP = sm + C::kOffP;
   float* rowC = reinterpret_cast<float*>(sm + C::kOffRow);     // [2][64] score multiplier per row
   int* rowLim = reinterpret_cast<int*>(rowC + 128);             // [2][64] last visible key per row (-1: padding)
-  float* red = reinterpret_cast<float*>(sm + C::kOffRed);       // [8 warps][64] maxima, then [64] row totals
+  float* red = reinterpret_cast<float*>(sm + C::kOffRed);       // [8 warps][64] maxima, [64] 1 / row totals, [64] M_r
+  float* refM = red + 9 * 64;                                   // reference maxima of the segment's rows (log2 units)
   float* redl = reinterpret_cast<float*>(sm + C::kOffRedL);     // [8 warps][64] row-sum partials
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   uint64_t* kfull = bars;
@@ -479,8 +480,15 @@ __global__ void __launch_bounds__(352, 1)
     stage_q(cu, wq0, 0);
     named_sync(bar_sync, 128);  // the group's row constants are visible to the group
 
-    // per owned column pair: minus the reference max, score multiplier (FP8), row-sum partial
-    float2 negm[NH / 2], crow2[NH / 2], l[NH / 2];
+    // Per owned column pair, this thread's row-sum partial l. The group-uniform per-column values (the
+    // reference maxima M_r, the FP8 score multiplier) are held one of two ways. Up to 24 columns a
+    // group they sit in registers (as -M_r); at 32 they would spill, and shared memory (broadcast
+    // reads) holds them instead. (Both ways measured: each is the faster one where it is used.)
+    constexpr bool kRegs = NH <= 24;
+    constexpr int kRP = kRegs ? NH / 2 : 1;
+    float2 l[NH / 2];
+    float2 negm[kRP], crow2[kRP];
+    const float* mref = refM + col0;
     int seg = 0, seg_t0 = 0;
 
     // A failed wait marks this thread and skips its later waits, but every
@@ -501,10 +509,13 @@ __global__ void __launch_bounds__(352, 1)
       if (seg_first) {
         seg_t0 = cu.t;
 #pragma unroll
-        for (int c = 0; c < NH / 2; ++c) {
-          negm[c] = make_float2(INFINITY, INFINITY);
-          crow2[c] = make_float2(rowC[sl * 64 + col0 + 2 * c], rowC[sl * 64 + col0 + 2 * c + 1]);
-          l[c] = make_float2(0.f, 0.f);
+        for (int c = 0; c < NH / 2; ++c) l[c] = make_float2(0.f, 0.f);
+        if constexpr (kRegs) {
+#pragma unroll
+          for (int c = 0; c < kRP; ++c) {
+            negm[c] = make_float2(INFINITY, INFINITY);
+            crow2[c] = reinterpret_cast<const float2*>(rowC + sl * 64 + col0)[c];
+          }
         }
         // the next segment's Q rows (the pair after this one, if the range reaches it) into L2
         if (cu.n_t - cu.t < n_tiles - i && gt < NH) {
@@ -559,7 +570,9 @@ __global__ void __launch_bounds__(352, 1)
         inv_sv = __frcp_rn(sv);
         const float2 sk2 = make_float2(sk, sk);
 #pragma unroll
-        for (int c = 0; c < NH / 2; ++c) y[c] = __ffma2_rn(__fmul2_rn(y[c], sk2), crow2[c], ls);
+        for (int c = 0; c < NH / 2; ++c)
+          y[c] = __ffma2_rn(__fmul2_rn(y[c], sk2),
+                            kRegs ? crow2[c % kRP] : reinterpret_cast<const float2*>(rowC + sl * 64 + col0)[c], ls);
       } else {
         const float2 s2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
@@ -577,63 +590,140 @@ __global__ void __launch_bounds__(352, 1)
           if (tabs > lim[2 * c + 1]) y[c].y = -INFINITY;
         }
       }
-      // d = y - M (log2 units); with M = -inf a finite score gives +inf (and a masked one NaN, dropped below)
+      // d = y - M (log2 units); with M = -inf a finite score gives +inf (and a masked one NaN, dropped
+      // below). (Shared-memory way: a segment's first tile has no reference yet and d holds y itself.)
       float2 dl[NH / 2];
-      float dmax = -INFINITY;
+      float dmax;
+      if constexpr (kRegs) {
+        dmax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < NH / 2; ++c) {
-        dl[c] = __fadd2_rn(y[c], negm[c]);
-        dmax = fmaxf(dmax, fmaxf(dl[c].x, dl[c].y));
+        for (int c = 0; c < NH / 2; ++c) {
+          dl[c] = __fadd2_rn(y[c], negm[c % kRP]);
+          dmax = fmaxf(dmax, fmaxf(dl[c].x, dl[c].y));
+        }
+      } else {
+        dmax = INFINITY;
+        if (!seg_first) {
+          dmax = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < NH / 2; ++c) {
+            const float2 m = reinterpret_cast<const float2*>(mref)[c];
+            dl[c] = __fadd2_rn(y[c], make_float2(-m.x, -m.y));
+            dmax = fmaxf(dmax, fmaxf(dl[c].x, dl[c].y));
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < NH / 2; ++c) dl[c] = y[c];
+        }
       }
       if (named_or(bar_or, 128, dmax > 8.f)) {
-        // ---- exact tile maxima of the owned columns, raise the references, rescale l and O
+        if constexpr (kRegs) {
+          // ---- exact tile maxima of the owned columns, raise the references, rescale l and O
 #pragma unroll
-        for (int c = 0; c < NH; ++c) {
-          const float m = warp_max((c & 1) ? y[c >> 1].y : y[c >> 1].x);
-          if (lane == 0) red[(warp - 2) * 64 + col0 + c] = m;
-        }
-        named_sync(bar_sync, 128);
-        const float* rg = red + wg * 4 * 64 + col0;  // this group's 4 warp rows
-        auto old_max = [&](int c) { return (c & 1) ? -negm[c >> 1].y : -negm[c >> 1].x; };
-        auto new_max = [&](int c) {
-          return fmaxf(old_max(c), fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
-        };
-        bool any_scale = false;
+          for (int c = 0; c < NH; ++c) {
+            const float m = warp_max((c & 1) ? y[c >> 1].y : y[c >> 1].x);
+            if (lane == 0) red[(warp - 2) * 64 + col0 + c] = m;
+          }
+          named_sync(bar_sync, 128);
+          const float* rg = red + wg * 4 * 64 + col0;  // this group's 4 warp rows
+          auto old_max = [&](int c) { return (c & 1) ? -negm[(c >> 1) % kRP].y : -negm[(c >> 1) % kRP].x; };
+          auto new_max = [&](int c) {
+            return fmaxf(old_max(c), fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
+          };
+          bool any_scale = false;
 #pragma unroll
-        for (int c = 0; c < NH; ++c) {
-          const float mn = new_max(c);
-          any_scale |= (mn != -INFINITY && mn != old_max(c));
-        }
-        if (any_scale && !seg_first) {
-          wait(&pfree[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u);  // PV of tile i-1 done
-          tc::fence_after_sync();
+          for (int c = 0; c < NH; ++c) {
+            const float mn = new_max(c);
+            any_scale |= (mn != -INFINITY && mn != old_max(c));
+          }
+          if (any_scale && !seg_first) {
+            wait(&pfree[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u);  // PV of tile i-1 done
+            tc::fence_after_sync();
 #pragma unroll
-          for (int c0 = 0; c0 < NH; c0 += 8) {
-            uint32_t r8[8];
-            tc::ld8(tO + lane_off + col0 + c0, r8);
-            tc::wait_ld();
+            for (int c0 = 0; c0 < NH; c0 += 8) {
+              uint32_t r8[8];
+              tc::ld8(tO + lane_off + col0 + c0, r8);
+              tc::wait_ld();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float mn = new_max(c0 + j), mo = old_max(c0 + j);
-              const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
-              r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+              for (int j = 0; j < 8; ++j) {
+                const float mn = new_max(c0 + j), mo = old_max(c0 + j);
+                const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
+                r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+              }
+              tc::st8(tO + lane_off + col0 + c0, r8);
             }
-            tc::st8(tO + lane_off + col0 + c0, r8);
+            tc::wait_st();
           }
-          tc::wait_st();
-        }
 #pragma unroll
-        for (int c = 0; c < NH; ++c) {
-          const float mn = new_max(c), mo = old_max(c);
-          if (mn != -INFINITY && mn != mo) {
-            float& lc = (c & 1) ? l[c >> 1].y : l[c >> 1].x;
-            lc *= fast_exp2(mo - mn);
-            if (c & 1) negm[c >> 1].y = -mn; else negm[c >> 1].x = -mn;
+          for (int c = 0; c < NH; ++c) {
+            const float mn = new_max(c), mo = old_max(c);
+            if (mn != -INFINITY && mn != mo) {
+              float& lc = (c & 1) ? l[c >> 1].y : l[c >> 1].x;
+              lc *= fast_exp2(mo - mn);
+              if (c & 1) negm[(c >> 1) % kRP].y = -mn; else negm[(c >> 1) % kRP].x = -mn;
+            }
           }
-        }
 #pragma unroll
-        for (int c = 0; c < NH / 2; ++c) dl[c] = __fadd2_rn(y[c], negm[c]);
-        // red is rewritten only after the next vote (a barrier of this group), when every read here is done
+          for (int c = 0; c < NH / 2; ++c) dl[c] = __fadd2_rn(y[c], negm[c % kRP]);
+          // red is rewritten only after the next vote (a barrier of this group), when every read here is done
+        } else {
+          // ---- exact tile maxima of the owned columns, raise the references, rescale l and O
+#pragma unroll
+          for (int c = 0; c < NH; ++c) {
+            // tile max of y = max of d + the group-uniform offset
+            const float m = warp_max((c & 1) ? dl[c >> 1].y : dl[c >> 1].x) + (seg_first ? 0.f : mref[c]);
+            if (lane == 0) red[(warp - 2) * 64 + col0 + c] = m;
+          }
+          named_sync(bar_sync, 128);
+          const float* rg = red + wg * 4 * 64 + col0;  // this group's 4 warp rows
+          auto old_max = [&](int c) { return seg_first ? -INFINITY : mref[c]; };
+          auto new_max = [&](int c) {
+            return fmaxf(old_max(c), fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
+          };
+          bool any_scale = false;
+#pragma unroll
+          for (int c = 0; c < NH; ++c) {
+            const float mn = new_max(c);
+            any_scale |= (mn != -INFINITY && mn != old_max(c));
+          }
+          if (any_scale && !seg_first) {
+            wait(&pfree[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u);  // PV of tile i-1 done
+            tc::fence_after_sync();
+#pragma unroll
+            for (int c0 = 0; c0 < NH; c0 += 8) {
+              uint32_t r8[8];
+              tc::ld8(tO + lane_off + col0 + c0, r8);
+              tc::wait_ld();
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float mn = new_max(c0 + j), mo = old_max(c0 + j);
+                const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
+                r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+              }
+              tc::st8(tO + lane_off + col0 + c0, r8);
+            }
+            tc::wait_st();
+          }
+#pragma unroll
+          for (int c = 0; c < NH; ++c) {
+            const float mn = new_max(c), mo = old_max(c);
+            if (mn != -INFINITY && mn != mo) {
+              float& lc = (c & 1) ? l[c >> 1].y : l[c >> 1].x;
+              lc *= fast_exp2(mo - mn);
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < NH / 2; ++c) {
+            const float o0 = seg_first ? 0.f : mref[2 * c], o1 = seg_first ? 0.f : mref[2 * c + 1];
+            dl[c] = __fadd2_rn(dl[c], make_float2(o0 - new_max(2 * c), o1 - new_max(2 * c + 1)));
+          }
+          // every thread of the group has read the old references: one thread per column writes the new one
+          const float mine = gt < NH ? new_max(gt) : 0.f;
+          named_sync(bar_sync, 128);
+          if (gt < NH) refM[col0 + gt] = mine;
+          named_sync(bar_sync, 128);
+          // red is rewritten only after the next vote (a barrier of this group), when every read here is done
+        }
       }
       // ---- P = 2^(y - M) (<= 2^8), row sums, P into shared memory as the MMA's B operand
       const int pb = i & 1;
@@ -739,11 +829,13 @@ __global__ void __launch_bounds__(352, 1)
           const float* rl = redl + wg * 4 * 64 + cc;
           const float s2 = (rl[0] + rl[64]) + (rl[128] + rl[192]);
           rinv[cc] = s2 > 0.f ? __frcp_rn(s2) : 0.f;
-          float mg = -INFINITY;  // this column's reference max (registers hold every column's)
+          float mg = kRegs ? -INFINITY : refM[cc];  // this column's reference max
+          if constexpr (kRegs) {
 #pragma unroll
-          for (int c = 0; c < NH / 2; ++c) {
-            if (2 * c == gt) mg = -negm[c].x;
-            if (2 * c + 1 == gt) mg = -negm[c].y;
+            for (int c = 0; c < NH / 2; ++c) {
+              if (2 * c == gt) mg = -negm[c % kRP].x;
+              if (2 * c + 1 == gt) mg = -negm[c % kRP].y;
+            }
           }
           if (ok_sm && !whole && cc < rows)
             p.part_lse[u * p.rows_max + cc] = s2 > 0.f ? mg + __log2f(s2) : -INFINITY;
