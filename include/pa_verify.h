@@ -151,6 +151,15 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
 int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info);
 
 /*
+ * A static flat plan's CTA ranges: starts_out[c] is CTA c's first tile and
+ * starts_out[num_units] = total_tiles (tile t = 128 tokens of the t-th place
+ * in the flat order of (sequence, KV head) pairs). Writes num_units + 1
+ * values and returns that count; PA_ERR_INVALID for other plans or when
+ * `capacity` is smaller. Host only, no CUDA call.
+ */
+int pa_verify_plan_get_cta_starts(pa_verify_plan_t plan, int32_t* starts_out, int32_t capacity);
+
+/*
  * Enqueues verify attention on `stream` and returns without waiting.
  *   q            [T, Hq, D] bf16, the q_b rows of each sequence packed in batch order
  *   k_cache      [N_pg, Hkv, 16, D] bf16 or E4M3 bytes, 16-byte aligned base

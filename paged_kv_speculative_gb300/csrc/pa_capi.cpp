@@ -49,6 +49,8 @@ struct pa_verify_plan_s {
   int32_t kernel = PA_KERNEL_WARP_MMA;
   int32_t dynamic = 0;           // capacity plan: the work table is built on the device each run
   int32_t flat = 0, per = 0, total_tiles = 0;  // flat plans (tcgen05 kernel): tiles per CTA, tiles in all
+  int32_t ranged = 0;            // flat plans: cta_start lists the CTAs' ranges
+  int32_t cta_start[kMaxCtaTable + 1];
   int64_t part_units = 0;        // partial slots in the workspace
   int32_t max_len = 0, max_q = 0, slots = 0;
   size_t off_dyn = 0, off_part = kWsHeader, off_lse = kWsHeader;  // workspace layout
@@ -177,6 +179,8 @@ void fill_params(SplitParams& p, pa_verify_plan_t plan, const void* q, const flo
   p.flat = plan->flat;
   p.per = plan->per;
   p.total_tiles = plan->total_tiles;
+  p.ranged = plan->ranged;
+  if (plan->ranged) std::memcpy(p.cta_start, plan->cta_start, sizeof(int32_t) * (plan->units + 1));
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
   std::memcpy(p.seq, plan->seq, sizeof(plan->seq));
 }
@@ -199,7 +203,7 @@ cudaError_t launch_all(pa_verify_plan_t plan, SplitParams& p, cudaStream_t s, bo
         : fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s)
               : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s);
   if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[1], s);
-  if (e == cudaSuccess && plan->needs_combine) e = launch_combine(d.head_dim, &p, s);
+  if (e == cudaSuccess && plan->needs_combine) e = launch_combine(d.head_dim, &p, plan->max_splits, s);
   if (e == cudaSuccess && prof) {
     e = cudaEventRecord(plan->ev[2], s);
     plan->profiled_runs++;
@@ -208,11 +212,59 @@ cudaError_t launch_all(pa_verify_plan_t plan, SplitParams& p, cudaStream_t s, bo
   return e;
 }
 
+// A CTA that moves from one (sequence, KV head) pair to the next pays for the
+// switch (the outgoing pair's epilogue, the incoming pair's Q and first-tile
+// maxima, mostly code that runs cold while HBM is saturated) about what ten
+// more tiles would cost: fitted on GB300 to whole-kernel times of plans with
+// and without switches (a tile is 1.5-1.8 us, a switch 10-15 us).
+constexpr int64_t kSwitchTiles = 10;
+
+// Cuts the pairs' tiles (in flat order, pair sizes `nt`) into consecutive CTA
+// ranges whose cost, tiles plus kSwitchTiles for every pair after the first,
+// stays within `tau`; returns the CTA count and, with `starts`, each CTA's
+// first tile followed by the total.
+int64_t pack_ranges(const std::vector<int64_t>& nt, int64_t tau, std::vector<int32_t>* starts) {
+  int64_t ctas = 0, load = 0, pos = 0;
+  bool open = false;
+  if (starts) starts->clear();
+  for (const int64_t n : nt) {
+    int64_t rem = n;
+    while (rem > 0) {
+      if (!open) {
+        if (starts) starts->push_back(static_cast<int32_t>(pos));
+        open = true;
+        load = 0;
+      }
+      const int64_t enter = load > 0 ? kSwitchTiles : 0;
+      const int64_t room = tau - load - enter;
+      if (room <= 0) {  // no tile of this pair fits any more: the next CTA takes it
+        ++ctas;
+        open = false;
+        continue;
+      }
+      const int64_t take = std::min(rem, room);
+      load += enter + take;
+      rem -= take;
+      pos += take;
+      if (load >= tau) {
+        ++ctas;
+        open = false;
+      }
+    }
+  }
+  if (open) ++ctas;
+  if (starts) starts->push_back(static_cast<int32_t>(pos));
+  return ctas;
+}
+
 // Flat plan of the tcgen05 kernel: the (sequence, KV head) pairs laid end to
-// end as 128-token tiles, longest sequences first, and every CTA the same
-// number of consecutive tiles, so one wave of CTAs finishes together whatever
-// the length mix. (`split_override` = n asks for ceil(longest pair / n) tiles
-// per CTA instead.)
+// end as 128-token tiles, longest sequences first, cut into one wave of
+// consecutive CTA ranges. The cut minimises the largest CTA cost (tiles plus
+// kSwitchTiles per pair switch): binary search on the cost bound, greedy
+// filling at each bound. So long pairs are split evenly while short ones are
+// packed whole, and a CTA crosses into the next pair only where that pays.
+// (`split_override` = n asks for ceil(longest pair / n) tiles per CTA instead,
+// and so do plans needing more CTAs than the range table holds.)
 int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, const int32_t* ql, int sms,
               pa_verify_plan_t* plan_out, size_t* workspace_bytes_out) {
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
@@ -254,13 +306,38 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
   }
   int64_t per = d.split_override > 0 ? (max_nt + d.split_override - 1) / d.split_override : (tiles + sms - 1) / sms;
   per = std::max<int64_t>(per, 1);
-  const int64_t n_cta = (tiles + per - 1) / per;
+  int64_t n_cta = (tiles + per - 1) / per;
+  P->ranged = 0;
+  if (d.split_override == 0 && tiles > 0) {
+    std::vector<int64_t> nt;
+    for (int k = 0; k < d.num_seqs; ++k)
+      for (int g = 0; g < Hkv; ++g) nt.push_back(P->seq[k].n_tiles);
+    int64_t lo = (tiles + sms - 1) / sms, hi = tiles;  // a bound of `tiles` always fits one CTA
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) / 2;
+      if (pack_ranges(nt, mid, nullptr) <= sms) hi = mid; else lo = mid + 1;
+    }
+    std::vector<int32_t> starts;
+    const int64_t n = pack_ranges(nt, lo, &starts);
+    if (n <= kMaxCtaTable) {
+      P->ranged = 1;
+      n_cta = n;
+      std::copy(starts.begin(), starts.end(), P->cta_start);
+      per = lo;  // the cost bound, reported as the chunk
+    }
+  }
+  // CTA holding tile f
+  auto cta_of = [&](int64_t f) -> int64_t {
+    if (!P->ranged) return f / per;
+    return static_cast<int64_t>(std::upper_bound(P->cta_start, P->cta_start + n_cta + 1, static_cast<int32_t>(f)) -
+                                P->cta_start) - 1;
+  };
   int max_splits = 0;
   for (int k = 0; k < d.num_seqs; ++k)
     for (int g = 0; g < Hkv; ++g) {
       const int64_t t0 = P->seq[k].tile_start + static_cast<int64_t>(g) * P->seq[k].n_tiles;
       const int64_t t1 = t0 + P->seq[k].n_tiles - 1;
-      max_splits = std::max<int>(max_splits, static_cast<int>(t1 / per - t0 / per + 1));
+      max_splits = std::max<int>(max_splits, static_cast<int>(cta_of(t1) - cta_of(t0) + 1));
     }
   P->kernel = PA_KERNEL_TCGEN05;
   P->flat = 1;
@@ -440,6 +517,17 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
   *plan_out = P;
   *workspace_bytes_out = ws;
   return PA_OK;
+}
+
+int pa_verify_plan_get_cta_starts(pa_verify_plan_t plan, int32_t* starts_out, int32_t capacity) {
+  g_last_error.clear();
+  if (!plan || !starts_out) return fail(PA_ERR_INVALID, "plan and starts_out must not be NULL");
+  if (!plan->flat || plan->dynamic) return fail(PA_ERR_INVALID, "only static flat plans have CTA ranges");
+  if (capacity < plan->units + 1) return fail(PA_ERR_INVALID, "capacity below num_units + 1");
+  for (int32_t c = 0; c <= plan->units; ++c)
+    starts_out[c] = plan->ranged ? plan->cta_start[c]
+                                 : static_cast<int32_t>(std::min<int64_t>(static_cast<int64_t>(c) * plan->per, plan->total_tiles));
+  return plan->units + 1;
 }
 
 int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info) {

@@ -16,6 +16,7 @@ constexpr int kMaxQueryLen = 8;
 constexpr int kWsHeader = 256;    // workspace bytes before the partials (device error word at offset 0)
 
 constexpr int kFlatTile = 128;   // tokens per tile of a flat plan
+constexpr int kMaxCtaTable = 512; // flat plans: CTAs whose tile ranges a plan can list in the kernel parameters
 
 // Per-sequence entry of the work description, sorted by decreasing context
 // length so that the longest units are scheduled first.
@@ -77,8 +78,10 @@ struct SplitParams {
   int32_t out_f32;
   int32_t num_rows;             // sum_b q_b * Hq (combine grid)
   int32_t flat;                 // 1: flat plan (tiles per CTA), 0: chunk plan
-  int32_t per;                  // flat plans: tiles per CTA
+  int32_t per;                  // flat plans: tiles per CTA (when no range table is given)
   int32_t total_tiles;          // flat plans: tiles of every pair
+  int32_t ranged;               // flat plans: 1 when cta_start lists every CTA's first tile
+  int32_t cta_start[kMaxCtaTable + 1];  // CTA c covers tiles [cta_start[c], cta_start[c + 1])
   float scale_log2;             // softmax_scale * log2(e)
   const DynWork* dyn;           // dynamic plans: the device-written work table; else null
   SeqInfo seq[kMaxSeqs];
@@ -91,12 +94,28 @@ struct SplitParams {
 struct WorkView {
   const SeqInfo* seq;
   int num_seqs, chunk, num_units, num_rows, per, total_tiles;
+  const int32_t* cta_start;  // flat plans with a range table, else null (CTA c starts at c * per)
 };
 __device__ __forceinline__ WorkView work_view(const SplitParams& p) {
   if (p.dyn)
     return WorkView{p.dyn->seq, p.num_seqs, p.dyn->chunk, p.dyn->num_units, p.dyn->num_rows, p.dyn->per,
-                    p.dyn->total_tiles};
-  return WorkView{p.seq, p.num_seqs, p.chunk, p.num_units, p.num_rows, p.per, p.total_tiles};
+                    p.dyn->total_tiles, nullptr};
+  return WorkView{p.seq, p.num_seqs, p.chunk, p.num_units, p.num_rows, p.per, p.total_tiles,
+                  p.ranged ? p.cta_start : nullptr};
+}
+// First tile of CTA c of a flat plan (c = num_units gives the end).
+__device__ __forceinline__ int flat_cta_start(const WorkView& wv, int c) {
+  return wv.cta_start ? wv.cta_start[c] : min(c * wv.per, wv.total_tiles);
+}
+// The CTA of a flat plan whose range holds tile f.
+__device__ __forceinline__ int flat_cta_of(const WorkView& wv, int f) {
+  if (!wv.cta_start) return f / wv.per;
+  int lo = 0, hi = wv.num_units - 1;  // the last CTA starting at or before f
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (wv.cta_start[mid] <= f) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 // Index of the entry whose tiles contain flat tile f (the last entry with tile_start <= f).
 __device__ __forceinline__ int flat_seq_of(const WorkView& wv, int f) {
@@ -123,7 +142,7 @@ __host__ __device__ constexpr int split_smem_bytes(int kv_fp8, int d) {
 // CTAs of the split kernel resident per SM (shared memory bound), used by the planner.
 __host__ __device__ constexpr int split_ctas_per_sm(int warps) { return warps <= 4 ? 2 : 1; }
 
-cudaError_t launch_combine(int head_dim, const SplitParams* p, cudaStream_t stream);
+cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, cudaStream_t stream);
 
 }  // namespace pav
 

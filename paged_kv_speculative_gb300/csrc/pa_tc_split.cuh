@@ -171,8 +171,8 @@ __global__ void __launch_bounds__(352, 1)
   const int cta = blockIdx.x;
   const WorkView wv = work_view(p);
   if (cta >= wv.num_units) return;  // a dynamic plan's grid covers its capacity
-  const int f_lo = cta * wv.per;
-  const int n_tiles = min(wv.per, wv.total_tiles - f_lo);
+  const int f_lo = flat_cta_start(wv, cta);
+  const int n_tiles = flat_cta_start(wv, cta + 1) - f_lo;
   const int Hkv = p.num_kv_heads, G = p.group;
 
   // Work that needs neither the barriers nor tensor memory starts before the

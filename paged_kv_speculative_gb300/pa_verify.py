@@ -42,7 +42,7 @@ DEVERR_TIMEOUT = 4
 EXPORTED = ("pa_verify_plan", "pa_verify_plan_get_info", "pa_verify_run", "pa_verify_free",
             "pa_verify_device_errors", "pa_verify_last_error", "pa_verify_profile_enable",
             "pa_verify_profile_read", "pa_kv_write", "pa_greedy_verdict_workspace_bytes",
-            "pa_greedy_verdict", "pa_verify_run_static", "pa_verify_plan_dynamic")
+            "pa_greedy_verdict", "pa_verify_run_static", "pa_verify_plan_dynamic", "pa_verify_plan_get_cta_starts")
 
 
 class PaVerifyError(RuntimeError):
@@ -93,6 +93,8 @@ def lib(path: Optional[str] = None):
     L.pa_verify_plan_dynamic.restype = ctypes.c_int
     L.pa_verify_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
     L.pa_verify_plan_get_info.restype = ctypes.c_int
+    L.pa_verify_plan_get_cta_starts.argtypes = [vp, i32p, ctypes.c_int32]
+    L.pa_verify_plan_get_cta_starts.restype = ctypes.c_int
     L.pa_verify_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     L.pa_verify_run.restype = ctypes.c_int
     L.pa_verify_run_static.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
@@ -137,6 +139,13 @@ class Plan:
         info = PlanInfo()
         _check(lib().pa_verify_plan_get_info(handle, ctypes.byref(info)))
         self.info = info
+
+    def cta_starts(self) -> list:
+        """A static flat plan's CTA ranges: CTA c covers flat tiles [s[c], s[c + 1])."""
+        buf = (ctypes.c_int32 * (self.info.num_units + 1))()
+        n = lib().pa_verify_plan_get_cta_starts(self.handle, buf, len(buf))
+        _check(min(n, 0))
+        return list(buf[:n])
 
     def free(self):
         if self.handle:

@@ -50,44 +50,88 @@ CASES = [([37, 100], [1, 6], 1), ([4096 + 7 * i for i in range(8)], [6] * 8, 4),
          ([1 << 20], [6], 1), ([5, 9000, 131072, 64], [3, 8, 1, 2], 2)]
 
 
+SWITCH_TILES = 10  # a pair switch costs about ten tiles (the planner's figure)
+
+
+def pack(nt, tau):
+    """Greedy cut of the tiles into CTA ranges of cost (tiles + 10 per pair switch) <= tau."""
+    starts, ctas, load, pos, open_ = [], 0, 0, 0, False
+    for n in nt:
+        rem = n
+        while rem > 0:
+            if not open_:
+                starts.append(pos)
+                open_, load = True, 0
+            enter = SWITCH_TILES if load > 0 else 0
+            room = tau - load - enter
+            if room <= 0:
+                ctas, open_ = ctas + 1, False
+                continue
+            take = min(rem, room)
+            load, rem, pos = load + enter + take, rem - take, pos + take
+            if load >= tau:
+                ctas, open_ = ctas + 1, False
+    ctas += open_
+    return ctas, starts + [pos]
+
+
 def flat_model(ctx, hkv, sms, split_override=0):
-    """Independent model of a flat plan: pairs (longest sequence first, then
-    KV head) end to end as 128-token tiles, the same tile count per CTA.
-    Returns (tiles per CTA, CTAs, every pair's (first CTA, last CTA))."""
+    """Independent model of a flat plan: pairs (longest sequence first, then KV
+    head) end to end as 128-token tiles, cut into CTA ranges. Returns (CTA
+    starts, every pair's (first tile, tiles))."""
     order = sorted(range(len(ctx)), key=lambda b: -ctx[b])  # stable: ties keep batch order
-    nt = [(c + 127) // 128 for c in ctx]
-    total = hkv * sum(nt)
+    nt = [(ctx[b] + 127) // 128 for b in order for _ in range(hkv)]
+    total = sum(nt)
+    pairs, t = [], 0
+    for n in nt:
+        pairs.append((t, n))
+        t += n
     if split_override:
         per = max(1, -(-max(nt) // split_override))
-    else:
-        per = max(1, -(-total // sms))
-    spans, t = [], 0
-    for b in order:
-        for _ in range(hkv):
-            spans.append((t // per, (t + nt[b] - 1) // per))
-            t += nt[b]
-    return per, -(-total // per), spans
+        return [min(c * per, total) for c in range(-(-total // per) + 1)], pairs
+    lo, hi = -(-total // sms), total
+    while lo < hi:
+        mid = (lo + hi) // 2
+        if pack(nt, mid)[0] <= sms:
+            hi = mid
+        else:
+            lo = mid + 1
+    return pack(nt, lo)[1], pairs
 
 
 @pytest.mark.parametrize("ctx,ql,hkv", CASES)
 @pytest.mark.parametrize("split", [0, 1, 4, 1000])
-def test_flat_plan_gives_every_cta_the_same_tiles(ctx, ql, hkv, split):
+def test_flat_plan_ranges(ctx, ql, hkv, split):
     p = mk(ctx, ql, hq=8 * hkv, hkv=hkv, split_override=split)
     i = p.info
     assert i.flat == 1 and i.kernel == pv.KERNEL_TCGEN05 and i.tile_tokens == 128
-    per, n_cta, spans = flat_model(ctx, hkv, 152, split)
-    assert i.total_tiles == hkv * sum((c + 127) // 128 for c in ctx)
-    assert i.chunk_tokens == 128 * per and i.num_units == n_cta
-    # every CTA but the last holds exactly `per` tiles: the tiles are covered once
-    assert (n_cta - 1) * per < i.total_tiles <= n_cta * per
+    starts, pairs = flat_model(ctx, hkv, 152, split)
+    assert p.cta_starts() == starts
+    assert i.total_tiles == hkv * sum((c + 127) // 128 for c in ctx) == starts[-1]
+    assert i.num_units == len(starts) - 1
+    # the ranges tile the flat space once, without empty CTAs
+    assert starts[0] == 0 and all(a < b for a, b in zip(starts, starts[1:]))
+    cta_of = lambda f: max(c for c in range(len(starts) - 1) if starts[c] <= f)
+    spans = [(cta_of(t0), cta_of(t0 + n - 1)) for t0, n in pairs]
     assert i.max_splits == max(b - a + 1 for a, b in spans)
     assert i.needs_combine == (i.max_splits > 1)
     assert i.kv_bytes == sum(ctx) * hkv * 128 * 4
     # slot c + pair of each CTA's piece of a pair is unique, and below CTAs + pairs (the workspace's slots)
     slots = [c + k for k, (a, b) in enumerate(spans) for c in range(a, b + 1)]
-    assert len(slots) == len(set(slots)) and max(slots) < n_cta + len(spans)
+    assert len(slots) == len(set(slots)) and max(slots) < i.num_units + len(spans)
     if split == 0:
-        assert n_cta <= 152
+        assert i.num_units <= 152
+        # no CTA costs more than the bound the plan reports (tiles + 10 per pair switch)
+        for c in range(i.num_units):
+            segs = sum(1 for a, b in spans if a <= c <= b)
+            assert starts[c + 1] - starts[c] + SWITCH_TILES * (segs - 1) <= i.chunk_tokens // 128
+
+
+def test_flat_plan_does_not_cross_pairs_needlessly():
+    # 8 equal pairs of 64 tiles on 16 SMs: two CTAs per pair, no CTA spanning two pairs
+    p = mk([8192] * 8, [6] * 8, hq=8, hkv=1, sms=16)
+    starts = p.cta_starts()
+    assert starts == list(range(0, 8 * 64 + 1, 32))
 
 
 @pytest.mark.parametrize("ctx,ql,hkv", CASES)
