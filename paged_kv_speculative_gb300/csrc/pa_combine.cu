@@ -2,9 +2,11 @@
 // MTP-5 routing page, Motivation):
 //   M = max_s lse_s,  out = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M)
 // where O_s is the normalised partial of split s and lse_s its log2-sum-exp.
-// A CTA has eight warps; W of them share an output row (token, q head), so a
-// CTA covers 8 / W rows. W grows with the plan's split count (1 up to 8
-// splits, 8 from 33 on): each warp takes every W-th split, eight splits a
+// W warps share an output row (token, q head); W grows with the plan's split
+// count (1 up to 8 splits, 8 from 33 on). With W = 1 a CTA is two warps (two
+// rows), small enough (64 threads, no shared memory) to sit on an SM beside a
+// split-kernel CTA, so the grid's first CTAs are resident and waiting when the
+// split kernel ends; otherwise a CTA is eight warps. Each warp takes every W-th split, eight splits a
 // round, loading their lse values and its lanes' D/32 columns together (one
 // memory round trip per round; rounds combine online, the running sums
 // rescaled when the maximum rises); the W warps of a row then merge in shared
@@ -16,7 +18,8 @@
 
 namespace pav {
 
-constexpr int kCombineWarps = 8;
+constexpr int kCombineWarpsWide = 8;  // CTAs with W > 1
+constexpr int kCombineWarpsNarrow = 2; // CTAs with W = 1
 
 __device__ __forceinline__ float ld_cg(const float* p) {
   float v;
@@ -29,18 +32,19 @@ int combine_warps_per_row(int max_splits) {
   return max_splits <= 8 ? 1 : max_splits <= 16 ? 2 : max_splits <= 32 ? 4 : 8;
 }
 
-template <int D>
-__global__ void __launch_bounds__(32 * kCombineWarps) pa_combine_kernel(const __grid_constant__ SplitParams p, int W) {
+template <int D, int kWarps>
+__global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_constant__ SplitParams p, int W) {
   constexpr int kPer = D / 32;  // columns per lane
   constexpr int kRound = 8;     // splits in flight per round
-  __shared__ float sm_m[kCombineWarps], sm_w[kCombineWarps];
-  __shared__ float sm_acc[kCombineWarps][D];
+  constexpr int kSm = kWarps > 2 ? kWarps : 1;  // the W = 1 form needs no shared memory
+  __shared__ float sm_m[kSm], sm_w[kSm];
+  __shared__ float sm_acc[kSm][kWarps > 2 ? D : 1];
 
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wi = warp % W;  // this warp's share of the row's splits
-  const int rho = blockIdx.x * (kCombineWarps / W) + warp / W;
+  const int rho = blockIdx.x * (kWarps / W) + warp / W;
   const WorkView wv = work_view(p);
   int n = 0, i = 0, h = 0;
   size_t u0 = 0, q_off = 0;
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps) pa_combine_kernel(const __
       M = m;
     }
   }
-  if (W > 1) {  // the row's W warps merge: each rescales to the row maximum
+  if (kWarps > 2 && W > 1) {  // the row's W warps merge: each rescales to the row maximum
     if (lane == 0) sm_m[warp] = M;
     __syncthreads();
     const int w0 = warp - wi;
@@ -124,7 +128,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps) pa_combine_kernel(const __
     const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - Mr);
     if (lane == 0) sm_w[warp] = wsum * a;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) sm_acc[warp][lane * kPer + e] = acc[e] * a;
+    for (int e = 0; e < kPer; ++e) sm_acc[warp % kSm][(lane * kPer + e) % (kWarps > 2 ? D : 1)] = acc[e] * a;
     __syncthreads();
     if (wi == 0) {
       wsum = 0.f;
@@ -133,7 +137,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps) pa_combine_kernel(const __
       for (int k = 0; k < W; ++k) {
         wsum += sm_w[w0 + k];
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) acc[e] += sm_acc[w0 + k][lane * kPer + e];
+        for (int e = 0; e < kPer; ++e) acc[e] += sm_acc[(w0 + k) % kSm][(lane * kPer + e) % (kWarps > 2 ? D : 1)];
       }
     }
   }
@@ -151,10 +155,11 @@ __global__ void __launch_bounds__(32 * kCombineWarps) pa_combine_kernel(const __
 cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, cudaStream_t stream) {
   if (p->num_rows <= 0) return cudaSuccess;
   const int W = combine_warps_per_row(max_splits);
-  const int rows_per_cta = kCombineWarps / W;
+  const int warps = W == 1 ? kCombineWarpsNarrow : kCombineWarpsWide;
+  const int rows_per_cta = warps / W;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p->num_rows + rows_per_cta - 1) / rows_per_cta);
-  cfg.blockDim = dim3(32 * kCombineWarps);
+  cfg.blockDim = dim3(32 * warps);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -162,8 +167,13 @@ cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64>, *p, W);
-  if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128>, *p, W);
+  if (W == 1) {
+    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsNarrow>, *p, W);
+    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsNarrow>, *p, W);
+  } else {
+    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsWide>, *p, W);
+    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsWide>, *p, W);
+  }
   return cudaErrorInvalidValue;
 }
 
