@@ -39,6 +39,9 @@ WORKLOAD_DESC = {
     "mixed_fp8": "mixed FP8 batch: B=64 q U{1..8} Hq=16 Hkv=2 D=128, ctx lognormal(median 8192, sigma 1, cap 131072) (seed 4)",
     "ctx1mi_bf16": "1Mi-token verify bf16 KV: B=1 q=6 Hq=8 Hkv=1 D=128, ctx 1048576, 65536-entry table, random page order (seed 5)",
 }
+for _bs in (1, 2, 4, 8):
+    WORKLOAD_DESC[f"d256_fp8_bs{_bs}"] = (f"head_dim 256 FP8 E4M3 KV + per-token fp32 scales: B={_bs} q=6 Hq=8 Hkv=1 "
+                                          "(48 rows), ctx 150000 each, scattered pages (seed 6)")
 
 
 def kernel_source_hash() -> str:
@@ -300,7 +303,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="mtp5_bf16", choices=list(synth.CONFIG_NAMES))
+    ap.add_argument("--config", default="mtp5_bf16", choices=list(synth.ALL_NAMES))
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=3.0, help="seconds of oracle time per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -29,8 +29,8 @@ cudaError_t launch_split_fp8(int head_dim, int warps, int units, const CUtensorM
 cudaError_t launch_dyn_plan(const int32_t* ctx, const int32_t* ql, DynWork* out, uint32_t* err, int flat, int num_seqs,
                             int num_q_heads, int num_kv_heads, int bt_stride, int max_len, int max_q, int slots, int tile,
                             int max_chunk, cudaStream_t stream);
-cudaError_t launch_tc_split(int kv_fp8, int rows_max, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
-                            const SplitParams* p, cudaStream_t stream);
+cudaError_t launch_tc_split(int head_dim, int kv_fp8, int rows_max, int units, const CUtensorMap* tmk,
+                            const CUtensorMap* tmv, const SplitParams* p, cudaStream_t stream);
 cudaError_t launch_kv_write(int head_dim, int fp8, int n_tokens, int num_kv_heads, int num_pages, const void* k_new,
                             const void* v_new, const int64_t* slot_mapping, void* k_cache, void* v_cache,
                             float* k_scale, float* v_scale, uint32_t* err, cudaStream_t stream);
@@ -199,7 +199,7 @@ cudaError_t launch_all(pa_verify_plan_t plan, SplitParams& p, cudaStream_t s, bo
   if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[0], s);
   if (e == cudaSuccess)
     e = plan->kernel == PA_KERNEL_TCGEN05
-            ? launch_tc_split(fp8 ? 1 : 0, plan->rows_max, plan->units, &plan->tmk, &plan->tmv, &p, s)
+            ? launch_tc_split(d.head_dim, fp8 ? 1 : 0, plan->rows_max, plan->units, &plan->tmk, &plan->tmv, &p, s)
         : fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s)
               : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s);
   if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[1], s);
@@ -389,8 +389,8 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
   if (d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_FP8_E4M3) return fail(PA_ERR_INVALID, "unknown kv_dtype");
   if (d.out_dtype != PA_OUT_BF16 && d.out_dtype != PA_OUT_F32) return fail(PA_ERR_INVALID, "unknown out_dtype");
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
-  if (fp8 ? d.head_dim != 128 : (d.head_dim != 64 && d.head_dim != 128))
-    return fail(PA_ERR_UNSUPPORTED, fp8 ? "FP8 KV needs head_dim 128" : "bf16 KV needs head_dim 64 or 128");
+  if (fp8 ? (d.head_dim != 128 && d.head_dim != 256) : (d.head_dim != 64 && d.head_dim != 128))
+    return fail(PA_ERR_UNSUPPORTED, fp8 ? "FP8 KV needs head_dim 128 or 256" : "bf16 KV needs head_dim 64 or 128");
   if (d.num_seqs > 0 && (d.num_pages < 1 || d.block_table_stride < 1))
     return fail(PA_ERR_INVALID, "num_pages and block_table_stride must be >= 1");
   if (static_cast<int64_t>(d.num_pages) * d.num_kv_heads * kPage >= (int64_t(1) << 31))
@@ -432,12 +432,16 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
     *workspace_bytes_out = P->ws_bytes;
     return PA_OK;
   }
-  const bool tc_ok = d.head_dim == 128 && rows_max <= 64;
+  const bool tc_ok = (d.head_dim == 128 || d.head_dim == 256) && rows_max <= 64;
   if (d.kernel == PA_KERNEL_TCGEN05 && !tc_ok) {
     delete P;
-    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs head_dim 128 and q_len * group <= 64");
+    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs head_dim 128 (or 256 with FP8 KV) and q_len * group <= 64");
   }
   const bool use_tc = d.kernel == PA_KERNEL_TCGEN05 || (d.kernel == PA_KERNEL_AUTO && tc_ok);
+  if (d.head_dim == 256 && !use_tc) {
+    delete P;
+    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only (q_len * group <= 64)");
+  }
   const int tile = use_tc ? 128 : tile_tokens(fp8 ? 1 : 0, d.head_dim);
   const int warps = supported_warps(rows_max);
   const int64_t slots = static_cast<int64_t>(sms) * (use_tc ? 1 : split_ctas_per_sm(warps));
@@ -705,8 +709,8 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
   if (d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_FP8_E4M3) return fail(PA_ERR_INVALID, "unknown kv_dtype");
   if (d.out_dtype != PA_OUT_BF16 && d.out_dtype != PA_OUT_F32) return fail(PA_ERR_INVALID, "unknown out_dtype");
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
-  if (fp8 ? d.head_dim != 128 : (d.head_dim != 64 && d.head_dim != 128))
-    return fail(PA_ERR_UNSUPPORTED, fp8 ? "FP8 KV needs head_dim 128" : "bf16 KV needs head_dim 64 or 128");
+  if (fp8 ? (d.head_dim != 128 && d.head_dim != 256) : (d.head_dim != 64 && d.head_dim != 128))
+    return fail(PA_ERR_UNSUPPORTED, fp8 ? "FP8 KV needs head_dim 128 or 256" : "bf16 KV needs head_dim 64 or 128");
   if (d.num_pages < 1 || d.block_table_stride < 1) return fail(PA_ERR_INVALID, "num_pages and block_table_stride must be >= 1");
   if (static_cast<int64_t>(d.num_pages) * d.num_kv_heads * kPage >= (int64_t(1) << 31))
     return fail(PA_ERR_UNSUPPORTED, "num_pages * num_kv_heads * 16 must stay below 2^31");
@@ -727,10 +731,12 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("SM count query failed: ") + cudaGetErrorString(e));
   }
-  const bool tc_ok = d.head_dim == 128 && rows_max <= 64;
+  const bool tc_ok = (d.head_dim == 128 || d.head_dim == 256) && rows_max <= 64;
   if (d.kernel == PA_KERNEL_TCGEN05 && !tc_ok)
-    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs head_dim 128 and q_len * group <= 64");
+    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs head_dim 128 (or 256 with FP8 KV) and q_len * group <= 64");
   const bool use_tc = d.kernel == PA_KERNEL_TCGEN05 || (d.kernel == PA_KERNEL_AUTO && tc_ok);
+  if (d.head_dim == 256 && !use_tc)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only (q_len * group <= 64)");
   const int warps = supported_warps(rows_max);
   const int64_t slots = static_cast<int64_t>(sms) * (use_tc ? 1 : split_ctas_per_sm(warps));
   const int64_t per_pair = (static_cast<int64_t>(max_context_len) + kMaxChunk - 1) / kMaxChunk;

@@ -170,9 +170,11 @@ cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, c
   if (W == 1) {
     if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsNarrow>, *p, W);
     if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsNarrow>, *p, W);
+    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<256, kCombineWarpsNarrow>, *p, W);
   } else {
     if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsWide>, *p, W);
     if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsWide>, *p, W);
+    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<256, kCombineWarpsWide>, *p, W);
   }
   return cudaErrorInvalidValue;
 }

@@ -45,19 +45,23 @@
 #include "pa_internal.h"
 #include "pa_tc.cuh"
 
+#include <type_traits>
+
 namespace pav {
 
-template <int KV_FP8, int NP>
+template <int KV_FP8, int NP, int D>
 struct TcCfg {
-  static constexpr int kD = 128;
+  static constexpr int kD = D;
   static constexpr int kTile = kFlatTile;                    // tokens per K/V tile = MMA M
-  static constexpr int kRowB = KV_FP8 ? 128 : 256;           // bytes per token row
-  static constexpr int kTileB = kTile * kRowB;               // 16 KB (fp8) / 32 KB (bf16)
-  static constexpr int KS = KV_FP8 ? 5 : 2;                  // K ring depth (a K slot frees once S is done)
-  static constexpr int VS = KV_FP8 ? 5 : 3;                  // V ring depth (a V slot frees only after PV)
+  static constexpr int kRowB = KV_FP8 ? D : 2 * D;           // bytes per token row
+  static constexpr int kHalves = kRowB / 128;                // 128-byte planes of a tile (TMA boxes per page)
+  static constexpr int kMh = D / 128;                        // PV M halves (O accumulators, 64 columns apart)
+  static constexpr int kTileB = kTile * kRowB;               // 16 KB (fp8 D128) / 32 KB (bf16 D128, fp8 D256)
+  static constexpr int KS = kTileB > 16384 ? 2 : 5;          // K ring depth (a K slot frees once S is done)
+  static constexpr int VS = kTileB > 16384 ? (KV_FP8 ? 2 : 3) : 5;  // V ring depth (a V slot frees only after PV)
   static constexpr int kVStage = kTileB + (KV_FP8 ? 2 * 4 * kTile : 0);  // V data + k/v scales
   static constexpr int kQPlane = 64 * 128;                   // one 128-byte-wide plane of 64 rows
-  static constexpr int kQB = 2 * kQPlane;                    // bf16: two 64-column halves; fp8: hi and lo
+  static constexpr int kQB = (KV_FP8 ? 2 : 1) * kHalves * kQPlane;  // bf16: 64-column halves; fp8: hi, lo by half
   static constexpr int kPPlane = KV_FP8 ? kTile * 64 : kTile * 128;  // bytes of one P plane
   static constexpr int kPBuf = KV_FP8 ? 2 * kPPlane : kPPlane;       // fp8: hi and lo planes
   static constexpr int kOffK = 0;
@@ -73,6 +77,7 @@ struct TcCfg {
   static_assert((NP / 2) % 8 == 0, "each softmax warpgroup owns a multiple of 8 columns");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(2 * KS + 2 * VS + 9 <= 30, "barriers fit their 256 bytes with the tmem slot and abort flag");
+  static_assert(D == 128 || (KV_FP8 && D == 256), "head_dim 128, or 256 with FP8 K/V");
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -136,11 +141,11 @@ struct TileCursor {
   __device__ __forceinline__ int pair(int hkv) const { return k * hkv + g; }
 };
 
-template <int KV_FP8, int NP>
+template <int KV_FP8, int NP, int D>
 __global__ void __launch_bounds__(352, 1)
     pa_tc_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ SplitParams p) {
-  using C = TcCfg<KV_FP8, NP>;
+  using C = TcCfg<KV_FP8, NP, D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = sm + C::kOffK;
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(352, 1)
   const bool is_prod = warp == 0 || warp == 10, is_sm = warp >= 2 && warp <= 9;
   const int wg = is_sm ? (warp - 2) >> 2 : 0;   // softmax warpgroup 0 or 1
   const int col0 = wg * NH;                     // first column this group owns
-  constexpr int kHalves = C::kRowB / 128;
+  constexpr int kHalves = C::kHalves;
   const bool is_k = warp == 0;
   // producer lanes: page (within the tile) of this lane's copy: boxes on lanes [0, 8 * halves), FP8 scales on 16-31
   const int jl = lane < 8 * kHalves ? lane / kHalves : ((KV_FP8 && warp == 10 && lane >= 16) ? (lane & 7) : 8);
@@ -196,23 +201,25 @@ __global__ void __launch_bounds__(352, 1)
     return jl < npages(cq) ? __ldg(p.block_table + static_cast<size_t>(cq.b) * p.bt_stride + cq.t * (C::kTile / kPage) + jl)
                            : -1;
   };
-  // a softmax warp's Q rows of a segment: row r = col0 + (warp - 2) % 4 + 4 m, 8 bytes per lane
-  auto q_load = [&](const TileCursor& cq, uint2 (&wq)[kRowsPerWarp]) {
+  // a softmax warp's Q rows of a segment: row r = col0 + (warp - 2) % 4 + 4 m, D / 32 bf16 per lane
+  using QV = typename std::conditional<(D > 128), uint4, uint2>::type;
+  auto q_load = [&](const TileCursor& cq, QV (&wq)[kRowsPerWarp]) {
     const int rows = cq.QL * G;
 #pragma unroll
     for (int m = 0; m < kRowsPerWarp; ++m) {
       const int r = col0 + ((warp - 2) & 3) + 4 * m;
-      wq[m] = make_uint2(0, 0);
+      wq[m] = QV{};
       if (r < rows) {
         const int i = r / G;
-        wq[m] = *reinterpret_cast<const uint2*>(
-            p.q + (static_cast<size_t>(cq.q_off + i) * p.num_q_heads + cq.g * G + (r - i * G)) * C::kD + 4 * lane);
+        wq[m] = *reinterpret_cast<const QV*>(
+            p.q + (static_cast<size_t>(cq.q_off + i) * p.num_q_heads + cq.g * G + (r - i * G)) * C::kD +
+            (C::kD / 32) * lane);
       }
     }
   };
   TileCursor cu0;  // producers: the first tile; softmax warps: the first segment
   int pg0 = -1;
-  uint2 wq0[kRowsPerWarp];
+  QV wq0[kRowsPerWarp];
   if (is_prod || is_sm) cu0.seek(wv, f_lo);
   if (is_prod) pg0 = fetch(cu0);
   if (is_sm) q_load(cu0, wq0);
@@ -355,10 +362,12 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
           for (int pl = 0; pl < 2; ++pl)  // Q hi then Q lo
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc::mma_f8(tS[sb], tc::sdesc(k0 + ks * 32, 16, 1024, tc::kSwizzle128B),
-                         tc::sdesc(aQ + pl * C::kQPlane + ks * 32, 16, 1024, tc::kSwizzle128B), idS,
-                         (pl > 0 || ks > 0) ? 1u : 0u);
+            for (int hf = 0; hf < kHalves; ++hf)  // 128 head-dim entries per plane
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                tc::mma_f8(tS[sb], tc::sdesc(k0 + hf * (C::kTile * 128) + ks * 32, 16, 1024, tc::kSwizzle128B),
+                           tc::sdesc(aQ + (pl * kHalves + hf) * C::kQPlane + ks * 32, 16, 1024, tc::kSwizzle128B),
+                           idS, (pl > 0 || hf > 0 || ks > 0) ? 1u : 0u);
         } else {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
@@ -384,13 +393,15 @@ __global__ void __launch_bounds__(352, 1)
         if (KV_FP8) {
           const int nks = (nv + 31) >> 5;  // 32 tokens per k-step; hi then lo plane of P
 #pragma unroll
-          for (int pl = 0; pl < 2; ++pl)
+          for (int h = 0; h < C::kMh; ++h)  // head-dim entries [128 h, 128 h + 128): V plane h, O accumulator h
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              if (ks < nks)
-                tc::mma_f8(tO, tc::sdesc(v0 + ks * 4096, 16384, 1024, tc::kSwizzle128B),
-                           tc::sdesc(p0 + pl * C::kPPlane + ks * 2048, 16384, 512, tc::kSwizzle64B), idPV,
-                           (!first || pl > 0 || ks > 0) ? 1u : 0u);
+            for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                if (ks < nks)
+                  tc::mma_f8(tO + 64 * h, tc::sdesc(v0 + h * (C::kTile * 128) + ks * 4096, 16384, 1024, tc::kSwizzle128B),
+                             tc::sdesc(p0 + pl * C::kPPlane + ks * 2048, 16384, 512, tc::kSwizzle64B), idPV,
+                             (!first || pl > 0 || ks > 0) ? 1u : 0u);
         } else {
           const int nks = (nv + 15) >> 4;  // 16 tokens per k-step
 #pragma unroll
@@ -428,21 +439,30 @@ __global__ void __launch_bounds__(352, 1)
 
     // ---- Q rows [col0, col0 + NH) of a segment into the Q buffer (one warp a row), their
     // constants into slot `sl`; then this warp's arrival on qready
-    auto stage_q = [&](const TileCursor& cq, const uint2 (&wq)[kRowsPerWarp], int sl) {
+    auto stage_q = [&](const TileCursor& cq, const QV (&wq)[kRowsPerWarp], int sl) {
       const int rows = cq.QL * G;
 #pragma unroll
       for (int m = 0; m < kRowsPerWarp; ++m) {
         const int r = col0 + ((warp - 2) & 3) + 4 * m;
-        const uint2 w = wq[m];
+        const QV w = wq[m];
         float cr = p.scale_log2;
-        if (!KV_FP8) {
+        if constexpr (!KV_FP8) {
           // 4 bf16 = 8 bytes at byte 8*lane of the 256-byte row: half lane/16, chunk (lane%16)/2
           const int hf = lane >> 4, ch = (lane & 15) >> 1;
           uint8_t* dst = sQ + hf * C::kQPlane + r * 128 + ((ch ^ (r & 7)) << 4) + (lane & 1) * 8;
           *reinterpret_cast<uint2*>(dst) = w;
         } else {
-          float x[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
-          float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+          constexpr int kE = C::kD / 32;  // head-dim entries of this lane: [kE * lane, kE * lane + kE)
+          const uint32_t* wv32 = reinterpret_cast<const uint32_t*>(&w);
+          float x[kE];
+#pragma unroll
+          for (int e = 0; e < kE / 2; ++e) {
+            x[2 * e] = bf16_lo(wv32[e]);
+            x[2 * e + 1] = bf16_hi(wv32[e]);
+          }
+          float mx = 0.f;
+#pragma unroll
+          for (int e = 0; e < kE; ++e) mx = fmaxf(mx, fabsf(x[e]));
 #pragma unroll
           for (int k = 16; k >= 1; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
           int ex = 0;
@@ -451,19 +471,27 @@ __global__ void __launch_bounds__(352, 1)
             frexpf(mx, &e2);  // mx in [2^(e2-1), 2^e2)
             ex = 8 - e2;      // scaled row max in [128, 256)
           }
-          uint32_t hw = 0, lw = 0;
+          uint32_t hw[kE / 4], lw[kE / 4];
 #pragma unroll
-          for (int e = 0; e < 4; e += 2) {
+          for (int e = 0; e < kE; e += 2) {
             const float a = ldexpf(x[e], ex), c = ldexpf(x[e + 1], ex);
             const float ah = __uint_as_float(__float_as_uint(a) & 0xFFF00000u);  // 3 mantissa bits
             const float ch2 = __uint_as_float(__float_as_uint(c) & 0xFFF00000u);
-            hw |= e4m3x2(ah, ch2) << (8 * e);
-            lw |= e4m3x2(a - ah, c - ch2) << (8 * e);
+            const int sh = 8 * (e & 3);
+            if ((e & 3) == 0) { hw[e >> 2] = 0; lw[e >> 2] = 0; }
+            hw[e >> 2] |= e4m3x2(ah, ch2) << sh;
+            lw[e >> 2] |= e4m3x2(a - ah, c - ch2) << sh;
           }
-          // 4 bytes at byte 4*lane of the 128-byte row: chunk lane/4
-          const uint32_t off = r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4;
-          *reinterpret_cast<uint32_t*>(sQ + off) = hw;
-          *reinterpret_cast<uint32_t*>(sQ + C::kQPlane + off) = lw;
+          // kE bytes at byte kE*lane of the D-byte row: plane b / 128, 16-byte chunk (b % 128) / 16
+          const int b = kE * lane, hf = b >> 7, ch = (b & 127) >> 4;
+          const uint32_t off = hf * C::kQPlane + r * 128 + ((ch ^ (r & 7)) << 4) + (b & 15);
+          if constexpr (kE == 4) {
+            *reinterpret_cast<uint32_t*>(sQ + off) = hw[0];
+            *reinterpret_cast<uint32_t*>(sQ + kHalves * C::kQPlane + off) = lw[0];
+          } else {
+            *reinterpret_cast<uint2*>(sQ + off) = make_uint2(hw[0], hw[1]);
+            *reinterpret_cast<uint2*>(sQ + kHalves * C::kQPlane + off) = make_uint2(lw[0], lw[1]);
+          }
           cr = ldexpf(p.scale_log2, -ex);
         }
         if (lane == 0) {
@@ -527,8 +555,8 @@ __global__ void __launch_bounds__(352, 1)
             const int qi = r / G;
             const uint16_t* qp =
                 p.q + (static_cast<size_t>(nx.q_off + qi) * p.num_q_heads + nx.g * G + (r - qi * G)) * C::kD;
-            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(qp));
-            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(qp + 64));
+#pragma unroll
+            for (int o = 0; o < C::kD; o += 64) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(qp + o));
           }
         }
       }
@@ -550,7 +578,7 @@ __global__ void __launch_bounds__(352, 1)
         // S(i), the last reader of this segment's Q, is done: stage the next segment's rows
         TileCursor nx = cu;
         nx.advance(wv, Hkv);
-        uint2 wq[kRowsPerWarp];
+        QV wq[kRowsPerWarp];
         q_load(nx, wq);  // every row's load first: one memory latency for the warp's rows
         stage_q(nx, wq, sl ^ 1);
       }
@@ -640,18 +668,20 @@ __global__ void __launch_bounds__(352, 1)
             wait(&pfree[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u);  // PV of tile i-1 done
             tc::fence_after_sync();
 #pragma unroll
-            for (int c0 = 0; c0 < NH; c0 += 8) {
-              uint32_t r8[8];
-              tc::ld8(tO + lane_off + col0 + c0, r8);
-              tc::wait_ld();
+            for (int h = 0; h < C::kMh; ++h)
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float mn = new_max(c0 + j), mo = old_max(c0 + j);
-                const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
-                r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+              for (int c0 = 0; c0 < NH; c0 += 8) {
+                uint32_t r8[8];
+                tc::ld8(tO + 64 * h + lane_off + col0 + c0, r8);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float mn = new_max(c0 + j), mo = old_max(c0 + j);
+                  const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
+                  r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+                }
+                tc::st8(tO + 64 * h + lane_off + col0 + c0, r8);
               }
-              tc::st8(tO + lane_off + col0 + c0, r8);
-            }
             tc::wait_st();
           }
 #pragma unroll
@@ -690,18 +720,20 @@ __global__ void __launch_bounds__(352, 1)
             wait(&pfree[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u);  // PV of tile i-1 done
             tc::fence_after_sync();
 #pragma unroll
-            for (int c0 = 0; c0 < NH; c0 += 8) {
-              uint32_t r8[8];
-              tc::ld8(tO + lane_off + col0 + c0, r8);
-              tc::wait_ld();
+            for (int h = 0; h < C::kMh; ++h)
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float mn = new_max(c0 + j), mo = old_max(c0 + j);
-                const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
-                r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+              for (int c0 = 0; c0 < NH; c0 += 8) {
+                uint32_t r8[8];
+                tc::ld8(tO + 64 * h + lane_off + col0 + c0, r8);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float mn = new_max(c0 + j), mo = old_max(c0 + j);
+                  const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
+                  r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+                }
+                tc::st8(tO + 64 * h + lane_off + col0 + c0, r8);
               }
-              tc::st8(tO + lane_off + col0 + c0, r8);
-            }
             tc::wait_st();
           }
 #pragma unroll
@@ -842,11 +874,12 @@ __global__ void __launch_bounds__(352, 1)
         }
         named_sync(bar_sync, 128);
         if (ok_sm) {
-          const int d = tok;  // O^T lanes are head-dim entries
 #pragma unroll 1
-          for (int c0 = 0; c0 < NH; c0 += 8) {
+          for (int hc = 0; hc < C::kMh * NH; hc += 8) {
+            const int h = hc / NH, c0 = hc - h * NH;
+            const int d = 128 * h + tok;  // O^T lanes are head-dim entries
             uint32_t r8[8];
-            tc::ld8(tO + lane_off + col0 + c0, r8);
+            tc::ld8(tO + 64 * h + lane_off + col0 + c0, r8);
             tc::wait_ld();
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -882,5 +915,23 @@ __global__ void __launch_bounds__(352, 1)
     tc::tmem_dealloc(tmem, 256);
   }
 }
+
+// Launches the kernel for one (KV type, padded rows, head_dim) instance.
+template <int F8, int NP, int D>
+cudaError_t run_tc(int units, const CUtensorMap* tmk, const CUtensorMap* tmv, const SplitParams* p,
+                   cudaStream_t stream) {
+  auto kern = pa_tc_split_kernel<F8, NP, D>;
+  constexpr int smem = TcCfg<F8, NP, D>::kSmem;
+  static bool attr_set = false;  // benign race: setting the attribute twice is harmless
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<units, 352, smem, stream>>>(*tmk, *tmv, *p);
+  return cudaGetLastError();
+}
+
+inline int tc_rows_pad(int rows_max) { return rows_max <= 16 ? 16 : rows_max <= 32 ? 32 : rows_max <= 48 ? 48 : 64; }
 
 }  // namespace pav

@@ -189,12 +189,29 @@ def test_empty_batch_plans():
     (dict(ctx=[100], ql=[2], hq=6, hkv=4), pv.ERR_INVALID),
     (dict(ctx=[100], ql=[2], stride=3), pv.ERR_INVALID),
     (dict(ctx=[10] * 65, ql=[1] * 65), pv.ERR_UNSUPPORTED),
+    (dict(ctx=[100], ql=[6], d=256), pv.ERR_UNSUPPORTED),  # head_dim 256 is an FP8 shape only
+    (dict(ctx=[100], ql=[8], hq=16, hkv=1, d=256, kv=pv.KV_FP8_E4M3), pv.ERR_UNSUPPORTED),  # 128 rows
+    (dict(ctx=[100], ql=[6], d=256, kv=pv.KV_FP8_E4M3, kernel=pv.KERNEL_WARP_MMA), pv.ERR_UNSUPPORTED),
 ])
 def test_plan_refusals(kw, status):
     with pytest.raises(pv.PaVerifyError) as e:
         mk(**kw)
     assert e.value.status == status
     assert pv.last_error()
+
+
+@pytest.mark.parametrize("ql,hq", [(6, 8), (1, 8), (8, 8), (2, 16), (4, 16)])
+def test_fp8_head_dim_256_plans_on_tensor_cores(ql, hq):
+    """FP8 K/V with head_dim 256 (the aiter follow-up's shape: GQA 8 x query 6 = 48 rows) plans on the
+    tcgen05 kernel, dynamic plans too; the workspace holds fp32 partials of 256 entries per row."""
+    p = mk([150000, 40000], [ql, ql], hq=hq, hkv=1, d=256, kv=pv.KV_FP8_E4M3)
+    assert p.info.kernel == pv.KERNEL_TCGEN05 and p.info.flat == 1
+    assert p.info.rows_max == ql * hq
+    q = mk([150000, 40000], [ql, ql], hq=hq, hkv=1, d=128, kv=pv.KV_FP8_E4M3)
+    assert p.info.num_units == q.info.num_units  # the same tiles: the split does not depend on head_dim
+    assert p.workspace_bytes > q.workspace_bytes
+    dyn = pv.plan_dynamic(hq, 1, 256, pv.KV_FP8_E4M3, pv.OUT_BF16, 20000, 9400, 4, 150000, ql, sm_count=152)
+    assert dyn.info.kernel == pv.KERNEL_TCGEN05
 
 
 def test_page_size_must_be_16():

@@ -27,7 +27,12 @@ def built():
 
 
 def tc_applies(prob):
-    return prob.head_dim == 128 and int(prob.query_lens.max()) * prob.group <= 64
+    d_ok = prob.head_dim == 128 or (prob.head_dim == 256 and prob.kv_dtype == synth.KV_FP8)
+    return d_ok and int(prob.query_lens.max()) * prob.group <= 64
+
+
+def mma_applies(prob):
+    return prob.head_dim != 256  # head_dim 256 runs on the tcgen05 kernel only
 
 
 KERNELS = [pv.KERNEL_WARP_MMA, pv.KERNEL_TCGEN05]
@@ -62,6 +67,11 @@ SMALL = [
     ("fp8_small", lambda: synth.make_problem([45, 29, 300], [6, 2, 8], 8, 1, 128, kv_dtype=synth.KV_FP8, seed=12)),
     ("fp8_multi_tile", lambda: synth.make_problem([1500, 257, 4099], [6, 1, 7], 16, 2, 128,
                                                   kv_dtype=synth.KV_FP8, seed=35)),
+    ("fp8_d256_small", lambda: synth.make_problem([45, 29, 300, 6], [6, 2, 8, 6], 8, 1, 256,
+                                                  kv_dtype=synth.KV_FP8, seed=13)),
+    ("fp8_d256_multi_tile", lambda: synth.make_problem([1500, 257, 4099, 128], [6, 1, 7, 3], 16, 2, 256,
+                                                       kv_dtype=synth.KV_FP8, seed=37)),
+    ("fp8_d256_rows16", lambda: synth.make_problem([700, 129], [2, 1], 8, 1, 256, kv_dtype=synth.KV_FP8, seed=38)),
 ]
 
 
@@ -72,6 +82,8 @@ def test_small_against_oracle(name, make, split, kernel):
     prob = make()
     if kernel == pv.KERNEL_TCGEN05 and not tc_applies(prob):
         pytest.skip("outside the tcgen05 kernel's envelope")
+    if kernel == pv.KERNEL_WARP_MMA and not mma_applies(prob):
+        pytest.skip("outside the warp-MMA kernel's envelope")
     ref = oracle.verify_attention(prob)
     got, va = gpu_run(prob, split_override=split, kernel=kernel)
     assert va.info["kernel"] == kernel
@@ -85,16 +97,20 @@ SEG_Q = [1, 6, 8, 2, 3, 6, 7, 1, 4, 6, 5, 8]
 
 
 @pytest.mark.parametrize("split", [17, 9, 6, 4, 0])
-@pytest.mark.parametrize("kv", [synth.KV_BF16, synth.KV_FP8], ids=["bf16", "fp8"])
-def test_flat_segments_against_oracle(kv, split):
-    prob = synth.make_problem(SEG_CTX, SEG_Q, 16, 2, 128, kv_dtype=kv, seed=36)
+@pytest.mark.parametrize("kv,d", [(synth.KV_BF16, 128), (synth.KV_FP8, 128), (synth.KV_FP8, 256)],
+                         ids=["bf16", "fp8", "fp8_d256"])
+def test_flat_segments_against_oracle(kv, d, split):
+    prob = synth.make_problem(SEG_CTX, SEG_Q, 16, 2, d, kv_dtype=kv, seed=36)
     ref = oracle.verify_attention(prob)
     got, va = gpu_run(prob, split_override=split, kernel=pv.KERNEL_TCGEN05)
     assert va.info["flat"] == 1
     assert max_err(got, ref) <= TOL[kv]
 
 
-@pytest.mark.parametrize("name,make", SMALL[:3] + SMALL[6:7], ids=[s[0] for s in SMALL[:3] + SMALL[6:7]])
+BF16_OUT = SMALL[:3] + SMALL[6:7] + SMALL[8:9]
+
+
+@pytest.mark.parametrize("name,make", BF16_OUT, ids=[s[0] for s in BF16_OUT])
 def test_bf16_output(name, make):
     prob = make()
     ref = oracle.verify_attention(prob)
@@ -109,6 +125,14 @@ def test_split_count_does_not_change_the_result(kernel):
     for o in outs[1:]:
         # P is rounded to bf16 against a split-dependent running max: 2^-8 relative per weight
         assert max_err(o, outs[0]) <= 2e-3
+
+
+def test_fp8_d256_split_count_does_not_change_the_result():
+    prob = synth.make_problem([3000, 1200], [6, 6], 8, 1, 256, kv_dtype=synth.KV_FP8, seed=47)
+    outs = [gpu_run(prob, split_override=k)[0] for k in (1, 2, 5, 1000)]
+    for o in outs[1:]:
+        # P's hi/lo E4M3 terms carry about 7 bits against a split-dependent running max
+        assert max_err(o, outs[0]) <= 4e-3
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=[KID[k] for k in KERNELS])
@@ -193,9 +217,11 @@ def sample_rows(prob, n, seed):
     return np.array(sorted(rows), dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", ["mtp5_bf16", "mtp5_fp8", "mixed_fp8", "ctx1mi_bf16"])
+@pytest.mark.parametrize("name", ["mtp5_bf16", "mtp5_fp8", "mixed_fp8", "ctx1mi_bf16", "d256_fp8_bs8"])
 @pytest.mark.parametrize("kernel", KERNELS, ids=[KID[k] for k in KERNELS])
 def test_full_workload_sampled_rows(name, kernel):
+    if kernel == pv.KERNEL_WARP_MMA and name.startswith("d256"):
+        pytest.skip("head_dim 256 runs on the tcgen05 kernel only")
     prob = _workload(name)
     got, va = gpu_run(prob, dev=_workload_dev(name), kernel=kernel)
     assert np.isfinite(got).all()

@@ -44,7 +44,7 @@ def test_fp8_quantisation_scales():
     assert (p.k_scale > 0).all()
 
 
-@pytest.mark.parametrize("name", synth.CONFIG_NAMES)
+@pytest.mark.parametrize("name", synth.ALL_NAMES)
 def test_workload_shapes(name):
     ctx, ql, hq, hkv, d, kvd, seed = synth.config_lengths(name)
     assert len(ctx) == len(ql)
@@ -60,6 +60,9 @@ def test_workload_shapes(name):
         assert len(ctx) == 64 and max(ctx) <= 131072 and (hq, hkv) == (16, 2)
     if name == "ctx1mi_bf16":
         assert ctx == [1 << 20] and (ctx[0] + 15) // 16 == 65536
+    if name in synth.EXTRA_NAMES:
+        assert set(ctx) == {150000} and set(ql) == {6} and (hq, hkv, d, kvd) == (8, 1, 256, synth.KV_FP8)
+        assert len(ctx) == int(name[-1]) and ql[0] * hq // hkv == 48
 
 
 def test_tiny_uses_a_32_page_pool():
@@ -73,3 +76,8 @@ def test_shard_sequences_cover_batch():
             parts = [synth.shard_sequences(n, w, r) for r in range(w)]
             allx = np.concatenate(parts)
             assert np.array_equal(np.sort(allx), np.arange(n))
+
+
+def test_bench_describes_every_workload():
+    import bench
+    assert set(synth.ALL_NAMES) <= set(bench.WORKLOAD_DESC)

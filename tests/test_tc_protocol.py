@@ -13,9 +13,13 @@ import random
 import pytest
 
 
-def run(seg_first, short_tile, fp8, slow, kernel_order=True):
+# ring depths (K, V) of the kernel's instances: bf16 head_dim 128; FP8 head_dim 128; FP8 head_dim 256
+DEPTHS = {False: [(2, 3)], True: [(5, 5), (2, 2)]}
+
+
+def run(seg_first, short_tile, fp8, slow, kernel_order=True, depths=None):
     n = len(seg_first)
-    KS, VS = (5, 5) if fp8 else (2, 3)
+    KS, VS = depths or DEPTHS[fp8][0]
     seg_last = [i == n - 1 or seg_first[i + 1] for i in range(n)]
     seg_of, s = [], -1
     for i in range(n):
@@ -104,7 +108,8 @@ def layouts(count, seed):
 
 def test_kernel_order_never_sticks():
     for seg_first, short, fp8, slow in layouts(4000, 1):
-        assert run(seg_first, short, fp8, slow), (seg_first, short, fp8, slow)
+        for dep in DEPTHS[fp8]:
+            assert run(seg_first, short, fp8, slow, depths=dep), (seg_first, short, fp8, slow, dep)
 
 
 def test_plain_order_sticks_on_one_tile_segments():
@@ -116,8 +121,8 @@ def test_plain_order_sticks_on_one_tile_segments():
         assert any(seg_first[j] and j + 1 < n and seg_first[j + 1] for j in range(n))
 
 
-@pytest.mark.parametrize("fp8", [False, True])
-def test_single_tile_segments_back_to_back(fp8):
+@pytest.mark.parametrize("fp8,dep", [(False, (2, 3)), (True, (5, 5)), (True, (2, 2))])
+def test_single_tile_segments_back_to_back(fp8, dep):
     n = 9
-    assert run([True] * n, [True] * n, fp8, [True] * n)
-    assert not run([True] * n, [True] * n, fp8, [True] * n, kernel_order=False)
+    assert run([True] * n, [True] * n, fp8, [True] * n, depths=dep)
+    assert not run([True] * n, [True] * n, fp8, [True] * n, kernel_order=False, depths=dep)
