@@ -46,6 +46,17 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, ui
   return d;
 }
 
+// The descriptor of the same layout `bytes` further on (a multiple of 16): one
+// 32-bit add on the start-address field (the low 14 bits, in 16-byte units).
+// Shared-memory addresses stay below 2^18 bytes, so the sum never carries
+// into the next field. An MMA loop builds its base descriptors once and steps
+// them this way: building a descriptor from an address costs several
+// dependent integer operations on the issuing thread.
+__device__ __forceinline__ uint64_t desc_plus(uint64_t d, uint32_t bytes) {
+  const uint32_t lo = static_cast<uint32_t>(d) + (bytes >> 4);
+  return (d & 0xFFFFFFFF00000000ull) | lo;
+}
+
 enum Fmt : uint32_t { kF16 = 0, kBF16 = 1, kE4M3 = 0 };
 enum Major : uint32_t { kKMajor = 0, kMNMajor = 1 };
 

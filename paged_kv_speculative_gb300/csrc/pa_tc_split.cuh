@@ -17,8 +17,8 @@
 // with both accumulators in tensor memory.
 //
 // Warp roles (352 threads): warps 0 and 10 gather pages through the block
-// table with 2-D TMA boxes into a KS-deep K ring and a VS-deep V ring (which
-// also carries the FP8 scales), one lane per box, reading the next tile's
+// table with 2-D TMA boxes into a KS-deep K ring and a VS-deep V ring (the K
+// producer also fills a ring of FP8 scales), one lane per box, reading the next tile's
 // page ids while the current tile is issued; warp 1 allocates tensor memory
 // and issues the MMAs (one thread); warps 2-9 are two softmax warpgroups, one
 // thread per token of the tile, each group owning half of the row columns and
@@ -59,24 +59,28 @@ struct TcCfg {
   static constexpr int kTileB = kTile * kRowB;               // 16 KB (fp8 D128) / 32 KB (bf16 D128, fp8 D256)
   static constexpr int KS = kTileB > 16384 ? 2 : 5;          // K ring depth (a K slot frees once S is done)
   static constexpr int VS = kTileB > 16384 ? (KV_FP8 ? 2 : 3) : 5;  // V ring depth (a V slot frees only after PV)
-  static constexpr int kVStage = kTileB + (KV_FP8 ? 2 * 4 * kTile : 0);  // V data + k/v scales
+  static constexpr int kVStage = kTileB;                     // V data
+  static constexpr int SS = KV_FP8 ? KS + 2 : 0;             // FP8 scale ring depth (see the K producer)
+  static constexpr int kScB = 2 * 4 * kTile;                 // one slot: k then v scales of a tile's tokens
   static constexpr int kQPlane = 64 * 128;                   // one 128-byte-wide plane of 64 rows
   static constexpr int kQB = (KV_FP8 ? 2 : 1) * kHalves * kQPlane;  // bf16: 64-column halves; fp8: hi, lo by half
   static constexpr int kPPlane = KV_FP8 ? kTile * 64 : kTile * 128;  // bytes of one P plane
   static constexpr int kPBuf = KV_FP8 ? 2 * kPPlane : kPPlane;       // fp8: hi and lo planes
+  static constexpr int PB = D > 128 ? 3 : 2;                 // P buffers (head_dim 256: PV takes twice the MMAs)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + KS * kTileB;
-  static constexpr int kOffQ = kOffV + ((VS * kVStage + 1023) / 1024) * 1024;
+  static constexpr int kOffSc = kOffV + ((VS * kVStage + 1023) / 1024) * 1024;
+  static constexpr int kOffQ = kOffSc + SS * kScB;
   static constexpr int kOffP = kOffQ + kQB;
-  static constexpr int kOffRow = kOffP + 2 * kPBuf;          // rowC[2][64] f32, rowLim[2][64] i32 (by segment parity)
+  static constexpr int kOffRow = kOffP + PB * kPBuf;         // rowC[2][64] f32, rowLim[2][64] i32 (by segment parity)
   static constexpr int kOffRed = kOffRow + 4 * 64 * 4;       // tile maxima [8 warps][64], 1 / row totals [64], reference maxima [64]
   static constexpr int kOffRedL = kOffRed + 10 * 64 * 4;     // row-sum partials [8 warps][64]
   static constexpr int kOffBar = kOffRedL + 8 * 64 * 4;
-  static constexpr int kSmem = kOffBar + 256 + 1024;         // barriers, tmem base, alignment slack
+  static constexpr int kSmem = kOffBar + 512 + 1024;         // barriers, tmem base, alignment slack
   static_assert(NP % 16 == 0 && NP >= 16 && NP <= 64, "N must be 16..64 in steps of 16");
   static_assert((NP / 2) % 8 == 0, "each softmax warpgroup owns a multiple of 8 columns");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
-  static_assert(2 * KS + 2 * VS + 9 <= 30, "barriers fit their 256 bytes with the tmem slot and abort flag");
+  static_assert(2 * KS + 2 * VS + 5 + 2 * PB + SS <= 62, "barriers fit their 512 bytes with the tmem slot and abort flag");
   static_assert(D == 128 || (KV_FP8 && D == 256), "head_dim 128, or 256 with FP8 K/V");
 };
 
@@ -151,6 +155,7 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* sK = sm + C::kOffK;
   uint8_t* sV = sm + C::kOffV;
   uint8_t* sQ = sm + C::kOffQ;
+  uint8_t* sSc = sm + C::kOffSc;  // FP8 scale ring
   uint8_t* sP = sm + C::kOffP;
   float* rowC = reinterpret_cast<float*>(sm + C::kOffRow);     // [2][64] score multiplier per row
   int* rowLim = reinterpret_cast<int*>(rowC + 128);             // [2][64] last visible key per row (-1: padding)
@@ -165,9 +170,10 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* sfull = vempty + C::VS;
   uint64_t* sfree = sfull + 2;
   uint64_t* pfull = sfree + 2;
-  uint64_t* pfree = pfull + 2;
-  uint64_t* qready = pfree + 2;
-  uint32_t* tbase_slot = reinterpret_cast<uint32_t*>(qready + 1);
+  uint64_t* pfree = pfull + C::PB;
+  uint64_t* qready = pfree + C::PB;
+  uint64_t* scfull = qready + 1;  // [SS] FP8 scale slots landed
+  uint32_t* tbase_slot = reinterpret_cast<uint32_t*>(scfull + C::SS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tbase_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -191,8 +197,9 @@ __global__ void __launch_bounds__(352, 1)
   const int col0 = wg * NH;                     // first column this group owns
   constexpr int kHalves = C::kHalves;
   const bool is_k = warp == 0;
-  // producer lanes: page (within the tile) of this lane's copy: boxes on lanes [0, 8 * halves), FP8 scales on 16-31
-  const int jl = lane < 8 * kHalves ? lane / kHalves : ((KV_FP8 && warp == 10 && lane >= 16) ? (lane & 7) : 8);
+  // producer lanes: page (within the tile) of this lane's copy: boxes on lanes [0, 8 * halves); on the K
+  // producer, the FP8 scale copies on lanes 16-31 (k scales 16-23, v scales 24-31)
+  const int jl = lane < 8 * kHalves ? lane / kHalves : ((KV_FP8 && warp == 0 && lane >= 16) ? (lane & 7) : 8);
   auto npages = [&](const TileCursor& cq) {
     return min(C::kTile / kPage, (cq.L - cq.t * C::kTile + kPage - 1) / kPage);
   };
@@ -230,10 +237,13 @@ __global__ void __launch_bounds__(352, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_addr(&sfull[s]), 1);
       mbar_init(smem_addr(&sfree[s]), 8);
+    }
+    for (int s = 0; s < C::PB; ++s) {
       mbar_init(smem_addr(&pfull[s]), 8);
       mbar_init(smem_addr(&pfree[s]), 1);
     }
     mbar_init(smem_addr(qready), 8);  // one phase per segment: each softmax warp staged its rows
+    for (int s = 0; s < C::SS; ++s) mbar_init(smem_addr(&scfull[s]), 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmk);
@@ -260,10 +270,16 @@ __global__ void __launch_bounds__(352, 1)
 
   if (warp == 0 || warp == 10) {
     // ============================================================ producers
-    // Warp 0 feeds the K ring, warp 10 the V ring (with the FP8 scales). A
-    // TMA issue costs its thread about one memory latency, so every page box
-    // (and scale copy) of a tile gets its own lane: lane 0 arms the stage's
-    // byte count, then the lanes issue together.
+    // Warp 0 feeds the K ring (and the FP8 scale ring), warp 10 the V ring.
+    // A TMA issue costs its thread about one memory latency, so every page
+    // box (and scale copy) of a tile gets its own lane: lane 0 arms the
+    // stages' byte counts, then the lanes issue together.
+    //
+    // Scale slot k % SS is refilled without a wait of its own: issuing tile k
+    // follows the end of S(k - KS) (the K slot's release), which the MMA
+    // thread issued only after the softmax released S(k - KS - 2), and the
+    // softmax reads a tile's scales before it releases the tile's S. So with
+    // SS = KS + 2 the slot's previous tile, k - SS, has been read.
     const int depth = is_k ? C::KS : C::VS;
     const CUtensorMap* map = is_k ? &tmk : &tmv;
     uint64_t* full = is_k ? kfull : vfull;
@@ -299,10 +315,15 @@ __global__ void __launch_bounds__(352, 1)
         atomicOr(p.err, 1u);
         pg = -1;
       }
-      // FP8 V: one k and one v scale copy per page inside the pool (lanes 16-23 hold the ids)
+      // FP8 (K producer): one k and one v scale copy per page inside the pool (lanes 16-23 hold the ids)
       const uint32_t nsc =
-          (KV_FP8 && !is_k) ? __popc(__ballot_sync(0xffffffffu, lane >= 16 && lane < 24 && pg >= 0)) : 0u;
-      if (lane == 0) mbar_arrive_expect_tx(bar, npg * (kPage * C::kRowB) + nsc * (2 * kPage * 4));
+          (KV_FP8 && is_k) ? __popc(__ballot_sync(0xffffffffu, lane >= 16 && lane < 24 && pg >= 0)) : 0u;
+      const int sslot = k % (C::SS > 0 ? C::SS : 1);  // scale slot (FP8)
+      const uint32_t scbar = KV_FP8 ? smem_addr(&scfull[sslot]) : 0u;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, npg * (kPage * C::kRowB));
+        if (KV_FP8 && is_k) mbar_arrive_expect_tx(scbar, nsc * (2 * kPage * 4));
+      }
       __syncwarp();
       if (lane < npg * kHalves) {
         const int hf = lane % kHalves;
@@ -310,11 +331,11 @@ __global__ void __launch_bounds__(352, 1)
         const int row = (pg >= 0 ? pg : p.num_pages) * Hkv * kPage + cu.g * kPage;
         tma_load_2d(smem_addr(dst + hf * (C::kTile * 128) + jl * kPage * 128), map, bar, hf * (KV_FP8 ? 128 : 64), row);
       }
-      if (KV_FP8 && !is_k && lane >= 16 && jl < npg && pg >= 0) {
+      if (KV_FP8 && is_k && lane >= 16 && jl < npg && pg >= 0) {
         const size_t so = (static_cast<size_t>(pg) * Hkv + cu.g) * kPage;
         const bool ksc = lane < 24;
-        bulk_load(smem_addr(dst + C::kTileB + (ksc ? 0 : C::kTile * 4) + jl * kPage * 4),
-                  (ksc ? p.k_scale : p.v_scale) + so, kPage * 4, bar);
+        bulk_load(smem_addr(sSc + sslot * C::kScB + (ksc ? 0 : C::kTile * 4) + jl * kPage * 4),
+                  (ksc ? p.k_scale : p.v_scale) + so, kPage * 4, scbar);
       }
       // (after the issue, off its path) the device lengths must be the planned ones
       if (is_k && lane == 0 && cu.t == 0 && cu.g == 0 && (p.dev_ctx[cu.b] != cu.L || p.dev_q[cu.b] != cu.QL))
@@ -326,9 +347,15 @@ __global__ void __launch_bounds__(352, 1)
     // No copy may land after the CTA exits: wait (bounded) for the last
     // copies of each ring slot; only this warp arms these barriers, so the
     // parity of tile k's phase is exact.
-    if (lane == 0)
+    if (lane == 0) {
       for (int k = max(0, issued - depth); k < issued; ++k)
         (void)mbar_wait_bounded(smem_addr(&full[k % depth]), static_cast<uint32_t>(k / depth) & 1u);
+      if constexpr (KV_FP8) {
+        if (is_k)
+          for (int k = max(0, issued - C::SS); k < issued; ++k)
+            (void)mbar_wait_bounded(smem_addr(&scfull[k % C::SS]), static_cast<uint32_t>(k / C::SS) & 1u);
+      }
+    }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     // One thread issues S^T = K Q^T of tile i and O^T += V^T P^T of tile j in
@@ -343,7 +370,10 @@ __global__ void __launch_bounds__(352, 1)
       constexpr uint32_t fa = KV_FP8 ? tc::kE4M3 : tc::kBF16;
       constexpr uint32_t idS = tc::idesc(fa, fa, tc::kKMajor, tc::kKMajor, 128, NP);
       constexpr uint32_t idPV = tc::idesc(fa, fa, tc::kMNMajor, tc::kMNMajor, 128, NP);
-      const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aP = smem_addr(sP);
+      const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aP = smem_addr(sP);
+      // Each MMA's operand descriptors are its stage's base descriptor plus a constant (one add): the issue
+      // cost of a thread per MMA is then close to the tensor core's own time for these small N.
+      const uint64_t dQ = tc::sdesc(smem_addr(sQ), 16, 1024, tc::kSwizzle128B);
       TileCursor cs, cv;  // the next S tile, the next PV tile
       cs.seek(wv, f_lo);
       cv = cs;
@@ -357,7 +387,7 @@ __global__ void __launch_bounds__(352, 1)
         if (i >= 2 && !mbar_wait_bounded(smem_addr(&sfree[sb]), static_cast<uint32_t>((i >> 1) - 1) & 1u))
           return false;
         tc::fence_after_sync();
-        const uint32_t k0 = aK + ks_ * C::kTileB;
+        const uint64_t dK = tc::sdesc(aK + ks_ * C::kTileB, 16, 1024, tc::kSwizzle128B);
         if (KV_FP8) {
 #pragma unroll
           for (int pl = 0; pl < 2; ++pl)  // Q hi then Q lo
@@ -365,15 +395,14 @@ __global__ void __launch_bounds__(352, 1)
             for (int hf = 0; hf < kHalves; ++hf)  // 128 head-dim entries per plane
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
-                tc::mma_f8(tS[sb], tc::sdesc(k0 + hf * (C::kTile * 128) + ks * 32, 16, 1024, tc::kSwizzle128B),
-                           tc::sdesc(aQ + (pl * kHalves + hf) * C::kQPlane + ks * 32, 16, 1024, tc::kSwizzle128B),
-                           idS, (pl > 0 || hf > 0 || ks > 0) ? 1u : 0u);
+                tc::mma_f8(tS[sb], tc::desc_plus(dK, hf * (C::kTile * 128) + ks * 32),
+                           tc::desc_plus(dQ, (pl * kHalves + hf) * C::kQPlane + ks * 32), idS,
+                           (pl > 0 || hf > 0 || ks > 0) ? 1u : 0u);
         } else {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc::mma_f16(tS[sb], tc::sdesc(k0 + (ks >> 2) * (C::kTile * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
-                        tc::sdesc(aQ + (ks >> 2) * C::kQPlane + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B), idS,
-                        ks > 0 ? 1u : 0u);
+            tc::mma_f16(tS[sb], tc::desc_plus(dK, (ks >> 2) * (C::kTile * 128) + (ks & 3) * 32),
+                        tc::desc_plus(dQ, (ks >> 2) * C::kQPlane + (ks & 3) * 32), idS, ks > 0 ? 1u : 0u);
         }
         tc::commit(&sfull[sb]);
         tc::commit(&kempty[ks_]);
@@ -381,10 +410,10 @@ __global__ void __launch_bounds__(352, 1)
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
-        const int vs = j % C::VS, pb = j & 1;
+        const int vs = j % C::VS, pb = j % C::PB;
         const bool first = j == 0 || cv.t == 0;  // the segment's first PV starts its accumulator
         if (!mbar_wait_bounded(smem_addr(&vfull[vs]), static_cast<uint32_t>(j / C::VS) & 1u)) return false;
-        if (!mbar_wait_bounded(smem_addr(&pfull[pb]), static_cast<uint32_t>(j >> 1) & 1u)) return false;
+        if (!mbar_wait_bounded(smem_addr(&pfull[pb]), static_cast<uint32_t>(j / C::PB) & 1u)) return false;
         tc::fence_after_sync();
         const uint32_t v0 = aV + vs * C::kVStage;
         const uint32_t p0 = aP + pb * C::kPBuf;
@@ -392,6 +421,8 @@ __global__ void __launch_bounds__(352, 1)
         const int nv = min(C::kTile, cv.L - cv.t * C::kTile);
         if (KV_FP8) {
           const int nks = (nv + 31) >> 5;  // 32 tokens per k-step; hi then lo plane of P
+          const uint64_t dV = tc::sdesc(v0, 16384, 1024, tc::kSwizzle128B);
+          const uint64_t dP = tc::sdesc(p0, 16384, 512, tc::kSwizzle64B);
 #pragma unroll
           for (int h = 0; h < C::kMh; ++h)  // head-dim entries [128 h, 128 h + 128): V plane h, O accumulator h
 #pragma unroll
@@ -399,16 +430,17 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
                 if (ks < nks)
-                  tc::mma_f8(tO + 64 * h, tc::sdesc(v0 + h * (C::kTile * 128) + ks * 4096, 16384, 1024, tc::kSwizzle128B),
-                             tc::sdesc(p0 + pl * C::kPPlane + ks * 2048, 16384, 512, tc::kSwizzle64B), idPV,
-                             (!first || pl > 0 || ks > 0) ? 1u : 0u);
+                  tc::mma_f8(tO + 64 * h, tc::desc_plus(dV, h * (C::kTile * 128) + ks * 4096),
+                             tc::desc_plus(dP, pl * C::kPPlane + ks * 2048), idPV, (!first || pl > 0 || ks > 0) ? 1u : 0u);
         } else {
           const int nks = (nv + 15) >> 4;  // 16 tokens per k-step
+          const uint64_t dV = tc::sdesc(v0, C::kTile * 128, 1024, tc::kSwizzle128B);
+          const uint64_t dP = tc::sdesc(p0, 16384, 1024, tc::kSwizzle128B);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             if (ks < nks)
-              tc::mma_f16(tO, tc::sdesc(v0 + ks * 2048, C::kTile * 128, 1024, tc::kSwizzle128B),
-                          tc::sdesc(p0 + ks * 2048, 16384, 1024, tc::kSwizzle128B), idPV, (!first || ks > 0) ? 1u : 0u);
+              tc::mma_f16(tO, tc::desc_plus(dV, ks * 2048), tc::desc_plus(dP, ks * 2048), idPV,
+                          (!first || ks > 0) ? 1u : 0u);
         }
         tc::commit(&vempty[vs]);
         tc::commit(&pfree[pb]);  // also tells the softmax warpgroups that O holds the segment's tiles up to j
@@ -571,6 +603,15 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int c = 0; c < NH / 2; ++c) y[c] = make_float2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
       }
+      float sk = 1.f, sv = 1.f;
+      if constexpr (KV_FP8) {
+        // the tile's scales, read before S is released (that release frees their slot for reuse)
+        const int ss = i % C::SS;
+        wait(&scfull[ss], static_cast<uint32_t>(i / C::SS) & 1u);
+        const float* sc = reinterpret_cast<const float*>(sSc + ss * C::kScB);
+        sk = sc[tok];
+        sv = sc[C::kTile + tok];
+      }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[sb]);
@@ -588,10 +629,6 @@ __global__ void __launch_bounds__(352, 1)
       const int vs = i % C::VS;
       float inv_sv = 1.f;
       if (KV_FP8) {
-        // the tile's scales ride in its V stage: every tile's V phase is observed in order
-        wait(&vfull[vs], static_cast<uint32_t>(i / C::VS) & 1u);
-        const float* sc = reinterpret_cast<const float*>(sV + vs * C::kVStage + C::kTileB);
-        float sk = sc[tok], sv = sc[C::kTile + tok];
         if (tabs >= L) { sk = 0.f; sv = 1.f; }
         sv = fmaxf(sv, 7.888609052210118e-31f);  // 2^-100 floor keeps log2 and 1/x finite
         const float2 ls = make_float2(__log2f(sv), __log2f(sv));
@@ -665,7 +702,7 @@ __global__ void __launch_bounds__(352, 1)
             any_scale |= (mn != -INFINITY && mn != old_max(c));
           }
           if (any_scale && !seg_first) {
-            wait(&pfree[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u);  // PV of tile i-1 done
+            wait(&pfree[(i - 1) % C::PB], static_cast<uint32_t>((i - 1) / C::PB) & 1u);  // PV of tile i-1 done
             tc::fence_after_sync();
 #pragma unroll
             for (int h = 0; h < C::kMh; ++h)
@@ -717,7 +754,7 @@ __global__ void __launch_bounds__(352, 1)
             any_scale |= (mn != -INFINITY && mn != old_max(c));
           }
           if (any_scale && !seg_first) {
-            wait(&pfree[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u);  // PV of tile i-1 done
+            wait(&pfree[(i - 1) % C::PB], static_cast<uint32_t>((i - 1) / C::PB) & 1u);  // PV of tile i-1 done
             tc::fence_after_sync();
 #pragma unroll
             for (int h = 0; h < C::kMh; ++h)
@@ -758,14 +795,18 @@ __global__ void __launch_bounds__(352, 1)
         }
       }
       // ---- P = 2^(y - M) (<= 2^8), row sums, P into shared memory as the MMA's B operand
-      const int pb = i & 1;
-      if (i >= 2) wait(&pfree[pb], static_cast<uint32_t>((i >> 1) - 1) & 1u);
+      const int pb = i % C::PB;
+      if (i >= C::PB) wait(&pfree[pb], static_cast<uint32_t>(i / C::PB - 1) & 1u);
       const int nv = L - cu.t * C::kTile;
       if (nv < C::kTile) {
         // Rows past the pair inside the last MMA k-step (a page's unused slots, or a page never loaded)
-        // may hold anything, and P = 0 times NaN would still poison O: they become zeros. bf16 looks at
-        // its V ring only here; PV(i-2) done implies every earlier phase of this slot completed.
-        if (!KV_FP8) wait(&vfull[vs], static_cast<uint32_t>(i / C::VS) & 1u);
+        // may hold anything, and P = 0 times NaN would still poison O: they become zeros. The softmax
+        // looks at the V ring only here, and its parity wait names tile i only once the slot's previous
+        // tile, i - VS, has landed: PV(i - PB) done implies that when VS >= PB; otherwise PV(i - VS),
+        // which read it, is awaited first (the slot cannot be past tile i: that needs P(i)).
+        if (C::VS < C::PB && i >= C::VS)
+          wait(&pfree[(i - C::VS) % C::PB], static_cast<uint32_t>((i - C::VS) / C::PB) & 1u);
+        wait(&vfull[vs], static_cast<uint32_t>(i / C::VS) & 1u);
         const int kend = KV_FP8 ? ((nv + 31) & ~31) : ((nv + 15) & ~15);
         if (wg == 0 && tok >= nv && tok < kend) {
 #pragma unroll
@@ -823,7 +864,7 @@ __global__ void __launch_bounds__(352, 1)
 
       if (seg_last) {
         // ---- segment epilogue: O / l for the owned columns (PV(i) done: O holds the segment)
-        wait(&pfree[pb], static_cast<uint32_t>(i >> 1) & 1u);
+        wait(&pfree[pb], static_cast<uint32_t>(i / C::PB) & 1u);
         tc::fence_after_sync();
         // Row sums over the group's 128 tokens. Within a warp, a halving butterfly: at each step a lane
         // keeps half of its columns, sends the other half to its partner and adds what it receives, so
