@@ -4,15 +4,14 @@
 // where O_s is the normalised partial of split s and lse_s its log2-sum-exp.
 // W warps share an output row (token, q head); W grows with the plan's split
 // count (1 up to 8 splits, 8 from 33 on). With W = 1 a CTA is two warps (two
-// rows), small enough (64 threads, no shared memory) to sit on an SM beside a
-// split-kernel CTA, so the grid's first CTAs are resident and waiting when the
-// split kernel ends; otherwise a CTA is eight warps. Each warp takes every W-th split, eight splits a
+// rows, no shared memory); otherwise a CTA is eight warps. Each warp takes every W-th split, eight splits a
 // round, loading their lse values and its lanes' D/32 columns together (one
 // memory round trip per round; rounds combine online, the running sums
 // rescaled when the maximum rises); the W warps of a row then merge in shared
 // memory. Rows whose (sequence, KV head) was not split were written by the
-// split kernel. Launched as a programmatic dependent of the split kernel: the
-// grid may be resident before the split kernel ends and waits for it here.
+// split kernel. A plain stream-ordered launch after the split kernel: launched
+// as its programmatic dependent instead, the call measured up to 14 us slower
+// on GB300 (batch 1 at head_dim 256) and never faster.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -25,6 +24,19 @@ __device__ __forceinline__ float ld_cg(const float* p) {
   float v;
   asm volatile("ld.global.cg.f32 %0, [%1];\n" : "=f"(v) : "l"(p));
   return v;
+}
+// n = 2 or a multiple of 4 consecutive floats (8-byte or 16-byte aligned), in vector loads.
+template <int n>
+__device__ __forceinline__ void ld_cg_vec(const float* p, float* v) {
+  if constexpr (n == 2) {
+    asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];\n" : "=f"(v[0]), "=f"(v[1]) : "l"(p));
+  } else {
+#pragma unroll
+    for (int k = 0; k < n; k += 4)
+      asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+                   : "=f"(v[k]), "=f"(v[k + 1]), "=f"(v[k + 2]), "=f"(v[k + 3])
+                   : "l"(p + k));
+  }
 }
 
 // Warps per output row for a plan whose rows have at most `max_splits` partials.
@@ -39,8 +51,6 @@ __global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_co
   constexpr int kSm = kWarps > 2 ? kWarps : 1;  // the W = 1 form needs no shared memory
   __shared__ float sm_m[kSm], sm_w[kSm];
   __shared__ float sm_acc[kSm][kWarps > 2 ? D : 1];
-
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wi = warp % W;  // this warp's share of the row's splits
@@ -96,9 +106,7 @@ __global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_co
         for (int e = 0; e < kPer; ++e) o[j][e] = 0.f;
         if (s < n) {
           lse[j] = ld_cg(lse_base + static_cast<size_t>(s) * p.rows_max);
-          const float* src = o_base + static_cast<size_t>(s) * o_stride;
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) o[j][e] = ld_cg(src + e);
+          ld_cg_vec<kPer>(o_base + static_cast<size_t>(s) * o_stride, o[j]);
         }
       }
       float m = M;
@@ -144,11 +152,25 @@ __global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_co
   if (!live || wi != 0) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   const size_t orow = (static_cast<size_t>(q_off + i) * p.num_q_heads + h) * D + lane * kPer;
+  float y[kPer];
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    const float y = acc[e] * inv;
-    if (p.out_f32) reinterpret_cast<float*>(p.out)[orow + e] = y;
-    else reinterpret_cast<uint16_t*>(p.out)[orow + e] = static_cast<uint16_t>(pack_bf16(y, 0.f) & 0xFFFFu);
+  for (int e = 0; e < kPer; ++e) y[e] = acc[e] * inv;
+  if (p.out_f32) {  // kPer consecutive floats: 8- or 16-byte stores
+    float* dst = reinterpret_cast<float*>(p.out) + orow;
+    if constexpr (kPer == 2) {
+      *reinterpret_cast<float2*>(dst) = make_float2(y[0], y[1]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < kPer; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
+    }
+  } else {  // kPer bf16: 4-, 8- or 16-byte stores
+    uint32_t w[kPer / 2];
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2) w[e / 2] = pack_bf16(y[e], y[e + 1]);
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + orow;
+    if constexpr (kPer == 2) *reinterpret_cast<uint32_t*>(dst) = w[0];
+    else if constexpr (kPer == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    else *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -162,11 +184,6 @@ cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, c
   cfg.blockDim = dim3(32 * warps);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (W == 1) {
     if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsNarrow>, *p, W);
     if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsNarrow>, *p, W);

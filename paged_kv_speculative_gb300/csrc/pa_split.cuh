@@ -102,9 +102,6 @@ __global__ void __launch_bounds__(NW * 32)
     fence_mbar_init();
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
-    // the combine grid (a programmatic dependent) may become resident now; it
-    // waits for this grid's completion before reading any partial
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     if (chunk_idx == 0 && kvh == 0 && (p.dev_ctx[b] != L || p.dev_q[b] != QL)) atomicOr(p.err, 2u);
   }
   {

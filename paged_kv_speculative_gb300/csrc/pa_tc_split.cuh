@@ -16,12 +16,12 @@
 //   O^T[d, r]   += V[:, d]^T . P^T[:, r]          (A = V tile, MN-major; B = P, MN-major)
 // with both accumulators in tensor memory.
 //
-// Warp roles (352 threads): warps 0 and 10 gather pages through the block
+// Warp roles (32 x (3 + 4 NWG) threads): warps 0 and V = 2 + 4 NWG gather pages through the block
 // table with 2-D TMA boxes into a KS-deep K ring and a VS-deep V ring (the K
 // producer also fills a ring of FP8 scales), one lane per box, reading the next tile's
 // page ids while the current tile is issued; warp 1 allocates tensor memory
-// and issues the MMAs (one thread); warps 2-9 are two softmax warpgroups, one
-// thread per token of the tile, each group owning half of the row columns and
+// and issues the MMAs (one thread); warps 2 .. V - 1 are NWG softmax warpgroups
+// (three for 48 rows, else two), one thread per token of the tile, each group owning NP / NWG row columns and
 // staging its own rows of Q. Stages hand over on mbarriers; every wait is
 // bounded. The rings run on across segment boundaries; Q is restaged once the
 // last S of a segment is done.
@@ -67,6 +67,12 @@ struct TcCfg {
   static constexpr int kPPlane = KV_FP8 ? kTile * 64 : kTile * 128;  // bytes of one P plane
   static constexpr int kPBuf = KV_FP8 ? 2 * kPPlane : kPPlane;       // fp8: hi and lo planes
   static constexpr int PB = D > 128 ? 3 : 2;                 // P buffers (head_dim 256: PV takes twice the MMAs)
+  // Softmax warpgroups: 48 rows at head_dim 256 take three groups of 16 columns (three warps per SM
+  // sub-partition; 480 threads leave 136 registers a thread), elsewhere two. Measured on GB300: three
+  // groups take 6 us off a batch-1 call at head_dim 256 and cost 2-4 us at larger batches and at 128.
+  static constexpr int NWG = (NP == 48 && D == 256) ? 3 : 2;
+  static constexpr int kThreads = 32 * (3 + 4 * NWG);
+  static constexpr int kVWarp = 2 + 4 * NWG;                 // the V producer (after the softmax warps)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + KS * kTileB;
   static constexpr int kOffSc = kOffV + ((VS * kVStage + 1023) / 1024) * 1024;
@@ -74,11 +80,11 @@ struct TcCfg {
   static constexpr int kOffP = kOffQ + kQB;
   static constexpr int kOffRow = kOffP + PB * kPBuf;         // rowC[2][64] f32, rowLim[2][64] i32 (by segment parity)
   static constexpr int kOffRed = kOffRow + 4 * 64 * 4;       // tile maxima [8 warps][64], 1 / row totals [64], reference maxima [64]
-  static constexpr int kOffRedL = kOffRed + 10 * 64 * 4;     // row-sum partials [8 warps][64]
-  static constexpr int kOffBar = kOffRedL + 8 * 64 * 4;
+  static constexpr int kOffRedL = kOffRed + (4 * NWG + 2) * 64 * 4;  // row-sum partials [4 NWG warps][64]
+  static constexpr int kOffBar = kOffRedL + 4 * NWG * 64 * 4;
   static constexpr int kSmem = kOffBar + 512 + 1024;         // barriers, tmem base, alignment slack
   static_assert(NP % 16 == 0 && NP >= 16 && NP <= 64, "N must be 16..64 in steps of 16");
-  static_assert((NP / 2) % 8 == 0, "each softmax warpgroup owns a multiple of 8 columns");
+  static_assert((NP / NWG) % 8 == 0 && NP % NWG == 0, "each softmax warpgroup owns a multiple of 8 columns");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(2 * KS + 2 * VS + 5 + 2 * PB + SS <= 62, "barriers fit their 512 bytes with the tmem slot and abort flag");
   static_assert(D == 128 || (KV_FP8 && D == 256), "head_dim 128, or 256 with FP8 K/V");
@@ -146,7 +152,7 @@ struct TileCursor {
 };
 
 template <int KV_FP8, int NP, int D>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
     pa_tc_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ SplitParams p) {
   using C = TcCfg<KV_FP8, NP, D>;
@@ -159,9 +165,9 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* sP = sm + C::kOffP;
   float* rowC = reinterpret_cast<float*>(sm + C::kOffRow);     // [2][64] score multiplier per row
   int* rowLim = reinterpret_cast<int*>(rowC + 128);             // [2][64] last visible key per row (-1: padding)
-  float* red = reinterpret_cast<float*>(sm + C::kOffRed);       // [8 warps][64] maxima, [64] 1 / row totals, [64] M_r
-  float* refM = red + 9 * 64;                                   // reference maxima of the segment's rows (log2 units)
-  float* redl = reinterpret_cast<float*>(sm + C::kOffRedL);     // [8 warps][64] row-sum partials
+  float* red = reinterpret_cast<float*>(sm + C::kOffRed);       // [4 NWG warps][64] maxima, [64] 1 / row totals, [64] M_r
+  float* refM = red + (4 * C::NWG + 1) * 64;                    // reference maxima of the segment's rows (log2 units)
+  float* redl = reinterpret_cast<float*>(sm + C::kOffRedL);     // [4 NWG warps][64] row-sum partials
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   uint64_t* kfull = bars;
   uint64_t* kempty = kfull + C::KS;
@@ -190,16 +196,17 @@ __global__ void __launch_bounds__(352, 1)
   // set-up, so that its memory reads are ahead of the rings' first TMA traffic:
   // the producers find their first tile and read its page ids, the softmax
   // warps find their first segment and load its Q rows.
-  constexpr int NH = NP / 2;                    // columns per softmax warpgroup
+  constexpr int NH = NP / C::NWG;               // columns per softmax warpgroup
   constexpr int kRowsPerWarp = NH / 4;          // Q rows each softmax warp stages
-  const bool is_prod = warp == 0 || warp == 10, is_sm = warp >= 2 && warp <= 9;
-  const int wg = is_sm ? (warp - 2) >> 2 : 0;   // softmax warpgroup 0 or 1
+  const bool is_prod = warp == 0 || warp == C::kVWarp, is_sm = warp >= 2 && warp < C::kVWarp;
+  const int wg = is_sm ? (warp - 2) >> 2 : 0;   // softmax warpgroup
   const int col0 = wg * NH;                     // first column this group owns
   constexpr int kHalves = C::kHalves;
   const bool is_k = warp == 0;
   // producer lanes: page (within the tile) of this lane's copy: boxes on lanes [0, 8 * halves); on the K
   // producer, the FP8 scale copies on lanes 16-31 (k scales 16-23, v scales 24-31)
   const int jl = lane < 8 * kHalves ? lane / kHalves : ((KV_FP8 && warp == 0 && lane >= 16) ? (lane & 7) : 8);
+  constexpr int kSmArrive = 4 * C::NWG;         // softmax warps: arrivals on sfree, pfull and qready
   auto npages = [&](const TileCursor& cq) {
     return min(C::kTile / kPage, (cq.L - cq.t * C::kTile + kPage - 1) / kPage);
   };
@@ -225,10 +232,24 @@ __global__ void __launch_bounds__(352, 1)
     }
   };
   TileCursor cu0;  // producers: the first tile; softmax warps: the first segment
-  int pg0 = -1;
+  TileCursor cu1, cu2;  // producers: the next two tiles (their page ids are read ahead)
+  int pg0 = -1, pg1 = -1, pg2 = -1;
   QV wq0[kRowsPerWarp];
   if (is_prod || is_sm) cu0.seek(wv, f_lo);
-  if (is_prod) pg0 = fetch(cu0);
+  if (is_prod) {
+    pg0 = fetch(cu0);
+    cu1 = cu0;
+    cu2 = cu0;
+    if (n_tiles > 1) {
+      cu1.advance(wv, Hkv);
+      pg1 = fetch(cu1);
+      cu2 = cu1;
+    }
+    if (n_tiles > 2) {
+      cu2.advance(wv, Hkv);
+      pg2 = fetch(cu2);
+    }
+  }
   if (is_sm) q_load(cu0, wq0);
 
   if (tid == 0) {
@@ -236,19 +257,18 @@ __global__ void __launch_bounds__(352, 1)
     for (int s = 0; s < C::VS; ++s) { mbar_init(smem_addr(&vfull[s]), 1); mbar_init(smem_addr(&vempty[s]), 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_addr(&sfull[s]), 1);
-      mbar_init(smem_addr(&sfree[s]), 8);
+      mbar_init(smem_addr(&sfree[s]), kSmArrive);
     }
     for (int s = 0; s < C::PB; ++s) {
-      mbar_init(smem_addr(&pfull[s]), 8);
+      mbar_init(smem_addr(&pfull[s]), kSmArrive);
       mbar_init(smem_addr(&pfree[s]), 1);
     }
-    mbar_init(smem_addr(qready), 8);  // one phase per segment: each softmax warp staged its rows
+    mbar_init(smem_addr(qready), kSmArrive);  // one phase per segment: each softmax warp staged its rows
     for (int s = 0; s < C::SS; ++s) mbar_init(smem_addr(&scfull[s]), 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   }
   if (warp == 1) {
     tc::tmem_alloc(tbase_slot, 256);
@@ -268,9 +288,9 @@ __global__ void __launch_bounds__(352, 1)
     atomicOr(p.err, 4u);
   };
 
-  if (warp == 0 || warp == 10) {
+  if (warp == 0 || warp == C::kVWarp) {
     // ============================================================ producers
-    // Warp 0 feeds the K ring (and the FP8 scale ring), warp 10 the V ring.
+    // Warp 0 feeds the K ring (and the FP8 scale ring), warp kVWarp the V ring.
     // A TMA issue costs its thread about one memory latency, so every page
     // box (and scale copy) of a tile gets its own lane: lane 0 arms the
     // stages' byte counts, then the lanes issue together.
@@ -284,16 +304,18 @@ __global__ void __launch_bounds__(352, 1)
     const CUtensorMap* map = is_k ? &tmk : &tmv;
     uint64_t* full = is_k ? kfull : vfull;
     uint64_t* empty = is_k ? kempty : vempty;
-    TileCursor cu = cu0;
-    int pg_raw = pg0;
+    // Page ids are read three tiles ahead (cursors cu, c1, c2 for tiles k, k+1, k+2, rotated by value):
+    // a tile's issue is much shorter than a load from the block table, so reading only the next tile's
+    // ids would hold the ring to about one tile per memory latency.
+    TileCursor cu = cu0, c1 = cu1, c2 = cu2;
+    int pg_raw = pg0, p1 = pg1, p2 = pg2;
     int issued = 0;
     for (int k = 0; k < n_tiles && !*abort_flag; ++k) {
-      // the next tile's page ids are read now; their latency hides behind this tile's wait and issue
-      TileCursor nx = cu;
-      int pg_next = -1;
-      if (k + 1 < n_tiles) {
-        nx.advance(wv, Hkv);
-        pg_next = fetch(nx);
+      TileCursor c3 = c2;
+      int p3 = -1;
+      if (k + 3 < n_tiles) {
+        c3.advance(wv, Hkv);
+        p3 = fetch(c3);
       }
 
       const int s = k % depth;
@@ -341,8 +363,12 @@ __global__ void __launch_bounds__(352, 1)
       if (is_k && lane == 0 && cu.t == 0 && cu.g == 0 && (p.dev_ctx[cu.b] != cu.L || p.dev_q[cu.b] != cu.QL))
         atomicOr(p.err, 2u);
       ++issued;
-      cu = nx;
-      pg_raw = pg_next;
+      cu = c1;
+      c1 = c2;
+      c2 = c3;
+      pg_raw = p1;
+      p1 = p2;
+      p2 = p3;
     }
     // No copy may land after the CTA exits: wait (bounded) for the last
     // copies of each ring slot; only this warp arms these barriers, so the
@@ -458,10 +484,10 @@ __global__ void __launch_bounds__(352, 1)
       }
       if (!ok) fail();
     }
-  } else if (warp >= 2 && warp <= 9) {
+  } else if (is_sm) {
     // ============================================================ softmax warpgroups
-    // Two warpgroups (warps 2-5 and 6-9). Each covers the 128 tokens of a tile
-    // (one per thread, = tensor-memory lane) for its own NH = NP/2 columns
+    // NWG warpgroups (warps 2-5, 6-9, 10-13). Each covers the 128 tokens of a tile
+    // (one per thread, = tensor-memory lane) for its own NH = NP / NWG columns
     // (rows of the pair); the groups never wait on each other inside the loop.
     const int gt = tid - 64 - wg * 128;           // 0..127 inside the group
     const int q4 = warp & 3;                      // tensor-memory lane quarter of this warp
@@ -896,7 +922,7 @@ __global__ void __launch_bounds__(352, 1)
         const int rows = cu.QL * G;
         const bool whole = seg_t0 == 0 && pair_last;  // the segment is the whole pair: no combine
         const size_t u = static_cast<size_t>(cta) + cu.pair(Hkv);
-        float* rinv = red + 8 * 64;  // 1 / row total (0 for an empty row)
+        float* rinv = red + 4 * C::NWG * 64;  // 1 / row total (0 for an empty row)
         if (gt < NH) {
           const int cc = col0 + gt;
           const float* rl = redl + wg * 4 * 64 + cc;
@@ -969,7 +995,7 @@ cudaError_t run_tc(int units, const CUtensorMap* tmk, const CUtensorMap* tmv, co
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<units, 352, smem, stream>>>(*tmk, *tmv, *p);
+  kern<<<units, TcCfg<F8, NP, D>::kThreads, smem, stream>>>(*tmk, *tmv, *p);
   return cudaGetLastError();
 }
 
