@@ -203,7 +203,7 @@ cudaError_t launch_all(pa_verify_plan_t plan, SplitParams& p, cudaStream_t s, bo
         : fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s)
               : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s);
   if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[1], s);
-  if (e == cudaSuccess && plan->needs_combine) e = launch_combine(d.head_dim, &p, plan->max_splits, s);
+  if (e == cudaSuccess && plan->needs_combine) e = launch_combine(d.head_dim, &p, plan->max_splits, d.sm_count, s);
   if (e == cudaSuccess && prof) {
     e = cudaEventRecord(plan->ev[2], s);
     plan->profiled_runs++;

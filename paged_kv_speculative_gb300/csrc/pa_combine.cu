@@ -4,8 +4,12 @@
 // where O_s is the normalised partial of split s and lse_s its log2-sum-exp.
 // W warps share an output row (token, q head); W grows with the plan's split
 // count (1 up to 8 splits, 8 from 33 on). With W = 1 a CTA is two warps (two
-// rows, no shared memory); otherwise a CTA is eight warps. Each warp takes every W-th split, eight splits a
-// round, loading their lse values and its lanes' D/32 columns together (one
+// rows, no shared memory); otherwise a CTA is eight warps, on a 64-column slice
+// of its rows when whole rows would occupy at most half of the SMs (a batch of
+// few rows with many splits: one sequence over the whole GPU; measured on
+// GB300, slicing loses once whole rows reach about one CTA per SM). Each warp
+// takes every W-th split, eight splits a
+// round, loading their lse values and its lanes' columns together (one
 // memory round trip per round; rounds combine online, the running sums
 // rescaled when the maximum rises); the W warps of a row then merge in shared
 // memory. Rows whose (sequence, KV head) was not split were written by the
@@ -19,6 +23,7 @@ namespace pav {
 
 constexpr int kCombineWarpsWide = 8;  // CTAs with W > 1
 constexpr int kCombineWarpsNarrow = 2; // CTAs with W = 1
+constexpr int kSliceCols = 64;         // columns of a row per CTA with W > 1
 
 __device__ __forceinline__ float ld_cg(const float* p) {
   float v;
@@ -44,17 +49,20 @@ int combine_warps_per_row(int max_splits) {
   return max_splits <= 8 ? 1 : max_splits <= 16 ? 2 : max_splits <= 32 ? 4 : 8;
 }
 
-template <int D, int kWarps>
+template <int D, int kWarps, int CW>
 __global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_constant__ SplitParams p, int W) {
-  constexpr int kPer = D / 32;  // columns per lane
+  constexpr int kPer = CW / 32;  // columns per lane
+  constexpr int kSlices = D / CW;  // column slices of a row (consecutive CTAs)
   constexpr int kRound = 8;     // splits in flight per round
   constexpr int kSm = kWarps > 2 ? kWarps : 1;  // the W = 1 form needs no shared memory
   __shared__ float sm_m[kSm], sm_w[kSm];
-  __shared__ float sm_acc[kSm][kWarps > 2 ? D : 1];
+  __shared__ float sm_acc[kSm][kWarps > 2 ? CW : 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wi = warp % W;  // this warp's share of the row's splits
-  const int rho = blockIdx.x * (kWarps / W) + warp / W;
+  const int slice = blockIdx.x % kSlices;
+  const int rho = (blockIdx.x / kSlices) * (kWarps / W) + warp / W;
+  const int col = slice * CW + lane * kPer;  // this lane's first column
   const WorkView wv = work_view(p);
   int n = 0, i = 0, h = 0;
   size_t u0 = 0, q_off = 0;
@@ -93,7 +101,7 @@ __global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_co
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
   if (live) {
     const float* lse_base = p.part_lse + u0 * p.rows_max + r;
-    const float* o_base = p.part_o + (u0 * p.rows_max + r) * D + lane * kPer;
+    const float* o_base = p.part_o + (u0 * p.rows_max + r) * D + col;
     const size_t o_stride = static_cast<size_t>(p.rows_max) * D;
     for (int s0 = wi * kRound; s0 < n; s0 += W * kRound) {
       float lse[kRound];
@@ -136,7 +144,7 @@ __global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_co
     const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - Mr);
     if (lane == 0) sm_w[warp] = wsum * a;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) sm_acc[warp % kSm][(lane * kPer + e) % (kWarps > 2 ? D : 1)] = acc[e] * a;
+    for (int e = 0; e < kPer; ++e) sm_acc[warp % kSm][(lane * kPer + e) % (kWarps > 2 ? CW : 1)] = acc[e] * a;
     __syncthreads();
     if (wi == 0) {
       wsum = 0.f;
@@ -145,13 +153,13 @@ __global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_co
       for (int k = 0; k < W; ++k) {
         wsum += sm_w[w0 + k];
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) acc[e] += sm_acc[(w0 + k) % kSm][(lane * kPer + e) % (kWarps > 2 ? D : 1)];
+        for (int e = 0; e < kPer; ++e) acc[e] += sm_acc[(w0 + k) % kSm][(lane * kPer + e) % (kWarps > 2 ? CW : 1)];
       }
     }
   }
   if (!live || wi != 0) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const size_t orow = (static_cast<size_t>(q_off + i) * p.num_q_heads + h) * D + lane * kPer;
+  const size_t orow = (static_cast<size_t>(q_off + i) * p.num_q_heads + h) * D + col;
   float y[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) y[e] = acc[e] * inv;
@@ -174,24 +182,31 @@ __global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_co
   }
 }
 
-cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, cudaStream_t stream) {
+cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, int sm_count, cudaStream_t stream) {
   if (p->num_rows <= 0) return cudaSuccess;
   const int W = combine_warps_per_row(max_splits);
   const int warps = W == 1 ? kCombineWarpsNarrow : kCombineWarpsWide;
   const int rows_per_cta = warps / W;
+  const int row_ctas = (p->num_rows + rows_per_cta - 1) / rows_per_cta;
+  const bool sliced = W > 1 && 2 * row_ctas <= sm_count;
+  const int slices = sliced ? head_dim / kSliceCols : 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p->num_rows + rows_per_cta - 1) / rows_per_cta);
+  cfg.gridDim = dim3(row_ctas * slices);
   cfg.blockDim = dim3(32 * warps);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   if (W == 1) {
-    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsNarrow>, *p, W);
-    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsNarrow>, *p, W);
-    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<256, kCombineWarpsNarrow>, *p, W);
+    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsNarrow, 64>, *p, W);
+    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsNarrow, 128>, *p, W);
+    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<256, kCombineWarpsNarrow, 256>, *p, W);
+  } else if (sliced) {
+    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsWide, kSliceCols>, *p, W);
+    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsWide, kSliceCols>, *p, W);
+    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<256, kCombineWarpsWide, kSliceCols>, *p, W);
   } else {
-    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsWide>, *p, W);
-    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsWide>, *p, W);
-    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<256, kCombineWarpsWide>, *p, W);
+    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsWide, 64>, *p, W);
+    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsWide, 128>, *p, W);
+    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<256, kCombineWarpsWide, 256>, *p, W);
   }
   return cudaErrorInvalidValue;
 }

@@ -142,7 +142,7 @@ __host__ __device__ constexpr int split_smem_bytes(int kv_fp8, int d) {
 // CTAs of the split kernel resident per SM (shared memory bound), used by the planner.
 __host__ __device__ constexpr int split_ctas_per_sm(int warps) { return warps <= 4 ? 2 : 1; }
 
-cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, cudaStream_t stream);
+cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, int sm_count, cudaStream_t stream);
 
 }  // namespace pav
 
