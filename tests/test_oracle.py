@@ -92,6 +92,18 @@ def test_fp8_equals_attention_on_dequantised_tensors():
     assert ok, det
 
 
+def test_fp8_head_dim_256_against_pins():
+    """The head-256 FP8 shape (GQA 8 over one KV head, the aiter follow-up's): brute force on the dequantised tensors,
+    ordinary decode at query length 1, and block-table permutation invariance."""
+    p = synth.make_problem([45, 20], [6, 3], 8, 1, 256, kv_dtype=synth.KV_FP8, seed=14)
+    for pin in (pins.pin_brute_force, pins.pin_page_permutation):
+        ok, det = pin(p)
+        assert ok, det
+    d = synth.make_problem([23, 50, 8], [1, 1, 1], 8, 1, 256, kv_dtype=synth.KV_FP8, seed=22)
+    ok, det = pins.pin_sdpa_decode(d)
+    assert ok, det
+
+
 def test_poisoned_slots_are_never_read():
     p = synth.make_config("tiny")
     out = oracle.verify_attention(p)
