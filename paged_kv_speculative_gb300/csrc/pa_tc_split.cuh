@@ -55,7 +55,15 @@ struct TcCfg {
   static constexpr int kTile = kFlatTile;                    // tokens per K/V tile = MMA M
   static constexpr int kRowB = KV_FP8 ? D : 2 * D;           // bytes per token row
   static constexpr int kHalves = kRowB / 128;                // 128-byte planes of a tile (TMA boxes per page)
-  static constexpr int kMh = D / 128;                        // PV M halves (O accumulators, 64 columns apart)
+  static constexpr int kMh = D / 128;                        // PV M halves (one O accumulator each)
+  // FP8 at head_dim 256: P's hi and lo planes form one B operand of N = 64 + NP (the lo plane is the operand's
+  // second 64-column atom), so a PV k-step is one MMA; the accumulator then holds O_hi in columns [0, NP) and O_lo
+  // from 64 on, and O = O_hi + O_lo. (One N = 112 MMA issues in about 61 clocks, two N = 48 ones in about 108.)
+  // Measured on GB300: 139 -> 127 us at batch 8 x 150k; at head_dim 128, 2 us slower, so there the two planes
+  // accumulate into the same columns by two MMAs.
+  static constexpr bool kStackP = KV_FP8 != 0 && D == 256;
+  static constexpr int kOCols = kStackP ? 128 : 64;          // tensor-memory columns of one O accumulator
+  static constexpr int kTmemCols = 128 + kMh * kOCols <= 256 ? 256 : 512;  // S 2 x 64, then the O accumulators
   static constexpr int kTileB = kTile * kRowB;               // 16 KB (fp8 D128) / 32 KB (bf16 D128, fp8 D256)
   static constexpr int KS = kTileB > 16384 ? 2 : 5;          // K ring depth (a K slot frees once S is done)
   static constexpr int VS = kTileB > 16384 ? (KV_FP8 ? 2 : 3) : 5;  // V ring depth (a V slot frees only after PV)
@@ -271,7 +279,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
     prefetch_tmap(&tmv);
   }
   if (warp == 1) {
-    tc::tmem_alloc(tbase_slot, 256);
+    tc::tmem_alloc(tbase_slot, C::kTmemCols);
     tc::tmem_relinquish();
   }
   // Each warp reconverges first: lanes that took different paths must reach the
@@ -395,7 +403,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t fa = KV_FP8 ? tc::kE4M3 : tc::kBF16;
       constexpr uint32_t idS = tc::idesc(fa, fa, tc::kKMajor, tc::kKMajor, 128, NP);
-      constexpr uint32_t idPV = tc::idesc(fa, fa, tc::kMNMajor, tc::kMNMajor, 128, NP);
+      constexpr uint32_t idPV = tc::idesc(fa, fa, tc::kMNMajor, tc::kMNMajor, 128, C::kStackP ? 64 + NP : NP);
       const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aP = smem_addr(sP);
       // Each MMA's operand descriptors are its stage's base descriptor plus a constant (one add): the issue
       // cost of a thread per MMA is then close to the tensor core's own time for these small N.
@@ -446,18 +454,31 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
         // only the k-steps holding tokens of the pair: rows past them may be stale or never loaded
         const int nv = min(C::kTile, cv.L - cv.t * C::kTile);
         if (KV_FP8) {
-          const int nks = (nv + 31) >> 5;  // 32 tokens per k-step; hi then lo plane of P
+          const int nks = (nv + 31) >> 5;  // 32 tokens per k-step
           const uint64_t dV = tc::sdesc(v0, 16384, 1024, tc::kSwizzle128B);
-          const uint64_t dP = tc::sdesc(p0, 16384, 512, tc::kSwizzle64B);
+          if constexpr (C::kStackP) {
+            // P: hi plane = the operand's first 64 columns, lo plane (kPPlane further on) the next ones
+            const uint64_t dP = tc::sdesc(p0, C::kPPlane, 512, tc::kSwizzle64B);
 #pragma unroll
-          for (int h = 0; h < C::kMh; ++h)  // head-dim entries [128 h, 128 h + 128): V plane h, O accumulator h
-#pragma unroll
-            for (int pl = 0; pl < 2; ++pl)
+            for (int h = 0; h < C::kMh; ++h)  // head-dim entries [128 h, 128 h + 128): V plane h, O accumulator h
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
                 if (ks < nks)
-                  tc::mma_f8(tO + 64 * h, tc::desc_plus(dV, h * (C::kTile * 128) + ks * 4096),
-                             tc::desc_plus(dP, pl * C::kPPlane + ks * 2048), idPV, (!first || pl > 0 || ks > 0) ? 1u : 0u);
+                  tc::mma_f8(tO + C::kOCols * h, tc::desc_plus(dV, h * (C::kTile * 128) + ks * 4096),
+                             tc::desc_plus(dP, ks * 2048), idPV, (!first || ks > 0) ? 1u : 0u);
+          } else {
+            const uint64_t dP = tc::sdesc(p0, 16384, 512, tc::kSwizzle64B);
+#pragma unroll
+            for (int h = 0; h < C::kMh; ++h)
+#pragma unroll
+              for (int pl = 0; pl < 2; ++pl)  // hi then lo plane of P, into the same columns
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                  if (ks < nks)
+                    tc::mma_f8(tO + C::kOCols * h, tc::desc_plus(dV, h * (C::kTile * 128) + ks * 4096),
+                               tc::desc_plus(dP, pl * C::kPPlane + ks * 2048), idPV,
+                               (!first || pl > 0 || ks > 0) ? 1u : 0u);
+          }
         } else {
           const int nks = (nv + 15) >> 4;  // 16 tokens per k-step
           const uint64_t dV = tc::sdesc(v0, C::kTile * 128, 1024, tc::kSwizzle128B);
@@ -733,18 +754,21 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
 #pragma unroll
             for (int h = 0; h < C::kMh; ++h)
 #pragma unroll
-              for (int c0 = 0; c0 < NH; c0 += 8) {
-                uint32_t r8[8];
-                tc::ld8(tO + 64 * h + lane_off + col0 + c0, r8);
-                tc::wait_ld();
+              for (int pt = 0; pt < (C::kStackP ? 2 : 1); ++pt)  // O_hi, then O_lo 64 columns on
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float mn = new_max(c0 + j), mo = old_max(c0 + j);
-                  const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
-                  r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+                for (int c0 = 0; c0 < NH; c0 += 8) {
+                  const uint32_t ta = tO + C::kOCols * h + 64 * pt + lane_off + col0 + c0;
+                  uint32_t r8[8];
+                  tc::ld8(ta, r8);
+                  tc::wait_ld();
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    const float mn = new_max(c0 + j), mo = old_max(c0 + j);
+                    const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
+                    r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+                  }
+                  tc::st8(ta, r8);
                 }
-                tc::st8(tO + 64 * h + lane_off + col0 + c0, r8);
-              }
             tc::wait_st();
           }
 #pragma unroll
@@ -785,18 +809,21 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
 #pragma unroll
             for (int h = 0; h < C::kMh; ++h)
 #pragma unroll
-              for (int c0 = 0; c0 < NH; c0 += 8) {
-                uint32_t r8[8];
-                tc::ld8(tO + 64 * h + lane_off + col0 + c0, r8);
-                tc::wait_ld();
+              for (int pt = 0; pt < (C::kStackP ? 2 : 1); ++pt)  // O_hi, then O_lo 64 columns on
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float mn = new_max(c0 + j), mo = old_max(c0 + j);
-                  const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
-                  r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+                for (int c0 = 0; c0 < NH; c0 += 8) {
+                  const uint32_t ta = tO + C::kOCols * h + 64 * pt + lane_off + col0 + c0;
+                  uint32_t r8[8];
+                  tc::ld8(ta, r8);
+                  tc::wait_ld();
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    const float mn = new_max(c0 + j), mo = old_max(c0 + j);
+                    const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
+                    r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
+                  }
+                  tc::st8(ta, r8);
                 }
-                tc::st8(tO + 64 * h + lane_off + col0 + c0, r8);
-              }
             tc::wait_st();
           }
 #pragma unroll
@@ -945,14 +972,16 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
           for (int hc = 0; hc < C::kMh * NH; hc += 8) {
             const int h = hc / NH, c0 = hc - h * NH;
             const int d = 128 * h + tok;  // O^T lanes are head-dim entries
-            uint32_t r8[8];
-            tc::ld8(tO + 64 * h + lane_off + col0 + c0, r8);
+            uint32_t r8[8], q8[8];
+            tc::ld8(tO + C::kOCols * h + lane_off + col0 + c0, r8);
+            if constexpr (C::kStackP) tc::ld8(tO + C::kOCols * h + 64 + lane_off + col0 + c0, q8);  // O_lo
             tc::wait_ld();
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int r = col0 + c0 + j;
               if (r >= rows) break;
-              const float val = __uint_as_float(r8[j]) * rinv[r];
+              const float o = C::kStackP ? __uint_as_float(r8[j]) + __uint_as_float(q8[j]) : __uint_as_float(r8[j]);
+              const float val = o * rinv[r];
               if (!whole) {
                 p.part_o[(u * p.rows_max + r) * C::kD + d] = val;
               } else {
@@ -979,7 +1008,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 256);
+    tc::tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
