@@ -1,8 +1,9 @@
 // Split-KV paged verify attention on 5th-generation tensor cores (tcgen05).
 //
 // Work. The (sequence, KV head) pairs are laid end to end as 128-token tiles
-// and CTA c takes the consecutive tiles [c * per, (c + 1) * per), so every SM
-// gets the same amount of K/V whatever the length mix. A CTA walks its range
+// and CTA c takes a consecutive range of them (the host planner's cost-bounded
+// cut, or [c * per, (c + 1) * per)), so every SM gets about the same amount of
+// K/V whatever the length mix. A CTA walks its range
 // as segments, one per pair the range touches. A segment covering a whole
 // pair writes the output; otherwise it writes a normalised partial and its
 // log2-sum-exp at slot c + pair for the combine kernel (the "reducer" of a
@@ -14,14 +15,15 @@
 // straight from the TMA-staged shared memory, once:
 //   S^T[tok, r]  = K[tok, :] . Q[r, :]           (A = K tile, K-major; B = Q, K-major)
 //   O^T[d, r]   += V[:, d]^T . P^T[:, r]          (A = V tile, MN-major; B = P, MN-major)
-// with both accumulators in tensor memory.
+// with both accumulators in tensor memory. head_dim 256 (FP8) runs PV as two
+// M = 128 halves of the head dimension, one accumulator each.
 //
 // Warp roles (32 x (3 + 4 NWG) threads): warps 0 and V = 2 + 4 NWG gather pages through the block
 // table with 2-D TMA boxes into a KS-deep K ring and a VS-deep V ring (the K
-// producer also fills a ring of FP8 scales), one lane per box, reading the next tile's
-// page ids while the current tile is issued; warp 1 allocates tensor memory
-// and issues the MMAs (one thread); warps 2 .. V - 1 are NWG softmax warpgroups
-// (three for 48 rows, else two), one thread per token of the tile, each group owning NP / NWG row columns and
+// producer also fills a ring of FP8 scales), one lane per box, reading page
+// ids three tiles ahead; warp 1 allocates tensor memory and issues the MMAs
+// (one thread); warps 2 .. V - 1 are NWG softmax warpgroups (three for 48 rows
+// at head_dim 256, else two), one thread per token of the tile, each group owning NP / NWG row columns and
 // staging its own rows of Q. Stages hand over on mbarriers; every wait is
 // bounded. The rings run on across segment boundaries; Q is restaged once the
 // last S of a segment is done.
@@ -35,7 +37,9 @@
 //
 // FP8 E4M3 K/V stay 8-bit all the way (kind::f8f6f4). Q and P are each split
 // into two E4M3 terms, x = hi + lo, and both terms go through the tensor core
-// into the same accumulator: Q row r is scaled by a power of two 2^e_r first,
+// (Q's into the same accumulator; P's too at head_dim 128, while at 256 they
+// are one operand of N = 64 + NP whose two column blocks are summed at the
+// end): Q row r is scaled by a power of two 2^e_r first,
 // and P (<= 2^8) has its mantissa cut to 3 bits for hi. The per-token scales
 // are constant along the head dimension, so s_k multiplies score column t and
 // log2 s_v enters the exponent, with l accumulating P / s_v.
