@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -44,12 +45,23 @@ for _bs in (1, 2, 4, 8):
                                           "(48 rows), ctx 150000 each, scattered pages (seed 6)")
 
 
+_C_TOKENS = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def _code_only(src: str) -> str:
+    """C/C++/CUDA source without comments, whitespace runs collapsed (string literals kept)."""
+    no_comments = _C_TOKENS.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", src)
+    return " ".join(no_comments.split())
+
+
 def kernel_source_hash() -> str:
+    """Identifies the library's code: comments and layout do not count, so a counter capture stays valid
+    across edits that change neither."""
     csrc = os.path.join(ROOT, "paged_kv_speculative_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

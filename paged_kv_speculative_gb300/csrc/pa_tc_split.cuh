@@ -91,7 +91,7 @@ struct TcCfg {
   static constexpr int kOffQ = kOffSc + SS * kScB;
   static constexpr int kOffP = kOffQ + kQB;
   static constexpr int kOffRow = kOffP + PB * kPBuf;         // rowC[2][64] f32, rowLim[2][64] i32 (by segment parity)
-  static constexpr int kOffRed = kOffRow + 4 * 64 * 4;       // tile maxima [8 warps][64], 1 / row totals [64], reference maxima [64]
+  static constexpr int kOffRed = kOffRow + 4 * 64 * 4;       // tile maxima [4 NWG warps][64], 1 / row totals [64], reference maxima [64]
   static constexpr int kOffRedL = kOffRed + (4 * NWG + 2) * 64 * 4;  // row-sum partials [4 NWG warps][64]
   static constexpr int kOffBar = kOffRedL + 4 * NWG * 64 * 4;
   static constexpr int kSmem = kOffBar + 512 + 1024;         // barriers, tmem base, alignment slack
