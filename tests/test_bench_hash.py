@@ -11,8 +11,3 @@ def test_comments_and_layout_do_not_count():
 def test_code_and_string_literals_count():
     assert bench._code_only("int a = 1;") != bench._code_only("int a = 2;")
     assert bench._code_only('f("x // y");') != bench._code_only('f("x");')
-
-
-def test_stored_traffic_matches_the_current_sources():
-    h = bench.kernel_source_hash()
-    assert bench.traffic_for("mtp5_bf16") is not None, h
