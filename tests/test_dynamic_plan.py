@@ -91,6 +91,36 @@ def test_dynamic_runs_match_oracle(kvd, kernel):
 
 
 @pytest.mark.gpu
+def test_dynamic_fp8_head_dim_256_matches_oracle():
+    """A capacity plan at the head-256 FP8 shape (GQA 8 over one KV head), over the padded scenarios."""
+    base = synth.make_problem([4000] * 4, [8] * 4, 8, 1, 256, kv_dtype=synth.KV_FP8, seed=62)
+    dev = to_device(base)
+    cap_rows = 4 * 8
+    plan = pv.plan_dynamic(8, 1, 256, synth.KV_FP8, pv.OUT_F32, base.num_pages, base.block_table.shape[1], capacity=4,
+                           max_context_len=4000, max_query_len=8)
+    assert plan.info.kernel == pv.KERNEL_TCGEN05
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    q_buf = torch.zeros((cap_rows, 8, 256), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((cap_rows, 8, 256), dtype=torch.float32, device="cuda")
+    for k, (ctx, ql) in enumerate(SCENARIOS[:3]):
+        prob = _scenario(base, ctx, ql, seed=200 + k)
+        T = int(sum(ql))
+        q_buf[:T].copy_(torch.from_numpy(prob.q.view(np.int16)).view(torch.bfloat16))
+        out.fill_(7.0)
+        ctx_d = torch.tensor(ctx, dtype=torch.int32, device="cuda")
+        ql_d = torch.tensor(ql, dtype=torch.int32, device="cuda")
+        pv.run(plan, q_buf, dev.k_cache, dev.v_cache, dev.k_scale, dev.v_scale, dev.block_table, ctx_d, ql_d,
+               base.softmax_scale, out, ws)
+        torch.cuda.synchronize()
+        assert pv.device_errors(ws) == 0
+        ref = oracle.verify_attention(prob)
+        got = out[:T].cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all()
+        assert float(np.abs(got - ref).max()) <= TOL[synth.KV_FP8], (ctx, ql)
+        assert bool((out[T:] == 7.0).all())
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("kvd", [synth.KV_BF16, synth.KV_FP8])
 def test_one_captured_graph_serves_every_batch(kvd):
     base = synth.make_problem([4000] * 4, [8] * 4, 16, 2, 128, kv_dtype=kvd, seed=62)

@@ -46,6 +46,28 @@ def test_static_scratch_matches_workspace_entry(kv, kernel):
         assert float(d.max()) <= TOL[kv]
 
 
+def test_static_scratch_fp8_head_dim_256():
+    _build.build()
+    lib = pv.lib()
+    prob = synth.make_problem([3000, 777, 5000], [6, 3, 8], 8, 1, 256, kv_dtype=synth.KV_FP8, seed=92)
+    dev = to_device(prob)
+    va = pv.VerifyAttention(8, 1, 256, synth.KV_FP8, prob.num_pages, prob.block_table.shape[1],
+                            prob.context_lens.tolist(), prob.query_lens.tolist(), split_override=5)
+    assert va.info["needs_combine"] == 1 and va.info["kernel"] == pv.KERNEL_TCGEN05
+    ref = va(*dev.args(), prob.softmax_scale)
+    torch.cuda.synchronize()
+    out = torch.full_like(ref, float("nan"))
+    stream = torch.cuda.current_stream()
+    rc = lib.pa_verify_run_static(
+        ctypes.c_void_p(va.plan.handle), _ptr(dev.q), _ptr(dev.k_cache), _ptr(dev.v_cache), _ptr(dev.k_scale),
+        _ptr(dev.v_scale), _ptr(dev.block_table), _ptr(dev.context_lens), _ptr(dev.query_lens),
+        ctypes.c_float(prob.softmax_scale), _ptr(out), ctypes.c_void_p(stream.cuda_stream))
+    assert rc == pv.OK, pv.last_error()
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    assert float((out - ref).abs().max()) <= TOL[synth.KV_FP8]
+
+
 def test_static_scratch_refuses_plans_that_do_not_fit():
     _build.build()
     lib = pv.lib()
