@@ -95,14 +95,21 @@ enum { PA_KERNEL_AUTO = 0, PA_KERNEL_WARP_MMA = 1, PA_KERNEL_TCGEN05 = 2 };
 /*
  * Two plan kinds. Chunk plans (warp-MMA kernel): one CTA per (sequence, KV
  * head, chunk of chunk_tokens). Flat plans (tcgen05 kernel): the (sequence,
- * KV head) pairs laid end to end as 128-token tiles and every CTA given the
- * same number of consecutive tiles (chunk_tokens / 128 of them), so one
- * wave ends together whatever the length mix.
+ * KV head) pairs laid end to end as 128-token tiles and cut into one wave of
+ * consecutive CTA ranges. A static plan picks the ranges that minimise the
+ * largest CTA cost, counting tiles plus ten tiles for every move to another
+ * pair inside a range (pa_verify_plan_get_cta_starts returns them); with
+ * split_override, and in dynamic plans, every CTA gets the same number of
+ * tiles (chunk_tokens / 128 of them). Either way one wave ends together
+ * whatever the length mix.
  */
 typedef struct {
   int32_t num_units;       /* CTAs of the split kernel: chunk plans sum_b Hkv * ceil(L_b / chunk),
-                              flat plans ceil(total_tiles / (chunk_tokens / 128)) */
-  int32_t chunk_tokens;    /* context tokens per unit (a multiple of tile_tokens) */
+                              flat plans the number of ranges (at most one per SM) */
+  int32_t chunk_tokens;    /* chunk plans: context tokens per unit (a multiple of tile_tokens);
+                              flat plans: 128 x the largest range cost (tiles, switches counted
+                              as ten), or 128 x the tiles per CTA of an even cut; dynamic
+                              plans 0 (the device picks it each run) */
   int32_t tile_tokens;     /* tokens per shared-memory stage (flat plans: 128) */
   int32_t rows_max;        /* max_b q_b * G */
   int32_t warps;           /* compute warps per CTA = ceil(rows_max / 16) (warp-MMA kernel) */
