@@ -170,7 +170,10 @@ int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info);
 int pa_verify_plan_get_cta_starts(pa_verify_plan_t plan, int32_t* starts_out, int32_t capacity);
 
 /*
- * Enqueues verify attention on `stream` and returns without waiting.
+ * Enqueues verify attention on `stream` and returns without waiting: the split
+ * kernel, then the combine kernel when some (sequence, KV head) is split
+ * (dynamic plans: a one-CTA planner kernel first). No host-device copy, no
+ * allocation, no synchronisation, so a fixed plan can be captured in a graph.
  *   q            [T, Hq, D] bf16, the q_b rows of each sequence packed in batch order
  *   k_cache      [N_pg, Hkv, 16, D] bf16 or E4M3 bytes, 16-byte aligned base
  *   v_cache      same layout as k_cache
