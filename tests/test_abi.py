@@ -99,13 +99,12 @@ def flat_model(ctx, hkv, sms, split_override=0):
     return pack(nt, lo)[1], pairs
 
 
-@pytest.mark.parametrize("ctx,ql,hkv", CASES)
-@pytest.mark.parametrize("split", [0, 1, 4, 1000])
-def test_flat_plan_ranges(ctx, ql, hkv, split):
-    p = mk(ctx, ql, hq=8 * hkv, hkv=hkv, split_override=split)
+def check_flat_plan(ctx, ql, hkv, split, sms=152):
+    """The library's flat plan equals the model's ranges and keeps every invariant the kernels rely on."""
+    p = mk(ctx, ql, hq=8 * hkv, hkv=hkv, split_override=split, sms=sms)
     i = p.info
     assert i.flat == 1 and i.kernel == pv.KERNEL_TCGEN05 and i.tile_tokens == 128
-    starts, pairs = flat_model(ctx, hkv, 152, split)
+    starts, pairs = flat_model(ctx, hkv, sms, split)
     assert p.cta_starts() == starts
     assert i.total_tiles == hkv * sum((c + 127) // 128 for c in ctx) == starts[-1]
     assert i.num_units == len(starts) - 1
@@ -120,11 +119,29 @@ def test_flat_plan_ranges(ctx, ql, hkv, split):
     slots = [c + k for k, (a, b) in enumerate(spans) for c in range(a, b + 1)]
     assert len(slots) == len(set(slots)) and max(slots) < i.num_units + len(spans)
     if split == 0:
-        assert i.num_units <= 152
+        assert i.num_units <= sms
         # no CTA costs more than the bound the plan reports (tiles + 10 per pair switch)
         for c in range(i.num_units):
             segs = sum(1 for a, b in spans if a <= c <= b)
             assert starts[c + 1] - starts[c] + SWITCH_TILES * (segs - 1) <= i.chunk_tokens // 128
+
+
+@pytest.mark.parametrize("ctx,ql,hkv", CASES)
+@pytest.mark.parametrize("split", [0, 1, 4, 1000])
+def test_flat_plan_ranges(ctx, ql, hkv, split):
+    check_flat_plan(ctx, ql, hkv, split)
+
+
+def test_flat_plan_ranges_on_random_batches():
+    """Seeded random batches (1-64 sequences, lognormal lengths up to 200k, 1-4 KV heads, several SM counts)."""
+    rng = np.random.default_rng(2024)
+    for _ in range(120):
+        B = int(rng.integers(1, 65))
+        ql = [int(x) for x in rng.integers(1, 9, B)]
+        ctx = [max(q, min(200000, int(np.exp(rng.normal(np.log(6000), 1.3))))) for q in ql]
+        hkv = int(rng.choice([1, 2, 4]))
+        sms = int(rng.choice([16, 132, 148, 152]))
+        check_flat_plan(ctx, ql, hkv, 0, sms=sms)
 
 
 def test_flat_plan_does_not_cross_pairs_needlessly():
