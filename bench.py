@@ -4,9 +4,14 @@ A step is one call of the whole path (split-KV kernel + log-sum-exp combine)
 over one batch of the MTP-5 bf16 verify workload: 8 sequences, 6 verify
 tokens each, 32 q / 4 KV heads, head_dim 128, context lengths uniform in
 [4096, 32768], 16-token pages scattered in the pool, q/K/V ~ N(0, 1).
-`value` is KV GB/s (algorithmic K+V bytes read once, divided by the call
-time), `ms_per_step` the call time. Under torchrun each rank runs its own
-batch (weak scaling, no data exchange); rank 0 prints the job aggregate.
+`value` is KV GB/s (algorithmic K+V bytes read once, divided by the median
+call time), `ms_per_step` the median call time. `roofline.frac` is the split
+kernel's own fraction of the HBM peak (its bytes over its event time);
+`roofline.frac_call` is the same bytes over the whole call. The other
+long-context workloads (MTP-5 FP8, the mixed FP8 batch, the 1 Mi-token
+context, head_dim 256 FP8 at batch 8) are measured the same way and reported
+under `other_configs`. Under torchrun each rank runs its own batch (weak
+scaling, no data exchange); rank 0 prints the job aggregate.
 
 `--impl reference` times the CPU fp64 oracle on the same workload instead
 (a bounded sample per step, on the host cores).
@@ -320,7 +325,10 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=3.0, help="seconds of oracle time per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--also", default="", help="comma-separated extra workloads to report under 'other_configs'")
+    ap.add_argument("--also", default="mtp5_fp8,mixed_fp8,ctx1mi_bf16,d256_fp8_bs8",
+                    help="comma-separated extra workloads to report under 'other_configs' ('' for none)")
+    ap.add_argument("--also-cpu-budget", type=float, default=3.0,
+                    help="seconds of oracle time for each extra workload's cpu_baseline")
     ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "tc"],
                     help="split kernel: automatic choice, warp-MMA, or tcgen05")
     ap.add_argument("--op", default="verify", choices=["verify", "kv_write", "verdict"],
@@ -402,12 +410,12 @@ def main():
         r = measure(args.config, args.steps, args.warmup, rank)
     clocks = clk.summary()
     prob, info = r["prob"], r["info"]
-    total_ms = float(sum(r["step_ms"]))
-    mean_ms = total_ms / args.steps
-    total_ms = replicas.max_over_ranks(total_ms, device=dev)
+    med_ms = float(np.median(r["step_ms"]))
+    mean_ms = float(np.mean(r["step_ms"]))
+    step_ms_job = replicas.max_over_ranks(med_ms, device=dev)  # the slowest rank's median call
     kv_bytes_rank = int(info["kv_bytes"])
     kv_bytes_all = replicas.sum_over_ranks(kv_bytes_rank, device=dev)
-    value = replicas.job_throughput(kv_bytes_all, args.steps, total_ms)
+    value = replicas.job_throughput(kv_bytes_all, 1, step_ms_job)
     split_avg = float(np.mean(r["split_ms"]))
     comb_avg = float(np.mean(r["comb_ms"]))
 
@@ -434,33 +442,47 @@ def main():
             e2e_ms.append(e0.elapsed_time(e1))
     e2e_val = replicas.job_throughput(kv_bytes_all, 1, replicas.max_over_ranks(float(np.mean(e2e_ms)), device=dev))
 
+    peaks, _ = load_peaks()
+    peak, peak_note = hbm_peak(peaks)
     others = {}
-    for name in [x for x in args.also.split(",") if x]:
+    for name in [x for x in args.also.split(",") if x and x != args.config]:
         o = measure(name, max(10, args.steps // 2), args.warmup, rank)
-        oms = float(np.mean(o["step_ms"]))
+        oms = float(np.median(o["step_ms"]))
         osplit = float(np.mean(o["split_ms"]))
-        others[name] = {"us_per_call": 1e3 * oms, "kv_gbs": o["info"]["kv_bytes"] / (oms * 1e-3) / 1e9,
-                        "split_kernel_us": 1e3 * osplit,
-                        "split_kernel_gbs": o["info"]["kv_bytes"] / (osplit * 1e-3) / 1e9,
+        ocomb = float(np.mean(o["comb_ms"]))
+        ob = o["info"]["kv_bytes"]
+        others[name] = {"workload": WORKLOAD_DESC[name], "us_per_call": 1e3 * oms,
+                        "kv_gbs": ob / (oms * 1e-3) / 1e9, "frac_call": ob / (oms * 1e-3) / 1e9 / peak,
+                        "split_kernel_us": 1e3 * osplit, "combine_kernel_us": 1e3 * ocomb,
+                        "split_kernel_gbs": ob / (osplit * 1e-3) / 1e9,
+                        "frac_split": ob / (osplit * 1e-3) / 1e9 / peak, "peak_source": peak_note,
+                        "kv_bytes_per_call": ob, "steps": len(o["step_ms"]),
+                        "traffic": traffic_for(name),
                         "units": o["info"]["num_units"], "chunk": o["info"]["chunk_tokens"],
+                        "splits_max": o["info"]["max_splits"],
                         "kernel": "tcgen05" if o["info"]["kernel"] == pv.KERNEL_TCGEN05 else "warp-mma",
                         "device_errors": o["errs"]}
+        if rank == 0 and not args.no_cpu_baseline:
+            gbs, threads, note, _ = cpu_oracle_sample(o["prob"], args.also_cpu_budget, "sample")
+            others[name]["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                            "sample": note}
+        del o
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return 0
 
-    peaks, _ = load_peaks()
-    peak, peak_note = hbm_peak(peaks)
     achieved = kv_bytes_rank / (split_avg * 1e-3) / 1e9
+    call_gbs = kv_bytes_rank / (med_ms * 1e-3) / 1e9
     cpu = None
     if not args.no_cpu_baseline:
         gbs, threads, note, _ = cpu_oracle_sample(prob, args.cpu_budget, "sample")
         cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": note}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "us_per_call": 1e3 * mean_ms,
+        "warmup": args.warmup, "ms_per_step": step_ms_job, "us_per_call": 1e3 * med_ms,
+        "us_per_call_mean": 1e3 * mean_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if prob.kv_dtype == 0 else "fp8-e4m3 KV, bf16 q",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC[args.config], "name": args.config,
@@ -470,6 +492,7 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_note, "traffic": traffic_for(args.config),
+                     "frac_call": call_gbs / peak, "call_gbs": call_gbs,
                      "kernel": "pa_tc_split_kernel" if info["kernel"] == pv.KERNEL_TCGEN05 else "pa_split_kernel",
                      "split_kernel_us": 1e3 * split_avg, "combine_kernel_us": 1e3 * comb_avg},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),

@@ -67,7 +67,7 @@ enum {
 enum {
   PA_DEVERR_PAGE_RANGE = 1u,  /* a block-table entry outside [0, num_pages): zeros were read instead */
   PA_DEVERR_LENGTHS = 2u,     /* device context_lens/query_lens differ from the planned ones */
-  PA_DEVERR_TIMEOUT = 4u      /* a wait for staged K/V timed out; the unit's output is invalid */
+  PA_DEVERR_TIMEOUT = 4u      /* a bounded wait inside a kernel ran out; that CTA's output is invalid */
 };
 
 typedef struct {
@@ -125,7 +125,12 @@ typedef struct {
 } pa_verify_plan_info;
 
 /*
- * Checks the batch and builds a plan. Reads context_lens_host[num_seqs] and
+ * Checks the batch and builds a plan. The feasibility check comes first and a
+ * batch outside the envelope is refused before any plan or scratch exists
+ * (the MTP-5 routing page, review and Change: check feasibility before the
+ * plan and scratch are built; raise instead of running outside the envelope);
+ * the split of the context into partitions plus a reducer follows the split
+ * decode the same page describes (Motivation). Reads context_lens_host[num_seqs] and
  * query_lens_host[num_seqs] (host memory, copied into the plan) and requires
  * 1 <= q_b <= 8, q_b <= L_b, ceil(L_b / 16) <= block_table_stride, and
  * (q_b * G) <= 128. On success *plan_out owns a host-side plan and
@@ -172,7 +177,12 @@ int pa_verify_plan_get_cta_starts(pa_verify_plan_t plan, int32_t* starts_out, in
 /*
  * Enqueues verify attention on `stream` and returns without waiting: the split
  * kernel, then the combine kernel when some (sequence, KV head) is split
- * (dynamic plans: a one-CTA planner kernel first). No host-device copy, no
+ * (dynamic plans: a one-CTA planner kernel first). The operation is the one
+ * stated at the top of this header: query rows = query length x GQA group
+ * over the paged context, with the block table and lengths handed to the
+ * kernel and per-token FP8 scales (MTP-5 routing page, Motivation, Change and
+ * Tests). Arguments are checked before anything is enqueued; a refused call
+ * launches nothing (same page, review). No host-device copy, no
  * allocation, no synchronisation, so a fixed plan can be captured in a graph.
  *   q            [T, Hq, D] bf16, the q_b rows of each sequence packed in batch order
  *   k_cache      [N_pg, Hkv, 16, D] bf16 or E4M3 bytes, 16-byte aligned base
@@ -226,9 +236,10 @@ int pa_verify_profile_read(pa_verify_plan_t plan, float* split_ms, float* combin
  * PA_ERR_WORKSPACE before anything is enqueued. The call allocates nothing and
  * calls neither cudaMalloc nor cudaFree. Every call shares the one array, which
  * keeps the last call's contents; the error word at its start is cleared on
- * the stream at the start of each call. Calls that overlap on the GPU (two
- * streams, two threads) race on the shared scratch: serialise them. Other
- * arguments, checks and return codes are those of pa_verify_run.
+ * the stream at the start of each call, and pa_verify_device_errors with a
+ * NULL workspace reads it. Calls that overlap on the GPU (two streams, two
+ * threads) race on the shared scratch: serialise them. Other arguments,
+ * checks and return codes are those of pa_verify_run.
  */
 #define PA_STATIC_SCRATCH_BYTES (16u << 20)
 int pa_verify_run_static(pa_verify_plan_t plan, const void* q, const void* k_cache, const void* v_cache,
@@ -240,8 +251,31 @@ int pa_verify_run_static(pa_verify_plan_t plan, const void* q, const void* k_cac
 void pa_verify_free(pa_verify_plan_t plan);
 
 /*
+ * Test hook for the bounded waits of the tensor-core (tcgen05) kernel: every
+ * wait of a run with this plan gives up after wait_limit_us microseconds
+ * (0: the default of one second), and CTA stall_cta (-1: none) first waits on
+ * a barrier that nothing completes, so that wait runs out. A wait that runs
+ * out sets PA_DEVERR_TIMEOUT; the CTA then waits (bounded) for its copies and
+ * MMAs in flight, frees its tensor memory and returns, and the output of its
+ * work is invalid. Nothing faults or waits without a limit. Host only, no CUDA
+ * call. (The pages have no counterpart; the MTP-5 routing page's rule of
+ * raising instead of running outside the envelope is what the error word
+ * reports.)
+ */
+int pa_verify_debug_stall(pa_verify_plan_t plan, int32_t stall_cta, uint32_t wait_limit_us);
+
+/*
  * Reads the device error word of `workspace` (PA_DEVERR_* bits) after
- * synchronising `stream`; clears it when `clear` is non-zero.
+ * synchronising `stream`; clears it when `clear` is non-zero. workspace = NULL
+ * reads the fixed scratch of pa_verify_run_static on the current device (its
+ * word is cleared at the start of every static call, so it holds the last
+ * static call's flags).
+ *
+ * Workspace layout seen by callers: the first 256 bytes are a header. Its
+ * 32-bit word 0 is the error word; word 1 counts, over all runs since the
+ * workspace was zeroed, the tiles on which the tensor-core kernel raised a
+ * row's running maximum inside a segment and rescaled the accumulated output
+ * (a diagnostic of the online softmax; never cleared by runs).
  */
 int pa_verify_device_errors(void* workspace, uint32_t* flags_out, int clear, pa_stream_t stream);
 

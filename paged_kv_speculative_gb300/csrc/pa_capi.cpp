@@ -66,6 +66,9 @@ struct pa_verify_plan_s {
   int profiled_runs = 0;
   int last_had_combine = 0;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  // bounded-wait test hook (pa_verify_debug_stall)
+  int32_t stall_cta = -1;
+  uint64_t wait_limit_ns = 0;
 };
 
 namespace {
@@ -182,6 +185,8 @@ void fill_params(SplitParams& p, pa_verify_plan_t plan, const void* q, const flo
   p.ranged = plan->ranged;
   if (plan->ranged) std::memcpy(p.cta_start, plan->cta_start, sizeof(int32_t) * (plan->units + 1));
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
+  p.wait_limit_ns = plan->wait_limit_ns;
+  p.stall_cta = plan->stall_cta;
   std::memcpy(p.seq, plan->seq, sizeof(plan->seq));
 }
 
@@ -783,6 +788,15 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
   return PA_OK;
 }
 
+int pa_verify_debug_stall(pa_verify_plan_t plan, int32_t stall_cta, uint32_t wait_limit_us) {
+  g_last_error.clear();
+  if (!plan) return fail(PA_ERR_INVALID, "plan must not be NULL");
+  if (stall_cta < -1) return fail(PA_ERR_INVALID, "stall_cta must be -1 (none) or a CTA index");
+  plan->stall_cta = stall_cta;
+  plan->wait_limit_ns = static_cast<uint64_t>(wait_limit_us) * 1000u;
+  return PA_OK;
+}
+
 void pa_verify_free(pa_verify_plan_t plan) {
   if (!plan) return;
   for (auto& e : plan->ev)
@@ -792,7 +806,13 @@ void pa_verify_free(pa_verify_plan_t plan) {
 
 int pa_verify_device_errors(void* workspace, uint32_t* flags_out, int clear, pa_stream_t stream) {
   g_last_error.clear();
-  if (!workspace || !flags_out) return fail(PA_ERR_INVALID, "workspace and flags_out must not be NULL");
+  if (!flags_out) return fail(PA_ERR_INVALID, "flags_out must not be NULL");
+  if (!workspace) {  // the fixed scratch of pa_verify_run_static on the current device
+    uint8_t* scratch = nullptr;
+    const int rc = static_scratch_address(&scratch);
+    if (rc != PA_OK) return rc;
+    workspace = scratch;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e == cudaSuccess) e = cudaMemcpy(flags_out, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost);

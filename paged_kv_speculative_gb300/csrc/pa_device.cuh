@@ -50,9 +50,11 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 // Waits for phase `parity` of the barrier; gives up after ~`limit_ns`
-// nanoseconds and returns false (the caller records an error and stops).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns = 1000000000ull) {
+// nanoseconds (0: one second) and returns false (the caller records an error
+// and stops).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (limit_ns == 0) limit_ns = 1000000000ull;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace pav {
 
 constexpr int kPage = 16;         // tokens per KV page
@@ -84,8 +86,15 @@ struct SplitParams {
   int32_t cta_start[kMaxCtaTable + 1];  // CTA c covers tiles [cta_start[c], cta_start[c + 1])
   float scale_log2;             // softmax_scale * log2(e)
   const DynWork* dyn;           // dynamic plans: the device-written work table; else null
+  uint64_t wait_limit_ns;       // a bounded wait gives up after this long (0: one second)
+  int32_t stall_cta;            // test hook: this CTA's MMA issuer first waits on a barrier that nothing
+                                // completes, so its bounded wait runs out (-1: none)
   SeqInfo seq[kMaxSeqs];
 };
+
+// Device error word and diagnostic counters at the start of a workspace.
+constexpr int kWsErrWord = 0;       // PA_DEVERR_* bits
+constexpr int kWsRescaleWord = 1;   // in-segment rescales of the O accumulator (tcgen05 kernel)
 
 #ifdef __CUDACC__
 // The work table a kernel follows: kernel parameters (plans built from host
@@ -142,6 +151,22 @@ __host__ __device__ constexpr int split_smem_bytes(int kv_fp8, int d) {
 // CTAs of the split kernel resident per SM (shared memory bound), used by the planner.
 __host__ __device__ constexpr int split_ctas_per_sm(int warps) { return warps <= 4 ? 2 : 1; }
 
+// Raises a kernel's dynamic shared-memory limit on the current device. The
+// attribute belongs to one device, so it is set once per device ordinal
+// (`done` holds one bit per ordinal below 64; higher ordinals set it on
+// every launch). Setting it twice is harmless, so no lock is needed.
+template <typename Kern>
+inline cudaError_t ensure_smem_attr(Kern kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, int sm_count, cudaStream_t stream);
 
 }  // namespace pav
@@ -158,5 +183,8 @@ int enqueue_with_scratch(pa_verify_plan_t plan, const void* q, const void* k_cac
                          uint8_t* scratch, size_t scratch_bytes, cudaStream_t stream);
 // Records `msg` as this thread's last error and returns `code`.
 int report_error(int code, const char* msg);
+// Device address of pa_verify_run_static's fixed scratch on the current device
+// (looked up on first use per device).
+int static_scratch_address(uint8_t** out);
 
 }  // namespace pav

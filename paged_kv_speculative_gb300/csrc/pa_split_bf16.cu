@@ -8,12 +8,9 @@ static cudaError_t run_bf16(int units, const CUtensorMap* tmk, const CUtensorMap
                             cudaStream_t stream) {
   auto kern = pa_split_kernel<0, D, NW>;
   constexpr int smem = split_smem_bytes(0, D);
-  static bool attr_set = false;  // benign race: setting the attribute twice is harmless
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};  // devices whose limit is raised
+  const cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
+  if (e != cudaSuccess) return e;
   kern<<<units, NW * 32, smem, stream>>>(*tmk, *tmv, *p);
   return cudaGetLastError();
 }

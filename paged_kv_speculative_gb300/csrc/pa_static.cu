@@ -19,8 +19,12 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 uint8_t* g_addr[kMaxDevices] = {};
 
+}  // namespace
+
+namespace pav {
+
 // Device address of g_scratch on the current device (set up on first use).
-int scratch_address(uint8_t** out) {
+int static_scratch_address(uint8_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return pav::report_error(PA_ERR_CUDA, "cudaGetDevice failed");
@@ -38,14 +42,14 @@ int scratch_address(uint8_t** out) {
   return PA_OK;
 }
 
-}  // namespace
+}  // namespace pav
 
 extern "C" int pa_verify_run_static(pa_verify_plan_t plan, const void* q, const void* k_cache, const void* v_cache,
                                     const float* k_scale, const float* v_scale, const int32_t* block_table,
                                     const int32_t* context_lens, const int32_t* query_lens, float softmax_scale,
                                     void* out, pa_stream_t stream) {
   uint8_t* scratch = nullptr;
-  const int rc = scratch_address(&scratch);
+  const int rc = pav::static_scratch_address(&scratch);
   if (rc != PA_OK) return rc;
   return pav::enqueue_with_scratch(plan, q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens, query_lens,
                                    softmax_scale, out, scratch, PA_STATIC_SCRATCH_BYTES,

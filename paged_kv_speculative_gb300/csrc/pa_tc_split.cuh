@@ -98,7 +98,7 @@ struct TcCfg {
   static_assert(NP % 16 == 0 && NP >= 16 && NP <= 64, "N must be 16..64 in steps of 16");
   static_assert((NP / NWG) % 8 == 0 && NP % NWG == 0, "each softmax warpgroup owns a multiple of 8 columns");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
-  static_assert(2 * KS + 2 * VS + 5 + 2 * PB + SS <= 62, "barriers fit their 512 bytes with the tmem slot and abort flag");
+  static_assert(2 * KS + 2 * VS + 7 + 2 * PB + SS <= 62, "barriers fit their 512 bytes with the tmem slot and abort flag");
   static_assert(D == 128 || (KV_FP8 && D == 256), "head_dim 128, or 256 with FP8 K/V");
 };
 
@@ -191,7 +191,9 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
   uint64_t* pfree = pfull + C::PB;
   uint64_t* qready = pfree + C::PB;
   uint64_t* scfull = qready + 1;  // [SS] FP8 scale slots landed
-  uint32_t* tbase_slot = reinterpret_cast<uint32_t*>(scfull + C::SS);
+  uint64_t* stall_bar = scfull + C::SS;  // never completed (the bounded-wait test hook waits on it)
+  uint64_t* drain_bar = stall_bar + 1;   // the MMA issuer's last MMAs, after a failure
+  uint32_t* tbase_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tbase_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -277,6 +279,8 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
     }
     mbar_init(smem_addr(qready), kSmArrive);  // one phase per segment: each softmax warp staged its rows
     for (int s = 0; s < C::SS; ++s) mbar_init(smem_addr(&scfull[s]), 1);
+    mbar_init(smem_addr(stall_bar), 1);
+    mbar_init(smem_addr(drain_bar), 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmk);
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       const int s = k % depth;
       if (k >= depth) {
         // lane 0 waits; the verdict is the same for every lane (no lane is left at a warp sync)
-        bool ok = lane != 0 || mbar_wait_bounded(smem_addr(&empty[s]), static_cast<uint32_t>(k / depth - 1) & 1u);
+        bool ok = lane != 0 || mbar_wait_bounded(smem_addr(&empty[s]), static_cast<uint32_t>(k / depth - 1) & 1u, p.wait_limit_ns);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           if (lane == 0) fail();
@@ -387,11 +391,11 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
     // parity of tile k's phase is exact.
     if (lane == 0) {
       for (int k = max(0, issued - depth); k < issued; ++k)
-        (void)mbar_wait_bounded(smem_addr(&full[k % depth]), static_cast<uint32_t>(k / depth) & 1u);
+        (void)mbar_wait_bounded(smem_addr(&full[k % depth]), static_cast<uint32_t>(k / depth) & 1u, p.wait_limit_ns);
       if constexpr (KV_FP8) {
         if (is_k)
           for (int k = max(0, issued - C::SS); k < issued; ++k)
-            (void)mbar_wait_bounded(smem_addr(&scfull[k % C::SS]), static_cast<uint32_t>(k / C::SS) & 1u);
+            (void)mbar_wait_bounded(smem_addr(&scfull[k % C::SS]), static_cast<uint32_t>(k / C::SS) & 1u, p.wait_limit_ns);
       }
     }
   } else if (warp == 1) {
@@ -419,10 +423,10 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       auto issue_s = [&](int i) -> bool {
         const int ks_ = i % C::KS, sb = i & 1;
         if (i > 0 && cs.t == 0) ++seg_s;
-        if ((i == 0 || cs.t == 0) && !mbar_wait_bounded(smem_addr(qready), static_cast<uint32_t>(seg_s) & 1u))
+        if ((i == 0 || cs.t == 0) && !mbar_wait_bounded(smem_addr(qready), static_cast<uint32_t>(seg_s) & 1u, p.wait_limit_ns))
           return false;
-        if (!mbar_wait_bounded(smem_addr(&kfull[ks_]), static_cast<uint32_t>(i / C::KS) & 1u)) return false;
-        if (i >= 2 && !mbar_wait_bounded(smem_addr(&sfree[sb]), static_cast<uint32_t>((i >> 1) - 1) & 1u))
+        if (!mbar_wait_bounded(smem_addr(&kfull[ks_]), static_cast<uint32_t>(i / C::KS) & 1u, p.wait_limit_ns)) return false;
+        if (i >= 2 && !mbar_wait_bounded(smem_addr(&sfree[sb]), static_cast<uint32_t>((i >> 1) - 1) & 1u, p.wait_limit_ns))
           return false;
         tc::fence_after_sync();
         const uint64_t dK = tc::sdesc(aK + ks_ * C::kTileB, 16, 1024, tc::kSwizzle128B);
@@ -450,8 +454,8 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       auto issue_pv = [&](int j) -> bool {
         const int vs = j % C::VS, pb = j % C::PB;
         const bool first = j == 0 || cv.t == 0;  // the segment's first PV starts its accumulator
-        if (!mbar_wait_bounded(smem_addr(&vfull[vs]), static_cast<uint32_t>(j / C::VS) & 1u)) return false;
-        if (!mbar_wait_bounded(smem_addr(&pfull[pb]), static_cast<uint32_t>(j / C::PB) & 1u)) return false;
+        if (!mbar_wait_bounded(smem_addr(&vfull[vs]), static_cast<uint32_t>(j / C::VS) & 1u, p.wait_limit_ns)) return false;
+        if (!mbar_wait_bounded(smem_addr(&pfull[pb]), static_cast<uint32_t>(j / C::PB) & 1u, p.wait_limit_ns)) return false;
         tc::fence_after_sync();
         const uint32_t v0 = aV + vs * C::kVStage;
         const uint32_t p0 = aP + pb * C::kPBuf;
@@ -498,7 +502,8 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
         if (j + 1 < n_tiles) cv.advance(wv, Hkv);
         return true;
       };
-      bool ok = true;
+      // test hook: a wait on a barrier that nothing completes runs out, and the CTA takes its failure path
+      bool ok = cta != p.stall_cta || mbar_wait_bounded(smem_addr(stall_bar), 0u, p.wait_limit_ns);
       for (int i = 0; ok && i < min(2, n_tiles); ++i) ok = issue_s(i);
       for (int j = 0; ok && j < n_tiles && !*abort_flag; ++j) {
         const bool s_next = j + 2 < n_tiles;
@@ -508,6 +513,10 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
         if (ok && s_new_seg) ok = issue_s(j + 2);
       }
       if (!ok) fail();
+      // After a failure (here or in another role) MMAs already issued may still be running: wait (bounded)
+      // for every one of them before tensor memory is freed. (On the normal path they are done already.)
+      tc::commit(drain_bar);
+      (void)mbar_wait_bounded(smem_addr(drain_bar), 0u, p.wait_limit_ns);
     }
   } else if (is_sm) {
     // ============================================================ softmax warpgroups
@@ -607,7 +616,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
     // group can be left behind at one.
     bool ok_sm = true;
     auto wait = [&](uint64_t* bar, uint32_t par) {
-      if (ok_sm && !mbar_wait_bounded(smem_addr(bar), par)) {
+      if (ok_sm && !mbar_wait_bounded(smem_addr(bar), par, p.wait_limit_ns)) {
         ok_sm = false;
         fail();
       }
@@ -753,6 +762,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
             any_scale |= (mn != -INFINITY && mn != old_max(c));
           }
           if (any_scale && !seg_first) {
+            if (gt == 0) atomicAdd(p.err + kWsRescaleWord, 1u);  // diagnostic count of O rescales
             wait(&pfree[(i - 1) % C::PB], static_cast<uint32_t>((i - 1) / C::PB) & 1u);  // PV of tile i-1 done
             tc::fence_after_sync();
 #pragma unroll
@@ -808,6 +818,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
             any_scale |= (mn != -INFINITY && mn != old_max(c));
           }
           if (any_scale && !seg_first) {
+            if (gt == 0) atomicAdd(p.err + kWsRescaleWord, 1u);  // diagnostic count of O rescales
             wait(&pfree[(i - 1) % C::PB], static_cast<uint32_t>((i - 1) / C::PB) & 1u);  // PV of tile i-1 done
             tc::fence_after_sync();
 #pragma unroll
@@ -1022,12 +1033,9 @@ cudaError_t run_tc(int units, const CUtensorMap* tmk, const CUtensorMap* tmv, co
                    cudaStream_t stream) {
   auto kern = pa_tc_split_kernel<F8, NP, D>;
   constexpr int smem = TcCfg<F8, NP, D>::kSmem;
-  static bool attr_set = false;  // benign race: setting the attribute twice is harmless
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};  // devices whose limit is raised
+  const cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
+  if (e != cudaSuccess) return e;
   kern<<<units, TcCfg<F8, NP, D>::kThreads, smem, stream>>>(*tmk, *tmv, *p);
   return cudaGetLastError();
 }

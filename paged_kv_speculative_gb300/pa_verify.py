@@ -42,7 +42,8 @@ DEVERR_TIMEOUT = 4
 EXPORTED = ("pa_verify_plan", "pa_verify_plan_get_info", "pa_verify_run", "pa_verify_free",
             "pa_verify_device_errors", "pa_verify_last_error", "pa_verify_profile_enable",
             "pa_verify_profile_read", "pa_kv_write", "pa_greedy_verdict_workspace_bytes",
-            "pa_greedy_verdict", "pa_verify_run_static", "pa_verify_plan_dynamic", "pa_verify_plan_get_cta_starts")
+            "pa_greedy_verdict", "pa_verify_run_static", "pa_verify_plan_dynamic", "pa_verify_plan_get_cta_starts",
+            "pa_verify_debug_stall")
 
 
 class PaVerifyError(RuntimeError):
@@ -99,6 +100,8 @@ def lib(path: Optional[str] = None):
     L.pa_verify_run.restype = ctypes.c_int
     L.pa_verify_run_static.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
     L.pa_verify_run_static.restype = ctypes.c_int
+    L.pa_verify_debug_stall.argtypes = [vp, ctypes.c_int32, ctypes.c_uint32]
+    L.pa_verify_debug_stall.restype = ctypes.c_int
     L.pa_verify_free.argtypes = [vp]
     L.pa_verify_free.restype = None
     L.pa_verify_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, vp]
@@ -239,11 +242,24 @@ def run_static(p: Plan, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
                                       float(softmax_scale), _ptr(out), s.cuda_stream))
 
 
-def device_errors(workspace: torch.Tensor, clear: bool = False, stream: Optional[torch.cuda.Stream] = None) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+def device_errors(workspace: Optional[torch.Tensor], clear: bool = False,
+                  stream: Optional[torch.cuda.Stream] = None) -> int:
+    """The device error word of ``workspace``; ``None`` reads the fixed scratch of ``run_static``."""
+    s = stream if stream is not None else torch.cuda.current_stream(
+        workspace.device if workspace is not None else None)
     flags = ctypes.c_uint32()
     _check(lib().pa_verify_device_errors(_ptr(workspace), ctypes.byref(flags), int(bool(clear)), s.cuda_stream))
     return int(flags.value)
+
+
+def rescale_count(workspace: torch.Tensor) -> int:
+    """Word 1 of a workspace header: in-segment rescales of the output accumulator so far."""
+    return int(workspace[4:8].view(torch.int32).item())
+
+
+def debug_stall(p: Plan, stall_cta: int, wait_limit_us: int = 0):
+    """pa_verify_debug_stall: bounded-wait test hook (stall_cta = -1 and 0 restore the defaults)."""
+    _check(lib().pa_verify_debug_stall(p.handle, int(stall_cta), int(wait_limit_us)))
 
 
 def profile_enable(p: Plan, enable: bool = True):

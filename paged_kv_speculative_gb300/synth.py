@@ -34,7 +34,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
-from typing import Optional, Sequence
+from typing import Optional, Sequence, Tuple
 
 import numpy as np
 import torch
@@ -125,10 +125,32 @@ def make_problem(
     softmax_scale: Optional[float] = None,
     name: str = "custom",
     contiguous: bool = False,
+    q_row_log2: Optional[Tuple[float, float]] = None,
+    k_ramp_log2: float = 0.0,
+    v_tok_log2: Optional[Tuple[float, float]] = None,
+    zero_frac: float = 0.0,
+    tiny_v_frac: float = 0.0,
 ) -> Problem:
     """Draw one batch. ``pool_pages`` defaults to the pages the batch needs
     plus ``extra_pages`` unreferenced ones. ``contiguous`` hands pages out in
-    pool order (block table = identity runs) instead of a random permutation."""
+    pool order (block table = identity runs) instead of a random permutation.
+
+    Value-distribution knobs (all off by default; when on, their random
+    numbers come from a second generator, so the default draws are unchanged).
+    Each multiplies the fp32 draw before rounding to bf16 or quantising:
+
+    * ``q_row_log2 = (lo, hi)``: every (token, q head) row of q times 2^u,
+      u ~ U[lo, hi] (rows of widely different norms).
+    * ``k_ramp_log2 = a``: the K row of position t of a sequence of L tokens
+      times 2^(a t / (L - 1)) (key norms, hence scores, growing along the
+      context, so that later tiles beat earlier maxima).
+    * ``v_tok_log2 = (lo, hi)``: every (token, KV head) V row times 2^u,
+      u ~ U[lo, hi] (FP8: per-token scales spread over several decades).
+    * ``zero_frac``: that fraction of (token, KV head) rows has K and V all
+      zero (FP8: amax = 0, so both scales are 1).
+    * ``tiny_v_frac``: that fraction of (token, KV head) V rows times 2^-104
+      (FP8: a V scale far below 2^-100).
+    """
     ctx = np.asarray(context_lens, dtype=np.int32)
     ql = np.asarray(query_lens, dtype=np.int32)
     assert ctx.shape == ql.shape and ctx.ndim == 1
@@ -150,7 +172,42 @@ def make_problem(
         pos += npg
 
     T = int(ql.sum())
-    q = _bf16_bits(torch.randn((T, Hq, D), generator=g, dtype=torch.float32))
+    qf = torch.randn((T, Hq, D), generator=g, dtype=torch.float32)
+    knobs = q_row_log2 is not None or k_ramp_log2 != 0.0 or v_tok_log2 is not None or zero_frac > 0 or tiny_v_frac > 0
+    g2 = torch.Generator().manual_seed(int(seed) * 7919 + 17) if knobs else None
+    if q_row_log2 is not None:
+        lo, hi = q_row_log2
+        qf = qf * torch.exp2(lo + (hi - lo) * torch.rand((T, Hq, 1), generator=g2, dtype=torch.float32))
+    q = _bf16_bits(qf)
+
+    # position of every pool slot in its sequence (-1: not referenced) and that sequence's length
+    slot_pos = np.full((n_pg, PAGE), -1, dtype=np.int64)
+    slot_len = np.ones((n_pg, PAGE), dtype=np.int64)
+    for b, npg in enumerate(pages_per_seq):
+        for j in range(npg):
+            slot_pos[table[b, j]] = 16 * j + np.arange(PAGE)
+            slot_len[table[b, j]] = int(ctx[b])
+
+    def token_factor(which: int, p0: int, p1: int) -> Optional[torch.Tensor]:
+        """[p1 - p0, Hkv, 16, 1] multiplier of pool slots for K (which 0) or V (1), or None."""
+        if not knobs:
+            return None
+        f = torch.ones((p1 - p0, Hkv, PAGE), dtype=torch.float32)
+        if which == 0 and k_ramp_log2 != 0.0:
+            pos = torch.from_numpy(np.maximum(slot_pos[p0:p1], 0)).float()
+            span = torch.from_numpy(np.maximum(slot_len[p0:p1] - 1, 1)).float()
+            f = f * torch.exp2(k_ramp_log2 * pos / span).unsqueeze(1)
+        if which == 1 and v_tok_log2 is not None:
+            lo, hi = v_tok_log2
+            f = f * torch.exp2(lo + (hi - lo) * torch.rand(f.shape, generator=g2, dtype=torch.float32))
+        if zero_frac > 0:
+            # the same rows for K and V: the draw for K is kept and reused for V
+            if which == 0:
+                token_factor.zero = torch.rand(f.shape, generator=g2) < zero_frac
+            f = torch.where(token_factor.zero, torch.zeros_like(f), f)
+        if which == 1 and tiny_v_frac > 0:
+            f = torch.where(torch.rand(f.shape, generator=g2) < tiny_v_frac, f * 2.0 ** -104, f)
+        return f.unsqueeze(-1)
 
     # K/V for the whole pool, drawn page block by page block to bound memory.
     if kv_dtype == KV_BF16:
@@ -163,10 +220,18 @@ def make_problem(
         k_scale = np.empty((n_pg, Hkv, PAGE), dtype=np.float32)
         v_scale = np.empty((n_pg, Hkv, PAGE), dtype=np.float32)
     blk = max(1, (1 << 22) // max(1, Hkv * PAGE * D))
-    for dst, sc in ((k_cache, k_scale), (v_cache, v_scale)):
+    zero_rows = {}
+    for which, (dst, sc) in enumerate(((k_cache, k_scale), (v_cache, v_scale))):
         for p0 in range(0, n_pg, blk):
             p1 = min(n_pg, p0 + blk)
             x = torch.randn((p1 - p0, Hkv, PAGE, D), generator=g, dtype=torch.float32)
+            if knobs:
+                if zero_frac > 0 and which == 1:
+                    token_factor.zero = zero_rows[p0]
+                f = token_factor(which, p0, p1)
+                if zero_frac > 0 and which == 0:
+                    zero_rows[p0] = token_factor.zero
+                x = x * f
             if kv_dtype == KV_BF16:
                 dst[p0:p1] = _bf16_bits(x)
             else:
