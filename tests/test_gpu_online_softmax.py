@@ -68,15 +68,20 @@ SHAPES = [
 ]
 
 
-def ramp_problem(kv, d, hq, hkv, ql, seed, **kw):
-    return synth.make_problem([3000, 1700], ql, hq, hkv, d, kv_dtype=kv, seed=seed, q_row_log2=(-2.0, 2.0),
-                              k_ramp_log2=4.0, **kw)
+def ramp_problem(kv, d, hq, hkv, ql, seed, ctx=(3000, 1700), ramp=4.0, **kw):
+    return synth.make_problem(list(ctx), ql, hq, hkv, d, kv_dtype=kv, seed=seed, q_row_log2=(-2.0, 2.0),
+                              k_ramp_log2=ramp, **kw)
 
 
 @pytest.mark.parametrize("split", [0, 1, 5], ids=["planner", "one_segment", "five_way"])
 @pytest.mark.parametrize("name,kv,d,hq,hkv,ql", SHAPES, ids=[s[0] for s in SHAPES])
 def test_rising_scores_rescale_inside_segments(name, kv, d, hq, hkv, ql, split):
-    prob = ramp_problem(kv, d, hq, hkv, ql, seed=51)
+    # The planner spreads the pairs' tiles over every SM: contexts of a few thousand tokens would
+    # leave one tile per CTA (no second tile in any segment), so its case takes 65 k tokens.
+    if split == 0:
+        prob = ramp_problem(kv, d, hq, hkv, ql, seed=51, ctx=(40000, 25000), ramp=6.0)
+    else:
+        prob = ramp_problem(kv, d, hq, hkv, ql, seed=51)
     ref = oracle.verify_attention(prob)
     got, va = run(prob, split=split, kernel=pv.KERNEL_TCGEN05)
     assert va.info["kernel"] == pv.KERNEL_TCGEN05
