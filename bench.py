@@ -459,7 +459,7 @@ def main():
                         "kv_bytes_per_call": ob, "steps": len(o["step_ms"]),
                         "traffic": traffic_for(name),
                         "units": o["info"]["num_units"], "chunk": o["info"]["chunk_tokens"],
-                        "splits_max": o["info"]["max_splits"], "fused_merge": o["info"]["fused_merge"],
+                        "splits_max": o["info"]["max_splits"],
                         "kernel": "tcgen05" if o["info"]["kernel"] == pv.KERNEL_TCGEN05 else "warp-mma",
                         "device_errors": o["errs"]}
         if rank == 0 and not args.no_cpu_baseline:
@@ -488,7 +488,6 @@ def main():
         "config": {"workload": WORKLOAD_DESC[args.config], "name": args.config,
                    "kv_bytes_per_call": kv_bytes_rank, "l2": "flushed between steps (256 MiB write, then 256 MiB read: L2 left clean; outside the events)",
                    "units": info["num_units"], "chunk_tokens": info["chunk_tokens"], "splits_max": info["max_splits"],
-                   "fused_merge": info["fused_merge"],
                    "kernel": "tcgen05" if info["kernel"] == pv.KERNEL_TCGEN05 else "warp-mma",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -498,7 +497,7 @@ def main():
                      "split_kernel_us": 1e3 * split_avg, "combine_kernel_us": 1e3 * comb_avg},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": float(np.mean(e2e_ms))},
-        "gpu_launches": args.steps * (1 + int(info["needs_combine"] and not info["fused_merge"])),
+        "gpu_launches": args.steps * (1 + int(info["needs_combine"])),
         "clocks": clocks,
         "device_errors": r["errs"],
     }

@@ -122,8 +122,6 @@ typedef struct {
   int32_t dynamic;         /* 1 for pa_verify_plan_dynamic plans (figures above are capacities) */
   int32_t flat;            /* 1 for flat plans */
   int32_t total_tiles;     /* flat plans: sum_b Hkv * ceil(L_b / 128) (dynamic plans: chosen per run, 0 here) */
-  int32_t fused_merge;     /* 1: split pairs are merged inside the split kernel, which is then launched
-                              cooperatively (all CTAs resident at once); no combine kernel */
 } pa_verify_plan_info;
 
 /*

@@ -35,7 +35,10 @@ def _deps_mtime() -> float:
 
 def _compile(src: str) -> str:
     obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+    # -fno-gnu-unique: the launchers' per-device "attribute set" flags are function-local statics of template
+    # instances; as GNU-unique symbols they would be shared with any other copy of this library loaded in the
+    # same process, whose kernels would then launch without their shared-memory limit raised.
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fno-gnu-unique", "-I", INCLUDE,
            "-c", os.path.join(CSRC, src), "-o", obj]
     if src.endswith(".cpp"):
         cmd[1:1] = ["-x", "cu"]

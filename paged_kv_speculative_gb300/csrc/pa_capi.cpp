@@ -52,8 +52,6 @@ struct pa_verify_plan_s {
   int32_t ranged = 0;            // flat plans: cta_start lists the CTAs' ranges
   int32_t cta_start[kMaxCtaTable + 1];
   int64_t part_units = 0;        // partial slots in the workspace
-  int32_t fused = 0;             // flat plans: split pairs merged inside the split kernel (no combine kernel)
-  size_t off_cnt = kWsHeader;    // fused merge: pair counters
   int32_t max_len = 0, max_q = 0, slots = 0;
   size_t off_dyn = 0, off_part = kWsHeader, off_lse = kWsHeader;  // workspace layout
   int64_t kv_bytes = 0;
@@ -168,8 +166,6 @@ void fill_params(SplitParams& p, pa_verify_plan_t plan, const void* q, const flo
     p.part_lse = reinterpret_cast<float*>(ws + plan->off_lse);
   }
   p.dyn = plan->dynamic ? reinterpret_cast<const DynWork*>(ws + plan->off_dyn) : nullptr;
-  p.fused = plan->fused;
-  p.pair_count = plan->fused ? reinterpret_cast<uint32_t*>(ws + plan->off_cnt) : nullptr;
   p.dev_ctx = context_lens;
   p.dev_q = query_lens;
   p.num_seqs = d.num_seqs;
@@ -206,19 +202,12 @@ cudaError_t launch_all(pa_verify_plan_t plan, SplitParams& p, cudaStream_t s, bo
                         kMaxChunk, s);
   prof = prof && plan->profiling && plan->ev[0];
   if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[0], s);
-  if (e == cudaSuccess) {
+  if (e == cudaSuccess)
     e = plan->kernel == PA_KERNEL_TCGEN05
             ? launch_tc_split(d.head_dim, fp8 ? 1 : 0, plan->rows_max, plan->units, &plan->tmk, &plan->tmv, &p, s)
         : fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s)
               : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s);
-    if (e == cudaErrorCooperativeLaunchTooLarge && p.fused) {
-      // the CTAs cannot all be resident on this device now (e.g. a partitioned GPU): split kernel + combine
-      (void)cudaGetLastError();
-      p.fused = 0;
-      e = launch_tc_split(d.head_dim, fp8 ? 1 : 0, plan->rows_max, plan->units, &plan->tmk, &plan->tmv, &p, s);
-    }
-  }
-  const bool combine = plan->needs_combine && !p.fused;
+  const bool combine = plan->needs_combine != 0;
   if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[1], s);
   if (e == cudaSuccess && combine) e = launch_combine(d.head_dim, &p, plan->max_splits, d.sm_count, s);
   if (e == cudaSuccess && prof) {
@@ -371,13 +360,7 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
   P->num_rows = static_cast<int32_t>(row);
   P->part_units = n_cta + static_cast<int64_t>(d.num_seqs) * Hkv;  // slot c + p < CTAs + pairs
   P->kv_bytes = work * (fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim));
-  // Split pairs are merged by the CTAs that made them when all CTAs fit one wave (cooperative launch).
-  P->fused = P->needs_combine && n_cta <= sms ? 1 : 0;
   size_t ws = kWsHeader;
-  if (P->fused) {
-    P->off_cnt = ws;
-    ws += align_up(static_cast<size_t>(d.num_seqs) * Hkv * 4, 256);
-  }
   if (P->needs_combine) {
     P->off_part = ws;
     ws += align_up(static_cast<size_t>(P->part_units) * rows_max * d.head_dim * 4, 256);
@@ -573,7 +556,6 @@ int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info) {
   info->dynamic = plan->dynamic;
   info->flat = plan->flat;
   info->total_tiles = plan->dynamic ? 0 : plan->total_tiles;
-  info->fused_merge = plan->fused;
   return PA_OK;
 }
 
@@ -627,9 +609,8 @@ int enqueue_with_scratch(pa_verify_plan_t plan, const void* q, const void* k_cac
   if (rc) return rc;
   SplitParams p{};
   fill_params(p, plan, q, k_scale, v_scale, block_table, context_lens, query_lens, softmax_scale, out, scratch);
-  // the error word (and a fused plan's pair counters) start each call at zero (the scratch keeps the last
-  // call's contents)
-  cudaError_t e = cudaMemsetAsync(scratch, 0, plan->fused ? plan->off_part : sizeof(uint32_t), s);
+  // the error word starts each call at zero (the scratch keeps the last call's contents)
+  cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess) e = launch_all(plan, p, s, false);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("kernel launch failed: ") + cudaGetErrorString(e));
   return PA_OK;

@@ -89,9 +89,6 @@ struct SplitParams {
   uint64_t wait_limit_ns;       // a bounded wait gives up after this long (0: one second)
   int32_t stall_cta;            // test hook: this CTA's MMA issuer first waits on a barrier that nothing
                                 // completes, so its bounded wait runs out (-1: none)
-  int32_t fused;                // flat plans: the split kernel merges split pairs itself (cooperative
-                                // launch), no combine kernel
-  uint32_t* pair_count;         // fused merge: one arrival counter per (sequence, KV head) pair
   SeqInfo seq[kMaxSeqs];
 };
 

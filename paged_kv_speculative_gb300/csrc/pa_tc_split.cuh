@@ -47,7 +47,6 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
-#include "pa_merge.cuh"
 #include "pa_tc.cuh"
 
 #include <type_traits>
@@ -1026,33 +1025,19 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, C::kTmemCols);
   }
-  // the pairs split over several CTAs are merged by those CTAs (the shared memory is free now)
-  if (p.fused) merge_split_pairs<D, C::kThreads>(p, reinterpret_cast<float*>(smem_raw + 1024 - (smem_addr(smem_raw) & 1023)));
 }
 
-// Launches the kernel for one (KV type, padded rows, head_dim) instance; a
-// plan with the fused merge is launched cooperatively (its CTAs wait on each
-// other, so all of them must be resident at once).
+// Launches the kernel for one (KV type, padded rows, head_dim) instance.
 template <int F8, int NP, int D>
 cudaError_t run_tc(int units, const CUtensorMap* tmk, const CUtensorMap* tmv, const SplitParams* p,
                    cudaStream_t stream) {
   auto kern = pa_tc_split_kernel<F8, NP, D>;
   constexpr int smem = TcCfg<F8, NP, D>::kSmem;
-  static_assert((D + 2) * (TcCfg<F8, NP, D>::kThreads / 32) * 4 + 4 <= smem, "merge scratch fits");
   static std::atomic<uint64_t> attr_done{0};  // devices whose limit is raised
-  cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
+  const cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(units);
-  cfg.blockDim = dim3(TcCfg<F8, NP, D>::kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = p->fused ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, *tmk, *tmv, *p);
+  kern<<<units, TcCfg<F8, NP, D>::kThreads, smem, stream>>>(*tmk, *tmv, *p);
+  return cudaGetLastError();
 }
 
 inline int tc_rows_pad(int rows_max) { return rows_max <= 16 ? 16 : rows_max <= 32 ? 32 : rows_max <= 48 ? 48 : 64; }
