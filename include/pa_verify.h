@@ -71,7 +71,7 @@ enum {
 };
 
 typedef struct {
-  int32_t num_seqs;           /* B, 0 .. 64 */
+  int32_t num_seqs;           /* B, 0 .. 1024 (dynamic plans: the capacity, 1 .. 1024) */
   int32_t num_q_heads;        /* Hq >= 1 */
   int32_t num_kv_heads;       /* Hkv >= 1, Hq % Hkv == 0, group G = Hq / Hkv */
   int32_t head_dim;           /* D: 64 or 128 (bf16 KV); 128 or 256 (FP8 KV; 256 on the tcgen05
@@ -83,7 +83,8 @@ typedef struct {
   int32_t num_pages;          /* pool size N_pg; block-table entries must lie in [0, N_pg) */
   int32_t block_table_stride; /* int32 entries per block-table row, >= ceil(L_b / 16) */
   int32_t split_override;     /* 0: the planner chooses; k > 0: chunk length
-                                 ceil(max_b L_b / k) rounded up to the staging tile */
+                                 ceil(max_b L_b / k) rounded up to the staging tile
+                                 (num_seqs <= 64 only) */
   int32_t sm_count;           /* 0: query the current device; > 0: plan for that many SMs */
   int32_t kernel;             /* PA_KERNEL_*: 0 picks the tensor-core (tcgen05) kernel where it
                                  applies (head_dim 128, or 256 with FP8 KV; q_b * G <= 64), else the
@@ -122,6 +123,10 @@ typedef struct {
   int32_t dynamic;         /* 1 for pa_verify_plan_dynamic plans (figures above are capacities) */
   int32_t flat;            /* 1 for flat plans */
   int32_t total_tiles;     /* flat plans: sum_b Hkv * ceil(L_b / 128) (dynamic plans: chosen per run, 0 here) */
+  int32_t device_table;    /* 1: each run builds the work table on the device from the device lengths
+                              (a one-CTA planner kernel ahead of the split kernel): dynamic plans, and
+                              plans of more than 64 sequences, whose table does not fit the kernel
+                              parameters */
 } pa_verify_plan_info;
 
 /*
@@ -137,6 +142,14 @@ typedef struct {
  * *workspace_bytes_out is the device workspace a run needs (0 is possible only
  * for an empty batch). On failure *plan_out is NULL; nothing is allocated and
  * no CUDA call is made (with sm_count > 0 the function makes no CUDA call at all).
+ *
+ * Up to 64 sequences the plan's work table travels in the kernel parameters.
+ * From 65 to 1024 sequences (the pages' reducer is sized for batches up to
+ * 1024: MTP-5 routing page, Motivation) it is the capacity plan of
+ * pa_verify_plan_dynamic with capacity num_seqs and the batch's longest
+ * lengths as bounds: each run builds the table on the device from the device
+ * lengths, whose values must then lie within those bounds (a length outside
+ * them sets PA_DEVERR_LENGTHS and that sequence writes nothing).
  */
 int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
                    const int32_t* query_lens_host, pa_verify_plan_t* plan_out,

@@ -48,6 +48,7 @@ struct pa_verify_plan_s {
   int32_t num_tokens = 0, num_rows = 0;
   int32_t kernel = PA_KERNEL_WARP_MMA;
   int32_t dynamic = 0;           // capacity plan: the work table is built on the device each run
+  int32_t host_lengths = 0;      // a capacity plan made by pa_verify_plan (more than kMaxSeqs sequences)
   int32_t flat = 0, per = 0, total_tiles = 0;  // flat plans (tcgen05 kernel): tiles per CTA, tiles in all
   int32_t ranged = 0;            // flat plans: cta_start lists the CTAs' ranges
   int32_t cta_start[kMaxCtaTable + 1];
@@ -373,6 +374,63 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
   return PA_OK;
 }
 
+// Capacity plan: the work table is built on the device at every run from the
+// device lengths (pa_dyn_plan.cu), for batches of up to `d.num_seqs` sequences
+// with context lengths <= max_len and query lengths <= max_q. Serves
+// pa_verify_plan_dynamic and host-length plans of more than kMaxSeqs
+// sequences (whose table does not fit the kernel parameters).
+int build_capacity_plan(const pa_verify_desc& d, int sms, int max_len, int max_q, bool use_tc,
+                        pa_verify_plan_t* plan_out, size_t* workspace_bytes_out) {
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  const int G = d.num_q_heads / d.num_kv_heads;
+  const int rows_max = max_q * G;
+  const int max_context_len = max_len, max_query_len = max_q;
+  const int warps = supported_warps(rows_max);
+  const int64_t slots = static_cast<int64_t>(sms) * (use_tc ? 1 : split_ctas_per_sm(warps));
+  const int64_t per_pair = (static_cast<int64_t>(max_context_len) + kMaxChunk - 1) / kMaxChunk;
+  const int64_t units_cap =
+      use_tc ? slots : std::max<int64_t>(slots, static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * per_pair);
+  // partial slots: a flat plan's CTA c writes pair p's partial at c + p
+  const int64_t part_cap = use_tc ? units_cap + static_cast<int64_t>(d.num_seqs) * d.num_kv_heads : units_cap;
+  const int64_t rows_cap = static_cast<int64_t>(d.num_seqs) * max_query_len * d.num_q_heads;
+  if (units_cap >= (int64_t(1) << 31) || rows_cap >= (int64_t(1) << 31))
+    return fail(PA_ERR_UNSUPPORTED, "capacity too large for one call");
+
+  pa_verify_plan_s* P = new (std::nothrow) pa_verify_plan_s();
+  if (!P) return fail(PA_ERR_NOMEM, "out of host memory");
+  P->d = d;
+  P->d.sm_count = sms;
+  P->dynamic = 1;
+  P->max_len = max_context_len;
+  P->max_q = max_query_len;
+  P->slots = static_cast<int32_t>(slots);
+  P->kernel = use_tc ? PA_KERNEL_TCGEN05 : PA_KERNEL_WARP_MMA;
+  P->flat = use_tc ? 1 : 0;  // flat: one CTA per SM, the tiles per CTA chosen on the device
+  P->tile = use_tc ? kFlatTile : tile_tokens(fp8 ? 1 : 0, d.head_dim);
+  P->chunk = 0;  // chosen on the device each run
+  P->units = static_cast<int32_t>(units_cap);
+  P->rows_max = rows_max;
+  P->warps = warps;
+  P->max_splits = static_cast<int32_t>(std::min<int64_t>(units_cap, (max_context_len + P->tile - 1) / P->tile));
+  P->needs_combine = 1;
+  P->num_tokens = d.num_seqs * max_query_len;
+  P->num_rows = static_cast<int32_t>(rows_cap);
+  const int64_t per_th = fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim);
+  P->kv_bytes = static_cast<int64_t>(d.num_seqs) * max_context_len * d.num_kv_heads * per_th;  // at capacity
+  P->part_units = part_cap;
+  size_t ws = kWsHeader;
+  P->off_dyn = ws;
+  ws += align_up(dyn_work_bytes(d.num_seqs), 256);
+  P->off_part = ws;
+  ws += align_up(static_cast<size_t>(part_cap) * rows_max * d.head_dim * 4, 256);
+  P->off_lse = ws;
+  ws += align_up(static_cast<size_t>(part_cap) * rows_max * 4, 256);
+  P->ws_bytes = ws;
+  *plan_out = P;
+  *workspace_bytes_out = ws;
+  return PA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -386,7 +444,9 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
   if (!desc || !plan_out || !workspace_bytes_out) return fail(PA_ERR_INVALID, "desc, plan_out and workspace_bytes_out must not be NULL");
   const pa_verify_desc& d = *desc;
   if (d.num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs < 0");
-  if (d.num_seqs > kMaxSeqs) return fail(PA_ERR_UNSUPPORTED, "num_seqs above " + std::to_string(kMaxSeqs));
+  if (d.num_seqs > kMaxBatch) return fail(PA_ERR_UNSUPPORTED, "num_seqs above " + std::to_string(kMaxBatch));
+  if (d.num_seqs > kMaxSeqs && d.split_override > 0)
+    return fail(PA_ERR_UNSUPPORTED, "split_override needs num_seqs <= " + std::to_string(kMaxSeqs));
   if (d.num_seqs > 0 && (!context_lens_host || !query_lens_host))
     return fail(PA_ERR_INVALID, "context_lens_host / query_lens_host must not be NULL");
   if (d.num_q_heads < 1 || d.num_kv_heads < 1 || d.num_q_heads % d.num_kv_heads != 0)
@@ -405,7 +465,7 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
   if (d.kernel < PA_KERNEL_AUTO || d.kernel > PA_KERNEL_TCGEN05) return fail(PA_ERR_INVALID, "unknown kernel");
 
   const int G = d.num_q_heads / d.num_kv_heads;
-  int rows_max = 0, max_len = 0;
+  int rows_max = 0, max_len = 0, max_q = 0;
   int64_t total_tokens = 0, work = 0;
   for (int b = 0; b < d.num_seqs; ++b) {
     const int L = context_lens_host[b], q = query_lens_host[b];
@@ -416,6 +476,7 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
     if (q * G > kMaxRows) return fail(PA_ERR_UNSUPPORTED, "query_len * group above 128 rows");
     rows_max = std::max(rows_max, q * G);
     max_len = std::max(max_len, L);
+    max_q = std::max(max_q, q);
     total_tokens += q;
     work += static_cast<int64_t>(L) * d.num_kv_heads;
   }
@@ -447,6 +508,20 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
   if (d.head_dim == 256 && !use_tc) {
     delete P;
     return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only (q_len * group <= 64)");
+  }
+  if (d.num_seqs > kMaxSeqs) {
+    // the table is too large for the kernel parameters: the device planner builds it at each run
+    delete P;
+    pa_verify_desc dd = d;
+    dd.sm_count = sms;
+    const int rc = build_capacity_plan(dd, sms, max_len, max_q, use_tc, plan_out, workspace_bytes_out);
+    if (rc != PA_OK) return rc;
+    pa_verify_plan_s* C = *plan_out;
+    C->host_lengths = 1;
+    C->num_tokens = static_cast<int32_t>(total_tokens);
+    C->kv_bytes = work * (fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim));
+    C->rows_max = rows_max;  // the plan's rows (the workspace was sized for max_q * G, the same)
+    return PA_OK;
   }
   const int tile = use_tc ? 128 : tile_tokens(fp8 ? 1 : 0, d.head_dim);
   const int warps = supported_warps(rows_max);
@@ -553,7 +628,8 @@ int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info) {
   info->kv_bytes = plan->kv_bytes;
   info->workspace_bytes = plan->ws_bytes;
   info->kernel = plan->kernel;
-  info->dynamic = plan->dynamic;
+  info->dynamic = plan->dynamic && !plan->host_lengths;
+  info->device_table = plan->dynamic;
   info->flat = plan->flat;
   info->total_tiles = plan->dynamic ? 0 : plan->total_tiles;
   return PA_OK;
@@ -708,7 +784,7 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
     return fail(PA_ERR_INVALID, "desc, plan_out and workspace_bytes_out must not be NULL");
   const pa_verify_desc& d = *desc;
   if (d.num_seqs < 1) return fail(PA_ERR_INVALID, "a dynamic plan needs num_seqs (the batch capacity) >= 1");
-  if (d.num_seqs > kMaxSeqs) return fail(PA_ERR_UNSUPPORTED, "num_seqs above " + std::to_string(kMaxSeqs));
+  if (d.num_seqs > kMaxBatch) return fail(PA_ERR_UNSUPPORTED, "num_seqs above " + std::to_string(kMaxBatch));
   if (d.num_q_heads < 1 || d.num_kv_heads < 1 || d.num_q_heads % d.num_kv_heads != 0)
     return fail(PA_ERR_INVALID, "need num_q_heads >= 1, num_kv_heads >= 1 and num_q_heads % num_kv_heads == 0");
   if (d.page_size != kPage) return fail(PA_ERR_UNSUPPORTED, "page_size must be 16");
@@ -743,50 +819,7 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
   const bool use_tc = d.kernel == PA_KERNEL_TCGEN05 || (d.kernel == PA_KERNEL_AUTO && tc_ok);
   if (d.head_dim == 256 && !use_tc)
     return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only (q_len * group <= 64)");
-  const int warps = supported_warps(rows_max);
-  const int64_t slots = static_cast<int64_t>(sms) * (use_tc ? 1 : split_ctas_per_sm(warps));
-  const int64_t per_pair = (static_cast<int64_t>(max_context_len) + kMaxChunk - 1) / kMaxChunk;
-  const int64_t units_cap =
-      use_tc ? slots : std::max<int64_t>(slots, static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * per_pair);
-  // partial slots: a flat plan's CTA c writes pair p's partial at c + p
-  const int64_t part_cap = use_tc ? units_cap + static_cast<int64_t>(d.num_seqs) * d.num_kv_heads : units_cap;
-  const int64_t rows_cap = static_cast<int64_t>(d.num_seqs) * max_query_len * d.num_q_heads;
-  if (units_cap >= (int64_t(1) << 31) || rows_cap >= (int64_t(1) << 31))
-    return fail(PA_ERR_UNSUPPORTED, "capacity too large for one call");
-
-  pa_verify_plan_s* P = new (std::nothrow) pa_verify_plan_s();
-  if (!P) return fail(PA_ERR_NOMEM, "out of host memory");
-  P->d = d;
-  P->d.sm_count = sms;
-  P->dynamic = 1;
-  P->max_len = max_context_len;
-  P->max_q = max_query_len;
-  P->slots = static_cast<int32_t>(slots);
-  P->kernel = use_tc ? PA_KERNEL_TCGEN05 : PA_KERNEL_WARP_MMA;
-  P->flat = use_tc ? 1 : 0;  // flat: one CTA per SM, the tiles per CTA chosen on the device
-  P->tile = use_tc ? kFlatTile : tile_tokens(fp8 ? 1 : 0, d.head_dim);
-  P->chunk = 0;  // chosen on the device each run
-  P->units = static_cast<int32_t>(units_cap);
-  P->rows_max = rows_max;
-  P->warps = warps;
-  P->max_splits = static_cast<int32_t>(std::min<int64_t>(units_cap, (max_context_len + P->tile - 1) / P->tile));
-  P->needs_combine = 1;
-  P->num_tokens = d.num_seqs * max_query_len;
-  P->num_rows = static_cast<int32_t>(rows_cap);
-  const int64_t per_th = fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim);
-  P->kv_bytes = static_cast<int64_t>(d.num_seqs) * max_context_len * d.num_kv_heads * per_th;  // at capacity
-  P->part_units = part_cap;
-  size_t ws = kWsHeader;
-  P->off_dyn = ws;
-  ws += align_up(sizeof(DynWork), 256);
-  P->off_part = ws;
-  ws += align_up(static_cast<size_t>(part_cap) * rows_max * d.head_dim * 4, 256);
-  P->off_lse = ws;
-  ws += align_up(static_cast<size_t>(part_cap) * rows_max * 4, 256);
-  P->ws_bytes = ws;
-  *plan_out = P;
-  *workspace_bytes_out = ws;
-  return PA_OK;
+  return build_capacity_plan(d, sms, max_context_len, max_query_len, use_tc, plan_out, workspace_bytes_out);
 }
 
 int pa_verify_debug_stall(pa_verify_plan_t plan, int32_t stall_cta, uint32_t wait_limit_us) {

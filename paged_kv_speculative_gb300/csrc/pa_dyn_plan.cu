@@ -3,19 +3,28 @@
 // follow, so that one captured CUDA graph serves every batch that fits the
 // plan's capacity. Sequences with query length 0 are padding: they get no
 // unit and no output row, so they write nothing (stores masked by row
-// liveness: DeepSeek-V4.1 page, description of the in-place KV stores).
+// liveness: DeepSeek-V4.1 page, description of the in-place KV stores). Plans
+// of more than 64 sequences built from host lengths use it too: their table
+// is too large for the kernel parameters.
 //
 // Same rules as the host planner. Chunk plans: the chunk is the smallest
 // multiple of the staging tile whose unit count fits `slots` (one wave),
 // capped at the page-id staging limit. Flat plans: the pairs' 128-token tiles
 // end to end, ceil(tiles / slots) of them per CTA. Sequences are scheduled
-// longest first.
+// longest first (ties by batch index), padded ones last.
+//
+// One CTA, one thread per sequence of the capacity (up to 1024): the order is
+// a bitonic sort of (length, index) keys in shared memory, the offsets are
+// block-wide prefix sums.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "pa_internal.h"
 
 namespace pav {
+
+constexpr int kPlanThreads = kMaxBatch;  // one thread per sequence of the capacity
+static_assert(kPlanThreads == 1024, "the block reductions assume 32 warps");
 
 struct DynPlanArgs {
   const int32_t* ctx;  // [B] device context lengths
@@ -26,10 +35,54 @@ struct DynPlanArgs {
   int32_t num_seqs, num_q_heads, num_kv_heads, bt_stride, max_len, max_q, slots, tile, max_chunk;
 };
 
-__global__ void __launch_bounds__(64) pa_dyn_plan_kernel(DynPlanArgs a) {
-  __shared__ int s_len[kMaxSeqs], s_q[kMaxSeqs], s_rank_units[kMaxSeqs], s_rank_rows[kMaxSeqs], s_rank_tiles[kMaxSeqs];
-  __shared__ int s_red[2];
-  __shared__ long long s_red64[2];
+// Inclusive prefix sum over the block's 1024 threads (thread order); *total gets the block sum.
+__device__ __forceinline__ long long block_scan(long long v, long long* red, long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  if (lane == 31) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = red[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += t;
+    }
+    red[lane] = w;
+  }
+  __syncthreads();
+  if (warp > 0) v += red[warp - 1];
+  *total = red[31];
+  __syncthreads();  // red is reused by the next call
+  return v;
+}
+
+__device__ __forceinline__ long long block_sum(long long v, long long* red) {
+  long long total;
+  (void)block_scan(v, red, &total);
+  return total;
+}
+
+__device__ __forceinline__ int block_max(int v, long long* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, m));
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  int r = 0;
+  for (int w = 0; w < 32; ++w) r = max(r, static_cast<int>(red[w]));
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) pa_dyn_plan_kernel(DynPlanArgs a) {
+  __shared__ unsigned long long s_key[kPlanThreads];
+  __shared__ int s_len[kPlanThreads], s_q[kPlanThreads], s_qoff[kPlanThreads];
+  __shared__ long long s_red[32];
   const int b = threadIdx.x;
   const bool live = b < a.num_seqs;
   int L = 0, q = 0;
@@ -42,29 +95,10 @@ __global__ void __launch_bounds__(64) pa_dyn_plan_kernel(DynPlanArgs a) {
   }
   s_len[b] = L;
   s_q[b] = q;
-  const int lane = b & 31, warp = b >> 5;
 
-  // block-wide sums / maximum over the 64 threads
-  auto sum64 = [&](long long v) {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-    __syncthreads();
-    if (lane == 0) s_red64[warp] = v;
-    __syncthreads();
-    return s_red64[0] + s_red64[1];
-  };
-  auto max64 = [&](int v) {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, m));
-    __syncthreads();
-    if (lane == 0) s_red[warp] = v;
-    __syncthreads();
-    return max(s_red[0], s_red[1]);
-  };
-  const long long work = sum64(static_cast<long long>(L) * a.num_kv_heads);
-  const int max_l = max64(L);
-  const long long n_live = sum64(q > 0 ? 1 : 0);
-  auto units_for = [&](long long c) { return sum64(L > 0 ? (L + c - 1) / c : 0) * a.num_kv_heads; };
+  const long long work = block_sum(static_cast<long long>(L) * a.num_kv_heads, s_red);
+  const int max_l = block_max(L, s_red);
+  auto units_for = [&](long long c) { return block_sum(L > 0 ? (L + c - 1) / c : 0, s_red) * a.num_kv_heads; };
 
   int chunk = a.tile;
   if (max_l > 0 && !a.flat) {
@@ -79,54 +113,58 @@ __global__ void __launch_bounds__(64) pa_dyn_plan_kernel(DynPlanArgs a) {
     }
     chunk = static_cast<int>(min(lo * a.tile, static_cast<long long>(a.max_chunk)));
   }
-  const int n_chunks = a.flat ? 0 : (L > 0 ? (L + chunk - 1) / chunk : 0);
-  const int n_tiles = (L + kFlatTile - 1) / kFlatTile;  // 0 for padding
 
-  // rank: live sequences by decreasing length (ties by index), then padding by index
-  int rank = 0;
-  for (int c = 0; c < a.num_seqs; ++c) {
-    if (c == b) continue;
-    const bool other_live = s_q[c] > 0;
-    if (q > 0) {
-      if (other_live && (s_len[c] > L || (s_len[c] == L && c < b))) ++rank;
-    } else {
-      if (other_live || c < b) ++rank;
+  // query-row offsets in batch order
+  long long tot_tokens;
+  s_qoff[b] = static_cast<int>(block_scan(q, s_red, &tot_tokens) - q);
+
+  // order: live sequences by decreasing length (ties by index), then padding by index; entries past the
+  // batch sort last and are not written
+  s_key[b] = q > 0 ? (static_cast<unsigned long long>(0x7FFFFFFF - L) << 32) | static_cast<unsigned>(b)
+                   : (1ull << 63) | static_cast<unsigned>(b);
+  __syncthreads();
+  for (int k = 2; k <= kPlanThreads; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const int o = b ^ j;
+      if (o > b) {
+        const unsigned long long x = s_key[b], y = s_key[o];
+        if ((x > y) == ((b & k) == 0)) {
+          s_key[b] = y;
+          s_key[o] = x;
+        }
+      }
+      __syncthreads();
     }
   }
-  // query-row offset in batch order
-  int q_off = 0;
-  for (int c = 0; c < b && c < a.num_seqs; ++c) q_off += s_q[c];
-  __syncthreads();
-  if (live) {
-    s_rank_units[rank] = n_chunks * a.num_kv_heads;
-    s_rank_rows[rank] = q * a.num_q_heads;
-    s_rank_tiles[rank] = n_tiles * a.num_kv_heads;
-  }
-  __syncthreads();
-  if (live) {
-    int us = 0, rs = 0, ts = 0;
-    for (int r = 0; r < rank; ++r) {
-      us += s_rank_units[r];
-      rs += s_rank_rows[r];
-      ts += s_rank_tiles[r];
-    }
+
+  // thread r builds entry r of the table: the sequence of rank r and its offsets in rank order
+  const int r = b;
+  const int src = static_cast<int>(s_key[r] & 0xFFFFFFFFu);
+  const bool in = r < a.num_seqs;
+  const int Ls = in ? s_len[src] : 0, qs = in ? s_q[src] : 0;
+  const int n_chunks = a.flat ? 0 : (Ls > 0 ? (Ls + chunk - 1) / chunk : 0);
+  const int n_tiles = (Ls + kFlatTile - 1) / kFlatTile;  // 0 for padding
+  const long long units_r = static_cast<long long>(n_chunks) * a.num_kv_heads;
+  const long long rows_r = static_cast<long long>(qs) * a.num_q_heads;
+  const long long tiles_r = static_cast<long long>(n_tiles) * a.num_kv_heads;
+  long long total_units, total_rows, total_tiles;
+  const long long us = block_scan(units_r, s_red, &total_units) - units_r;
+  const long long rs = block_scan(rows_r, s_red, &total_rows) - rows_r;
+  const long long ts = block_scan(tiles_r, s_red, &total_tiles) - tiles_r;
+  if (in) {
     SeqInfo si;
-    si.ctx_len = L;
-    si.q_len = q;
-    si.q_off = q_off;
-    si.unit_start = us;
-    si.row_start = rs;
+    si.ctx_len = Ls;
+    si.q_len = qs;
+    si.q_off = s_qoff[src];
+    si.unit_start = static_cast<int>(us);
+    si.row_start = static_cast<int>(rs);
     si.n_chunks = n_chunks;
-    si.b = b;
-    si.tile_start = ts;
+    si.b = src;
+    si.tile_start = static_cast<int>(ts);
     si.n_tiles = n_tiles;
     si.pad = 0;
-    a.out->seq[rank] = si;
+    dyn_seq(a.out)[r] = si;
   }
-  const long long total_units = sum64(static_cast<long long>(n_chunks) * a.num_kv_heads);
-  const long long total_rows = sum64(static_cast<long long>(q) * a.num_q_heads);
-  const long long total_tokens = sum64(q);
-  const long long total_tiles = sum64(static_cast<long long>(n_tiles) * a.num_kv_heads);
   if (b == 0) {
     long long per = 1, n_cta = 0;
     if (total_tiles > 0) {
@@ -138,17 +176,17 @@ __global__ void __launch_bounds__(64) pa_dyn_plan_kernel(DynPlanArgs a) {
     a.out->total_tiles = static_cast<int>(total_tiles);
     a.out->chunk = a.flat ? kFlatTile : chunk;
     a.out->num_rows = static_cast<int>(total_rows);
-    a.out->num_tokens = static_cast<int>(total_tokens);
+    a.out->num_tokens = static_cast<int>(tot_tokens);
   }
-  (void)n_live;
 }
 
 cudaError_t launch_dyn_plan(const int32_t* ctx, const int32_t* ql, DynWork* out, uint32_t* err, int flat, int num_seqs,
                             int num_q_heads, int num_kv_heads, int bt_stride, int max_len, int max_q, int slots, int tile,
                             int max_chunk, cudaStream_t stream) {
+  if (num_seqs > kPlanThreads) return cudaErrorInvalidValue;
   DynPlanArgs a{ctx, ql, out, err, flat, num_seqs, num_q_heads, num_kv_heads, bt_stride, max_len, max_q, slots, tile,
                 max_chunk};
-  pa_dyn_plan_kernel<<<1, 64, 0, stream>>>(a);
+  pa_dyn_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -10,7 +10,8 @@
 namespace pav {
 
 constexpr int kPage = 16;         // tokens per KV page
-constexpr int kMaxSeqs = 64;      // sequences per call (the per-sequence table travels in kernel parameters)
+constexpr int kMaxSeqs = 64;      // sequences whose table travels in the kernel parameters (plans built on the host)
+constexpr int kMaxBatch = 1024;   // sequences per call; above kMaxSeqs the table is built on the device at each run
 constexpr int kStages = 3;        // shared-memory ring depth of the split kernel
 constexpr int kMaxChunk = 16384;  // context tokens per work unit (bounds the page-id staging array)
 constexpr int kMaxRows = 128;     // q_len * group rows per (sequence, KV head)
@@ -45,7 +46,9 @@ struct SeqInfo {
 };
 
 // Work description written on the device by the planner kernel of a
-// dynamic (capacity) plan, from the device lengths of the call.
+// dynamic (capacity) plan, from the device lengths of the call. The header is
+// followed by the per-sequence table, one SeqInfo per sequence of the
+// capacity: live sequences by decreasing length, then padded ones.
 struct DynWork {
   int32_t num_units;  // split units (flat plans: CTAs with work) of this call
   int32_t chunk;      // context tokens per unit (flat plans: 128)
@@ -54,8 +57,11 @@ struct DynWork {
   int32_t per;        // flat plans: tiles per CTA
   int32_t total_tiles;
   int32_t pad[2];
-  SeqInfo seq[kMaxSeqs];  // live sequences by decreasing length, then padded ones
 };
+__host__ __device__ inline SeqInfo* dyn_seq(DynWork* w) { return reinterpret_cast<SeqInfo*>(w + 1); }
+__host__ __device__ inline const SeqInfo* dyn_seq(const DynWork* w) { return reinterpret_cast<const SeqInfo*>(w + 1); }
+// Workspace bytes of a device work table for `capacity` sequences.
+inline size_t dyn_work_bytes(int capacity) { return sizeof(DynWork) + static_cast<size_t>(capacity) * sizeof(SeqInfo); }
 
 struct SplitParams {
   const uint16_t* q;            // [T, Hq, D] bf16
@@ -107,7 +113,7 @@ struct WorkView {
 };
 __device__ __forceinline__ WorkView work_view(const SplitParams& p) {
   if (p.dyn)
-    return WorkView{p.dyn->seq, p.num_seqs, p.dyn->chunk, p.dyn->num_units, p.dyn->num_rows, p.dyn->per,
+    return WorkView{dyn_seq(p.dyn), p.num_seqs, p.dyn->chunk, p.dyn->num_units, p.dyn->num_rows, p.dyn->per,
                     p.dyn->total_tiles, nullptr};
   return WorkView{p.seq, p.num_seqs, p.chunk, p.num_units, p.num_rows, p.per, p.total_tiles,
                   p.ranged ? p.cta_start : nullptr};

@@ -68,7 +68,7 @@ class PlanInfo(ctypes.Structure):
         ("rows_max", ctypes.c_int32), ("warps", ctypes.c_int32), ("max_splits", ctypes.c_int32),
         ("needs_combine", ctypes.c_int32), ("num_tokens", ctypes.c_int32), ("kv_bytes", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_size_t), ("kernel", ctypes.c_int32), ("dynamic", ctypes.c_int32),
-        ("flat", ctypes.c_int32), ("total_tiles", ctypes.c_int32)]
+        ("flat", ctypes.c_int32), ("total_tiles", ctypes.c_int32), ("device_table", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}

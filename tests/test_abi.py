@@ -205,7 +205,7 @@ def test_empty_batch_plans():
     (dict(ctx=[100], ql=[8], hq=32, hkv=1), pv.ERR_UNSUPPORTED),
     (dict(ctx=[100], ql=[2], hq=6, hkv=4), pv.ERR_INVALID),
     (dict(ctx=[100], ql=[2], stride=3), pv.ERR_INVALID),
-    (dict(ctx=[10] * 65, ql=[1] * 65), pv.ERR_UNSUPPORTED),
+    (dict(ctx=[10] * 1025, ql=[1] * 1025), pv.ERR_UNSUPPORTED),
     (dict(ctx=[100], ql=[6], d=256), pv.ERR_UNSUPPORTED),  # head_dim 256 is an FP8 shape only
     (dict(ctx=[100], ql=[8], hq=16, hkv=1, d=256, kv=pv.KV_FP8_E4M3), pv.ERR_UNSUPPORTED),  # 128 rows
     (dict(ctx=[100], ql=[6], d=256, kv=pv.KV_FP8_E4M3, kernel=pv.KERNEL_WARP_MMA), pv.ERR_UNSUPPORTED),
@@ -269,3 +269,25 @@ def test_fp8_run_needs_scales():
 
 def test_free_accepts_null():
     pv.lib().pa_verify_free(None)
+
+
+def test_batches_above_64_sequences_build_their_table_on_the_device():
+    rng = np.random.default_rng(3)
+    for B in (65, 128, 256, 1024):
+        ctx = rng.integers(6, 5000, B).tolist()
+        ql = rng.integers(1, 9, B).tolist()
+        p = mk(ctx, ql, hq=16, hkv=2, sms=152)
+        i = p.info
+        assert i.device_table == 1 and i.dynamic == 0
+        assert i.num_tokens == sum(ql)
+        assert i.kv_bytes == sum(ctx) * 2 * 512
+        assert i.rows_max == max(ql) * 8
+        assert i.kernel == pv.KERNEL_TCGEN05 and i.flat == 1
+        # header, the device table, then partials for one wave of CTAs plus one slot per (sequence, KV head)
+        table = 32 + 40 * B
+        assert p.workspace_bytes >= 256 + table + (152 + 2 * B) * max(ql) * 8 * 129 * 4
+    with pytest.raises(pv.PaVerifyError) as e:
+        mk([100] * 65, [6] * 65, split_override=2)
+    assert e.value.status == pv.ERR_UNSUPPORTED
+    small = mk([100] * 64, [6] * 64)
+    assert small.info.device_table == 0

@@ -32,7 +32,7 @@ def test_capacity_figures():
     (dict(max_query_len=9), pv.ERR_INVALID),
     (dict(max_context_len=3, max_query_len=6), pv.ERR_INVALID),
     (dict(max_context_len=1 << 20), pv.ERR_INVALID),  # more pages than the block-table stride
-    (dict(capacity=65), pv.ERR_UNSUPPORTED),
+    (dict(capacity=1025), pv.ERR_UNSUPPORTED),
 ])
 def test_dynamic_plan_refusals(kw, status):
     args = dict(capacity=8, max_context_len=4096, max_query_len=6)
