@@ -53,6 +53,9 @@ struct pa_verify_plan_s {
   int32_t ranged = 0;            // flat plans: cta_start lists the CTAs' ranges
   int32_t cta_start[kMaxCtaTable + 1];
   int64_t part_units = 0;        // partial slots in the workspace
+  // split pairs for the combine (plans built from host lengths; -1: more than the table holds, or none built)
+  int32_t n_split_pairs = -1, split_rows = 0;
+  CombinePair split_pairs[kMaxCombinePairs];
   int32_t max_len = 0, max_q = 0, slots = 0;
   size_t off_dyn = 0, off_part = kWsHeader, off_lse = kWsHeader;  // workspace layout
   int64_t kv_bytes = 0;
@@ -210,13 +213,54 @@ cudaError_t launch_all(pa_verify_plan_t plan, SplitParams& p, cudaStream_t s, bo
               : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s);
   const bool combine = plan->needs_combine != 0;
   if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[1], s);
-  if (e == cudaSuccess && combine) e = launch_combine(d.head_dim, &p, plan->max_splits, d.sm_count, s);
+  if (e == cudaSuccess && combine) {
+    if (plan->n_split_pairs >= 0 && !plan->dynamic) {
+      CombineTable t;
+      t.part_o = p.part_o;
+      t.part_lse = p.part_lse;
+      t.out = p.out;
+      t.rows_max = p.rows_max;
+      t.num_q_heads = p.num_q_heads;
+      t.group = p.group;
+      t.out_f32 = p.out_f32;
+      t.n_pairs = plan->n_split_pairs;
+      t.num_rows = plan->split_rows;
+      std::memcpy(t.pair, plan->split_pairs, sizeof(CombinePair) * plan->n_split_pairs);
+      e = launch_combine(d.head_dim, &p, &t, plan->max_splits, d.sm_count, s);
+    } else {
+      e = launch_combine(d.head_dim, &p, nullptr, plan->max_splits, d.sm_count, s);
+    }
+  }
   if (e == cudaSuccess && prof) {
     e = cudaEventRecord(plan->ev[2], s);
     plan->profiled_runs++;
     plan->last_had_combine = combine ? 1 : 0;
   }
   return e;
+}
+
+// Lists the split pairs of a plan built from host lengths for the combine's
+// table (in plan order); n_split_pairs stays -1 when they do not fit it.
+void list_split_pairs(pa_verify_plan_s* P, int hkv, int G, const std::vector<int32_t>& u0,
+                      const std::vector<int32_t>& n) {
+  int32_t cnt = 0, rows = 0;
+  bool fits = true;
+  for (int k = 0; k < P->d.num_seqs; ++k)
+    for (int g = 0; g < hkv; ++g) {
+      const int pr = k * hkv + g;
+      if (n[pr] <= 1) continue;
+      if (cnt == kMaxCombinePairs) { fits = false; break; }
+      CombinePair& c = P->split_pairs[cnt++];
+      c.u0 = u0[pr];
+      c.n = n[pr];
+      c.q_off = P->seq[k].q_off;
+      c.head0 = g * G;
+      c.rows = P->seq[k].q_len * G;
+      c.row_base = rows;
+      rows += c.rows;
+    }
+  P->n_split_pairs = fits ? cnt : -1;
+  P->split_rows = fits ? rows : 0;
 }
 
 // A CTA that moves from one (sequence, KV head) pair to the next pays for the
@@ -340,12 +384,17 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
                                 P->cta_start) - 1;
   };
   int max_splits = 0;
+  std::vector<int32_t> pu0(static_cast<size_t>(d.num_seqs) * Hkv), pn(pu0.size());
   for (int k = 0; k < d.num_seqs; ++k)
     for (int g = 0; g < Hkv; ++g) {
       const int64_t t0 = P->seq[k].tile_start + static_cast<int64_t>(g) * P->seq[k].n_tiles;
       const int64_t t1 = t0 + P->seq[k].n_tiles - 1;
-      max_splits = std::max<int>(max_splits, static_cast<int>(cta_of(t1) - cta_of(t0) + 1));
+      const int pr = k * Hkv + g;
+      pn[pr] = static_cast<int32_t>(cta_of(t1) - cta_of(t0) + 1);
+      pu0[pr] = static_cast<int32_t>(cta_of(t0) + pr);  // CTA c writes pair p's partial at slot c + p
+      max_splits = std::max<int>(max_splits, pn[pr]);
     }
+  list_split_pairs(P, Hkv, G, pu0, pn);
   P->kernel = PA_KERNEL_TCGEN05;
   P->flat = 1;
   P->tile = kFlatTile;
@@ -577,6 +626,16 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
   if (unit >= (int64_t(1) << 31) || row >= (int64_t(1) << 31)) {
     delete P;
     return fail(PA_ERR_UNSUPPORTED, "work too large for one call");
+  }
+  {
+    std::vector<int32_t> pu0(static_cast<size_t>(d.num_seqs) * d.num_kv_heads), pn(pu0.size());
+    for (int k = 0; k < d.num_seqs; ++k)
+      for (int g = 0; g < d.num_kv_heads; ++g) {
+        const int pr = k * d.num_kv_heads + g;
+        pn[pr] = P->seq[k].n_chunks;
+        pu0[pr] = P->seq[k].unit_start + g * P->seq[k].n_chunks;  // units: KV head major, then chunk
+      }
+    list_split_pairs(P, d.num_kv_heads, G, pu0, pn);
   }
   P->kernel = use_tc ? PA_KERNEL_TCGEN05 : PA_KERNEL_WARP_MMA;
   P->tile = tile;

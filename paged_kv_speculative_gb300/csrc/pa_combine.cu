@@ -13,7 +13,11 @@
 // memory round trip per round; rounds combine online, the running sums
 // rescaled when the maximum rises); the W warps of a row then merge in shared
 // memory. Rows whose (sequence, KV head) was not split were written by the
-// split kernel. A plain stream-ordered launch after the split kernel: launched
+// split kernel. Plans built from host lengths pass a table of their split pairs
+// (CombineTable), so the grid covers only split rows and a row is found by one
+// search of that table; plans whose work table lives on the device (or with
+// more split pairs than the table holds) cover every row and find it in the
+// work table. A plain stream-ordered launch after the split kernel: launched
 // as its programmatic dependent instead, the call measured up to 14 us slower
 // on GB300 (batch 1 at head_dim 256) and never faster.
 #include "pa_device.cuh"
@@ -49,8 +53,70 @@ int combine_warps_per_row(int max_splits) {
   return max_splits <= 8 ? 1 : max_splits <= 16 ? 2 : max_splits <= 32 ? 4 : 8;
 }
 
-template <int D, int kWarps, int CW>
-__global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_constant__ SplitParams p, int W) {
+// A split row: its partials (n of them from slot u0, row r of each) and its place in `out`.
+struct RowRef {
+  int n;        // partials (1: not split, nothing to merge)
+  int r;        // row of the pair inside a partial
+  size_t u0;    // slot of the first partial
+  size_t orow;  // (token row * Hq + q head), the output row
+};
+
+// Row rho of a plan's work table (every row of the batch).
+__device__ __forceinline__ RowRef resolve_row(const SplitParams& p, int rho) {
+  RowRef rr{0, 0, 0, 0};
+  const WorkView wv = work_view(p);
+  if (rho >= wv.num_rows) return rr;  // a dynamic plan's grid covers its capacity
+  int lo = 0, hi = wv.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (wv.seq[mid].row_start <= rho) lo = mid; else hi = mid - 1;
+  }
+  const SeqInfo si = wv.seq[lo];
+  const int local = rho - si.row_start;
+  const int i = local / p.num_q_heads;
+  const int h = local - i * p.num_q_heads;
+  const int G = p.group;
+  const int kvh = h / G;
+  rr.r = i * G + (h - kvh * G);
+  rr.orow = static_cast<size_t>(si.q_off + i) * p.num_q_heads + h;
+  if (p.flat) {
+    // pair (lo, kvh) covers tiles [t0, t0 + n_tiles); CTA c wrote its piece at slot c + pair
+    const int pair = lo * p.num_kv_heads + kvh;
+    const int t0 = si.tile_start + kvh * si.n_tiles;
+    const int c0 = flat_cta_of(wv, t0);
+    rr.n = flat_cta_of(wv, t0 + si.n_tiles - 1) - c0 + 1;
+    rr.u0 = static_cast<size_t>(c0) + pair;
+  } else {
+    rr.n = si.n_chunks;
+    rr.u0 = static_cast<size_t>(si.unit_start) + static_cast<size_t>(kvh) * rr.n;
+  }
+  return rr;
+}
+
+// Row rho of a split-pair table (split rows only).
+__device__ __forceinline__ RowRef resolve_row(const CombineTable& t, int rho) {
+  RowRef rr{0, 0, 0, 0};
+  if (rho >= t.num_rows) return rr;
+  int lo = 0, hi = t.n_pairs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (t.pair[mid].row_base <= rho) lo = mid; else hi = mid - 1;
+  }
+  const CombinePair cp = t.pair[lo];
+  const int r = rho - cp.row_base;
+  const int i = r / t.group;
+  rr.n = cp.n;
+  rr.r = r;
+  rr.u0 = static_cast<size_t>(cp.u0);
+  rr.orow = static_cast<size_t>(cp.q_off + i) * t.num_q_heads + cp.head0 + (r - i * t.group);
+  return rr;
+}
+
+__device__ __forceinline__ int combine_rows(const SplitParams& p) { return work_view(p).num_rows; }
+__device__ __forceinline__ int combine_rows(const CombineTable& t) { return t.num_rows; }
+
+template <typename Args, int D, int kWarps, int CW>
+__global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_constant__ Args p, int W) {
   constexpr int kPer = CW / 32;  // columns per lane
   constexpr int kSlices = D / CW;  // column slices of a row (consecutive CTAs)
   constexpr int kRound = 8;     // splits in flight per round
@@ -63,36 +129,9 @@ __global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_co
   const int slice = blockIdx.x % kSlices;
   const int rho = (blockIdx.x / kSlices) * (kWarps / W) + warp / W;
   const int col = slice * CW + lane * kPer;  // this lane's first column
-  const WorkView wv = work_view(p);
-  int n = 0, i = 0, h = 0;
-  size_t u0 = 0, q_off = 0;
-  int r = 0;
-  if (rho < wv.num_rows) {  // a dynamic plan's grid covers its capacity
-    int lo = 0, hi = wv.num_seqs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (wv.seq[mid].row_start <= rho) lo = mid; else hi = mid - 1;
-    }
-    const SeqInfo si = wv.seq[lo];
-    const int local = rho - si.row_start;
-    i = local / p.num_q_heads;
-    h = local - i * p.num_q_heads;
-    const int G = p.group;
-    const int kvh = h / G;
-    r = i * G + (h - kvh * G);
-    q_off = si.q_off;
-    if (p.flat) {
-      // pair (lo, kvh) covers tiles [t0, t0 + n_tiles); CTA c wrote its piece at slot c + pair
-      const int pair = lo * p.num_kv_heads + kvh;
-      const int t0 = si.tile_start + kvh * si.n_tiles;
-      const int c0 = flat_cta_of(wv, t0);
-      n = flat_cta_of(wv, t0 + si.n_tiles - 1) - c0 + 1;
-      u0 = static_cast<size_t>(c0) + pair;
-    } else {
-      n = si.n_chunks;
-      u0 = static_cast<size_t>(si.unit_start) + static_cast<size_t>(kvh) * n;
-    }
-  }
+  const RowRef rr = resolve_row(p, rho);
+  const int n = rr.n, r = rr.r;
+  const size_t u0 = rr.u0;
   const bool live = n > 1;  // (warp-uniform; every warp still reaches the barrier below)
 
   float M = -INFINITY, wsum = 0.f;
@@ -159,7 +198,7 @@ __global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_co
   }
   if (!live || wi != 0) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const size_t orow = (static_cast<size_t>(q_off + i) * p.num_q_heads + h) * D + col;
+  const size_t orow = rr.orow * D + col;
   float y[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) y[e] = acc[e] * inv;
@@ -182,12 +221,14 @@ __global__ void __launch_bounds__(32 * kWarps) pa_combine_kernel(const __grid_co
   }
 }
 
-cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, int sm_count, cudaStream_t stream) {
-  if (p->num_rows <= 0) return cudaSuccess;
+template <typename Args>
+static cudaError_t launch_combine_args(int head_dim, const Args& a, int num_rows, int max_splits, int sm_count,
+                                       cudaStream_t stream) {
+  if (num_rows <= 0) return cudaSuccess;
   const int W = combine_warps_per_row(max_splits);
   const int warps = W == 1 ? kCombineWarpsNarrow : kCombineWarpsWide;
   const int rows_per_cta = warps / W;
-  const int row_ctas = (p->num_rows + rows_per_cta - 1) / rows_per_cta;
+  const int row_ctas = (num_rows + rows_per_cta - 1) / rows_per_cta;
   const bool sliced = W > 1 && 2 * row_ctas <= sm_count;
   const int slices = sliced ? head_dim / kSliceCols : 1;
   cudaLaunchConfig_t cfg = {};
@@ -196,19 +237,25 @@ cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, i
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   if (W == 1) {
-    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsNarrow, 64>, *p, W);
-    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsNarrow, 128>, *p, W);
-    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<256, kCombineWarpsNarrow, 256>, *p, W);
+    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<Args, 64, kCombineWarpsNarrow, 64>, a, W);
+    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<Args, 128, kCombineWarpsNarrow, 128>, a, W);
+    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<Args, 256, kCombineWarpsNarrow, 256>, a, W);
   } else if (sliced) {
-    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsWide, kSliceCols>, *p, W);
-    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsWide, kSliceCols>, *p, W);
-    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<256, kCombineWarpsWide, kSliceCols>, *p, W);
+    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<Args, 64, kCombineWarpsWide, kSliceCols>, a, W);
+    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<Args, 128, kCombineWarpsWide, kSliceCols>, a, W);
+    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<Args, 256, kCombineWarpsWide, kSliceCols>, a, W);
   } else {
-    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<64, kCombineWarpsWide, 64>, *p, W);
-    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<128, kCombineWarpsWide, 128>, *p, W);
-    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<256, kCombineWarpsWide, 256>, *p, W);
+    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<Args, 64, kCombineWarpsWide, 64>, a, W);
+    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<Args, 128, kCombineWarpsWide, 128>, a, W);
+    if (head_dim == 256) return cudaLaunchKernelEx(&cfg, pa_combine_kernel<Args, 256, kCombineWarpsWide, 256>, a, W);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_combine(int head_dim, const SplitParams* p, const CombineTable* t, int max_splits, int sm_count,
+                           cudaStream_t stream) {
+  if (t) return launch_combine_args(head_dim, *t, t->num_rows, max_splits, sm_count, stream);
+  return launch_combine_args(head_dim, *p, p->num_rows, max_splits, sm_count, stream);
 }
 
 }  // namespace pav

@@ -173,7 +173,30 @@ inline cudaError_t ensure_smem_attr(Kern kern, int bytes, std::atomic<uint64_t>&
   return e;
 }
 
-cudaError_t launch_combine(int head_dim, const SplitParams* p, int max_splits, int sm_count, cudaStream_t stream);
+// A (sequence, KV head) pair split over several units, as the combine kernel
+// sees it: its n partials sit at slots u0 .. u0 + n - 1, its q_len * G rows are
+// rows row_base .. row_base + rows - 1 of the combine grid.
+struct CombinePair {
+  int32_t u0, n;      // first partial slot, partial count
+  int32_t q_off;      // first token row of the sequence in q / out
+  int32_t head0;      // first q head of the pair (kv head * G)
+  int32_t rows;       // q_len * G
+  int32_t row_base;   // combine rows of the pairs before this one
+};
+constexpr int kMaxCombinePairs = 256;  // split pairs a table can list (else every row is covered)
+// The combine's arguments for plans built from host lengths: only split rows.
+struct CombineTable {
+  const float* part_o;
+  const float* part_lse;
+  void* out;
+  int32_t rows_max, num_q_heads, group, out_f32;
+  int32_t n_pairs, num_rows;  // split pairs listed, their rows in all
+  CombinePair pair[kMaxCombinePairs];
+};
+
+// The combine: over the split rows of `t` when given, else over every row of the plan's work table.
+cudaError_t launch_combine(int head_dim, const SplitParams* p, const CombineTable* t, int max_splits, int sm_count,
+                           cudaStream_t stream);
 
 }  // namespace pav
 

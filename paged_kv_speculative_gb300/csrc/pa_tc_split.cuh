@@ -654,6 +654,12 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       }
       wait(&sfull[sb], static_cast<uint32_t>(i >> 1) & 1u);
       tc::fence_after_sync();
+      // Columns of this group that hold rows of the pair (a batch whose pairs have fewer rows than the
+      // instance's N): in the 64-row instances (the ones a batch of mixed query lengths runs) the P work of
+      // 8-column chunks past them is skipped. Their P columns keep stale values, which reach only output
+      // columns that are never read, and their row sums stay zero. (Elsewhere the branch cost registers:
+      // the 48-row FP8 instance spilled 116 bytes a thread with it, 64 without.)
+      const int act = min(NH, max(0, cu.QL * G - col0));  // chunk c0 is live iff c0 < act
       float2 y[NH / 2];  // scores of the owned columns, in pairs (packed f32x2 arithmetic)
       {
         uint32_t r[NH];
@@ -889,6 +895,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       const float2 iv2 = make_float2(inv_sv, inv_sv);
 #pragma unroll
       for (int c0 = 0; c0 < NH; c0 += 8) {
+        if (NP == 64 && c0 >= act) continue;  // no row of the pair in these columns (64-row instances)
         float2 pv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
