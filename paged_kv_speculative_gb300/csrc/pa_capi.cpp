@@ -263,44 +263,49 @@ void list_split_pairs(pa_verify_plan_s* P, int hkv, int G, const std::vector<int
   P->split_rows = fits ? rows : 0;
 }
 
-// A CTA that moves from one (sequence, KV head) pair to the next pays for the
-// switch (the outgoing pair's epilogue, the incoming pair's Q and first-tile
-// maxima, mostly code that runs cold while HBM is saturated) about what ten
-// more tiles would cost: fitted on GB300 to whole-kernel times of plans with
-// and without switches (a tile is 1.5-1.8 us, a switch 10-15 us).
-constexpr int64_t kSwitchTiles = 10;
+// Cost model of a CTA's range, in units of 1/32 of a 128-token tile, fitted on
+// GB300 to per-CTA end times (%globaltimer) of the MTP-5, mixed-batch and
+// head_dim-256 workloads:
+// - A CTA that moves from one (sequence, KV head) pair to the next pays for the
+//   switch (the outgoing pair's epilogue, the incoming pair's Q and first-tile
+//   maxima, mostly code that runs cold while HBM is saturated) about what ten
+//   more tiles would cost (8 to 10 measured), fifteen in the 64-row instances,
+//   whose epilogue and exact-maximum path are the heaviest.
+// - A tile costs the same whatever the pair's rows, except in the 64-row
+//   instances, which skip the P work of column chunks without rows: there a
+//   tile of r rows costs about 1 + r / 320 tiles (a 64-row tile 1.2).
+constexpr int64_t kCostUnit = 32;  // cost of one tile of a pair without rows
+inline int64_t switch_cost(int np) { return np == 64 ? 15 * kCostUnit : 10 * kCostUnit; }
+inline int64_t tile_cost(int np, int rows) { return np == 64 ? kCostUnit + rows / 10 : kCostUnit; }
 
-// Cuts the pairs' tiles (in flat order, pair sizes `nt`) into consecutive CTA
-// ranges whose cost, tiles plus kSwitchTiles for every pair after the first,
-// stays within `tau`; returns the CTA count and, with `starts`, each CTA's
-// first tile followed by the total.
-int64_t pack_ranges(const std::vector<int64_t>& nt, int64_t tau, std::vector<int32_t>* starts) {
+// Cuts the pairs' tiles (in flat order: pair sizes `nt`, tile costs `w`) into
+// consecutive CTA ranges whose cost, the tiles' costs plus `sw` for every pair
+// after the first, stays within `tau` (>= every tile cost); returns the CTA
+// count and, with `starts`, each CTA's first tile followed by the total.
+int64_t pack_ranges(const std::vector<int64_t>& nt, const std::vector<int64_t>& w, int64_t sw, int64_t tau,
+                    std::vector<int32_t>* starts) {
   int64_t ctas = 0, load = 0, pos = 0;
   bool open = false;
   if (starts) starts->clear();
-  for (const int64_t n : nt) {
-    int64_t rem = n;
+  for (size_t k = 0; k < nt.size(); ++k) {
+    int64_t rem = nt[k];
     while (rem > 0) {
       if (!open) {
         if (starts) starts->push_back(static_cast<int32_t>(pos));
         open = true;
         load = 0;
       }
-      const int64_t enter = load > 0 ? kSwitchTiles : 0;
+      const int64_t enter = load > 0 ? sw : 0;
       const int64_t room = tau - load - enter;
-      if (room <= 0) {  // no tile of this pair fits any more: the next CTA takes it
+      if (room < w[k]) {  // no tile of this pair fits any more: the next CTA takes it
         ++ctas;
         open = false;
         continue;
       }
-      const int64_t take = std::min(rem, room);
-      load += enter + take;
+      const int64_t take = std::min(rem, room / w[k]);
+      load += enter + take * w[k];
       rem -= take;
       pos += take;
-      if (load >= tau) {
-        ++ctas;
-        open = false;
-      }
     }
   }
   if (open) ++ctas;
@@ -310,9 +315,9 @@ int64_t pack_ranges(const std::vector<int64_t>& nt, int64_t tau, std::vector<int
 
 // Flat plan of the tcgen05 kernel: the (sequence, KV head) pairs laid end to
 // end as 128-token tiles, longest sequences first, cut into one wave of
-// consecutive CTA ranges. The cut minimises the largest CTA cost (tiles plus
-// kSwitchTiles per pair switch): binary search on the cost bound, greedy
-// filling at each bound. So long pairs are split evenly while short ones are
+// consecutive CTA ranges. The cut minimises the largest CTA cost (tile costs
+// plus a switch cost per pair switch, the model above): binary search on the
+// cost bound, greedy filling at each bound. So long pairs are split evenly while short ones are
 // packed whole, and a CTA crosses into the next pair only where that pays.
 // (`split_override` = n asks for ceil(longest pair / n) tiles per CTA instead,
 // and so do plans needing more CTAs than the range table holds.)
@@ -360,21 +365,30 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
   int64_t n_cta = (tiles + per - 1) / per;
   P->ranged = 0;
   if (d.split_override == 0 && tiles > 0) {
-    std::vector<int64_t> nt;
+    const int np = tc_rows_pad(rows_max);  // the kernel instance's N
+    const int64_t sw = switch_cost(np);
+    std::vector<int64_t> nt, w;
+    int64_t total = 0, w_max = 0;
     for (int k = 0; k < d.num_seqs; ++k)
-      for (int g = 0; g < Hkv; ++g) nt.push_back(P->seq[k].n_tiles);
-    int64_t lo = (tiles + sms - 1) / sms, hi = tiles;  // a bound of `tiles` always fits one CTA
+      for (int g = 0; g < Hkv; ++g) {
+        nt.push_back(P->seq[k].n_tiles);
+        w.push_back(tile_cost(np, P->seq[k].q_len * G));
+        total += nt.back() * w.back();
+        w_max = std::max(w_max, w.back());
+      }
+    // a bound of the whole cost always fits one CTA
+    int64_t lo = std::max((total + sms - 1) / sms, w_max), hi = total + sw * static_cast<int64_t>(nt.size());
     while (lo < hi) {
       const int64_t mid = (lo + hi) / 2;
-      if (pack_ranges(nt, mid, nullptr) <= sms) hi = mid; else lo = mid + 1;
+      if (pack_ranges(nt, w, sw, mid, nullptr) <= sms) hi = mid; else lo = mid + 1;
     }
     std::vector<int32_t> starts;
-    const int64_t n = pack_ranges(nt, lo, &starts);
+    const int64_t n = pack_ranges(nt, w, sw, lo, &starts);
     if (n <= kMaxCtaTable) {
       P->ranged = 1;
       n_cta = n;
       std::copy(starts.begin(), starts.end(), P->cta_start);
-      per = lo;  // the cost bound, reported as the chunk
+      per = (lo + kCostUnit - 1) / kCostUnit;  // the cost bound in tiles, reported as the chunk
     }
   }
   // CTA holding tile f

@@ -154,6 +154,8 @@ __host__ __device__ constexpr int split_smem_bytes(int kv_fp8, int d) {
   return kStages * stage_bytes(kv_fp8, d) + (kv_fp8 ? 16 * tile_tokens(kv_fp8, d) : 0) +
          4 * (kMaxChunk / kPage) + 64 + 1024;
 }
+// The tcgen05 kernel instance's N (q_len * group rows padded to 16, 32, 48 or 64).
+inline int tc_rows_pad(int rows_max) { return rows_max <= 16 ? 16 : rows_max <= 32 ? 32 : rows_max <= 48 ? 48 : 64; }
 // CTAs of the split kernel resident per SM (shared memory bound), used by the planner.
 __host__ __device__ constexpr int split_ctas_per_sm(int warps) { return warps <= 4 ? 2 : 1; }
 

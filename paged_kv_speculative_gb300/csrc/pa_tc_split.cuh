@@ -215,6 +215,16 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
   const bool is_prod = warp == 0 || warp == C::kVWarp, is_sm = warp >= 2 && warp < C::kVWarp;
   const int wg = is_sm ? (warp - 2) >> 2 : 0;   // softmax warpgroup
   const int col0 = wg * NH;                     // first column this group owns
+  // Column of the MMAs' N <-> row of the pair. In the 64-row instances (the ones that skip empty column
+  // chunks) the rows are dealt to the softmax warpgroups in chunks of 8, round robin (row chunk m sits in
+  // group m % NWG, as that group's chunk m / NWG), so a pair with fewer rows than N keeps every group about
+  // equally busy; each group still owns NH consecutive columns. Elsewhere column = row (the mapping cost
+  // the three-warpgroup instance registers).
+  auto row_of_col = [](int col) {
+    if constexpr (NP != 64) return col;
+    const int w = col / NH, c = col - w * NH;
+    return ((c >> 3) * C::NWG + w) * 8 + (c & 7);
+  };
   constexpr int kHalves = C::kHalves;
   const bool is_k = warp == 0;
   // producer lanes: page (within the tile) of this lane's copy: boxes on lanes [0, 8 * halves); on the K
@@ -229,13 +239,13 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
     return jl < npages(cq) ? __ldg(p.block_table + static_cast<size_t>(cq.b) * p.bt_stride + cq.t * (C::kTile / kPage) + jl)
                            : -1;
   };
-  // a softmax warp's Q rows of a segment: row r = col0 + (warp - 2) % 4 + 4 m, D / 32 bf16 per lane
+  // a softmax warp's Q rows of a segment: column col0 + (warp - 2) % 4 + 4 m, D / 32 bf16 per lane
   using QV = typename std::conditional<(D > 128), uint4, uint2>::type;
   auto q_load = [&](const TileCursor& cq, QV (&wq)[kRowsPerWarp]) {
     const int rows = cq.QL * G;
 #pragma unroll
     for (int m = 0; m < kRowsPerWarp; ++m) {
-      const int r = col0 + ((warp - 2) & 3) + 4 * m;
+      const int r = row_of_col(col0 + ((warp - 2) & 3) + 4 * m);
       wq[m] = QV{};
       if (r < rows) {
         const int i = r / G;
@@ -529,13 +539,14 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const int bar_sync = 1 + 2 * wg, bar_or = 2 + 2 * wg;
 
-    // ---- Q rows [col0, col0 + NH) of a segment into the Q buffer (one warp a row), their
+    // ---- Q rows of columns [col0, col0 + NH) of a segment into the Q buffer (one warp a row), their
     // constants into slot `sl`; then this warp's arrival on qready
     auto stage_q = [&](const TileCursor& cq, const QV (&wq)[kRowsPerWarp], int sl) {
       const int rows = cq.QL * G;
 #pragma unroll
       for (int m = 0; m < kRowsPerWarp; ++m) {
-        const int r = col0 + ((warp - 2) & 3) + 4 * m;
+        const int r = col0 + ((warp - 2) & 3) + 4 * m;  // column (the Q buffer's row)
+        const int pr = row_of_col(r);                   // row of the pair
         const QV w = wq[m];
         float cr = p.scale_log2;
         if constexpr (!KV_FP8) {
@@ -588,7 +599,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
         }
         if (lane == 0) {
           rowC[sl * 64 + r] = cr;
-          rowLim[sl * 64 + r] = r < rows ? cq.L - cq.QL + r / G : -1;
+          rowLim[sl * 64 + r] = pr < rows ? cq.L - cq.QL + pr / G : -1;
         }
       }
       fence_proxy_async();
@@ -642,7 +653,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
           TileCursor nx = cu;
           nx.t = cu.n_t - 1;
           nx.advance(wv, Hkv);
-          const int r = col0 + gt;
+          const int r = row_of_col(col0 + gt);
           if (r < nx.QL * G) {
             const int qi = r / G;
             const uint16_t* qp =
@@ -659,7 +670,9 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       // 8-column chunks past them is skipped. Their P columns keep stale values, which reach only output
       // columns that are never read, and their row sums stay zero. (Elsewhere the branch cost registers:
       // the 48-row FP8 instance spilled 116 bytes a thread with it, 64 without.)
-      const int act = min(NH, max(0, cu.QL * G - col0));  // chunk c0 is live iff c0 < act
+      // row chunks of the pair dealt to this group: chunk c0 of the group is live iff c0 < act
+      const int act = NP != 64 ? min(NH, max(0, cu.QL * G - col0))
+                               : min(NH, 8 * max(0, ((cu.QL * G + 7) / 8 - wg + C::NWG - 1) / C::NWG));
       float2 y[NH / 2];  // scores of the owned columns, in pairs (packed f32x2 arithmetic)
       {
         uint32_t r[NH];
@@ -985,8 +998,9 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
               if (2 * c + 1 == gt) mg = -negm[c % kRP].y;
             }
           }
-          if (ok_sm && !whole && cc < rows)
-            p.part_lse[u * p.rows_max + cc] = s2 > 0.f ? mg + __log2f(s2) : -INFINITY;
+          const int pr = row_of_col(cc);
+          if (ok_sm && !whole && pr < rows)
+            p.part_lse[u * p.rows_max + pr] = s2 > 0.f ? mg + __log2f(s2) : -INFINITY;
         }
         named_sync(bar_sync, 128);
         if (ok_sm) {
@@ -1000,10 +1014,11 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
             tc::wait_ld();
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const int r = col0 + c0 + j;
+              const int cj = col0 + c0 + j;
+              const int r = row_of_col(cj);  // a chunk's columns hold consecutive rows
               if (r >= rows) break;
               const float o = C::kStackP ? __uint_as_float(r8[j]) + __uint_as_float(q8[j]) : __uint_as_float(r8[j]);
-              const float val = o * rinv[r];
+              const float val = o * rinv[cj];
               if (!whole) {
                 p.part_o[(u * p.rows_max + r) * C::kD + d] = val;
               } else {
@@ -1047,6 +1062,5 @@ cudaError_t run_tc(int units, const CUtensorMap* tmk, const CUtensorMap* tmv, co
   return cudaGetLastError();
 }
 
-inline int tc_rows_pad(int rows_max) { return rows_max <= 16 ? 16 : rows_max <= 32 ? 32 : rows_max <= 48 ? 48 : 64; }
 
 }  // namespace pav

@@ -50,37 +50,42 @@ CASES = [([37, 100], [1, 6], 1), ([4096 + 7 * i for i in range(8)], [6] * 8, 4),
          ([1 << 20], [6], 1), ([5, 9000, 131072, 64], [3, 8, 1, 2], 2)]
 
 
-SWITCH_TILES = 10  # a pair switch costs about ten tiles (the planner's figure)
+# The planner's cost model, in 1/32 of a tile: a tile costs 32 (64-row instances: 32 + rows // 10, since
+# they skip the P work of empty column chunks), a pair switch 320 (64-row instances: 480).
+def costs(rows_max, rows):
+    np_ = 16 if rows_max <= 16 else 32 if rows_max <= 32 else 48 if rows_max <= 48 else 64
+    return (32 + rows // 10 if np_ == 64 else 32), (480 if np_ == 64 else 320)
 
 
-def pack(nt, tau):
-    """Greedy cut of the tiles into CTA ranges of cost (tiles + 10 per pair switch) <= tau."""
+def pack(nt, w, sw, tau):
+    """Greedy cut of the tiles into CTA ranges of cost (tile costs + sw per pair switch) <= tau."""
     starts, ctas, load, pos, open_ = [], 0, 0, 0, False
-    for n in nt:
+    for n, wk in zip(nt, w):
         rem = n
         while rem > 0:
             if not open_:
                 starts.append(pos)
                 open_, load = True, 0
-            enter = SWITCH_TILES if load > 0 else 0
+            enter = sw if load > 0 else 0
             room = tau - load - enter
-            if room <= 0:
+            if room < wk:
                 ctas, open_ = ctas + 1, False
                 continue
-            take = min(rem, room)
-            load, rem, pos = load + enter + take, rem - take, pos + take
-            if load >= tau:
-                ctas, open_ = ctas + 1, False
+            take = min(rem, room // wk)
+            load, rem, pos = load + enter + take * wk, rem - take, pos + take
     ctas += open_
     return ctas, starts + [pos]
 
 
-def flat_model(ctx, hkv, sms, split_override=0):
+def flat_model(ctx, ql, hkv, sms, split_override=0, group=8):
     """Independent model of a flat plan: pairs (longest sequence first, then KV
     head) end to end as 128-token tiles, cut into CTA ranges. Returns (CTA
-    starts, every pair's (first tile, tiles))."""
+    starts, every pair's (first tile, tiles), the cost bound)."""
     order = sorted(range(len(ctx)), key=lambda b: -ctx[b])  # stable: ties keep batch order
     nt = [(ctx[b] + 127) // 128 for b in order for _ in range(hkv)]
+    rows_max = max(ql) * group
+    w = [costs(rows_max, ql[b] * group)[0] for b in order for _ in range(hkv)]
+    sw = costs(rows_max, 0)[1]
     total = sum(nt)
     pairs, t = [], 0
     for n in nt:
@@ -88,15 +93,16 @@ def flat_model(ctx, hkv, sms, split_override=0):
         t += n
     if split_override:
         per = max(1, -(-max(nt) // split_override))
-        return [min(c * per, total) for c in range(-(-total // per) + 1)], pairs
-    lo, hi = -(-total // sms), total
+        return [min(c * per, total) for c in range(-(-total // per) + 1)], pairs, None
+    cost = sum(n * wk for n, wk in zip(nt, w))
+    lo, hi = max(-(-cost // sms), max(w)), cost + sw * len(nt)
     while lo < hi:
         mid = (lo + hi) // 2
-        if pack(nt, mid)[0] <= sms:
+        if pack(nt, w, sw, mid)[0] <= sms:
             hi = mid
         else:
             lo = mid + 1
-    return pack(nt, lo)[1], pairs
+    return pack(nt, w, sw, lo)[1], pairs, (lo, w, sw)
 
 
 def check_flat_plan(ctx, ql, hkv, split, sms=152):
@@ -104,7 +110,7 @@ def check_flat_plan(ctx, ql, hkv, split, sms=152):
     p = mk(ctx, ql, hq=8 * hkv, hkv=hkv, split_override=split, sms=sms)
     i = p.info
     assert i.flat == 1 and i.kernel == pv.KERNEL_TCGEN05 and i.tile_tokens == 128
-    starts, pairs = flat_model(ctx, hkv, sms, split)
+    starts, pairs, bound = flat_model(ctx, ql, hkv, sms, split)
     assert p.cta_starts() == starts
     assert i.total_tiles == hkv * sum((c + 127) // 128 for c in ctx) == starts[-1]
     assert i.num_units == len(starts) - 1
@@ -120,10 +126,14 @@ def check_flat_plan(ctx, ql, hkv, split, sms=152):
     assert len(slots) == len(set(slots)) and max(slots) < i.num_units + len(spans)
     if split == 0:
         assert i.num_units <= sms
-        # no CTA costs more than the bound the plan reports (tiles + 10 per pair switch)
+        # no CTA costs more than the bound, which the plan reports in whole tiles as the chunk
+        tau, w, sw = bound
+        assert i.chunk_tokens // 128 == -(-tau // 32)
         for c in range(i.num_units):
-            segs = sum(1 for a, b in spans if a <= c <= b)
-            assert starts[c + 1] - starts[c] + SWITCH_TILES * (segs - 1) <= i.chunk_tokens // 128
+            cost = sw * (sum(1 for a, b in spans if a <= c <= b) - 1)
+            for k, (t0, n) in enumerate(pairs):
+                cost += w[k] * max(0, min(t0 + n, starts[c + 1]) - max(t0, starts[c]))
+            assert cost <= tau
 
 
 @pytest.mark.parametrize("ctx,ql,hkv", CASES)
