@@ -17,7 +17,7 @@ LIBDIR = os.path.join(HERE, "_lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "libpa_verify.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["pa_capi.cpp", "pa_split_bf16.cu", "pa_split_fp8.cu", "pa_combine.cu", "pa_kv_write.cu", "pa_verdict.cu", "pa_tc_split.cu", "pa_tc_split_d256.cu", "pa_static.cu", "pa_dyn_plan.cu"]
+SOURCES = ["pa_capi.cpp", "pa_split_bf16.cu", "pa_split_fp8.cu", "pa_combine.cu", "pa_kv_write.cu", "pa_verdict.cu", "pa_tc_split.cu", "pa_tc_split_d256.cu", "pa_tc_split_d64.cu", "pa_static.cu", "pa_dyn_plan.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

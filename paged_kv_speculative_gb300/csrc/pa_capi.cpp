@@ -562,10 +562,10 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
     *workspace_bytes_out = P->ws_bytes;
     return PA_OK;
   }
-  const bool tc_ok = (d.head_dim == 128 || d.head_dim == 256) && rows_max <= 64;
+  const bool tc_ok = d.head_dim >= 64 && rows_max <= 64;  // head_dim 64 (bf16), 128, 256 (FP8)
   if (d.kernel == PA_KERNEL_TCGEN05 && !tc_ok) {
     delete P;
-    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs head_dim 128 (or 256 with FP8 KV) and q_len * group <= 64");
+    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs q_len * group <= 64");
   }
   const bool use_tc = d.kernel == PA_KERNEL_TCGEN05 || (d.kernel == PA_KERNEL_AUTO && tc_ok);
   if (d.head_dim == 256 && !use_tc) {
@@ -886,9 +886,9 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("SM count query failed: ") + cudaGetErrorString(e));
   }
-  const bool tc_ok = (d.head_dim == 128 || d.head_dim == 256) && rows_max <= 64;
+  const bool tc_ok = d.head_dim >= 64 && rows_max <= 64;  // head_dim 64 (bf16), 128, 256 (FP8)
   if (d.kernel == PA_KERNEL_TCGEN05 && !tc_ok)
-    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs head_dim 128 (or 256 with FP8 KV) and q_len * group <= 64");
+    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs q_len * group <= 64");
   const bool use_tc = d.kernel == PA_KERNEL_TCGEN05 || (d.kernel == PA_KERNEL_AUTO && tc_ok);
   if (d.head_dim == 256 && !use_tc)
     return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only (q_len * group <= 64)");

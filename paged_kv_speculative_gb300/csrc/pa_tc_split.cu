@@ -9,9 +9,13 @@ namespace pav {
 cudaError_t launch_tc_split_d256(int kv_fp8, int rows_max, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                  const SplitParams* p, cudaStream_t stream);
 
+cudaError_t launch_tc_split_d64(int kv_fp8, int rows_max, int units, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                const SplitParams* p, cudaStream_t stream);
+
 cudaError_t launch_tc_split(int head_dim, int kv_fp8, int rows_max, int units, const CUtensorMap* tmk,
                             const CUtensorMap* tmv, const SplitParams* p, cudaStream_t stream) {
   if (head_dim == 256) return launch_tc_split_d256(kv_fp8, rows_max, units, tmk, tmv, p, stream);
+  if (head_dim == 64) return launch_tc_split_d64(kv_fp8, rows_max, units, tmk, tmv, p, stream);
   if (head_dim != 128) return cudaErrorInvalidValue;
   const int np = tc_rows_pad(rows_max);
 #define PAV_TC(F, N) \

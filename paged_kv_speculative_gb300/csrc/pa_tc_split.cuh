@@ -59,7 +59,10 @@ struct TcCfg {
   static constexpr int kTile = kFlatTile;                    // tokens per K/V tile = MMA M
   static constexpr int kRowB = KV_FP8 ? D : 2 * D;           // bytes per token row
   static constexpr int kHalves = kRowB / 128;                // 128-byte planes of a tile (TMA boxes per page)
-  static constexpr int kMh = D / 128;                        // PV M halves (one O accumulator each)
+  // PV M halves (one O accumulator each). head_dim 64 (bf16) keeps one M = 128 accumulator: its second
+  // 64-row atom reads the 16 KB after the V slot (the next slot, or Q and P after the last one, always
+  // inside the allocation), which fills only output rows d >= 64, never read.
+  static constexpr int kMh = D >= 128 ? D / 128 : 1;
   // FP8 at head_dim 256: P's hi and lo planes form one B operand of N = 64 + NP (the lo plane is the operand's
   // second 64-column atom), so a PV k-step is one MMA; the accumulator then holds O_hi in columns [0, NP) and O_lo
   // from 64 on, and O = O_hi + O_lo. (One N = 112 MMA issues in about 61 clocks, two N = 48 ones in about 108.)
@@ -99,7 +102,10 @@ struct TcCfg {
   static_assert((NP / NWG) % 8 == 0 && NP % NWG == 0, "each softmax warpgroup owns a multiple of 8 columns");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(2 * KS + 2 * VS + 7 + 2 * PB + SS <= 62, "barriers fit their 512 bytes with the tmem slot and abort flag");
-  static_assert(D == 128 || (KV_FP8 && D == 256), "head_dim 128, or 256 with FP8 K/V");
+  static_assert(D == 128 || (KV_FP8 && D == 256) || (!KV_FP8 && D == 64),
+                "head_dim 128, 256 with FP8 K/V, or 64 with bf16 K/V");
+  static_assert(D != 64 || kOffQ - kOffV - VS * kVStage + kQB + PB * kPBuf >= 16384,
+                "head_dim 64: 16 KB of the allocation follow the last V slot");
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -240,7 +246,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
                            : -1;
   };
   // a softmax warp's Q rows of a segment: column col0 + (warp - 2) % 4 + 4 m, D / 32 bf16 per lane
-  using QV = typename std::conditional<(D > 128), uint4, uint2>::type;
+  using QV = typename std::conditional<(D > 128), uint4, typename std::conditional<(D == 128), uint2, uint32_t>::type>::type;
   auto q_load = [&](const TileCursor& cq, QV (&wq)[kRowsPerWarp]) {
     const int rows = cq.QL * G;
 #pragma unroll
@@ -452,7 +458,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
                            (pl > 0 || hf > 0 || ks > 0) ? 1u : 0u);
         } else {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
+          for (int ks = 0; ks < 4 * kHalves; ++ks)  // 16 head-dim entries a k-step, 4 per 128-byte plane
             tc::mma_f16(tS[sb], tc::desc_plus(dK, (ks >> 2) * (C::kTile * 128) + (ks & 3) * 32),
                         tc::desc_plus(dQ, (ks >> 2) * C::kQPlane + (ks & 3) * 32), idS, ks > 0 ? 1u : 0u);
         }
@@ -550,10 +556,11 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
         const QV w = wq[m];
         float cr = p.scale_log2;
         if constexpr (!KV_FP8) {
-          // 4 bf16 = 8 bytes at byte 8*lane of the 256-byte row: half lane/16, chunk (lane%16)/2
-          const int hf = lane >> 4, ch = (lane & 15) >> 1;
-          uint8_t* dst = sQ + hf * C::kQPlane + r * 128 + ((ch ^ (r & 7)) << 4) + (lane & 1) * 8;
-          *reinterpret_cast<uint2*>(dst) = w;
+          // D / 32 bf16 = D / 16 bytes at byte b = (D / 16) * lane of the row: plane b / 128, 16-byte chunk
+          // (b % 128) / 16 (head_dim 128: 8 bytes, half lane / 16; head_dim 64: 4 bytes, one plane)
+          const int b = (C::kD / 16) * lane, hf = b >> 7, ch = (b & 127) >> 4;
+          uint8_t* dst = sQ + hf * C::kQPlane + r * 128 + ((ch ^ (r & 7)) << 4) + (b & 15);
+          *reinterpret_cast<QV*>(dst) = w;
         } else {
           constexpr int kE = C::kD / 32;  // head-dim entries of this lane: [kE * lane, kE * lane + kE)
           const uint32_t* wv32 = reinterpret_cast<const uint32_t*>(&w);
@@ -1019,6 +1026,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
               if (r >= rows) break;
               const float o = C::kStackP ? __uint_as_float(r8[j]) + __uint_as_float(q8[j]) : __uint_as_float(r8[j]);
               const float val = o * rinv[cj];
+              if (C::kD < 128 && d >= C::kD) continue;  // head_dim 64: lanes past it hold unused rows of O
               if (!whole) {
                 p.part_o[(u * p.rows_max + r) * C::kD + d] = val;
               } else {

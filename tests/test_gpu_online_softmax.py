@@ -59,6 +59,8 @@ SHAPES = [
     ("bf16_r16", synth.KV_BF16, 128, 16, 2, [2, 1]),
     ("bf16_r48", synth.KV_BF16, 128, 16, 2, [6, 4]),
     ("bf16_r64", synth.KV_BF16, 128, 16, 2, [8, 7]),
+    ("bf16_d64_r48", synth.KV_BF16, 64, 16, 2, [6, 4]),
+    ("bf16_d64_r64", synth.KV_BF16, 64, 16, 2, [8, 5]),
     ("fp8_r32", synth.KV_FP8, 128, 16, 2, [4, 3]),
     ("fp8_r48", synth.KV_FP8, 128, 16, 2, [6, 4]),
     ("fp8_r64", synth.KV_FP8, 128, 16, 2, [8, 7]),

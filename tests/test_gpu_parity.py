@@ -27,7 +27,8 @@ def built():
 
 
 def tc_applies(prob):
-    d_ok = prob.head_dim == 128 or (prob.head_dim == 256 and prob.kv_dtype == synth.KV_FP8)
+    # head_dim 64 (bf16 K/V), 128, or 256 (FP8 K/V)
+    d_ok = prob.head_dim in (64, 128) or (prob.head_dim == 256 and prob.kv_dtype == synth.KV_FP8)
     return d_ok and int(prob.query_lens.max()) * prob.group <= 64
 
 
@@ -222,6 +223,21 @@ def test_full_workload_every_row(name, kernel):
     got, va = gpu_run(prob, dev=_workload_dev(name), kernel=kernel)
     assert va.info["kernel"] == kernel
     assert max_err(got, _workload_ref(name)) <= TOL[prob.kv_dtype], name
+
+
+def test_tiny_workload_runs_on_the_tcgen05_kernel():
+    prob = synth.make_config("tiny")
+    got, va = gpu_run(prob)
+    assert va.info["kernel"] == pv.KERNEL_TCGEN05
+    assert max_err(got, oracle.verify_attention(prob)) <= TOL[synth.KV_BF16]
+
+
+@pytest.mark.parametrize("split", [0, 1, 4, 17])
+def test_head_dim_64_flat_segments(split):
+    # every segment layout of the flat plans at head_dim 64, mixed row counts (8 .. 64) in the 64-row instance
+    prob = synth.make_problem(SEG_CTX, SEG_Q, 16, 2, 64, seed=39)
+    got, va = gpu_run(prob, split_override=split, kernel=pv.KERNEL_TCGEN05)
+    assert max_err(got, oracle.verify_attention(prob)) <= TOL[synth.KV_BF16]
 
 
 # --------------------------------------------------------------- plans beyond one wave
