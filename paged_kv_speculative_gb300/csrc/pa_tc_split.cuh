@@ -71,10 +71,7 @@ struct TcCfg {
   static constexpr bool kStackP = KV_FP8 != 0 && D == 256;
   static constexpr int kOCols = kStackP ? 128 : 64;          // tensor-memory columns of one O accumulator
   static constexpr int kTmemCols = 128 + kMh * kOCols <= 256 ? 256 : 512;  // S 2 x 64, then the O accumulators
-  static constexpr int kTileB = kTile * kRowB;               // 16 KB (fp8 D128, bf16 D64) / 32 KB (bf16 D128, fp8 D256)
-  // Tiles a producer issues together: a TMA issue costs its lane about the same whatever the box, so with
-  // 16 KB tiles a producer iteration takes two tiles (16 boxes on 16 lanes), as with 32 KB tiles it takes one.
-  static constexpr int kIssue = kTileB <= 16384 ? 2 : 1;
+  static constexpr int kTileB = kTile * kRowB;               // 16 KB (fp8 D128) / 32 KB (bf16 D128, fp8 D256)
   static constexpr int KS = kTileB > 16384 ? 2 : 5;          // K ring depth (a K slot frees once S is done)
   static constexpr int VS = kTileB > 16384 ? (KV_FP8 ? 2 : 3) : 5;  // V ring depth (a V slot frees only after PV)
   static constexpr int kVStage = kTileB;                     // V data
@@ -236,19 +233,9 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
   };
   constexpr int kHalves = C::kHalves;
   const bool is_k = warp == 0;
-  // Producer lanes: this lane's tile within an issue group (tt) and page within that tile (jl; 8: no copy).
-  // Boxes on lanes [0, 8 * halves * kIssue); on the K producer, the FP8 scale copies on lanes 16-31 (one
-  // tile: k scales on 16-23, v scales on 24-31; two tiles: lanes 16-23 the first, 24-31 the second, each lane
-  // both copies of its page).
-  constexpr int kIssue = C::kIssue;
-  int tt = 0, jl = 8;
-  if (lane < 8 * kHalves * kIssue) {
-    tt = lane / (8 * kHalves);
-    jl = (lane / kHalves) & 7;
-  } else if (KV_FP8 && warp == 0 && lane >= 16) {
-    tt = kIssue == 2 ? (lane >> 3) & 1 : 0;
-    jl = lane & 7;
-  }
+  // producer lanes: page (within the tile) of this lane's copy: boxes on lanes [0, 8 * halves); on the K
+  // producer, the FP8 scale copies on lanes 16-31 (k scales 16-23, v scales 24-31)
+  const int jl = lane < 8 * kHalves ? lane / kHalves : ((KV_FP8 && warp == 0 && lane >= 16) ? (lane & 7) : 8);
   constexpr int kSmArrive = 4 * C::NWG;         // softmax warps: arrivals on sfree, pfull and qready
   auto npages = [&](const TileCursor& cq) {
     return min(C::kTile / kPage, (cq.L - cq.t * C::kTile + kPage - 1) / kPage);
@@ -274,25 +261,24 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       }
     }
   };
-  TileCursor cu0;  // producers: this lane's first tile; softmax warps: the first segment
-  TileCursor cu1, cu2;  // producers: this lane's tiles of the next two issue groups (page ids read ahead)
+  TileCursor cu0;  // producers: the first tile; softmax warps: the first segment
+  TileCursor cu1, cu2;  // producers: the next two tiles (their page ids are read ahead)
   int pg0 = -1, pg1 = -1, pg2 = -1;
   QV wq0[kRowsPerWarp];
   if (is_prod || is_sm) cu0.seek(wv, f_lo);
-  // moves a producer lane's cursor to its tile of the next issue group, if the range has it
-  auto next_group = [&](TileCursor& c, int tile) {
-    for (int u = 0; u < kIssue; ++u)
-      if (tile + u + 1 < n_tiles) c.advance(wv, Hkv);
-  };
   if (is_prod) {
-    if (tt > 0 && tt < n_tiles) cu0.advance(wv, Hkv);
-    if (tt < n_tiles) pg0 = fetch(cu0);
+    pg0 = fetch(cu0);
     cu1 = cu0;
-    next_group(cu1, tt);
-    if (tt + kIssue < n_tiles) pg1 = fetch(cu1);
-    cu2 = cu1;
-    next_group(cu2, tt + kIssue);
-    if (tt + 2 * kIssue < n_tiles) pg2 = fetch(cu2);
+    cu2 = cu0;
+    if (n_tiles > 1) {
+      cu1.advance(wv, Hkv);
+      pg1 = fetch(cu1);
+      cu2 = cu1;
+    }
+    if (n_tiles > 2) {
+      cu2.advance(wv, Hkv);
+      pg2 = fetch(cu2);
+    }
   }
   if (is_sm) q_load(cu0, wq0);
 
@@ -350,71 +336,50 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
     const CUtensorMap* map = is_k ? &tmk : &tmv;
     uint64_t* full = is_k ? kfull : vfull;
     uint64_t* empty = is_k ? kempty : vempty;
-    // Page ids are read three issue groups ahead (cursors cu, c1, c2 for this lane's tiles of groups k, k+1,
-    // k+2, rotated by value): a group's issue is much shorter than a load from the block table, so reading
-    // only the next group's ids would hold the ring to about one group per memory latency.
+    // Page ids are read three tiles ahead (cursors cu, c1, c2 for tiles k, k+1, k+2, rotated by value):
+    // a tile's issue is much shorter than a load from the block table, so reading only the next tile's
+    // ids would hold the ring to about one tile per memory latency.
     TileCursor cu = cu0, c1 = cu1, c2 = cu2;
     int pg_raw = pg0, p1 = pg1, p2 = pg2;
     int issued = 0;
-    for (int k = 0; k < n_tiles; k += kIssue) {
-      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;  // one verdict for the whole warp
-      const int my = k + tt;             // this lane's tile
-      const bool mine = my < n_tiles;
+    for (int k = 0; k < n_tiles && !*abort_flag; ++k) {
       TileCursor c3 = c2;
       int p3 = -1;
-      if (my + 3 * kIssue < n_tiles) {
-        next_group(c3, my + 2 * kIssue);
+      if (k + 3 < n_tiles) {
+        c3.advance(wv, Hkv);
         p3 = fetch(c3);
       }
-      const int ng = min(kIssue, n_tiles - k);  // tiles in this group
-      {
-        // lane 0 waits for the group's slots; the verdict is the same for every lane (no lane is left at a
-        // warp sync)
-        bool ok = true;
-        if (lane == 0)
-          for (int u = 0; u < ng && ok; ++u)
-            if (k + u >= depth)
-              ok = mbar_wait_bounded(smem_addr(&empty[(k + u) % depth]),
-                                     static_cast<uint32_t>((k + u) / depth - 1) & 1u, p.wait_limit_ns);
+
+      const int s = k % depth;
+      if (k >= depth) {
+        // lane 0 waits; the verdict is the same for every lane (no lane is left at a warp sync)
+        bool ok = lane != 0 || mbar_wait_bounded(smem_addr(&empty[s]), static_cast<uint32_t>(k / depth - 1) & 1u, p.wait_limit_ns);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           if (lane == 0) fail();
           break;
         }
       }
-      const int s = my % depth;
       uint8_t* dst = is_k ? sK + s * C::kTileB : sV + s * C::kVStage;
       const uint32_t bar = smem_addr(&full[s]);
-      const int npg = mine ? npages(cu) : 0;
+      const int npg = npages(cu);
       // an id outside the pool is flagged and read past the tensor's end, where TMA fills zeros
       int pg = pg_raw;
       if (jl < npg && static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages)) {
         atomicOr(p.err, 1u);
         pg = -1;
       }
-      // the pages of each tile of the group (from the first box lane of that tile) and, FP8 K producer,
-      // the scale copies (k and v, 64 bytes each) of its pages inside the pool
-      int npg_t[kIssue];
-      uint32_t nsc_t[kIssue];
-#pragma unroll
-      for (int u = 0; u < kIssue; ++u) {
-        npg_t[u] = __shfl_sync(0xffffffffu, npg, u * 8 * kHalves);
-        const int lo = kIssue == 2 ? 16 + 8 * u : 16;  // the lanes holding tile u's scale pages
-        nsc_t[u] = (KV_FP8 && is_k) ? __popc(__ballot_sync(0xffffffffu, lane >= lo && lane < lo + 8 && pg >= 0)) : 0u;
-      }
-      const int sslot = my % (C::SS > 0 ? C::SS : 1);  // scale slot (FP8)
+      // FP8 (K producer): one k and one v scale copy per page inside the pool (lanes 16-23 hold the ids)
+      const uint32_t nsc =
+          (KV_FP8 && is_k) ? __popc(__ballot_sync(0xffffffffu, lane >= 16 && lane < 24 && pg >= 0)) : 0u;
+      const int sslot = k % (C::SS > 0 ? C::SS : 1);  // scale slot (FP8)
       const uint32_t scbar = KV_FP8 ? smem_addr(&scfull[sslot]) : 0u;
       if (lane == 0) {
-#pragma unroll
-        for (int u = 0; u < kIssue; ++u)
-          if (u < ng) {
-            mbar_arrive_expect_tx(smem_addr(&full[(k + u) % depth]), npg_t[u] * (kPage * C::kRowB));
-            if (KV_FP8 && is_k)
-              mbar_arrive_expect_tx(smem_addr(&scfull[(k + u) % (C::SS > 0 ? C::SS : 1)]), nsc_t[u] * (2 * kPage * 4));
-          }
+        mbar_arrive_expect_tx(bar, npg * (kPage * C::kRowB));
+        if (KV_FP8 && is_k) mbar_arrive_expect_tx(scbar, nsc * (2 * kPage * 4));
       }
       __syncwarp();
-      if (lane < 8 * kHalves * kIssue && jl < npg) {
+      if (lane < npg * kHalves) {
         const int hf = lane % kHalves;
         // an id outside the pool reads past the tensor's end: TMA fills zeros
         const int row = (pg >= 0 ? pg : p.num_pages) * Hkv * kPage + cu.g * kPage;
@@ -422,20 +387,14 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       }
       if (KV_FP8 && is_k && lane >= 16 && jl < npg && pg >= 0) {
         const size_t so = (static_cast<size_t>(pg) * Hkv + cu.g) * kPage;
-        uint8_t* sdst = sSc + sslot * C::kScB + jl * kPage * 4;
-        if (kIssue == 2) {  // both copies of this lane's page
-          bulk_load(smem_addr(sdst), p.k_scale + so, kPage * 4, scbar);
-          bulk_load(smem_addr(sdst + C::kTile * 4), p.v_scale + so, kPage * 4, scbar);
-        } else {
-          const bool ksc = lane < 24;
-          bulk_load(smem_addr(sdst + (ksc ? 0 : C::kTile * 4)), (ksc ? p.k_scale : p.v_scale) + so, kPage * 4, scbar);
-        }
+        const bool ksc = lane < 24;
+        bulk_load(smem_addr(sSc + sslot * C::kScB + (ksc ? 0 : C::kTile * 4) + jl * kPage * 4),
+                  (ksc ? p.k_scale : p.v_scale) + so, kPage * 4, scbar);
       }
       // (after the issue, off its path) the device lengths must be the planned ones
-      if (is_k && (lane % (8 * kHalves)) == 0 && lane < 8 * kHalves * kIssue && mine && cu.t == 0 && cu.g == 0 &&
-          (p.dev_ctx[cu.b] != cu.L || p.dev_q[cu.b] != cu.QL))
+      if (is_k && lane == 0 && cu.t == 0 && cu.g == 0 && (p.dev_ctx[cu.b] != cu.L || p.dev_q[cu.b] != cu.QL))
         atomicOr(p.err, 2u);
-      issued += ng;
+      ++issued;
       cu = c1;
       c1 = c2;
       c2 = c3;

@@ -16,9 +16,7 @@ unsound wait, for each instance's ring depths; the plain order
 S(j+2)-before-PV(j) gets stuck on some layouts (a segment of a single tile),
 which shows that the model tells them apart. The FP8 scale ring (KS + 2 slots,
 refilled by the K producer without a wait of its own) never overwrites a slot
-whose scales the softmax has not read; one slot fewer would. With 16 KB tiles
-a producer issues two tiles at a time (it first waits for both slots), which
-keeps every wait sound and the scale ring safe. With three P
+whose scales the softmax has not read; one slot fewer would. With three P
 buffers and a two-deep V ring, the V slot of a short tile can still be a phase
 behind when the softmax gets there, so its parity wait would be unsound; the
 kernel first waits for PV of the slot's previous tile (waiting for that tile's
@@ -28,13 +26,11 @@ import random
 
 import pytest
 
-# (K ring, V ring, P buffers, FP8, tiles a producer issues together) of the kernel's instances
-INSTANCES = {"bf16_d128": (2, 3, 2, False, 1), "fp8_d128": (5, 5, 2, True, 2), "fp8_d256": (2, 2, 3, True, 1),
-             "bf16_d64": (5, 5, 2, False, 2)}
+# (K ring, V ring, P buffers, FP8) of the kernel's instances
+INSTANCES = {"bf16_d128": (2, 3, 2, False), "fp8_d128": (5, 5, 2, True), "fp8_d256": (2, 2, 3, True)}
 
 
-def run(seg_first, short_tile, slow, ks, vs, pb, fp8, issue=1, kernel_order=True, scale_slack=2, short_wait="pv",
-        sched=None):
+def run(seg_first, short_tile, slow, ks, vs, pb, fp8, kernel_order=True, scale_slack=2, short_wait="pv", sched=None):
     """Returns (finished, unsound waits, scale-slot overwrites). Without `sched` each role runs as far as it
     can in turn (producers furthest ahead); with a random.Random, the roles take turns in random order and
     each moves a random number of steps, so producers may also lag."""
@@ -49,18 +45,14 @@ def run(seg_first, short_tile, slow, ks, vs, pb, fp8, issue=1, kernel_order=True
     unsound, overwritten = [], []
 
     def producer(kind, depth):
-        # `issue` tiles at a time: first every slot of the group is free, then all of its copies are issued
-        for k0 in range(0, n, issue):
-            group = range(k0, min(n, k0 + issue))
-            for k in group:
-                if k >= depth:  # the slot frees when S (K ring) or PV (V ring) of tile k - depth is done
-                    yield ("S" if kind == "K" else "PV", k - depth, depth)
-            for k in group:
-                if fp8 and kind == "K" and k >= ss and ("sread", k - ss) not in ev:
-                    overwritten.append(k)
-                ev.add((kind + "full", k))
-                if fp8 and kind == "K":
-                    ev.add(("SCfull", k))
+        for k in range(n):
+            if k >= depth:  # the slot frees when S (K ring) or PV (V ring) of tile k - depth is done
+                yield ("S" if kind == "K" else "PV", k - depth, depth)
+            if fp8 and kind == "K" and k >= ss and ("sread", k - ss) not in ev:
+                overwritten.append(k)
+            ev.add((kind + "full", k))
+            if fp8 and kind == "K":
+                ev.add(("SCfull", k))
 
     def issuer():
         def S(i):
@@ -153,26 +145,26 @@ def layouts(count, seed):
 
 @pytest.mark.parametrize("inst", list(INSTANCES))
 def test_kernel_order_never_sticks_and_waits_soundly(inst):
-    ks, vs, pb, fp8, issue = INSTANCES[inst]
+    ks, vs, pb, fp8 = INSTANCES[inst]
     for lay in layouts(4000, 1):
-        done, unsound, over = run(*lay, ks, vs, pb, fp8, issue)
+        done, unsound, over = run(*lay, ks, vs, pb, fp8)
         assert done and not unsound and not over, (lay, unsound, over)
 
 
 @pytest.mark.parametrize("inst", list(INSTANCES))
 def test_random_schedules_wait_soundly(inst):
-    ks, vs, pb, fp8, issue = INSTANCES[inst]
+    ks, vs, pb, fp8 = INSTANCES[inst]
     sched = random.Random(7)
     for lay in layouts(1500, 4):
         for _ in range(3):
-            done, unsound, over = run(*lay, ks, vs, pb, fp8, issue, sched=sched)
+            done, unsound, over = run(*lay, ks, vs, pb, fp8, sched=sched)
             assert done and not unsound and not over, (lay, unsound, over)
 
 
 @pytest.mark.parametrize("inst", list(INSTANCES))
 def test_plain_order_sticks_on_one_tile_segments(inst):
-    ks, vs, pb, fp8, issue = INSTANCES[inst]
-    stuck = [lay for lay in layouts(4000, 1) if not run(*lay, ks, vs, pb, fp8, issue, kernel_order=False)[0]]
+    ks, vs, pb, fp8 = INSTANCES[inst]
+    stuck = [lay for lay in layouts(4000, 1) if not run(*lay, ks, vs, pb, fp8, kernel_order=False)[0]]
     assert stuck
     # every stuck layout has a one-tile segment followed by another segment
     for seg_first, _, _ in stuck:
@@ -182,22 +174,22 @@ def test_plain_order_sticks_on_one_tile_segments(inst):
 
 @pytest.mark.parametrize("inst", list(INSTANCES))
 def test_single_tile_segments_back_to_back(inst):
-    ks, vs, pb, fp8, issue = INSTANCES[inst]
+    ks, vs, pb, fp8 = INSTANCES[inst]
     n = 9
-    assert run([True] * n, [True] * n, [True] * n, ks, vs, pb, fp8, issue)[0]
-    assert not run([True] * n, [True] * n, [True] * n, ks, vs, pb, fp8, issue, kernel_order=False)[0]
+    assert run([True] * n, [True] * n, [True] * n, ks, vs, pb, fp8)[0]
+    assert not run([True] * n, [True] * n, [True] * n, ks, vs, pb, fp8, kernel_order=False)[0]
 
 
 def test_a_shallower_scale_ring_would_be_overwritten():
     for inst in ("fp8_d128", "fp8_d256"):
-        ks, vs, pb, fp8, issue = INSTANCES[inst]
-        assert any(run(*lay, ks, vs, pb, fp8, issue, scale_slack=1)[2] for lay in layouts(500, 2)), inst
+        ks, vs, pb, fp8 = INSTANCES[inst]
+        assert any(run(*lay, ks, vs, pb, fp8, scale_slack=1)[2] for lay in layouts(500, 2)), inst
 
 
 @pytest.mark.parametrize("other", ["none", "prev_v"])
 def test_short_tile_waits_for_pv_of_the_slots_previous_tile(other):
-    ks, vs, pb, fp8, issue = INSTANCES["fp8_d256"]
-    bad = [lay for lay in layouts(2000, 3) if run(*lay, ks, vs, pb, fp8, issue, short_wait=other)[1]]
+    ks, vs, pb, fp8 = INSTANCES["fp8_d256"]
+    bad = [lay for lay in layouts(2000, 3) if run(*lay, ks, vs, pb, fp8, short_wait=other)[1]]
     assert bad  # a single parity wait meets the slot a phase behind; a wait on the previous phase, a phase ahead
     for lay in bad:
-        assert run(*lay, ks, vs, pb, fp8, issue)[0:2] == (True, [])
+        assert run(*lay, ks, vs, pb, fp8)[0:2] == (True, [])
