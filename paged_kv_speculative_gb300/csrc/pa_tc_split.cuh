@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
     TileCursor cu = cu0, c1 = cu1, c2 = cu2;
     int pg_raw = pg0, p1 = pg1, p2 = pg2;
     int issued = 0;
-    for (int k = 0; k < n_tiles && !*abort_flag; ++k) {
+    for (int k = 0; k < n_tiles; ++k) {
       TileCursor c3 = c2;
       int p3 = -1;
       if (k + 3 < n_tiles) {
@@ -352,11 +352,16 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
 
       const int s = k % depth;
       if (k >= depth) {
-        // lane 0 waits; the verdict is the same for every lane (no lane is left at a warp sync)
-        bool ok = lane != 0 || mbar_wait_bounded(smem_addr(&empty[s]), static_cast<uint32_t>(k / depth - 1) & 1u, p.wait_limit_ns);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          if (lane == 0) fail();
+        // lane 0 checks the abort flag (another role failed) and waits for the slot; one verdict for the
+        // whole warp, so no lane is left at a warp sync: 0 go on, 1 stop, 2 the wait ran out
+        int st = 0;
+        if (lane == 0)
+          st = *abort_flag ? 1
+                           : (mbar_wait_bounded(smem_addr(&empty[s]), static_cast<uint32_t>(k / depth - 1) & 1u,
+                                                p.wait_limit_ns) ? 0 : 2);
+        st = __shfl_sync(0xffffffffu, st, 0);
+        if (st != 0) {
+          if (st == 2 && lane == 0) fail();
           break;
         }
       }

@@ -27,7 +27,8 @@ import random
 import pytest
 
 # (K ring, V ring, P buffers, FP8) of the kernel's instances
-INSTANCES = {"bf16_d128": (2, 3, 2, False), "fp8_d128": (5, 5, 2, True), "fp8_d256": (2, 2, 3, True)}
+INSTANCES = {"bf16_d128": (2, 3, 2, False), "fp8_d128": (5, 5, 2, True), "fp8_d256": (2, 2, 3, True),
+             "bf16_d64": (5, 5, 2, False)}
 
 
 def run(seg_first, short_tile, slow, ks, vs, pb, fp8, kernel_order=True, scale_slack=2, short_wait="pv", sched=None):
