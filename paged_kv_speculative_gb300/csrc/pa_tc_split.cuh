@@ -350,15 +350,17 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
         p3 = fetch(c3);
       }
 
-      const int s = k % depth;
+      // ring slot and phase of tile k, by the ring's compile-time depth (a division by a run-time depth
+      // would put an integer-division sequence on the producer's path every tile)
+      const int s = is_k ? k % C::KS : k % C::VS;
+      const uint32_t ph = static_cast<uint32_t>(is_k ? k / C::KS : k / C::VS) & 1u;
       if (k >= depth) {
         // lane 0 checks the abort flag (another role failed) and waits for the slot; one verdict for the
         // whole warp, so no lane is left at a warp sync: 0 go on, 1 stop, 2 the wait ran out
         int st = 0;
         if (lane == 0)
           st = *abort_flag ? 1
-                           : (mbar_wait_bounded(smem_addr(&empty[s]), static_cast<uint32_t>(k / depth - 1) & 1u,
-                                                p.wait_limit_ns) ? 0 : 2);
+                           : (mbar_wait_bounded(smem_addr(&empty[s]), ph ^ 1u, p.wait_limit_ns) ? 0 : 2);
         st = __shfl_sync(0xffffffffu, st, 0);
         if (st != 0) {
           if (st == 2 && lane == 0) fail();
