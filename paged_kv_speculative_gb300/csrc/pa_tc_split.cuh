@@ -233,9 +233,8 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
   };
   constexpr int kHalves = C::kHalves;
   const bool is_k = warp == 0;
-  // producer lanes: page (within the tile) of this lane's copy: boxes on lanes [0, 8 * halves); on the K
-  // producer, the FP8 scale copies on lanes 16-31 (k scales 16-23, v scales 24-31)
-  const int jl = lane < 8 * kHalves ? lane / kHalves : ((KV_FP8 && warp == 0 && lane >= 16) ? (lane & 7) : 8);
+  // producer lanes: page (within the tile) of this lane's box, on lanes [0, 8 * halves) (8: none)
+  const int jl = lane < 8 * kHalves ? lane / kHalves : 8;
   constexpr int kSmArrive = 4 * C::NWG;         // softmax warps: arrivals on sfree, pfull and qready
   auto npages = [&](const TileCursor& cq) {
     return min(C::kTile / kPage, (cq.L - cq.t * C::kTile + kPage - 1) / kPage);
@@ -294,7 +293,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       mbar_init(smem_addr(&pfree[s]), 1);
     }
     mbar_init(smem_addr(qready), kSmArrive);  // one phase per segment: each softmax warp staged its rows
-    for (int s = 0; s < C::SS; ++s) mbar_init(smem_addr(&scfull[s]), 1);
+    for (int s = 0; s < C::SS; ++s) mbar_init(smem_addr(&scfull[s]), 32);  // the K producer's 32 lanes (cp.async)
     mbar_init(smem_addr(stall_bar), 1);
     mbar_init(smem_addr(drain_bar), 1);
     *abort_flag = 0;
@@ -377,14 +376,8 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
         pg = -1;
       }
       // FP8 (K producer): one k and one v scale copy per page inside the pool (lanes 16-23 hold the ids)
-      const uint32_t nsc =
-          (KV_FP8 && is_k) ? __popc(__ballot_sync(0xffffffffu, lane >= 16 && lane < 24 && pg >= 0)) : 0u;
       const int sslot = k % (C::SS > 0 ? C::SS : 1);  // scale slot (FP8)
-      const uint32_t scbar = KV_FP8 ? smem_addr(&scfull[sslot]) : 0u;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar, npg * (kPage * C::kRowB));
-        if (KV_FP8 && is_k) mbar_arrive_expect_tx(scbar, nsc * (2 * kPage * 4));
-      }
+      if (lane == 0) mbar_arrive_expect_tx(bar, npg * (kPage * C::kRowB));
       __syncwarp();
       if (lane < npg * kHalves) {
         const int hf = lane % kHalves;
@@ -392,11 +385,24 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
         const int row = (pg >= 0 ? pg : p.num_pages) * Hkv * kPage + cu.g * kPage;
         tma_load_2d(smem_addr(dst + hf * (C::kTile * 128) + jl * kPage * 128), map, bar, hf * (KV_FP8 ? 128 : 64), row);
       }
-      if (KV_FP8 && is_k && lane >= 16 && jl < npg && pg >= 0) {
-        const size_t so = (static_cast<size_t>(pg) * Hkv + cu.g) * kPage;
-        const bool ksc = lane < 24;
-        bulk_load(smem_addr(sSc + sslot * C::kScB + (ksc ? 0 : C::kTile * 4) + jl * kPage * 4),
-                  (ksc ? p.k_scale : p.v_scale) + so, kPage * 4, scbar);
+      if constexpr (KV_FP8) {
+        if (is_k) {
+          // The tile's per-token scales (64 bytes of k and 64 of v a page) by 16-byte cp.async through the
+          // load/store path, two a lane: lane l takes page l / 4, k (l / 2 even) or v, bytes 32 (l % 2) ..
+          // +31. (As TMA copies they doubled the TMA requests of a tile.) Every lane then arrives on the
+          // slot's barrier once its copies have landed.
+          const int sp = lane >> 2;
+          const int spg = __shfl_sync(0xffffffffu, pg, sp * kHalves);  // page id (after the pool check)
+          if (sp < npg && spg >= 0) {
+            const bool vsc = (lane >> 1) & 1;
+            const int part = (lane & 1) * 8;  // floats
+            const float* src = (vsc ? p.v_scale : p.k_scale) + (static_cast<size_t>(spg) * Hkv + cu.g) * kPage + part;
+            const uint32_t dst = smem_addr(sSc + sslot * C::kScB + (vsc ? C::kTile * 4 : 0) + sp * kPage * 4 + part * 4);
+            cp_async_16(dst, src);
+            cp_async_16(dst + 16, src + 4);
+          }
+          cp_async_mbar_arrive(smem_addr(&scfull[sslot]));
+        }
       }
       // (after the issue, off its path) the device lengths must be the planned ones
       if (is_k && lane == 0 && cu.t == 0 && cu.g == 0 && (p.dev_ctx[cu.b] != cu.L || p.dev_q[cu.b] != cu.QL))
