@@ -48,6 +48,8 @@ WORKLOAD_DESC = {
 for _bs in (1, 2, 4, 8):
     WORKLOAD_DESC[f"d256_fp8_bs{_bs}"] = (f"head_dim 256 FP8 E4M3 KV + per-token fp32 scales: B={_bs} q=6 Hq=8 Hkv=1 "
                                           "(48 rows), ctx 150000 each, scattered pages (seed 6)")
+WORKLOAD_DESC["d256_bf16_bs8"] = ("head_dim 256 bf16 KV: B=8 q=6 Hq=8 Hkv=1 (48 rows), ctx 150000 each, scattered pages "
+                                  "(seed 6)")
 
 
 _C_TOKENS = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/', re.S)

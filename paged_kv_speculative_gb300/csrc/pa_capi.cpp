@@ -518,8 +518,8 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
   if (d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_FP8_E4M3) return fail(PA_ERR_INVALID, "unknown kv_dtype");
   if (d.out_dtype != PA_OUT_BF16 && d.out_dtype != PA_OUT_F32) return fail(PA_ERR_INVALID, "unknown out_dtype");
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
-  if (fp8 ? (d.head_dim != 128 && d.head_dim != 256) : (d.head_dim != 64 && d.head_dim != 128))
-    return fail(PA_ERR_UNSUPPORTED, fp8 ? "FP8 KV needs head_dim 128 or 256" : "bf16 KV needs head_dim 64 or 128");
+  if (fp8 ? (d.head_dim != 128 && d.head_dim != 256) : (d.head_dim != 64 && d.head_dim != 128 && d.head_dim != 256))
+    return fail(PA_ERR_UNSUPPORTED, fp8 ? "FP8 KV needs head_dim 128 or 256" : "bf16 KV needs head_dim 64, 128 or 256");
   if (d.num_seqs > 0 && (d.num_pages < 1 || d.block_table_stride < 1))
     return fail(PA_ERR_INVALID, "num_pages and block_table_stride must be >= 1");
   if (static_cast<int64_t>(d.num_pages) * d.num_kv_heads * kPage >= (int64_t(1) << 31))
@@ -864,8 +864,8 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
   if (d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_FP8_E4M3) return fail(PA_ERR_INVALID, "unknown kv_dtype");
   if (d.out_dtype != PA_OUT_BF16 && d.out_dtype != PA_OUT_F32) return fail(PA_ERR_INVALID, "unknown out_dtype");
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
-  if (fp8 ? (d.head_dim != 128 && d.head_dim != 256) : (d.head_dim != 64 && d.head_dim != 128))
-    return fail(PA_ERR_UNSUPPORTED, fp8 ? "FP8 KV needs head_dim 128 or 256" : "bf16 KV needs head_dim 64 or 128");
+  if (fp8 ? (d.head_dim != 128 && d.head_dim != 256) : (d.head_dim != 64 && d.head_dim != 128 && d.head_dim != 256))
+    return fail(PA_ERR_UNSUPPORTED, fp8 ? "FP8 KV needs head_dim 128 or 256" : "bf16 KV needs head_dim 64, 128 or 256");
   if (d.num_pages < 1 || d.block_table_stride < 1) return fail(PA_ERR_INVALID, "num_pages and block_table_stride must be >= 1");
   if (static_cast<int64_t>(d.num_pages) * d.num_kv_heads * kPage >= (int64_t(1) << 31))
     return fail(PA_ERR_UNSUPPORTED, "num_pages * num_kv_heads * 16 must stay below 2^31");

@@ -72,8 +72,10 @@ struct TcCfg {
   static constexpr int kOCols = kStackP ? 128 : 64;          // tensor-memory columns of one O accumulator
   static constexpr int kTmemCols = 128 + kMh * kOCols <= 256 ? 256 : 512;  // S 2 x 64, then the O accumulators
   static constexpr int kTileB = kTile * kRowB;               // 16 KB (fp8 D128) / 32 KB (bf16 D128, fp8 D256)
-  static constexpr int KS = kTileB > 16384 ? 2 : 5;          // K ring depth (a K slot frees once S is done)
-  static constexpr int VS = kTileB > 16384 ? (KV_FP8 ? 2 : 3) : 5;  // V ring depth (a V slot frees only after PV)
+  // K ring depth (a K slot frees once S is done) and V ring depth (a V slot frees only after PV); bf16 at
+  // head_dim 256 (64 KB tiles) has room for one stage of each next to Q (32 KB) and P
+  static constexpr int KS = kTileB > 32768 ? 1 : kTileB > 16384 ? 2 : 5;
+  static constexpr int VS = kTileB > 32768 ? 1 : kTileB > 16384 ? (KV_FP8 ? 2 : 3) : 5;
   static constexpr int kVStage = kTileB;                     // V data
   static constexpr int SS = KV_FP8 ? KS + 2 : 0;             // FP8 scale ring depth (see the K producer)
   static constexpr int kScB = 2 * 4 * kTile;                 // one slot: k then v scales of a tile's tokens
@@ -102,8 +104,7 @@ struct TcCfg {
   static_assert((NP / NWG) % 8 == 0 && NP % NWG == 0, "each softmax warpgroup owns a multiple of 8 columns");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(2 * KS + 2 * VS + 7 + 2 * PB + SS <= 62, "barriers fit their 512 bytes with the tmem slot and abort flag");
-  static_assert(D == 128 || (KV_FP8 && D == 256) || (!KV_FP8 && D == 64),
-                "head_dim 128, 256 with FP8 K/V, or 64 with bf16 K/V");
+  static_assert(D == 128 || D == 256 || (!KV_FP8 && D == 64), "head_dim 128 or 256, or 64 with bf16 K/V");
   static_assert(D != 64 || kOffQ - kOffV - VS * kVStage + kQB + PB * kPBuf >= 16384,
                 "head_dim 64: 16 KB of the allocation follow the last V slot");
 };
@@ -521,10 +522,12 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
           const uint64_t dV = tc::sdesc(v0, C::kTile * 128, 1024, tc::kSwizzle128B);
           const uint64_t dP = tc::sdesc(p0, 16384, 1024, tc::kSwizzle128B);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            if (ks < nks)
-              tc::mma_f16(tO, tc::desc_plus(dV, ks * 2048), tc::desc_plus(dP, ks * 2048), idPV,
-                          (!first || ks > 0) ? 1u : 0u);
+          for (int h = 0; h < C::kMh; ++h)  // head-dim entries [128 h, 128 h + 128): V planes 2h, 2h + 1
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              if (ks < nks)
+                tc::mma_f16(tO + C::kOCols * h, tc::desc_plus(dV, 2 * h * (C::kTile * 128) + ks * 2048),
+                            tc::desc_plus(dP, ks * 2048), idPV, (!first || ks > 0) ? 1u : 0u);
         }
         tc::commit(&vempty[vs]);
         tc::commit(&pfree[pb]);  // also tells the softmax warpgroups that O holds the segment's tiles up to j

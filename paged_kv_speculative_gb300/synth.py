@@ -274,7 +274,7 @@ CONFIG_NAMES = ("tiny", "mtp5_bf16", "mtp5_fp8", "mixed_fp8", "ctx1mi_bf16")
 # The head_dim-256 FP8 shape of the aiter follow-up on the MTP-5 routing page:
 # GQA 8 x query length 6 = 48 rows over one KV head, context 150,000 tokens,
 # batch 1, 2, 4 or 8.
-EXTRA_NAMES = ("d256_fp8_bs1", "d256_fp8_bs2", "d256_fp8_bs4", "d256_fp8_bs8")
+EXTRA_NAMES = ("d256_fp8_bs1", "d256_fp8_bs2", "d256_fp8_bs4", "d256_fp8_bs8", "d256_bf16_bs8")
 ALL_NAMES = CONFIG_NAMES + EXTRA_NAMES
 
 
@@ -299,7 +299,7 @@ def config_lengths(name: str):
         return [1 << 20], [6], 8, 1, 128, KV_BF16, 5
     if name in EXTRA_NAMES:
         bs = int(name.rsplit("bs", 1)[1])
-        return [150000] * bs, [6] * bs, 8, 1, 256, KV_FP8, 6
+        return [150000] * bs, [6] * bs, 8, 1, 256, (KV_BF16 if "bf16" in name else KV_FP8), 6
     raise KeyError(name)
 
 

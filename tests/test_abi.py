@@ -216,7 +216,9 @@ def test_empty_batch_plans():
     (dict(ctx=[100], ql=[2], hq=6, hkv=4), pv.ERR_INVALID),
     (dict(ctx=[100], ql=[2], stride=3), pv.ERR_INVALID),
     (dict(ctx=[10] * 1025, ql=[1] * 1025), pv.ERR_UNSUPPORTED),
-    (dict(ctx=[100], ql=[6], d=256), pv.ERR_UNSUPPORTED),  # head_dim 256 is an FP8 shape only
+    (dict(ctx=[100], ql=[6], d=256, kernel=pv.KERNEL_WARP_MMA), pv.ERR_UNSUPPORTED),  # 256: tcgen05 only
+    (dict(ctx=[100], ql=[8], hq=16, hkv=1, d=256), pv.ERR_UNSUPPORTED),  # bf16 256 with 128 rows
+    (dict(ctx=[100], ql=[6], d=32), pv.ERR_UNSUPPORTED),
     (dict(ctx=[100], ql=[8], hq=16, hkv=1, d=256, kv=pv.KV_FP8_E4M3), pv.ERR_UNSUPPORTED),  # 128 rows
     (dict(ctx=[100], ql=[6], d=256, kv=pv.KV_FP8_E4M3, kernel=pv.KERNEL_WARP_MMA), pv.ERR_UNSUPPORTED),
 ])
@@ -301,3 +303,9 @@ def test_batches_above_64_sequences_build_their_table_on_the_device():
     assert e.value.status == pv.ERR_UNSUPPORTED
     small = mk([100] * 64, [6] * 64)
     assert small.info.device_table == 0
+
+
+def test_bf16_head_dim_256_plans_on_tensor_cores():
+    p = mk([150000, 40000], [6, 6], hq=8, hkv=1, d=256)
+    assert p.info.kernel == pv.KERNEL_TCGEN05 and p.info.rows_max == 48
+    assert p.info.kv_bytes == 190000 * 1024

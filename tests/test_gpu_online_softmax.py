@@ -67,6 +67,8 @@ SHAPES = [
     ("fp8_d256_r16", synth.KV_FP8, 256, 8, 1, [2, 1]),
     ("fp8_d256_r48", synth.KV_FP8, 256, 8, 1, [6, 5]),
     ("fp8_d256_r64", synth.KV_FP8, 256, 16, 2, [8, 7]),
+    ("bf16_d256_r48", synth.KV_BF16, 256, 8, 1, [6, 5]),
+    ("bf16_d256_r64", synth.KV_BF16, 256, 16, 2, [8, 7]),
 ]
 
 

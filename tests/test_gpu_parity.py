@@ -27,9 +27,7 @@ def built():
 
 
 def tc_applies(prob):
-    # head_dim 64 (bf16 K/V), 128, or 256 (FP8 K/V)
-    d_ok = prob.head_dim in (64, 128) or (prob.head_dim == 256 and prob.kv_dtype == synth.KV_FP8)
-    return d_ok and int(prob.query_lens.max()) * prob.group <= 64
+    return int(prob.query_lens.max()) * prob.group <= 64  # every head_dim
 
 
 def mma_applies(prob):
@@ -73,6 +71,8 @@ SMALL = [
     ("fp8_d256_multi_tile", lambda: synth.make_problem([1500, 257, 4099, 128], [6, 1, 7, 3], 16, 2, 256,
                                                        kv_dtype=synth.KV_FP8, seed=37)),
     ("fp8_d256_rows16", lambda: synth.make_problem([700, 129], [2, 1], 8, 1, 256, kv_dtype=synth.KV_FP8, seed=38)),
+    ("bf16_d256_small", lambda: synth.make_problem([45, 29, 300, 6], [6, 2, 8, 6], 8, 1, 256, seed=14)),
+    ("bf16_d256_multi_tile", lambda: synth.make_problem([1500, 257, 4099, 128], [6, 1, 7, 3], 16, 2, 256, seed=15)),
 ]
 
 
@@ -98,8 +98,8 @@ SEG_Q = [1, 6, 8, 2, 3, 6, 7, 1, 4, 6, 5, 8]
 
 
 @pytest.mark.parametrize("split", [17, 9, 6, 4, 0])
-@pytest.mark.parametrize("kv,d", [(synth.KV_BF16, 128), (synth.KV_FP8, 128), (synth.KV_FP8, 256)],
-                         ids=["bf16", "fp8", "fp8_d256"])
+@pytest.mark.parametrize("kv,d", [(synth.KV_BF16, 128), (synth.KV_FP8, 128), (synth.KV_FP8, 256),
+                                  (synth.KV_BF16, 256)], ids=["bf16", "fp8", "fp8_d256", "bf16_d256"])
 def test_flat_segments_against_oracle(kv, d, split):
     prob = synth.make_problem(SEG_CTX, SEG_Q, 16, 2, d, kv_dtype=kv, seed=36)
     ref = oracle.verify_attention(prob)
