@@ -61,7 +61,8 @@ def test_workload_shapes(name):
     if name == "ctx1mi_bf16":
         assert ctx == [1 << 20] and (ctx[0] + 15) // 16 == 65536
     if name in synth.EXTRA_NAMES:
-        assert set(ctx) == {150000} and set(ql) == {6} and (hq, hkv, d, kvd) == (8, 1, 256, synth.KV_FP8)
+        kv = synth.KV_BF16 if "bf16" in name else synth.KV_FP8
+        assert set(ctx) == {150000} and set(ql) == {6} and (hq, hkv, d, kvd) == (8, 1, 256, kv)
         assert len(ctx) == int(name[-1]) and ql[0] * hq // hkv == 48
 
 
