@@ -91,10 +91,11 @@ def test_small_against_oracle(name, make, split, kernel):
     assert max_err(got, ref) <= TOL[prob.kv_dtype], name
 
 
-# Flat plans: tiles per CTA of 1, 2, 3 and 5 (split_override = ceil(17 / per)) put segment
-# boundaries everywhere, one-tile segments and CTAs spanning several sequences included.
-SEG_CTX = [1, 17, 128, 129, 255, 300, 640, 1000, 5, 2049, 16, 383]
-SEG_Q = [1, 6, 8, 2, 3, 6, 7, 1, 4, 6, 5, 8]
+# Flat plans: a few tiles per CTA (split_override = ceil(longest pair's tiles / per)) put segment
+# boundaries everywhere, one-tile segments and CTAs spanning several sequences included. The lengths
+# end on, just after and just before 128-token tile edges.
+SEG_CTX = [1, 17, 128, 129, 255, 300, 640, 1000, 5, 2049, 16, 383, 256, 513]
+SEG_Q = [1, 6, 8, 2, 3, 6, 7, 1, 4, 6, 5, 8, 2, 7]
 
 
 @pytest.mark.parametrize("split", [17, 9, 6, 4, 0])
