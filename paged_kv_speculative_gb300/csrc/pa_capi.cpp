@@ -263,19 +263,32 @@ void list_split_pairs(pa_verify_plan_s* P, int hkv, int G, const std::vector<int
   P->split_rows = fits ? rows : 0;
 }
 
-// Cost model of a CTA's range, in units of 1/32 of a 128-token tile, fitted on
-// GB300 to per-CTA end times (%globaltimer) of the MTP-5, mixed-batch and
-// head_dim-256 workloads:
+// Cost model of a CTA's range, in units of 1/32 of one of the instance's K/V
+// tiles, fitted on GB300 to per-CTA run times (%globaltimer at entry and exit)
+// of batches whose CTAs hold one to six segments, then checked by timing the
+// split kernel under neighbouring tables:
 // - A CTA that moves from one (sequence, KV head) pair to the next pays for the
-//   switch (the outgoing pair's epilogue, the incoming pair's Q and first-tile
-//   maxima, mostly code that runs cold while HBM is saturated) about what ten
-//   more tiles would cost (8 to 10 measured), fifteen in the 64-row instances,
-//   whose epilogue and exact-maximum path are the heaviest.
+//   switch: the outgoing pair's epilogue, the incoming pair's Q staging and the
+//   exact maxima of its first tile, code that largely runs cold while HBM is
+//   saturated. In tiles of the instance it grows with the rows (the epilogue's
+//   rows, the columns of the maxima): about 2 tiles at 16 rows, 8 (head_dim 256)
+//   to 10 (256-token FP8 tiles) at 48 and 13 to 20 at 64, where the instances
+//   keep their per-column values in shared memory. (bf16 at head_dim 128: the
+//   per-CTA fit gives 6 and 11 tiles at 48 and 64 rows, but the kernel times
+//   best at 10 and 13. The 32-row entries and the head_dim-64 row are
+//   interpolated or copied, not measured.)
 // - A tile costs the same whatever the pair's rows, except in the 64-row
 //   instances, which skip the P work of column chunks without rows: there a
 //   tile of r rows costs about 1 + r / 320 tiles (a 64-row tile 1.2).
 constexpr int64_t kCostUnit = 32;  // cost of one tile of a pair without rows
-inline int64_t switch_cost(int np) { return np == 64 ? 15 * kCostUnit : 10 * kCostUnit; }
+inline int64_t switch_cost(bool fp8, int head_dim, int np) {
+  // half tiles, by N = 16, 32, 48, 64
+  static constexpr int kBf16[3][4] = {{4, 10, 20, 26}, {4, 10, 20, 26}, {4, 6, 7, 14}};  // head_dim 64, 128, 256
+  static constexpr int kFp8[2][4] = {{4, 11, 20, 26}, {4, 8, 16, 40}};                 // head_dim 128, 256
+  const int n = np / 16 - 1, hd = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
+  const int half = fp8 ? kFp8[hd - 1][n] : kBf16[hd][n];
+  return half * kCostUnit / 2;
+}
 inline int64_t tile_cost(int np, int rows) { return np == 64 ? kCostUnit + rows / 10 : kCostUnit; }
 
 // Cuts the pairs' tiles (in flat order: pair sizes `nt`, tile costs `w`) into
@@ -314,7 +327,7 @@ int64_t pack_ranges(const std::vector<int64_t>& nt, const std::vector<int64_t>& 
 }
 
 // Flat plan of the tcgen05 kernel: the (sequence, KV head) pairs laid end to
-// end as 128-token tiles, longest sequences first, cut into one wave of
+// end as the kernel's K/V tiles (tc_tile_tokens), longest sequences first, cut into one wave of
 // consecutive CTA ranges. The cut minimises the largest CTA cost (tile costs
 // plus a switch cost per pair switch, the model above): binary search on the
 // cost bound, greedy filling at each bound. So long pairs are split evenly while short ones are
@@ -325,6 +338,9 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
               pa_verify_plan_t* plan_out, size_t* workspace_bytes_out) {
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
   const int G = d.num_q_heads / d.num_kv_heads, Hkv = d.num_kv_heads;
+  int rows_all = 0;
+  for (int b = 0; b < d.num_seqs; ++b) rows_all = std::max(rows_all, ql[b] * G);
+  const int T = tc_tile_tokens(fp8 ? 1 : 0, d.head_dim, tc_rows_pad(rows_all));  // tokens per tile
   std::vector<int> order(d.num_seqs);
   for (int b = 0; b < d.num_seqs; ++b) order[b] = b;
   std::stable_sort(order.begin(), order.end(), [&](int a, int c) { return ctx[a] > ctx[c]; });
@@ -347,7 +363,7 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
     s.n_chunks = 0;
     s.b = b;
     s.tile_start = static_cast<int32_t>(std::min<int64_t>(tiles, INT32_MAX));
-    s.n_tiles = (s.ctx_len + kFlatTile - 1) / kFlatTile;
+    s.n_tiles = (s.ctx_len + T - 1) / T;
     s.pad = 0;
     tiles += static_cast<int64_t>(s.n_tiles) * Hkv;
     row += static_cast<int64_t>(s.q_len) * d.num_q_heads;
@@ -366,7 +382,7 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
   P->ranged = 0;
   if (d.split_override == 0 && tiles > 0) {
     const int np = tc_rows_pad(rows_max);  // the kernel instance's N
-    const int64_t sw = switch_cost(np);
+    const int64_t sw = switch_cost(fp8, d.head_dim, np);
     std::vector<int64_t> nt, w;
     int64_t total = 0, w_max = 0;
     for (int k = 0; k < d.num_seqs; ++k)
@@ -411,10 +427,10 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
   list_split_pairs(P, Hkv, G, pu0, pn);
   P->kernel = PA_KERNEL_TCGEN05;
   P->flat = 1;
-  P->tile = kFlatTile;
+  P->tile = T;
   P->per = static_cast<int32_t>(per);
   P->total_tiles = static_cast<int32_t>(tiles);
-  P->chunk = static_cast<int32_t>(std::min<int64_t>(per * kFlatTile, INT32_MAX));
+  P->chunk = static_cast<int32_t>(std::min<int64_t>(per * T, INT32_MAX));
   P->units = static_cast<int32_t>(n_cta);
   P->rows_max = rows_max;
   P->warps = supported_warps(rows_max);
@@ -469,7 +485,7 @@ int build_capacity_plan(const pa_verify_desc& d, int sms, int max_len, int max_q
   P->slots = static_cast<int32_t>(slots);
   P->kernel = use_tc ? PA_KERNEL_TCGEN05 : PA_KERNEL_WARP_MMA;
   P->flat = use_tc ? 1 : 0;  // flat: one CTA per SM, the tiles per CTA chosen on the device
-  P->tile = use_tc ? kFlatTile : tile_tokens(fp8 ? 1 : 0, d.head_dim);
+  P->tile = use_tc ? tc_tile_tokens(fp8 ? 1 : 0, d.head_dim, tc_rows_pad(rows_max)) : tile_tokens(fp8 ? 1 : 0, d.head_dim);
   P->chunk = 0;  // chosen on the device each run
   P->units = static_cast<int32_t>(units_cap);
   P->rows_max = rows_max;

@@ -9,8 +9,8 @@
 //
 // Same rules as the host planner. Chunk plans: the chunk is the smallest
 // multiple of the staging tile whose unit count fits `slots` (one wave),
-// capped at the page-id staging limit. Flat plans: the pairs' 128-token tiles
-// end to end, ceil(tiles / slots) of them per CTA. Sequences are scheduled
+// capped at the page-id staging limit. Flat plans: the pairs' K/V tiles of the
+// tensor-core kernel end to end, ceil(tiles / slots) of them per CTA. Sequences are scheduled
 // longest first (ties by batch index), padded ones last.
 //
 // One CTA, one thread per sequence of the capacity (up to 1024): the order is
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kPlanThreads) pa_dyn_plan_kernel(DynPlanArgs a
   const bool in = r < a.num_seqs;
   const int Ls = in ? s_len[src] : 0, qs = in ? s_q[src] : 0;
   const int n_chunks = a.flat ? 0 : (Ls > 0 ? (Ls + chunk - 1) / chunk : 0);
-  const int n_tiles = (Ls + kFlatTile - 1) / kFlatTile;  // 0 for padding
+  const int n_tiles = (Ls + a.tile - 1) / a.tile;  // flat plans (the kernel's K/V tiles); 0 for padding
   const long long units_r = static_cast<long long>(n_chunks) * a.num_kv_heads;
   const long long rows_r = static_cast<long long>(qs) * a.num_q_heads;
   const long long tiles_r = static_cast<long long>(n_tiles) * a.num_kv_heads;
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kPlanThreads) pa_dyn_plan_kernel(DynPlanArgs a
     a.out->num_units = a.flat ? static_cast<int>(n_cta) : static_cast<int>(total_units);
     a.out->per = static_cast<int>(per);
     a.out->total_tiles = static_cast<int>(total_tiles);
-    a.out->chunk = a.flat ? kFlatTile : chunk;
+    a.out->chunk = a.flat ? a.tile : chunk;
     a.out->num_rows = static_cast<int>(total_rows);
     a.out->num_tokens = static_cast<int>(tot_tokens);
   }

@@ -18,7 +18,18 @@ constexpr int kMaxRows = 128;     // q_len * group rows per (sequence, KV head)
 constexpr int kMaxQueryLen = 8;
 constexpr int kWsHeader = 256;    // workspace bytes before the partials (device error word at offset 0)
 
-constexpr int kFlatTile = 128;   // tokens per tile of a flat plan
+constexpr int kFlatTile = 128;   // tokens per MMA sub-tile of the tcgen05 kernel (the MMA's M)
+// 128-token sub-tiles per K/V tile of the tcgen05 kernel: two for FP8 K/V at head_dim 128 with up to 48
+// rows (np: rows padded to the instance's N), one elsewhere. (Measured on GB300, split kernel: MTP-5 FP8
+// 174 -> 160 us with two; bf16 slower with two, 65 -> 78 us at MTP-5, as its 64 KB tiles leave room for
+// one ring stage each; the 64-row FP8 instance spills with two.)
+__host__ __device__ constexpr int tc_subtiles(int kv_fp8, int head_dim, int np) {
+  return kv_fp8 && head_dim == 128 && np <= 48 ? 2 : 1;
+}
+// tokens per tile of a flat plan (the tcgen05 kernel's K/V tile)
+__host__ __device__ constexpr int tc_tile_tokens(int kv_fp8, int head_dim, int np) {
+  return kFlatTile * tc_subtiles(kv_fp8, head_dim, np);
+}
 constexpr int kMaxCtaTable = 512; // flat plans: CTAs whose tile ranges a plan can list in the kernel parameters
 
 // Per-sequence entry of the work description, sorted by decreasing context
@@ -26,7 +37,7 @@ constexpr int kMaxCtaTable = 512; // flat plans: CTAs whose tile ranges a plan c
 //
 // Two kinds of plan share it. A chunk plan (warp-MMA kernel) gives every
 // (sequence, KV head, chunk) its own CTA. A flat plan (tcgen05 kernel) lays
-// the (sequence, KV head) pairs end to end as 128-token tiles, pair p =
+// the (sequence, KV head) pairs end to end as K/V tiles (tc_tile_tokens), pair p =
 // k * Hkv + g for the k-th entry and head g, and hands every CTA the same
 // number of consecutive tiles (`per`): CTA c works through the pieces
 // ("segments") of the pairs its range [c * per, (c + 1) * per) touches. The
@@ -41,7 +52,7 @@ struct SeqInfo {
   int32_t n_chunks;    // chunk plans: ceil(L_b / chunk)
   int32_t b;           // index of the sequence in the caller's batch
   int32_t tile_start;  // flat plans: first tile of head 0 (head g starts at tile_start + g * n_tiles)
-  int32_t n_tiles;     // flat plans: ceil(L_b / 128) tiles per KV head (0 for a padded sequence)
+  int32_t n_tiles;     // flat plans: ceil(L_b / tile) tiles per KV head (0 for a padded sequence)
   int32_t pad;
 };
 

@@ -53,10 +53,14 @@
 
 namespace pav {
 
-template <int KV_FP8, int NP, int D>
+template <int KV_FP8, int NP, int D, int SUB = 1>
 struct TcCfg {
   static constexpr int kD = D;
-  static constexpr int kTile = kFlatTile;                    // tokens per K/V tile = MMA M
+  // Tokens per K/V tile: SUB sub-tiles of 128 tokens (the MMA's M) a tile. With two (head_dim 128) every
+  // softmax thread takes two tokens of a tile and S has two accumulators, so the hand-offs between the
+  // roles, the softmax vote and the ring waits are paid once per 256 tokens.
+  static constexpr int kSub = SUB;
+  static constexpr int kTile = 128 * SUB;
   static constexpr int kRowB = KV_FP8 ? D : 2 * D;           // bytes per token row
   static constexpr int kHalves = kRowB / 128;                // 128-byte planes of a tile (TMA boxes per page)
   // PV M halves (one O accumulator each). head_dim 64 (bf16) keeps one M = 128 accumulator: its second
@@ -70,7 +74,8 @@ struct TcCfg {
   // accumulate into the same columns by two MMAs.
   static constexpr bool kStackP = KV_FP8 != 0 && D == 256;
   static constexpr int kOCols = kStackP ? 128 : 64;          // tensor-memory columns of one O accumulator
-  static constexpr int kTmemCols = 128 + kMh * kOCols <= 256 ? 256 : 512;  // S 2 x 64, then the O accumulators
+  static constexpr int kSCols = 128 * SUB;                   // S: 2 buffers x SUB sub-tiles x 64 columns
+  static constexpr int kTmemCols = kSCols + kMh * kOCols <= 256 ? 256 : 512;  // S, then the O accumulators
   static constexpr int kTileB = kTile * kRowB;               // 16 KB (fp8 D128) / 32 KB (bf16 D128, fp8 D256)
   // K ring depth (a K slot frees once S is done) and V ring depth (a V slot frees only after PV); bf16 at
   // head_dim 256 (64 KB tiles) has room for one stage of each next to Q (32 KB) and P
@@ -170,11 +175,11 @@ struct TileCursor {
   __device__ __forceinline__ int pair(int hkv) const { return k * hkv + g; }
 };
 
-template <int KV_FP8, int NP, int D>
-__global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
+template <int KV_FP8, int NP, int D, int SUB = 1>
+__global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
     pa_tc_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ SplitParams p) {
-  using C = TcCfg<KV_FP8, NP, D>;
+  using C = TcCfg<KV_FP8, NP, D, SUB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = sm + C::kOffK;
@@ -234,8 +239,10 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
   };
   constexpr int kHalves = C::kHalves;
   const bool is_k = warp == 0;
-  // producer lanes: page (within the tile) of this lane's box, on lanes [0, 8 * halves) (8: none)
-  const int jl = lane < 8 * kHalves ? lane / kHalves : 8;
+  // producer lanes: page (within the tile) of this lane's box, on lanes [0, pages * halves) (pages: none)
+  constexpr int kTilePages = C::kTile / kPage;
+  static_assert(kTilePages * kHalves <= 32, "one box per lane");
+  const int jl = lane < kTilePages * kHalves ? lane / kHalves : kTilePages;
   constexpr int kSmArrive = 4 * C::NWG;         // softmax warps: arrivals on sfree, pfull and qready
   auto npages = [&](const TileCursor& cq) {
     return min(C::kTile / kPage, (cq.L - cq.t * C::kTile + kPage - 1) / kPage);
@@ -313,8 +320,8 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tbase_slot;
-  const uint32_t tS[2] = {tmem, tmem + 64};
-  const uint32_t tO = tmem + 128;
+  const uint32_t tS[2] = {tmem, tmem + 64 * SUB};  // S buffer b, sub-tile h at tS[b] + 64 h
+  const uint32_t tO = tmem + C::kSCols;
   auto fail = [&]() {
     *abort_flag = 1;
     atomicOr(p.err, 4u);
@@ -389,18 +396,21 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       if constexpr (KV_FP8) {
         if (is_k) {
           // The tile's per-token scales (64 bytes of k and 64 of v a page) by 16-byte cp.async through the
-          // load/store path, two a lane: lane l takes page l / 4, k (l / 2 even) or v, bytes 32 (l % 2) ..
-          // +31. (As TMA copies they doubled the TMA requests of a tile.) Every lane then arrives on the
-          // slot's barrier once its copies have landed.
-          const int sp = lane >> 2;
+          // load/store path: the lanes split the pages' 128 bytes evenly (128-token tiles: lane l takes
+          // page l / 4, 32 bytes; 256-token tiles: page l / 2, 64 bytes), k bytes first. (As TMA copies
+          // they doubled the TMA requests of a tile.) Every lane then arrives on the slot's barrier once
+          // its copies have landed.
+          constexpr int kLanesPage = 32 / kTilePages, kLaneBytes = 128 / kLanesPage;
+          const int sp = lane / kLanesPage;
           const int spg = __shfl_sync(0xffffffffu, pg, sp * kHalves);  // page id (after the pool check)
           if (sp < npg && spg >= 0) {
-            const bool vsc = (lane >> 1) & 1;
-            const int part = (lane & 1) * 8;  // floats
+            const int ob = (lane % kLanesPage) * kLaneBytes;  // byte of [k scales | v scales] of the page
+            const bool vsc = ob >= 64;
+            const int part = (ob & 63) / 4;  // floats
             const float* src = (vsc ? p.v_scale : p.k_scale) + (static_cast<size_t>(spg) * Hkv + cu.g) * kPage + part;
             const uint32_t dst = smem_addr(sSc + sslot * C::kScB + (vsc ? C::kTile * 4 : 0) + sp * kPage * 4 + part * 4);
-            cp_async_16(dst, src);
-            cp_async_16(dst + 16, src + 4);
+#pragma unroll
+            for (int cpy = 0; cpy < kLaneBytes / 16; ++cpy) cp_async_16(dst + 16 * cpy, src + 4 * cpy);
           }
           cp_async_mbar_arrive(smem_addr(&scfull[sslot]));
         }
@@ -460,21 +470,26 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
           return false;
         tc::fence_after_sync();
         const uint64_t dK = tc::sdesc(aK + ks_ * C::kTileB, 16, 1024, tc::kSwizzle128B);
-        if (KV_FP8) {
+        // sub-tile h: tokens [128 h, 128 h + 128) of the tile, 16 KB further into each plane
 #pragma unroll
-          for (int pl = 0; pl < 2; ++pl)  // Q hi then Q lo
+        for (int h = 0; h < SUB; ++h) {
+          if (KV_FP8) {
 #pragma unroll
-            for (int hf = 0; hf < kHalves; ++hf)  // 128 head-dim entries per plane
+            for (int pl = 0; pl < 2; ++pl)  // Q hi then Q lo
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                tc::mma_f8(tS[sb], tc::desc_plus(dK, hf * (C::kTile * 128) + ks * 32),
-                           tc::desc_plus(dQ, (pl * kHalves + hf) * C::kQPlane + ks * 32), idS,
-                           (pl > 0 || hf > 0 || ks > 0) ? 1u : 0u);
-        } else {
+              for (int hf = 0; hf < kHalves; ++hf)  // 128 head-dim entries per plane
 #pragma unroll
-          for (int ks = 0; ks < 4 * kHalves; ++ks)  // 16 head-dim entries a k-step, 4 per 128-byte plane
-            tc::mma_f16(tS[sb], tc::desc_plus(dK, (ks >> 2) * (C::kTile * 128) + (ks & 3) * 32),
-                        tc::desc_plus(dQ, (ks >> 2) * C::kQPlane + (ks & 3) * 32), idS, ks > 0 ? 1u : 0u);
+                for (int ks = 0; ks < 4; ++ks)
+                  tc::mma_f8(tS[sb] + 64 * h, tc::desc_plus(dK, hf * (C::kTile * 128) + h * 16384 + ks * 32),
+                             tc::desc_plus(dQ, (pl * kHalves + hf) * C::kQPlane + ks * 32), idS,
+                             (pl > 0 || hf > 0 || ks > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < 4 * kHalves; ++ks)  // 16 head-dim entries a k-step, 4 per 128-byte plane
+              tc::mma_f16(tS[sb] + 64 * h,
+                          tc::desc_plus(dK, (ks >> 2) * (C::kTile * 128) + h * 16384 + (ks & 3) * 32),
+                          tc::desc_plus(dQ, (ks >> 2) * C::kQPlane + (ks & 3) * 32), idS, ks > 0 ? 1u : 0u);
+          }
         }
         tc::commit(&sfull[sb]);
         tc::commit(&kempty[ks_]);
@@ -500,7 +515,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
 #pragma unroll
             for (int h = 0; h < C::kMh; ++h)  // head-dim entries [128 h, 128 h + 128): V plane h, O accumulator h
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
+              for (int ks = 0; ks < C::kTile / 32; ++ks)
                 if (ks < nks)
                   tc::mma_f8(tO + C::kOCols * h, tc::desc_plus(dV, h * (C::kTile * 128) + ks * 4096),
                              tc::desc_plus(dP, ks * 2048), idPV, (!first || ks > 0) ? 1u : 0u);
@@ -511,7 +526,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
 #pragma unroll
               for (int pl = 0; pl < 2; ++pl)  // hi then lo plane of P, into the same columns
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
+                for (int ks = 0; ks < C::kTile / 32; ++ks)
                   if (ks < nks)
                     tc::mma_f8(tO + C::kOCols * h, tc::desc_plus(dV, h * (C::kTile * 128) + ks * 4096),
                                tc::desc_plus(dP, pl * C::kPPlane + ks * 2048), idPV,
@@ -524,7 +539,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
 #pragma unroll
           for (int h = 0; h < C::kMh; ++h)  // head-dim entries [128 h, 128 h + 128): V planes 2h, 2h + 1
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
+            for (int ks = 0; ks < C::kTile / 16; ++ks)
               if (ks < nks)
                 tc::mma_f16(tO + C::kOCols * h, tc::desc_plus(dV, 2 * h * (C::kTile * 128) + ks * 2048),
                             tc::desc_plus(dP, ks * 2048), idPV, (!first || ks > 0) ? 1u : 0u);
@@ -636,9 +651,10 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
 
     // Per owned column pair, this thread's row-sum partial l. The group-uniform per-column values (the
     // reference maxima M_r, the FP8 score multiplier) are held one of two ways. Up to 24 columns a
-    // group they sit in registers (as -M_r); at 32 they would spill, and shared memory (broadcast
-    // reads) holds them instead. (Both ways measured: each is the faster one where it is used.)
-    constexpr bool kRegs = NH <= 24;
+    // group, one token a thread, they sit in registers (as -M_r); at 32 columns, or two tokens a thread
+    // (256-token tiles), they would spill, and shared memory (broadcast reads) holds them instead. (Both
+    // ways measured: each is the faster one where it is used.)
+    constexpr bool kRegs = NH <= 24 && SUB == 1;
     constexpr int kRP = kRegs ? NH / 2 : 1;
     float2 l[NH / 2];
     float2 negm[kRP], crow2[kRP];
@@ -696,23 +712,36 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       // row chunks of the pair dealt to this group: chunk c0 of the group is live iff c0 < act
       const int act = NP != 64 ? min(NH, max(0, cu.QL * G - col0))
                                : min(NH, 8 * max(0, ((cu.QL * G + 7) / 8 - wg + C::NWG - 1) / C::NWG));
-      float2 y[NH / 2];  // scores of the owned columns, in pairs (packed f32x2 arithmetic)
+      // Scores of the owned columns for this thread's token of every sub-tile, in pairs (packed f32x2
+      // arithmetic).
+      float2 y[SUB][NH / 2];
       {
-        uint32_t r[NH];
+        uint32_t r[SUB][NH];
 #pragma unroll
-        for (int c0 = 0; c0 < NH; c0 += 8) tc::ld8(tS[sb] + lane_off + col0 + c0, *reinterpret_cast<uint32_t(*)[8]>(r + c0));
+        for (int h = 0; h < SUB; ++h)
+#pragma unroll
+          for (int c0 = 0; c0 < NH; c0 += 8)
+            tc::ld8(tS[sb] + 64 * h + lane_off + col0 + c0, *reinterpret_cast<uint32_t(*)[8]>(&r[h][c0]));
         tc::wait_ld();
 #pragma unroll
-        for (int c = 0; c < NH / 2; ++c) y[c] = make_float2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
+        for (int h = 0; h < SUB; ++h)
+#pragma unroll
+          for (int c = 0; c < NH / 2; ++c)
+            y[h][c] = make_float2(__uint_as_float(r[h][2 * c]), __uint_as_float(r[h][2 * c + 1]));
       }
-      float sk = 1.f, sv = 1.f;
+      float sk[SUB], sv[SUB];
+#pragma unroll
+      for (int h = 0; h < SUB; ++h) { sk[h] = 1.f; sv[h] = 1.f; }
       if constexpr (KV_FP8) {
         // the tile's scales, read before S is released (that release frees their slot for reuse)
         const int ss = i % C::SS;
         wait(&scfull[ss], static_cast<uint32_t>(i / C::SS) & 1u);
         const float* sc = reinterpret_cast<const float*>(sSc + ss * C::kScB);
-        sk = sc[tok];
-        sv = sc[C::kTile + tok];
+#pragma unroll
+        for (int h = 0; h < SUB; ++h) {
+          sk[h] = sc[tok + 128 * h];
+          sv[h] = sc[C::kTile + tok + 128 * h];
+        }
       }
       tc::fence_before_sync();
       __syncwarp();
@@ -727,47 +756,54 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
       }
 
       const int L = cu.L;
-      const int tabs = cu.t * C::kTile + tok;
+      const int tabs0 = cu.t * C::kTile + tok;  // this thread's token of sub-tile h: tabs0 + 128 h
       const int vs = i % C::VS;
-      float inv_sv = 1.f;
-      if (KV_FP8) {
-        if (tabs >= L) { sk = 0.f; sv = 1.f; }
-        sv = fmaxf(sv, 7.888609052210118e-31f);  // 2^-100 floor keeps log2 and 1/x finite
-        const float2 ls = make_float2(__log2f(sv), __log2f(sv));
-        inv_sv = __frcp_rn(sv);
-        const float2 sk2 = make_float2(sk, sk);
+      float inv_sv[SUB];
 #pragma unroll
-        for (int c = 0; c < NH / 2; ++c)
-          y[c] = __ffma2_rn(__fmul2_rn(y[c], sk2),
-                            kRegs ? crow2[c % kRP] : reinterpret_cast<const float2*>(rowC + sl * 64 + col0)[c], ls);
-      } else {
-        const float2 s2 = make_float2(p.scale_log2, p.scale_log2);
+      for (int h = 0; h < SUB; ++h) {
+        const int tabs = tabs0 + 128 * h;
+        inv_sv[h] = 1.f;
+        if (KV_FP8) {
+          if (tabs >= L) { sk[h] = 0.f; sv[h] = 1.f; }
+          const float svh = fmaxf(sv[h], 7.888609052210118e-31f);  // 2^-100 floor keeps log2 and 1/x finite
+          const float2 ls = make_float2(__log2f(svh), __log2f(svh));
+          inv_sv[h] = __frcp_rn(svh);
+          const float2 sk2 = make_float2(sk[h], sk[h]);
 #pragma unroll
-        for (int c = 0; c < NH / 2; ++c) y[c] = __fmul2_rn(y[c], s2);
-      }
-      // causal mask inside the drafts / pair end / padding rows
-      if (tabs >= L) {
+          for (int c = 0; c < NH / 2; ++c)
+            y[h][c] = __ffma2_rn(__fmul2_rn(y[h][c], sk2),
+                                 kRegs ? crow2[c % kRP] : reinterpret_cast<const float2*>(rowC + sl * 64 + col0)[c], ls);
+        } else {
+          const float2 s2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-        for (int c = 0; c < NH / 2; ++c) y[c] = make_float2(-INFINITY, -INFINITY);
-      } else if (tabs > L - cu.QL) {
-        const int* lim = rowLim + sl * 64 + col0;
+          for (int c = 0; c < NH / 2; ++c) y[h][c] = __fmul2_rn(y[h][c], s2);
+        }
+        // causal mask inside the drafts / pair end / padding rows
+        if (tabs >= L) {
 #pragma unroll
-        for (int c = 0; c < NH / 2; ++c) {
-          if (tabs > lim[2 * c]) y[c].x = -INFINITY;
-          if (tabs > lim[2 * c + 1]) y[c].y = -INFINITY;
+          for (int c = 0; c < NH / 2; ++c) y[h][c] = make_float2(-INFINITY, -INFINITY);
+        } else if (tabs > L - cu.QL) {
+          const int* lim = rowLim + sl * 64 + col0;
+#pragma unroll
+          for (int c = 0; c < NH / 2; ++c) {
+            if (tabs > lim[2 * c]) y[h][c].x = -INFINITY;
+            if (tabs > lim[2 * c + 1]) y[h][c].y = -INFINITY;
+          }
         }
       }
       // d = y - M (log2 units); with M = -inf a finite score gives +inf (and a masked one NaN, dropped
       // below). (Shared-memory way: a segment's first tile has no reference yet and d holds y itself.)
-      float2 dl[NH / 2];
+      float2 dl[SUB][NH / 2];
       float dmax;
       if constexpr (kRegs) {
         dmax = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < NH / 2; ++c) {
-          dl[c] = __fadd2_rn(y[c], negm[c % kRP]);
-          dmax = fmaxf(dmax, fmaxf(dl[c].x, dl[c].y));
-        }
+        for (int h = 0; h < SUB; ++h)
+#pragma unroll
+          for (int c = 0; c < NH / 2; ++c) {
+            dl[h][c] = __fadd2_rn(y[h][c], negm[c % kRP]);
+            dmax = fmaxf(dmax, fmaxf(dl[h][c].x, dl[h][c].y));
+          }
       } else {
         dmax = INFINITY;
         if (!seg_first) {
@@ -775,134 +811,103 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < NH / 2; ++c) {
             const float2 m = reinterpret_cast<const float2*>(mref)[c];
-            dl[c] = __fadd2_rn(y[c], make_float2(-m.x, -m.y));
-            dmax = fmaxf(dmax, fmaxf(dl[c].x, dl[c].y));
+#pragma unroll
+            for (int h = 0; h < SUB; ++h) {
+              dl[h][c] = __fadd2_rn(y[h][c], make_float2(-m.x, -m.y));
+              dmax = fmaxf(dmax, fmaxf(dl[h][c].x, dl[h][c].y));
+            }
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < NH / 2; ++c) dl[c] = y[c];
+          for (int h = 0; h < SUB; ++h)
+#pragma unroll
+            for (int c = 0; c < NH / 2; ++c) dl[h][c] = y[h][c];
         }
       }
       if (named_or(bar_or, 128, dmax > 8.f)) {
-        if constexpr (kRegs) {
-          // ---- exact tile maxima of the owned columns, raise the references, rescale l and O
+        // ---- exact tile maxima of the owned columns, raise the references, rescale l and O
+        // (registers: the maxima of y; shared memory: of d, plus the group-uniform offset M, so that y is
+        // not kept next to d)
 #pragma unroll
-          for (int c = 0; c < NH; ++c) {
-            const float m = warp_max((c & 1) ? y[c >> 1].y : y[c >> 1].x);
-            if (lane == 0) red[(warp - 2) * 64 + col0 + c] = m;
-          }
-          named_sync(bar_sync, 128);
-          const float* rg = red + wg * 4 * 64 + col0;  // this group's 4 warp rows
-          auto old_max = [&](int c) { return (c & 1) ? -negm[(c >> 1) % kRP].y : -negm[(c >> 1) % kRP].x; };
-          auto new_max = [&](int c) {
-            return fmaxf(old_max(c), fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
-          };
-          bool any_scale = false;
+        for (int c = 0; c < NH; ++c) {
+          float v = kRegs ? ((c & 1) ? y[0][c >> 1].y : y[0][c >> 1].x) : ((c & 1) ? dl[0][c >> 1].y : dl[0][c >> 1].x);
 #pragma unroll
-          for (int c = 0; c < NH; ++c) {
-            const float mn = new_max(c);
-            any_scale |= (mn != -INFINITY && mn != old_max(c));
-          }
-          if (any_scale && !seg_first) {
-            if (gt == 0) atomicAdd(p.err + kWsRescaleWord, 1u);  // diagnostic count of O rescales
-            wait(&pfree[(i - 1) % C::PB], static_cast<uint32_t>((i - 1) / C::PB) & 1u);  // PV of tile i-1 done
-            tc::fence_after_sync();
+          for (int h = 1; h < SUB; ++h)
+            v = fmaxf(v, kRegs ? ((c & 1) ? y[h][c >> 1].y : y[h][c >> 1].x)
+                               : ((c & 1) ? dl[h][c >> 1].y : dl[h][c >> 1].x));
+          if constexpr (!kRegs) v += seg_first ? 0.f : mref[c];
+          const float m = warp_max(v);
+          if (lane == 0) red[(warp - 2) * 64 + col0 + c] = m;
+        }
+        named_sync(bar_sync, 128);
+        const float* rg = red + wg * 4 * 64 + col0;  // this group's 4 warp rows
+        auto old_max = [&](int c) {
+          if constexpr (kRegs) return (c & 1) ? -negm[(c >> 1) % kRP].y : -negm[(c >> 1) % kRP].x;
+          else return seg_first ? -INFINITY : mref[c];
+        };
+        auto new_max = [&](int c) {
+          return fmaxf(old_max(c), fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
+        };
+        bool any_scale = false;
 #pragma unroll
-            for (int h = 0; h < C::kMh; ++h)
+        for (int c = 0; c < NH; ++c) {
+          const float mn = new_max(c);
+          any_scale |= (mn != -INFINITY && mn != old_max(c));
+        }
+        if (any_scale && !seg_first) {
+          if (gt == 0) atomicAdd(p.err + kWsRescaleWord, 1u);  // diagnostic count of O rescales
+          wait(&pfree[(i - 1) % C::PB], static_cast<uint32_t>((i - 1) / C::PB) & 1u);  // PV of tile i-1 done
+          tc::fence_after_sync();
 #pragma unroll
-              for (int pt = 0; pt < (C::kStackP ? 2 : 1); ++pt)  // O_hi, then O_lo 64 columns on
+          for (int h = 0; h < C::kMh; ++h)
 #pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 8) {
-                  const uint32_t ta = tO + C::kOCols * h + 64 * pt + lane_off + col0 + c0;
-                  uint32_t r8[8];
-                  tc::ld8(ta, r8);
-                  tc::wait_ld();
+            for (int pt = 0; pt < (C::kStackP ? 2 : 1); ++pt)  // O_hi, then O_lo 64 columns on
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    const float mn = new_max(c0 + j), mo = old_max(c0 + j);
-                    const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
-                    r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
-                  }
-                  tc::st8(ta, r8);
+              for (int c0 = 0; c0 < NH; c0 += 8) {
+                const uint32_t ta = tO + C::kOCols * h + 64 * pt + lane_off + col0 + c0;
+                uint32_t r8[8];
+                tc::ld8(ta, r8);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float mn = new_max(c0 + j), mo = old_max(c0 + j);
+                  const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
+                  r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
                 }
-            tc::wait_st();
-          }
+                tc::st8(ta, r8);
+              }
+          tc::wait_st();
+        }
 #pragma unroll
-          for (int c = 0; c < NH; ++c) {
-            const float mn = new_max(c), mo = old_max(c);
-            if (mn != -INFINITY && mn != mo) {
-              float& lc = (c & 1) ? l[c >> 1].y : l[c >> 1].x;
-              lc *= fast_exp2(mo - mn);
+        for (int c = 0; c < NH; ++c) {
+          const float mn = new_max(c), mo = old_max(c);
+          if (mn != -INFINITY && mn != mo) {
+            float& lc = (c & 1) ? l[c >> 1].y : l[c >> 1].x;
+            lc *= fast_exp2(mo - mn);
+            if constexpr (kRegs) {
               if (c & 1) negm[(c >> 1) % kRP].y = -mn; else negm[(c >> 1) % kRP].x = -mn;
             }
           }
+        }
 #pragma unroll
-          for (int c = 0; c < NH / 2; ++c) dl[c] = __fadd2_rn(y[c], negm[c % kRP]);
-          // red is rewritten only after the next vote (a barrier of this group), when every read here is done
-        } else {
-          // ---- exact tile maxima of the owned columns, raise the references, rescale l and O
-#pragma unroll
-          for (int c = 0; c < NH; ++c) {
-            // tile max of y = max of d + the group-uniform offset
-            const float m = warp_max((c & 1) ? dl[c >> 1].y : dl[c >> 1].x) + (seg_first ? 0.f : mref[c]);
-            if (lane == 0) red[(warp - 2) * 64 + col0 + c] = m;
-          }
-          named_sync(bar_sync, 128);
-          const float* rg = red + wg * 4 * 64 + col0;  // this group's 4 warp rows
-          auto old_max = [&](int c) { return seg_first ? -INFINITY : mref[c]; };
-          auto new_max = [&](int c) {
-            return fmaxf(old_max(c), fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
-          };
-          bool any_scale = false;
-#pragma unroll
-          for (int c = 0; c < NH; ++c) {
-            const float mn = new_max(c);
-            any_scale |= (mn != -INFINITY && mn != old_max(c));
-          }
-          if (any_scale && !seg_first) {
-            if (gt == 0) atomicAdd(p.err + kWsRescaleWord, 1u);  // diagnostic count of O rescales
-            wait(&pfree[(i - 1) % C::PB], static_cast<uint32_t>((i - 1) / C::PB) & 1u);  // PV of tile i-1 done
-            tc::fence_after_sync();
-#pragma unroll
-            for (int h = 0; h < C::kMh; ++h)
-#pragma unroll
-              for (int pt = 0; pt < (C::kStackP ? 2 : 1); ++pt)  // O_hi, then O_lo 64 columns on
-#pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 8) {
-                  const uint32_t ta = tO + C::kOCols * h + 64 * pt + lane_off + col0 + c0;
-                  uint32_t r8[8];
-                  tc::ld8(ta, r8);
-                  tc::wait_ld();
-#pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    const float mn = new_max(c0 + j), mo = old_max(c0 + j);
-                    const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
-                    r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
-                  }
-                  tc::st8(ta, r8);
-                }
-            tc::wait_st();
-          }
-#pragma unroll
-          for (int c = 0; c < NH; ++c) {
-            const float mn = new_max(c), mo = old_max(c);
-            if (mn != -INFINITY && mn != mo) {
-              float& lc = (c & 1) ? l[c >> 1].y : l[c >> 1].x;
-              lc *= fast_exp2(mo - mn);
-            }
-          }
+        for (int h = 0; h < SUB; ++h)
 #pragma unroll
           for (int c = 0; c < NH / 2; ++c) {
-            const float o0 = seg_first ? 0.f : mref[2 * c], o1 = seg_first ? 0.f : mref[2 * c + 1];
-            dl[c] = __fadd2_rn(dl[c], make_float2(o0 - new_max(2 * c), o1 - new_max(2 * c + 1)));
+            if constexpr (kRegs) {
+              dl[h][c] = __fadd2_rn(y[h][c], negm[c % kRP]);
+            } else {
+              const float o0 = seg_first ? 0.f : mref[2 * c], o1 = seg_first ? 0.f : mref[2 * c + 1];
+              dl[h][c] = __fadd2_rn(dl[h][c], make_float2(o0 - new_max(2 * c), o1 - new_max(2 * c + 1)));
+            }
           }
+        if constexpr (!kRegs) {
           // every thread of the group has read the old references: one thread per column writes the new one
           const float mine = gt < NH ? new_max(gt) : 0.f;
           named_sync(bar_sync, 128);
           if (gt < NH) refM[col0 + gt] = mine;
           named_sync(bar_sync, 128);
-          // red is rewritten only after the next vote (a barrier of this group), when every read here is done
         }
+        // red is rewritten only after the next vote (a barrier of this group), when every read here is done
       }
       // ---- P = 2^(y - M) (<= 2^8), row sums, P into shared memory as the MMA's B operand
       const int pb = i % C::PB;
@@ -918,54 +923,62 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
           wait(&pfree[(i - C::VS) % C::PB], static_cast<uint32_t>((i - C::VS) / C::PB) & 1u);
         wait(&vfull[vs], static_cast<uint32_t>(i / C::VS) & 1u);
         const int kend = KV_FP8 ? ((nv + 31) & ~31) : ((nv + 15) & ~15);
-        if (wg == 0 && tok >= nv && tok < kend) {
 #pragma unroll
-          for (int hf = 0; hf < C::kRowB / 128; ++hf) {
-            uint4* z = reinterpret_cast<uint4*>(sV + vs * C::kVStage + hf * (C::kTile * 128) + tok * 128);
+        for (int h = 0; h < SUB; ++h) {
+          const int t = tok + 128 * h;  // token of the tile
+          if (wg == 0 && t >= nv && t < kend) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) z[k] = make_uint4(0, 0, 0, 0);
+            for (int hf = 0; hf < C::kRowB / 128; ++hf) {
+              uint4* z = reinterpret_cast<uint4*>(sV + vs * C::kVStage + hf * (C::kTile * 128) + t * 128);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) z[k] = make_uint4(0, 0, 0, 0);
+            }
           }
         }
       }
       uint8_t* prow = sP + pb * C::kPBuf;
-      const float2 iv2 = make_float2(inv_sv, inv_sv);
 #pragma unroll
       for (int c0 = 0; c0 < NH; c0 += 8) {
         if (NP == 64 && c0 >= act) continue;  // no row of the pair in these columns (64-row instances)
-        float2 pv[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 d = dl[c0 / 2 + j];
-          // exp2 of max(d, -200): a masked score (-inf, or NaN against M = -inf) gives 0 after flush-to-zero
-          pv[j] = make_float2(fast_exp2(fmaxf(d.x, -200.f)), fast_exp2(fmaxf(d.y, -200.f)));
-          l[c0 / 2 + j] = __ffma2_rn(pv[j], iv2, l[c0 / 2 + j]);
-        }
         const int cg = col0 + c0;  // first global column of these 8
-        if (!KV_FP8) {
-          uint4 w;
-          w.x = pack_bf16(pv[0].x, pv[0].y);
-          w.y = pack_bf16(pv[1].x, pv[1].y);
-          w.z = pack_bf16(pv[2].x, pv[2].y);
-          w.w = pack_bf16(pv[3].x, pv[3].y);
-          const int ch = cg >> 3;  // 16-byte chunk of the 128-byte token row
-          *reinterpret_cast<uint4*>(prow + tok * 128 + ((ch ^ (tok & 7)) << 4)) = w;
-        } else {
-          uint32_t hw0 = 0, hw1 = 0, lw0 = 0, lw1 = 0;
+#pragma unroll
+        for (int h = 0; h < SUB; ++h) {
+          const int t = tok + 128 * h;  // token of the tile (row of P)
+          const float2 iv2 = make_float2(inv_sv[h], inv_sv[h]);
+          float2 pv[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float2 a = pv[j];
-            const float2 ah = make_float2(__uint_as_float(__float_as_uint(a.x) & 0xFFF00000u),
-                                          __uint_as_float(__float_as_uint(a.y) & 0xFFF00000u));  // 3 mantissa bits
-            const float2 al = __ffma2_rn(ah, make_float2(-1.f, -1.f), a);                      // exact remainder
-            const uint32_t hb = e4m3x2(ah.x, ah.y), lb = e4m3x2(al.x, al.y);
-            if (j < 2) { hw0 |= hb << (16 * j); lw0 |= lb << (16 * j); }
-            else { hw1 |= hb << (16 * (j - 2)); lw1 |= lb << (16 * (j - 2)); }
+            const float2 d = dl[h][c0 / 2 + j];
+            // exp2 of max(d, -200): a masked score (-inf, or NaN against M = -inf) gives 0 after flush-to-zero
+            pv[j] = make_float2(fast_exp2(fmaxf(d.x, -200.f)), fast_exp2(fmaxf(d.y, -200.f)));
+            l[c0 / 2 + j] = __ffma2_rn(pv[j], iv2, l[c0 / 2 + j]);
           }
-          // 8 bytes at byte cg of the 64-byte token row (64B swizzle: chunk ^= (tok/2)%4)
-          const int ch = cg >> 4;
-          const uint32_t off = tok * 64 + ((ch ^ ((tok >> 1) & 3)) << 4) + (cg & 8);
-          *reinterpret_cast<uint2*>(prow + off) = make_uint2(hw0, hw1);
-          *reinterpret_cast<uint2*>(prow + C::kPPlane + off) = make_uint2(lw0, lw1);
+          if (!KV_FP8) {
+            uint4 w;
+            w.x = pack_bf16(pv[0].x, pv[0].y);
+            w.y = pack_bf16(pv[1].x, pv[1].y);
+            w.z = pack_bf16(pv[2].x, pv[2].y);
+            w.w = pack_bf16(pv[3].x, pv[3].y);
+            const int ch = cg >> 3;  // 16-byte chunk of the 128-byte token row
+            *reinterpret_cast<uint4*>(prow + t * 128 + ((ch ^ (t & 7)) << 4)) = w;
+          } else {
+            uint32_t hw0 = 0, hw1 = 0, lw0 = 0, lw1 = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 a = pv[j];
+              const float2 ah = make_float2(__uint_as_float(__float_as_uint(a.x) & 0xFFF00000u),
+                                            __uint_as_float(__float_as_uint(a.y) & 0xFFF00000u));  // 3 mantissa bits
+              const float2 al = __ffma2_rn(ah, make_float2(-1.f, -1.f), a);                      // exact remainder
+              const uint32_t hb = e4m3x2(ah.x, ah.y), lb = e4m3x2(al.x, al.y);
+              if (j < 2) { hw0 |= hb << (16 * j); lw0 |= lb << (16 * j); }
+              else { hw1 |= hb << (16 * (j - 2)); lw1 |= lb << (16 * (j - 2)); }
+            }
+            // 8 bytes at byte cg of the 64-byte token row (64B swizzle: chunk ^= (t/2)%4)
+            const int ch = cg >> 4;
+            const uint32_t off = t * 64 + ((ch ^ ((t >> 1) & 3)) << 4) + (cg & 8);
+            *reinterpret_cast<uint2*>(prow + off) = make_uint2(hw0, hw1);
+            *reinterpret_cast<uint2*>(prow + C::kPPlane + off) = make_uint2(lw0, lw1);
+          }
         }
       }
       fence_proxy_async();
@@ -1074,15 +1087,15 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D>::kThreads, 1)
 }
 
 // Launches the kernel for one (KV type, padded rows, head_dim) instance.
-template <int F8, int NP, int D>
+template <int F8, int NP, int D, int SUB = 1>
 cudaError_t run_tc(int units, const CUtensorMap* tmk, const CUtensorMap* tmv, const SplitParams* p,
                    cudaStream_t stream) {
-  auto kern = pa_tc_split_kernel<F8, NP, D>;
-  constexpr int smem = TcCfg<F8, NP, D>::kSmem;
+  auto kern = pa_tc_split_kernel<F8, NP, D, SUB>;
+  constexpr int smem = TcCfg<F8, NP, D, SUB>::kSmem;
   static std::atomic<uint64_t> attr_done{0};  // devices whose limit is raised
   const cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<units, TcCfg<F8, NP, D>::kThreads, smem, stream>>>(*tmk, *tmv, *p);
+  kern<<<units, TcCfg<F8, NP, D, SUB>::kThreads, smem, stream>>>(*tmk, *tmv, *p);
   return cudaGetLastError();
 }
 

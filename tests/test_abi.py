@@ -50,11 +50,23 @@ CASES = [([37, 100], [1, 6], 1), ([4096 + 7 * i for i in range(8)], [6] * 8, 4),
          ([1 << 20], [6], 1), ([5, 9000, 131072, 64], [3, 8, 1, 2], 2)]
 
 
-# The planner's cost model, in 1/32 of a tile: a tile costs 32 (64-row instances: 32 + rows // 10, since
-# they skip the P work of empty column chunks), a pair switch 320 (64-row instances: 480).
-def costs(rows_max, rows):
+def tc_tile(kv, d, rows_max):
+    """Tokens per K/V tile of the tensor-core kernel: 256 for FP8 K/V at head_dim 128 with up to 48 rows
+    (two 128-token MMA sub-tiles), 128 elsewhere."""
+    return 256 if kv == pv.KV_FP8_E4M3 and d == 128 and rows_max <= 48 else 128
+
+
+# The planner's cost model, in 1/32 of the instance's tile: a tile costs 32 (64-row instances: 32 + rows // 10,
+# since they skip the P work of empty column chunks); a pair switch costs the measured number of tiles below,
+# in half tiles by (K/V type, head_dim) and N = 16, 32, 48, 64.
+SWITCH_HALF_TILES = {(pv.KV_BF16, 64): (4, 10, 20, 26), (pv.KV_BF16, 128): (4, 10, 20, 26),
+                     (pv.KV_BF16, 256): (4, 6, 7, 14), (pv.KV_FP8_E4M3, 128): (4, 11, 20, 26),
+                     (pv.KV_FP8_E4M3, 256): (4, 8, 16, 40)}
+
+
+def costs(rows_max, rows, kv=pv.KV_BF16, d=128):
     np_ = 16 if rows_max <= 16 else 32 if rows_max <= 32 else 48 if rows_max <= 48 else 64
-    return (32 + rows // 10 if np_ == 64 else 32), (480 if np_ == 64 else 320)
+    return (32 + rows // 10 if np_ == 64 else 32), SWITCH_HALF_TILES[(kv, d)][np_ // 16 - 1] * 16
 
 
 def pack(nt, w, sw, tau):
@@ -77,15 +89,15 @@ def pack(nt, w, sw, tau):
     return ctas, starts + [pos]
 
 
-def flat_model(ctx, ql, hkv, sms, split_override=0, group=8):
+def flat_model(ctx, ql, hkv, sms, split_override=0, group=8, tile=128, kv=pv.KV_BF16, d=128):
     """Independent model of a flat plan: pairs (longest sequence first, then KV
-    head) end to end as 128-token tiles, cut into CTA ranges. Returns (CTA
+    head) end to end as `tile`-token tiles, cut into CTA ranges. Returns (CTA
     starts, every pair's (first tile, tiles), the cost bound)."""
     order = sorted(range(len(ctx)), key=lambda b: -ctx[b])  # stable: ties keep batch order
-    nt = [(ctx[b] + 127) // 128 for b in order for _ in range(hkv)]
+    nt = [-(-ctx[b] // tile) for b in order for _ in range(hkv)]
     rows_max = max(ql) * group
-    w = [costs(rows_max, ql[b] * group)[0] for b in order for _ in range(hkv)]
-    sw = costs(rows_max, 0)[1]
+    w = [costs(rows_max, ql[b] * group, kv, d)[0] for b in order for _ in range(hkv)]
+    sw = costs(rows_max, 0, kv, d)[1]
     total = sum(nt)
     pairs, t = [], 0
     for n in nt:
@@ -105,14 +117,15 @@ def flat_model(ctx, ql, hkv, sms, split_override=0, group=8):
     return pack(nt, w, sw, lo)[1], pairs, (lo, w, sw)
 
 
-def check_flat_plan(ctx, ql, hkv, split, sms=152):
+def check_flat_plan(ctx, ql, hkv, split, sms=152, kv=pv.KV_BF16):
     """The library's flat plan equals the model's ranges and keeps every invariant the kernels rely on."""
-    p = mk(ctx, ql, hq=8 * hkv, hkv=hkv, split_override=split, sms=sms)
+    p = mk(ctx, ql, hq=8 * hkv, hkv=hkv, split_override=split, sms=sms, kv=kv)
     i = p.info
-    assert i.flat == 1 and i.kernel == pv.KERNEL_TCGEN05 and i.tile_tokens == 128
-    starts, pairs, bound = flat_model(ctx, ql, hkv, sms, split)
+    T = tc_tile(kv, 128, 8 * max(ql))
+    assert i.flat == 1 and i.kernel == pv.KERNEL_TCGEN05 and i.tile_tokens == T
+    starts, pairs, bound = flat_model(ctx, ql, hkv, sms, split, tile=T, kv=kv)
     assert p.cta_starts() == starts
-    assert i.total_tiles == hkv * sum((c + 127) // 128 for c in ctx) == starts[-1]
+    assert i.total_tiles == hkv * sum(-(-c // T) for c in ctx) == starts[-1]
     assert i.num_units == len(starts) - 1
     # the ranges tile the flat space once, without empty CTAs
     assert starts[0] == 0 and all(a < b for a, b in zip(starts, starts[1:]))
@@ -120,7 +133,7 @@ def check_flat_plan(ctx, ql, hkv, split, sms=152):
     spans = [(cta_of(t0), cta_of(t0 + n - 1)) for t0, n in pairs]
     assert i.max_splits == max(b - a + 1 for a, b in spans)
     assert i.needs_combine == (i.max_splits > 1)
-    assert i.kv_bytes == sum(ctx) * hkv * 128 * 4
+    assert i.kv_bytes == sum(ctx) * hkv * (128 * 4 if kv == pv.KV_BF16 else 128 * 2 + 8)
     # slot c + pair of each CTA's piece of a pair is unique, and below CTAs + pairs (the workspace's slots)
     slots = [c + k for k, (a, b) in enumerate(spans) for c in range(a, b + 1)]
     assert len(slots) == len(set(slots)) and max(slots) < i.num_units + len(spans)
@@ -128,7 +141,7 @@ def check_flat_plan(ctx, ql, hkv, split, sms=152):
         assert i.num_units <= sms
         # no CTA costs more than the bound, which the plan reports in whole tiles as the chunk
         tau, w, sw = bound
-        assert i.chunk_tokens // 128 == -(-tau // 32)
+        assert i.chunk_tokens // T == -(-tau // 32)
         for c in range(i.num_units):
             cost = sw * (sum(1 for a, b in spans if a <= c <= b) - 1)
             for k, (t0, n) in enumerate(pairs):
@@ -136,10 +149,11 @@ def check_flat_plan(ctx, ql, hkv, split, sms=152):
             assert cost <= tau
 
 
+@pytest.mark.parametrize("kv", [pv.KV_BF16, pv.KV_FP8_E4M3], ids=["bf16", "fp8"])
 @pytest.mark.parametrize("ctx,ql,hkv", CASES)
 @pytest.mark.parametrize("split", [0, 1, 4, 1000])
-def test_flat_plan_ranges(ctx, ql, hkv, split):
-    check_flat_plan(ctx, ql, hkv, split)
+def test_flat_plan_ranges(ctx, ql, hkv, split, kv):
+    check_flat_plan(ctx, ql, hkv, split, kv=kv)
 
 
 def test_flat_plan_ranges_on_random_batches():
@@ -151,7 +165,7 @@ def test_flat_plan_ranges_on_random_batches():
         ctx = [max(q, min(200000, int(np.exp(rng.normal(np.log(6000), 1.3))))) for q in ql]
         hkv = int(rng.choice([1, 2, 4]))
         sms = int(rng.choice([16, 132, 148, 152]))
-        check_flat_plan(ctx, ql, hkv, 0, sms=sms)
+        check_flat_plan(ctx, ql, hkv, 0, sms=sms, kv=int(rng.choice([pv.KV_BF16, pv.KV_FP8_E4M3])))
 
 
 def test_flat_plan_does_not_cross_pairs_needlessly():
@@ -236,8 +250,10 @@ def test_fp8_head_dim_256_plans_on_tensor_cores(ql, hq):
     p = mk([150000, 40000], [ql, ql], hq=hq, hkv=1, d=256, kv=pv.KV_FP8_E4M3)
     assert p.info.kernel == pv.KERNEL_TCGEN05 and p.info.flat == 1
     assert p.info.rows_max == ql * hq
+    assert p.info.tile_tokens == 128 and p.info.total_tiles == -(-150000 // 128) + -(-40000 // 128)
     q = mk([150000, 40000], [ql, ql], hq=hq, hkv=1, d=128, kv=pv.KV_FP8_E4M3)
-    assert p.info.num_units == q.info.num_units  # the same tiles: the split does not depend on head_dim
+    T = tc_tile(pv.KV_FP8_E4M3, 128, ql * hq)
+    assert q.info.tile_tokens == T and q.info.total_tiles == -(-150000 // T) + -(-40000 // T)
     assert p.workspace_bytes > q.workspace_bytes
     dyn = pv.plan_dynamic(hq, 1, 256, pv.KV_FP8_E4M3, pv.OUT_BF16, 20000, 9400, 4, 150000, ql, sm_count=152)
     assert dyn.info.kernel == pv.KERNEL_TCGEN05
@@ -309,3 +325,13 @@ def test_bf16_head_dim_256_plans_on_tensor_cores():
     p = mk([150000, 40000], [6, 6], hq=8, hkv=1, d=256)
     assert p.info.kernel == pv.KERNEL_TCGEN05 and p.info.rows_max == 48
     assert p.info.kv_bytes == 190000 * 1024
+
+
+@pytest.mark.parametrize("kv,d,ql,hq,T", [(pv.KV_FP8_E4M3, 128, 6, 8, 256), (pv.KV_FP8_E4M3, 128, 8, 8, 128),
+                                          (pv.KV_FP8_E4M3, 128, 2, 8, 256), (pv.KV_BF16, 128, 6, 8, 128),
+                                          (pv.KV_FP8_E4M3, 256, 6, 8, 128), (pv.KV_BF16, 64, 6, 8, 128)])
+def test_tensor_core_tile_sizes(kv, d, ql, hq, T):
+    """Static and capacity plans agree on the kernel's tile: 256 tokens for FP8 at head_dim 128 up to 48 rows."""
+    assert mk([5000, 300], [ql, 1], hq=hq, d=d, kv=kv).info.tile_tokens == T
+    dyn = pv.plan_dynamic(hq, 1, d, kv, pv.OUT_BF16, 20000, 9400, 4, 150000, ql, sm_count=152)
+    assert dyn.info.tile_tokens == T

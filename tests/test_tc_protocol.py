@@ -27,8 +27,9 @@ import random
 import pytest
 
 # (K ring, V ring, P buffers, FP8) of the kernel's instances
-INSTANCES = {"bf16_d128": (2, 3, 2, False), "fp8_d128": (5, 5, 2, True), "fp8_d256": (2, 2, 3, True),
-             "bf16_d64": (5, 5, 2, False), "bf16_d256": (1, 1, 3, False)}
+# (FP8 at head_dim 128: 256-token tiles up to 48 rows, 128-token tiles in the 64-row instance)
+INSTANCES = {"bf16_d128": (2, 3, 2, False), "fp8_d128": (2, 2, 2, True), "fp8_d128_r64": (5, 5, 2, True),
+             "fp8_d256": (2, 2, 3, True), "bf16_d64": (5, 5, 2, False), "bf16_d256": (1, 1, 3, False)}
 
 
 def run(seg_first, short_tile, slow, ks, vs, pb, fp8, kernel_order=True, scale_slack=2, short_wait="pv", sched=None):
