@@ -840,72 +840,53 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
           if (lane == 0) red[(warp - 2) * 64 + col0 + c] = m;
         }
         named_sync(bar_sync, 128);
-        const float* rg = red + wg * 4 * 64 + col0;  // this group's 4 warp rows
-        auto old_max = [&](int c) {
-          if constexpr (kRegs) return (c & 1) ? -negm[(c >> 1) % kRP].y : -negm[(c >> 1) % kRP].x;
-          else return seg_first ? -INFINITY : mref[c];
-        };
-        auto new_max = [&](int c) {
-          return fmaxf(old_max(c), fmaxf(fmaxf(rg[c], rg[64 + c]), fmaxf(rg[128 + c], rg[192 + c])));
-        };
-        bool any_scale = false;
-#pragma unroll
-        for (int c = 0; c < NH; ++c) {
-          const float mn = new_max(c);
-          any_scale |= (mn != -INFINITY && mn != old_max(c));
+        // One thread per column takes the new reference M' = max(M, tile max), writes it to refM, and leaves in
+        // the group's first two warp rows of red the column's offset for d (the old offset minus M') and its
+        // factor 2^(M - M') for l and O (1 where M is unchanged, M' = -inf or on a segment's first tile). Every
+        // thread then applies them with a few vector loops: the code runs cold, once per segment, so it is kept
+        // short, and each column's new reference is taken once, not in every loop that needs it.
+        float* rg = red + wg * 4 * 64 + col0;  // this group's 4 warp rows
+        bool scaled = false;
+        if (gt < NH) {
+          const float mo = seg_first ? -INFINITY : refM[col0 + gt];
+          const float mn = fmaxf(mo, fmaxf(fmaxf(rg[gt], rg[64 + gt]), fmaxf(rg[128 + gt], rg[192 + gt])));
+          scaled = !seg_first && mn != -INFINITY && mn != mo;
+          rg[gt] = (seg_first ? 0.f : mo) - mn;
+          rg[64 + gt] = scaled ? fast_exp2(mo - mn) : 1.f;
+          refM[col0 + gt] = mn;
         }
-        if (any_scale && !seg_first) {
+        // the group's OR, and the barrier that orders the writes above before the reads below
+        if (named_or(bar_or, 128, scaled)) {
           if (gt == 0) atomicAdd(p.err + kWsRescaleWord, 1u);  // diagnostic count of O rescales
           wait(&pfree[(i - 1) % C::PB], static_cast<uint32_t>((i - 1) / C::PB) & 1u);  // PV of tile i-1 done
           tc::fence_after_sync();
+#pragma unroll 1
+          for (int hc = 0; hc < C::kMh * (C::kStackP ? 2 : 1) * NH; hc += 8) {
+            const int h = hc / ((C::kStackP ? 2 : 1) * NH), rem = hc - h * (C::kStackP ? 2 : 1) * NH;
+            const int pt = rem / NH, c0 = rem - pt * NH;  // O_hi, then O_lo 64 columns on
+            const uint32_t ta = tO + C::kOCols * h + 64 * pt + lane_off + col0 + c0;
+            uint32_t r8[8];
+            tc::ld8(ta, r8);
+            tc::wait_ld();
 #pragma unroll
-          for (int h = 0; h < C::kMh; ++h)
-#pragma unroll
-            for (int pt = 0; pt < (C::kStackP ? 2 : 1); ++pt)  // O_hi, then O_lo 64 columns on
-#pragma unroll
-              for (int c0 = 0; c0 < NH; c0 += 8) {
-                const uint32_t ta = tO + C::kOCols * h + 64 * pt + lane_off + col0 + c0;
-                uint32_t r8[8];
-                tc::ld8(ta, r8);
-                tc::wait_ld();
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float mn = new_max(c0 + j), mo = old_max(c0 + j);
-                  const float a = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
-                  r8[j] = __float_as_uint(__uint_as_float(r8[j]) * a);
-                }
-                tc::st8(ta, r8);
-              }
+            for (int j = 0; j < 8; ++j) r8[j] = __float_as_uint(__uint_as_float(r8[j]) * rg[64 + c0 + j]);
+            tc::st8(ta, r8);
+          }
           tc::wait_st();
         }
 #pragma unroll
-        for (int c = 0; c < NH; ++c) {
-          const float mn = new_max(c), mo = old_max(c);
-          if (mn != -INFINITY && mn != mo) {
-            float& lc = (c & 1) ? l[c >> 1].y : l[c >> 1].x;
-            lc *= fast_exp2(mo - mn);
-            if constexpr (kRegs) {
-              if (c & 1) negm[(c >> 1) % kRP].y = -mn; else negm[(c >> 1) % kRP].x = -mn;
-            }
-          }
-        }
+        for (int c = 0; c < NH / 2; ++c) {
+          l[c] = __fmul2_rn(l[c], reinterpret_cast<const float2*>(rg + 64)[c]);
+          if constexpr (kRegs) {
+            const float2 m = reinterpret_cast<const float2*>(refM + col0)[c];
+            negm[c % kRP] = make_float2(-m.x, -m.y);
 #pragma unroll
-        for (int h = 0; h < SUB; ++h)
+            for (int h = 0; h < SUB; ++h) dl[h][c] = __fadd2_rn(y[h][c], negm[c % kRP]);
+          } else {
+            const float2 dd = reinterpret_cast<const float2*>(rg)[c];
 #pragma unroll
-          for (int c = 0; c < NH / 2; ++c) {
-            if constexpr (kRegs) {
-              dl[h][c] = __fadd2_rn(y[h][c], negm[c % kRP]);
-            } else {
-              const float o0 = seg_first ? 0.f : mref[2 * c], o1 = seg_first ? 0.f : mref[2 * c + 1];
-              dl[h][c] = __fadd2_rn(dl[h][c], make_float2(o0 - new_max(2 * c), o1 - new_max(2 * c + 1)));
-            }
+            for (int h = 0; h < SUB; ++h) dl[h][c] = __fadd2_rn(dl[h][c], dd);
           }
-        if constexpr (!kRegs) {
-          // every thread of the group has read the old references: one thread per column writes the new one
-          const float mine = gt < NH ? new_max(gt) : 0.f;
-          named_sync(bar_sync, 128);
-          if (gt < NH) refM[col0 + gt] = mine;
-          named_sync(bar_sync, 128);
         }
         // red is rewritten only after the next vote (a barrier of this group), when every read here is done
       }
@@ -1026,14 +1007,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
           const float* rl = redl + wg * 4 * 64 + cc;
           const float s2 = (rl[0] + rl[64]) + (rl[128] + rl[192]);
           rinv[cc] = s2 > 0.f ? __frcp_rn(s2) : 0.f;
-          float mg = kRegs ? -INFINITY : refM[cc];  // this column's reference max
-          if constexpr (kRegs) {
-#pragma unroll
-            for (int c = 0; c < NH / 2; ++c) {
-              if (2 * c == gt) mg = -negm[c % kRP].x;
-              if (2 * c + 1 == gt) mg = -negm[c % kRP].y;
-            }
-          }
+          const float mg = refM[cc];  // this column's reference max (a column without a finite score has s2 = 0)
           const int pr = row_of_col(cc);
           if (ok_sm && !whole && pr < rows)
             p.part_lse[u * p.rows_max + pr] = s2 > 0.f ? mg + __log2f(s2) : -INFINITY;
