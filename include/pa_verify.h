@@ -96,22 +96,27 @@ enum { PA_KERNEL_AUTO = 0, PA_KERNEL_WARP_MMA = 1, PA_KERNEL_TCGEN05 = 2 };
 /*
  * Two plan kinds. Chunk plans (warp-MMA kernel): one CTA per (sequence, KV
  * head, chunk of chunk_tokens). Flat plans (tcgen05 kernel): the (sequence,
- * KV head) pairs laid end to end as 128-token tiles and cut into one wave of
- * consecutive CTA ranges. A static plan picks the ranges that minimise the
- * largest CTA cost, counting tiles plus ten tiles for every move to another
- * pair inside a range (pa_verify_plan_get_cta_starts returns them); with
- * split_override, and in dynamic plans, every CTA gets the same number of
- * tiles (chunk_tokens / 128 of them). Either way one wave ends together
- * whatever the length mix.
+ * KV head) pairs laid end to end as tiles of tile_tokens and cut into one wave
+ * of consecutive CTA ranges. A static plan picks the ranges that minimise the
+ * largest CTA cost, counting tiles plus, for every move to another pair inside
+ * a range, a switch cost measured per kernel instance (about 2 tiles at 16
+ * rows, 5 to 10 at 48, 13 to 20 at 64); pa_verify_plan_get_cta_starts returns
+ * them. With split_override, and in dynamic plans, every CTA gets the same
+ * number of tiles (chunk_tokens / tile_tokens of them). Either way one wave
+ * ends together whatever the length mix. A static FP8 plan at head_dim 128
+ * whose batch mixes pairs of up to 48 rows with pairs of more makes two such
+ * cuts, one per class, and runs them as two launches (info.launches).
  */
 typedef struct {
   int32_t num_units;       /* CTAs of the split kernel: chunk plans sum_b Hkv * ceil(L_b / chunk),
                               flat plans the number of ranges (at most one per SM) */
   int32_t chunk_tokens;    /* chunk plans: context tokens per unit (a multiple of tile_tokens);
-                              flat plans: 128 x the largest range cost (tiles, switches counted
-                              as ten), or 128 x the tiles per CTA of an even cut; dynamic
-                              plans 0 (the device picks it each run) */
-  int32_t tile_tokens;     /* tokens per shared-memory stage (flat plans: 128) */
+                              flat plans: tile_tokens x the largest range cost (in tiles, a
+                              switch of pair counted at the instance's switch cost), or
+                              tile_tokens x the tiles per CTA of an even cut; dynamic plans 0
+                              (the device picks it each run) */
+  int32_t tile_tokens;     /* tokens per shared-memory stage (flat plans: 256 for FP8 K/V at head_dim
+                              128 with up to 48 rows, else 128) */
   int32_t rows_max;        /* max_b q_b * G */
   int32_t warps;           /* compute warps per CTA = ceil(rows_max / 16) (warp-MMA kernel) */
   int32_t max_splits;      /* most units one (sequence, KV head) is spread over */
@@ -122,11 +127,20 @@ typedef struct {
   int32_t kernel;          /* PA_KERNEL_WARP_MMA or PA_KERNEL_TCGEN05 */
   int32_t dynamic;         /* 1 for pa_verify_plan_dynamic plans (figures above are capacities) */
   int32_t flat;            /* 1 for flat plans */
-  int32_t total_tiles;     /* flat plans: sum_b Hkv * ceil(L_b / 128) (dynamic plans: chosen per run, 0 here) */
+  int32_t total_tiles;     /* flat plans: sum_b Hkv * ceil(L_b / tile_tokens) (dynamic plans: chosen per
+                              run, 0 here) */
   int32_t device_table;    /* 1: each run builds the work table on the device from the device lengths
                               (a one-CTA planner kernel ahead of the split kernel): dynamic plans, and
                               plans of more than 64 sequences, whose table does not fit the kernel
                               parameters */
+  int32_t launches;        /* split-kernel launches a run makes: 2 for a static FP8 head_dim-128 plan
+                              whose batch mixes pairs of up to 48 rows with pairs of more (each
+                              class on its own kernel instance, one combine after both); else 1.
+                              num_units and total_tiles then count both launches; the rest of the
+                              figures describe the first launch (pa_verify_plan_get_second) */
+  int32_t split_pairs;     /* static plans: (sequence, KV head) pairs spread over more than one unit,
+                              i.e. the pairs the combine merges, over both launches; -1 when they
+                              are not listed (more than 256, or a device-built table) */
 } pa_verify_plan_info;
 
 /*
@@ -180,12 +194,24 @@ int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info);
 
 /*
  * A static flat plan's CTA ranges: starts_out[c] is CTA c's first tile and
- * starts_out[num_units] = total_tiles (tile t = 128 tokens of the t-th place
- * in the flat order of (sequence, KV head) pairs). Writes num_units + 1
- * values and returns that count; PA_ERR_INVALID for other plans or when
- * `capacity` is smaller. Host only, no CUDA call.
+ * starts_out[n] = the launch's tiles, n = its CTAs (tile t = tile_tokens
+ * tokens of the t-th place in the flat order of (sequence, KV head) pairs).
+ * Writes n + 1 values and returns that count; PA_ERR_INVALID for other plans
+ * or when `capacity` is smaller. For a two-launch plan these are the first
+ * launch's ranges (the second's: pa_verify_plan_get_second). Host only, no
+ * CUDA call.
  */
 int pa_verify_plan_get_cta_starts(pa_verify_plan_t plan, int32_t* starts_out, int32_t capacity);
+
+/*
+ * The second launch of a two-launch plan (info.launches == 2), NULL for
+ * other plans. The handle is owned by `plan`: pass it only to
+ * pa_verify_plan_get_info and pa_verify_plan_get_cta_starts (its figures
+ * describe that launch alone), never to pa_verify_run or pa_verify_free.
+ * Host only. No counterpart in the pages: it exposes the planner's split of
+ * a mixed batch for tests and tuning.
+ */
+pa_verify_plan_t pa_verify_plan_get_second(pa_verify_plan_t plan);
 
 /*
  * Enqueues verify attention on `stream` and returns without waiting: the split

@@ -47,6 +47,11 @@ struct pa_verify_plan_s {
   int32_t tile = 0, chunk = 0, units = 0, rows_max = 0, warps = 0, max_splits = 0, needs_combine = 0;
   int32_t num_tokens = 0, num_rows = 0;
   int32_t kernel = PA_KERNEL_WARP_MMA;
+  int32_t n_entries = -1;        // entries of seq[] (-1: one per sequence of the batch)
+  int32_t part_rows = 0;         // row stride of the partials (0: rows_max)
+  int32_t slot_base = 0;         // first partial slot of this launch
+  int32_t batch_rows = 0;        // rows of the whole batch, when this plan covers part of it
+  pa_verify_plan_s* second = nullptr;  // two-launch plans: the second launch (sequences with more rows)
   int32_t dynamic = 0;           // capacity plan: the work table is built on the device each run
   int32_t host_lengths = 0;      // a capacity plan made by pa_verify_plan (more than kMaxSeqs sequences)
   int32_t flat = 0, per = 0, total_tiles = 0;  // flat plans (tcgen05 kernel): tiles per CTA, tiles in all
@@ -154,6 +159,20 @@ int encode_maps(pa_verify_plan_t plan, const void* k_cache, const void* v_cache)
   return PA_OK;
 }
 
+// The fields that differ between the launches of a two-launch plan: its work table and CTA ranges.
+void set_launch_fields(SplitParams& p, const pa_verify_plan_s* plan) {
+  p.num_seqs = plan->n_entries >= 0 ? plan->n_entries : plan->d.num_seqs;
+  p.chunk = plan->chunk;
+  p.num_units = plan->units;
+  p.flat = plan->flat;
+  p.per = plan->per;
+  p.total_tiles = plan->total_tiles;
+  p.ranged = plan->ranged;
+  if (plan->ranged) std::memcpy(p.cta_start, plan->cta_start, sizeof(int32_t) * (plan->units + 1));
+  p.slot_base = plan->slot_base;
+  std::memcpy(p.seq, plan->seq, sizeof(plan->seq));
+}
+
 void fill_params(SplitParams& p, pa_verify_plan_t plan, const void* q, const float* k_scale, const float* v_scale,
                  const int32_t* block_table, const int32_t* context_lens, const int32_t* query_lens,
                  float softmax_scale, void* out, uint8_t* ws) {
@@ -172,26 +191,18 @@ void fill_params(SplitParams& p, pa_verify_plan_t plan, const void* q, const flo
   p.dyn = plan->dynamic ? reinterpret_cast<const DynWork*>(ws + plan->off_dyn) : nullptr;
   p.dev_ctx = context_lens;
   p.dev_q = query_lens;
-  p.num_seqs = d.num_seqs;
   p.num_q_heads = d.num_q_heads;
   p.num_kv_heads = d.num_kv_heads;
   p.group = d.num_q_heads / d.num_kv_heads;
   p.bt_stride = d.block_table_stride;
   p.num_pages = d.num_pages;
-  p.chunk = plan->chunk;
-  p.num_units = plan->units;
-  p.rows_max = plan->rows_max;
+  p.rows_max = plan->part_rows > 0 ? plan->part_rows : plan->rows_max;
   p.out_f32 = d.out_dtype == PA_OUT_F32 ? 1 : 0;
   p.num_rows = plan->num_rows;
-  p.flat = plan->flat;
-  p.per = plan->per;
-  p.total_tiles = plan->total_tiles;
-  p.ranged = plan->ranged;
-  if (plan->ranged) std::memcpy(p.cta_start, plan->cta_start, sizeof(int32_t) * (plan->units + 1));
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
   p.wait_limit_ns = plan->wait_limit_ns;
   p.stall_cta = plan->stall_cta;
-  std::memcpy(p.seq, plan->seq, sizeof(plan->seq));
+  set_launch_fields(p, plan);
 }
 
 // Enqueues (dynamic plans: the device planner, then) the split kernel and the
@@ -211,6 +222,13 @@ cudaError_t launch_all(pa_verify_plan_t plan, SplitParams& p, cudaStream_t s, bo
             ? launch_tc_split(d.head_dim, fp8 ? 1 : 0, plan->rows_max, plan->units, &plan->tmk, &plan->tmv, &p, s)
         : fp8 ? launch_split_fp8(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s)
               : launch_split_bf16(d.head_dim, plan->warps, plan->units, &plan->tmk, &plan->tmv, &p, s);
+  if (e == cudaSuccess && plan->second) {
+    // two-launch plan: the sequences with more rows, on their own instance, into the same workspace
+    SplitParams p2 = p;
+    set_launch_fields(p2, plan->second);
+    e = launch_tc_split(d.head_dim, fp8 ? 1 : 0, plan->second->rows_max, plan->second->units, &plan->tmk, &plan->tmv,
+                        &p2, s);
+  }
   const bool combine = plan->needs_combine != 0;
   if (e == cudaSuccess && prof) e = cudaEventRecord(plan->ev[1], s);
   if (e == cudaSuccess && combine) {
@@ -245,7 +263,8 @@ void list_split_pairs(pa_verify_plan_s* P, int hkv, int G, const std::vector<int
                       const std::vector<int32_t>& n) {
   int32_t cnt = 0, rows = 0;
   bool fits = true;
-  for (int k = 0; k < P->d.num_seqs; ++k)
+  const int n_ent = P->n_entries >= 0 ? P->n_entries : P->d.num_seqs;
+  for (int k = 0; k < n_ent; ++k)
     for (int g = 0; g < hkv; ++g) {
       const int pr = k * hkv + g;
       if (n[pr] <= 1) continue;
@@ -335,14 +354,18 @@ int64_t pack_ranges(const std::vector<int64_t>& nt, const std::vector<int64_t>& 
 // (`split_override` = n asks for ceil(longest pair / n) tiles per CTA instead,
 // and so do plans needing more CTAs than the range table holds.)
 int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, const int32_t* ql, int sms,
-              pa_verify_plan_t* plan_out, size_t* workspace_bytes_out) {
+              pa_verify_plan_t* plan_out, size_t* workspace_bytes_out, const std::vector<char>* member = nullptr) {
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
   const int G = d.num_q_heads / d.num_kv_heads, Hkv = d.num_kv_heads;
+  // the sequences this plan covers (all, or those of `member`); q offsets stay the batch's
+  std::vector<int> order;
+  for (int b = 0; b < d.num_seqs; ++b)
+    if (!member || (*member)[b]) order.push_back(b);
+  const int n_ent = static_cast<int>(order.size());
+  P->n_entries = n_ent;  // before anything walks the table (list_split_pairs)
   int rows_all = 0;
-  for (int b = 0; b < d.num_seqs; ++b) rows_all = std::max(rows_all, ql[b] * G);
+  for (int b : order) rows_all = std::max(rows_all, ql[b] * G);
   const int T = tc_tile_tokens(fp8 ? 1 : 0, d.head_dim, tc_rows_pad(rows_all));  // tokens per tile
-  std::vector<int> order(d.num_seqs);
-  for (int b = 0; b < d.num_seqs; ++b) order[b] = b;
   std::stable_sort(order.begin(), order.end(), [&](int a, int c) { return ctx[a] > ctx[c]; });
   std::vector<int32_t> q_off(d.num_seqs);
   int32_t acc = 0;
@@ -352,7 +375,7 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
   }
   int64_t tiles = 0, row = 0, work = 0, max_nt = 0, total_tokens = 0;
   int rows_max = 0;
-  for (int k = 0; k < d.num_seqs; ++k) {
+  for (int k = 0; k < n_ent; ++k) {
     const int b = order[k];
     SeqInfo& s = P->seq[k];
     s.ctx_len = ctx[b];
@@ -385,7 +408,7 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
     const int64_t sw = switch_cost(fp8, d.head_dim, np);
     std::vector<int64_t> nt, w;
     int64_t total = 0, w_max = 0;
-    for (int k = 0; k < d.num_seqs; ++k)
+    for (int k = 0; k < n_ent; ++k)
       for (int g = 0; g < Hkv; ++g) {
         nt.push_back(P->seq[k].n_tiles);
         w.push_back(tile_cost(np, P->seq[k].q_len * G));
@@ -414,8 +437,8 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
                                 P->cta_start) - 1;
   };
   int max_splits = 0;
-  std::vector<int32_t> pu0(static_cast<size_t>(d.num_seqs) * Hkv), pn(pu0.size());
-  for (int k = 0; k < d.num_seqs; ++k)
+  std::vector<int32_t> pu0(static_cast<size_t>(n_ent) * Hkv), pn(pu0.size());
+  for (int k = 0; k < n_ent; ++k)
     for (int g = 0; g < Hkv; ++g) {
       const int64_t t0 = P->seq[k].tile_start + static_cast<int64_t>(g) * P->seq[k].n_tiles;
       const int64_t t1 = t0 + P->seq[k].n_tiles - 1;
@@ -438,7 +461,7 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
   P->needs_combine = max_splits > 1 ? 1 : 0;
   P->num_tokens = static_cast<int32_t>(total_tokens);
   P->num_rows = static_cast<int32_t>(row);
-  P->part_units = n_cta + static_cast<int64_t>(d.num_seqs) * Hkv;  // slot c + p < CTAs + pairs
+  P->part_units = n_cta + static_cast<int64_t>(n_ent) * Hkv;  // slot c + p < CTAs + pairs
   P->kv_bytes = work * (fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim));
   size_t ws = kWsHeader;
   if (P->needs_combine) {
@@ -448,6 +471,86 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
     ws += align_up(static_cast<size_t>(P->part_units) * rows_max * 4, 256);
   }
   P->ws_bytes = ws;
+  *plan_out = P;
+  *workspace_bytes_out = ws;
+  return PA_OK;
+}
+
+// Two-launch plan for a batch that mixes pairs of up to 48 rows with pairs of
+// more (FP8 K/V at head_dim 128): each class gets its own flat plan and kernel
+// instance (256-token tiles up to 48 rows, the 64-row instance above), launched
+// one after the other into one workspace, followed by one combine over both.
+// Measured on GB300 (the mixed FP8 batch, µs a call): one launch of the 64-row
+// instance 230; the two classes alone 136 and 79, back to back about 215. The
+// second launch's partial slots follow the first's; both use the larger row
+// stride. Falls back to one launch when the merged combine table does not fit.
+int plan_two_launch(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, const int32_t* ql, int sms,
+                    pa_verify_plan_t* plan_out, size_t* workspace_bytes_out) {
+  const int G = d.num_q_heads / d.num_kv_heads;
+  const pa_verify_desc dd = P->d;
+  std::vector<char> lo(d.num_seqs, 0), hi(d.num_seqs, 0);
+  for (int b = 0; b < d.num_seqs; ++b) (ql[b] * G <= 48 ? lo : hi)[b] = 1;
+  pa_verify_plan_s* B = new (std::nothrow) pa_verify_plan_s();
+  if (!B) {
+    delete P;
+    return fail(PA_ERR_NOMEM, "out of host memory");
+  }
+  B->d = dd;
+  pa_verify_plan_t pa = nullptr, pb = nullptr;
+  size_t wa = 0, wb = 0;
+  int rc = plan_flat(P, d, ctx, ql, sms, &pa, &wa, &lo);  // deletes P on failure
+  if (rc != PA_OK) {
+    delete B;
+    return rc;
+  }
+  rc = plan_flat(B, d, ctx, ql, sms, &pb, &wb, &hi);
+  if (rc != PA_OK) {
+    delete P;
+    return rc;
+  }
+  const bool comb = P->needs_combine || B->needs_combine;
+  if (comb && (P->n_split_pairs < 0 || B->n_split_pairs < 0 ||
+               P->n_split_pairs + B->n_split_pairs > kMaxCombinePairs)) {
+    delete P;
+    delete B;
+    pa_verify_plan_s* S = new (std::nothrow) pa_verify_plan_s();
+    if (!S) return fail(PA_ERR_NOMEM, "out of host memory");
+    S->d = dd;
+    return plan_flat(S, d, ctx, ql, sms, plan_out, workspace_bytes_out);
+  }
+  const int stride = std::max(P->rows_max, B->rows_max);
+  B->slot_base = static_cast<int32_t>(P->part_units);
+  const int64_t units_all = P->part_units + B->part_units;
+  if (comb) {
+    for (int j = 0; j < B->n_split_pairs; ++j) {
+      CombinePair c = B->split_pairs[j];
+      c.u0 += B->slot_base;
+      c.row_base += P->split_rows;
+      P->split_pairs[P->n_split_pairs++] = c;
+    }
+    P->split_rows += B->split_rows;
+  }
+  size_t ws = kWsHeader;
+  if (comb) {
+    P->off_part = ws;
+    ws += align_up(static_cast<size_t>(units_all) * stride * d.head_dim * 4, 256);
+    P->off_lse = ws;
+    ws += align_up(static_cast<size_t>(units_all) * stride * 4, 256);
+  }
+  for (pa_verify_plan_s* X : {P, B}) {
+    X->part_rows = stride;
+    X->needs_combine = comb ? 1 : 0;
+    X->off_part = P->off_part;
+    X->off_lse = P->off_lse;
+    X->ws_bytes = ws;
+  }
+  P->max_splits = std::max(P->max_splits, B->max_splits);
+  P->part_units = units_all;
+  P->num_tokens += B->num_tokens;
+  P->num_rows += B->num_rows;
+  P->kv_bytes += B->kv_bytes;
+  P->batch_rows = stride;
+  P->second = B;
   *plan_out = P;
   *workspace_bytes_out = ws;
   return PA_OK;
@@ -610,7 +713,13 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
     for (int b = 0; b < d.num_seqs; ++b) u += (context_lens_host[b] + c - 1) / c;
     return u * d.num_kv_heads;
   };
-  if (use_tc) return plan_flat(P, d, context_lens_host, query_lens_host, sms, plan_out, workspace_bytes_out);
+  if (use_tc) {
+    bool low = false, high = false;
+    for (int b = 0; b < d.num_seqs; ++b) (query_lens_host[b] * G <= 48 ? low : high) = true;
+    if (fp8 && d.head_dim == 128 && d.split_override == 0 && low && high)
+      return plan_two_launch(P, d, context_lens_host, query_lens_host, sms, plan_out, workspace_bytes_out);
+    return plan_flat(P, d, context_lens_host, query_lens_host, sms, plan_out, workspace_bytes_out);
+  }
   const int64_t max_tile_len = align_up(static_cast<size_t>(max_len), static_cast<size_t>(tile));
   int64_t chunk;
   if (d.split_override > 0) {
@@ -706,10 +815,10 @@ int pa_verify_plan_get_cta_starts(pa_verify_plan_t plan, int32_t* starts_out, in
 
 int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info) {
   if (!plan || !info) return fail(PA_ERR_INVALID, "plan and info must not be NULL");
-  info->num_units = plan->units;
+  info->num_units = plan->units + (plan->second ? plan->second->units : 0);
   info->chunk_tokens = plan->chunk;
   info->tile_tokens = plan->tile;
-  info->rows_max = plan->rows_max;
+  info->rows_max = plan->batch_rows > 0 ? plan->batch_rows : plan->rows_max;
   info->warps = plan->warps;
   info->max_splits = plan->max_splits;
   info->needs_combine = plan->needs_combine;
@@ -720,9 +829,13 @@ int pa_verify_plan_get_info(pa_verify_plan_t plan, pa_verify_plan_info* info) {
   info->dynamic = plan->dynamic && !plan->host_lengths;
   info->device_table = plan->dynamic;
   info->flat = plan->flat;
-  info->total_tiles = plan->dynamic ? 0 : plan->total_tiles;
+  info->total_tiles = plan->dynamic ? 0 : plan->total_tiles + (plan->second ? plan->second->total_tiles : 0);
+  info->launches = plan->second ? 2 : 1;
+  info->split_pairs = plan->dynamic ? -1 : plan->n_split_pairs;
   return PA_OK;
 }
+
+pa_verify_plan_t pa_verify_plan_get_second(pa_verify_plan_t plan) { return plan ? plan->second : nullptr; }
 
 int pa_verify_run(pa_verify_plan_t plan, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                   const float* v_scale, const int32_t* block_table, const int32_t* context_lens,
@@ -924,6 +1037,7 @@ void pa_verify_free(pa_verify_plan_t plan) {
   if (!plan) return;
   for (auto& e : plan->ev)
     if (e) cudaEventDestroy(e);
+  delete plan->second;
   delete plan;
 }
 

@@ -93,7 +93,8 @@ struct SplitParams {
   int32_t num_pages;
   int32_t chunk;
   int32_t num_units;
-  int32_t rows_max;
+  int32_t rows_max;             // row stride of the partials
+  int32_t slot_base;            // flat plans: first partial slot of this launch (CTA c, pair p: slot_base + c + p)
   int32_t out_f32;
   int32_t num_rows;             // sum_b q_b * Hq (combine grid)
   int32_t flat;                 // 1: flat plan (tiles per CTA), 0: chunk plan

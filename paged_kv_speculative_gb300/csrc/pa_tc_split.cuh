@@ -1000,7 +1000,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
         named_sync(bar_sync, 128);
         const int rows = cu.QL * G;
         const bool whole = seg_t0 == 0 && pair_last;  // the segment is the whole pair: no combine
-        const size_t u = static_cast<size_t>(cta) + cu.pair(Hkv);
+        const size_t u = static_cast<size_t>(p.slot_base) + cta + cu.pair(Hkv);
         float* rinv = red + 4 * C::NWG * 64;  // 1 / row total (0 for an empty row)
         if (gt < NH) {
           const int cc = col0 + gt;

@@ -43,7 +43,7 @@ EXPORTED = ("pa_verify_plan", "pa_verify_plan_get_info", "pa_verify_run", "pa_ve
             "pa_verify_device_errors", "pa_verify_last_error", "pa_verify_profile_enable",
             "pa_verify_profile_read", "pa_kv_write", "pa_greedy_verdict_workspace_bytes",
             "pa_greedy_verdict", "pa_verify_run_static", "pa_verify_plan_dynamic", "pa_verify_plan_get_cta_starts",
-            "pa_verify_debug_stall")
+            "pa_verify_debug_stall", "pa_verify_plan_get_second")
 
 
 class PaVerifyError(RuntimeError):
@@ -68,7 +68,8 @@ class PlanInfo(ctypes.Structure):
         ("rows_max", ctypes.c_int32), ("warps", ctypes.c_int32), ("max_splits", ctypes.c_int32),
         ("needs_combine", ctypes.c_int32), ("num_tokens", ctypes.c_int32), ("kv_bytes", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_size_t), ("kernel", ctypes.c_int32), ("dynamic", ctypes.c_int32),
-        ("flat", ctypes.c_int32), ("total_tiles", ctypes.c_int32), ("device_table", ctypes.c_int32)]
+        ("flat", ctypes.c_int32), ("total_tiles", ctypes.c_int32), ("device_table", ctypes.c_int32),
+        ("launches", ctypes.c_int32), ("split_pairs", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -96,6 +97,8 @@ def lib(path: Optional[str] = None):
     L.pa_verify_plan_get_info.restype = ctypes.c_int
     L.pa_verify_plan_get_cta_starts.argtypes = [vp, i32p, ctypes.c_int32]
     L.pa_verify_plan_get_cta_starts.restype = ctypes.c_int
+    L.pa_verify_plan_get_second.argtypes = [vp]
+    L.pa_verify_plan_get_second.restype = vp
     L.pa_verify_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     L.pa_verify_run.restype = ctypes.c_int
     L.pa_verify_run_static.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
@@ -135,13 +138,23 @@ def _check(status: int):
 class Plan:
     """A host-side plan (owns the C handle)."""
 
-    def __init__(self, handle: int, desc: Desc, workspace_bytes: int):
+    def __init__(self, handle: int, desc: Desc, workspace_bytes: int, owned: bool = True):
         self.handle = handle
         self.desc = desc
         self.workspace_bytes = workspace_bytes
+        self.owned = owned
         info = PlanInfo()
         _check(lib().pa_verify_plan_get_info(handle, ctypes.byref(info)))
         self.info = info
+
+    def second(self) -> Optional["Plan"]:
+        """The second launch of a two-launch plan (a view owned by this plan), or None."""
+        h = lib().pa_verify_plan_get_second(self.handle)
+        if not h:
+            return None
+        v = Plan(h, self.desc, self.workspace_bytes, owned=False)
+        v.parent = self  # keeps the owner alive while the view is used
+        return v
 
     def cta_starts(self) -> list:
         """A static flat plan's CTA ranges: CTA c covers flat tiles [s[c], s[c + 1])."""
@@ -151,9 +164,9 @@ class Plan:
         return list(buf[:n])
 
     def free(self):
-        if self.handle:
+        if self.handle and self.owned:
             lib().pa_verify_free(self.handle)
-            self.handle = None
+        self.handle = None
 
     def __del__(self):
         try:

@@ -19,7 +19,7 @@ def built():
 
 def header_symbols():
     txt = open(os.path.join(ROOT, "include", "pa_verify.h")).read()
-    return sorted(set(re.findall(r"^(?:int|void|size_t|const char\*)\s+(pa_\w+)\s*\(", txt, flags=re.M)))
+    return sorted(set(re.findall(r"^(?:int|void|size_t|const char\*|pa_verify_plan_t)\s+(pa_\w+)\s*\(", txt, flags=re.M)))
 
 
 def test_header_symbols_exported():
@@ -117,36 +117,64 @@ def flat_model(ctx, ql, hkv, sms, split_override=0, group=8, tile=128, kv=pv.KV_
     return pack(nt, w, sw, lo)[1], pairs, (lo, w, sw)
 
 
-def check_flat_plan(ctx, ql, hkv, split, sms=152, kv=pv.KV_BF16):
-    """The library's flat plan equals the model's ranges and keeps every invariant the kernels rely on."""
-    p = mk(ctx, ql, hq=8 * hkv, hkv=hkv, split_override=split, sms=sms, kv=kv)
-    i = p.info
+def check_launch(starts, chunk_tokens, ctx, ql, hkv, split, sms, kv):
+    """One launch's CTA ranges equal the model's and keep the invariants the kernels rely on; returns the
+    pairs' CTA spans."""
     T = tc_tile(kv, 128, 8 * max(ql))
-    assert i.flat == 1 and i.kernel == pv.KERNEL_TCGEN05 and i.tile_tokens == T
-    starts, pairs, bound = flat_model(ctx, ql, hkv, sms, split, tile=T, kv=kv)
-    assert p.cta_starts() == starts
-    assert i.total_tiles == hkv * sum(-(-c // T) for c in ctx) == starts[-1]
-    assert i.num_units == len(starts) - 1
+    m_starts, pairs, bound = flat_model(ctx, ql, hkv, sms, split, tile=T, kv=kv)
+    assert starts == m_starts
+    assert starts[-1] == hkv * sum(-(-c // T) for c in ctx)
     # the ranges tile the flat space once, without empty CTAs
     assert starts[0] == 0 and all(a < b for a, b in zip(starts, starts[1:]))
-    cta_of = lambda f: max(c for c in range(len(starts) - 1) if starts[c] <= f)
-    spans = [(cta_of(t0), cta_of(t0 + n - 1)) for t0, n in pairs]
-    assert i.max_splits == max(b - a + 1 for a, b in spans)
-    assert i.needs_combine == (i.max_splits > 1)
-    assert i.kv_bytes == sum(ctx) * hkv * (128 * 4 if kv == pv.KV_BF16 else 128 * 2 + 8)
-    # slot c + pair of each CTA's piece of a pair is unique, and below CTAs + pairs (the workspace's slots)
-    slots = [c + k for k, (a, b) in enumerate(spans) for c in range(a, b + 1)]
-    assert len(slots) == len(set(slots)) and max(slots) < i.num_units + len(spans)
+    n = len(starts) - 1
+    cta_of = lambda f: max(c for c in range(n) if starts[c] <= f)
+    spans = [(cta_of(t0), cta_of(t0 + nt - 1)) for t0, nt in pairs]
     if split == 0:
-        assert i.num_units <= sms
+        assert n <= sms
         # no CTA costs more than the bound, which the plan reports in whole tiles as the chunk
         tau, w, sw = bound
-        assert i.chunk_tokens // T == -(-tau // 32)
-        for c in range(i.num_units):
+        assert chunk_tokens // T == -(-tau // 32)
+        for c in range(n):
             cost = sw * (sum(1 for a, b in spans if a <= c <= b) - 1)
-            for k, (t0, n) in enumerate(pairs):
-                cost += w[k] * max(0, min(t0 + n, starts[c + 1]) - max(t0, starts[c]))
+            for k, (t0, nt) in enumerate(pairs):
+                cost += w[k] * max(0, min(t0 + nt, starts[c + 1]) - max(t0, starts[c]))
             assert cost <= tau
+    return spans
+
+
+def check_flat_plan(ctx, ql, hkv, split, sms=152, kv=pv.KV_BF16):
+    """The library's flat plan equals the model's ranges and keeps every invariant the kernels rely on. A batch
+    of FP8 pairs with up to 48 rows and pairs with more is planned as two launches, one per class."""
+    p = mk(ctx, ql, hq=8 * hkv, hkv=hkv, split_override=split, sms=sms, kv=kv)
+    i = p.info
+    assert i.flat == 1 and i.kernel == pv.KERNEL_TCGEN05
+    lo = [b for b in range(len(ctx)) if 8 * ql[b] <= 48]
+    two = kv == pv.KV_FP8_E4M3 and split == 0 and 0 < len(lo) < len(ctx)
+    assert i.launches == (2 if two else 1)
+    parts = [(p, list(range(len(ctx))))] if not two else [(p, lo), (p.second(), [b for b in range(len(ctx)) if b not in lo])]
+    slots, base, units, tiles, splits, n_split = [], 0, 0, 0, 0, 0
+    for part, mem in parts:
+        c_ctx, c_ql = [ctx[b] for b in mem], [ql[b] for b in mem]
+        starts = part.cta_starts()
+        T = tc_tile(kv, 128, 8 * max(c_ql))
+        assert part.info.tile_tokens == T
+        spans = check_launch(starts, part.info.chunk_tokens, c_ctx, c_ql, hkv, split, sms, kv)
+        n = len(starts) - 1
+        # slot base + c + pair of each CTA's piece of a pair: unique over both launches
+        slots += [base + c + k for k, (a, b) in enumerate(spans) for c in range(a, b + 1)]
+        base += n + len(spans)
+        units, tiles = units + n, tiles + starts[-1]
+        splits = max(splits, max(b - a + 1 for a, b in spans))
+        n_split += sum(1 for a, b in spans if b > a)
+    assert len(slots) == len(set(slots)) and max(slots) < base
+    assert i.split_pairs == n_split  # the combine's table lists every split pair of both launches
+    assert i.num_units == units and i.total_tiles == tiles
+    assert i.max_splits == splits and i.needs_combine == (splits > 1)
+    assert i.rows_max == 8 * max(ql)
+    assert i.kv_bytes == sum(ctx) * hkv * (128 * 4 if kv == pv.KV_BF16 else 128 * 2 + 8)
+    if two:
+        q = p.second()
+        assert q.info.launches == 1 and q.second() is None and q.info.workspace_bytes == i.workspace_bytes
 
 
 @pytest.mark.parametrize("kv", [pv.KV_BF16, pv.KV_FP8_E4M3], ids=["bf16", "fp8"])
@@ -332,6 +360,25 @@ def test_bf16_head_dim_256_plans_on_tensor_cores():
                                           (pv.KV_FP8_E4M3, 256, 6, 8, 128), (pv.KV_BF16, 64, 6, 8, 128)])
 def test_tensor_core_tile_sizes(kv, d, ql, hq, T):
     """Static and capacity plans agree on the kernel's tile: 256 tokens for FP8 at head_dim 128 up to 48 rows."""
-    assert mk([5000, 300], [ql, 1], hq=hq, d=d, kv=kv).info.tile_tokens == T
+    assert mk([5000, 300], [ql, ql], hq=hq, d=d, kv=kv).info.tile_tokens == T
     dyn = pv.plan_dynamic(hq, 1, d, kv, pv.OUT_BF16, 20000, 9400, 4, 150000, ql, sm_count=152)
     assert dyn.info.tile_tokens == T
+
+
+@pytest.mark.parametrize("kv,d,ql,split,launches", [
+    (pv.KV_FP8_E4M3, 128, [6, 8, 2], 0, 2),   # FP8 rows 48 / 64 / 16: one launch per class
+    (pv.KV_FP8_E4M3, 128, [6, 2, 1], 0, 1),   # every pair up to 48 rows
+    (pv.KV_FP8_E4M3, 128, [7, 8, 8], 0, 1),   # every pair above 48 rows
+    (pv.KV_FP8_E4M3, 128, [6, 8, 2], 3, 1),   # split_override keeps one launch
+    (pv.KV_FP8_E4M3, 256, [6, 8, 2], 0, 1),   # head_dim 256: one instance family
+    (pv.KV_BF16, 128, [6, 8, 2], 0, 1),       # bf16: one launch
+])
+def test_two_launch_plans_only_where_they_apply(kv, d, ql, split, launches):
+    p = mk([20000, 9000, 300], ql, hq=8, d=d, kv=kv, split_override=split)
+    assert p.info.launches == launches
+    assert (p.second() is not None) == (launches == 2)
+    if launches == 2:
+        q = p.second()
+        assert p.info.tile_tokens == 256 and q.info.tile_tokens == 128
+        assert q.info.rows_max == 64 and p.info.rows_max == 64
+        assert p.info.num_units == len(p.cta_starts()) - 1 + q.info.num_units

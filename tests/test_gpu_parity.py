@@ -251,3 +251,33 @@ def test_flat_plans_beyond_one_wave(kv, d, hq, hkv):
     assert va.info["num_units"] > torch.cuda.get_device_properties(0).multi_processor_count
     assert va.info["needs_combine"] == 1
     assert max_err(got, ref) <= TOL[kv]
+
+
+# --------------------------------------------------------------- two-launch plans
+@pytest.mark.parametrize("out_dtype", [pv.OUT_F32, pv.OUT_BF16], ids=["f32", "bf16"])
+def test_two_launch_plan_against_oracle(out_dtype):
+    """FP8 pairs of up to 48 rows and pairs of more, long enough that both classes split over several CTAs:
+    two split launches (256-token tiles, then the 64-row instance) into one workspace, one combine."""
+    prob = synth.make_problem([90000, 300, 50000, 70, 120000, 2500, 33], [6, 8, 2, 7, 8, 1, 8], 16, 2, 128,
+                              kv_dtype=synth.KV_FP8, seed=57)
+    ref = oracle.verify_attention(prob)
+    got, va = gpu_run(prob, out_dtype=out_dtype)
+    assert va.info["launches"] == 2 and va.info["needs_combine"] == 1
+    second = va.plan.second()
+    assert second.info.max_splits > 1 and va.info["max_splits"] > 1
+    assert max_err(got, ref) <= TOL[synth.KV_FP8] + (1e-2 if out_dtype == pv.OUT_BF16 else 0.0)
+
+
+def test_two_launch_plan_static_entry_point_matches():
+    """The entry point without a workspace runs both launches too, bit for bit the same output."""
+    prob = synth.make_problem([40000, 700, 25000, 9000], [7, 3, 8, 5], 16, 2, 128, kv_dtype=synth.KV_FP8, seed=58)
+    dev = to_device(prob)
+    va = pv.VerifyAttention(16, 2, 128, synth.KV_FP8, prob.num_pages, prob.block_table.shape[1],
+                            prob.context_lens.tolist(), prob.query_lens.tolist())
+    assert va.info["launches"] == 2
+    a = va(*dev.args(), prob.softmax_scale)
+    b = torch.empty_like(a)
+    pv.run_static(va.plan, *dev.args(), prob.softmax_scale, b)
+    torch.cuda.synchronize()
+    assert pv.device_errors(None) == 0
+    assert torch.equal(a, b)
