@@ -50,6 +50,7 @@ struct pa_verify_plan_s {
   int32_t n_entries = -1;        // entries of seq[] (-1: one per sequence of the batch)
   int32_t part_rows = 0;         // row stride of the partials (0: rows_max)
   int32_t slot_base = 0;         // first partial slot of this launch
+  int32_t rows_split = 0;        // some entry has two row halves (SeqInfo::halves)
   int32_t batch_rows = 0;        // rows of the whole batch, when this plan covers part of it
   pa_verify_plan_s* second = nullptr;  // two-launch plans: the second launch (sequences with more rows)
   int32_t dynamic = 0;           // capacity plan: the work table is built on the device each run
@@ -170,6 +171,7 @@ void set_launch_fields(SplitParams& p, const pa_verify_plan_s* plan) {
   p.ranged = plan->ranged;
   if (plan->ranged) std::memcpy(p.cta_start, plan->cta_start, sizeof(int32_t) * (plan->units + 1));
   p.slot_base = plan->slot_base;
+  p.rows_split = plan->rows_split;
   std::memcpy(p.seq, plan->seq, sizeof(plan->seq));
 }
 
@@ -260,24 +262,33 @@ cudaError_t launch_all(pa_verify_plan_t plan, SplitParams& p, cudaStream_t s, bo
 // Lists the split pairs of a plan built from host lengths for the combine's
 // table (in plan order); n_split_pairs stays -1 when they do not fit it.
 void list_split_pairs(pa_verify_plan_s* P, int hkv, int G, const std::vector<int32_t>& u0,
-                      const std::vector<int32_t>& n) {
+                      const std::vector<int32_t>& n, bool flat = false) {
   int32_t cnt = 0, rows = 0;
   bool fits = true;
   const int n_ent = P->n_entries >= 0 ? P->n_entries : P->d.num_seqs;
-  for (int k = 0; k < n_ent; ++k)
-    for (int g = 0; g < hkv; ++g) {
-      const int pr = k * hkv + g;
-      if (n[pr] <= 1) continue;
-      if (cnt == kMaxCombinePairs) { fits = false; break; }
-      CombinePair& c = P->split_pairs[cnt++];
-      c.u0 = u0[pr];
-      c.n = n[pr];
-      c.q_off = P->seq[k].q_off;
-      c.head0 = g * G;
-      c.rows = P->seq[k].q_len * G;
-      c.row_base = rows;
-      rows += c.rows;
-    }
+  for (int k = 0; k < n_ent && fits; ++k) {
+    const SeqInfo& s = P->seq[k];
+    const int hv = flat ? std::max(1, s.halves) : 1;
+    for (int g = 0; g < hkv && fits; ++g)
+      for (int h = 0; h < hv; ++h) {
+        // (virtual) pair index: flat plans number them from the entry's first one
+        const int pr = flat ? s.unit_start + g * hv + h : k * hkv + g;
+        if (n[pr] <= 1) continue;
+        if (cnt == kMaxCombinePairs) {
+          fits = false;
+          break;
+        }
+        CombinePair& c = P->split_pairs[cnt++];
+        c.u0 = u0[pr];
+        c.n = n[pr];
+        c.q_off = s.q_off;
+        c.head0 = g * G;
+        c.rows = hv > 1 ? std::min(64, s.q_len * G - 64 * h) : s.q_len * G;
+        c.row0 = 64 * h;
+        c.row_base = rows;
+        rows += c.rows;
+      }
+  }
   P->n_split_pairs = fits ? cnt : -1;
   P->split_rows = fits ? rows : 0;
 }
@@ -373,22 +384,26 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
     q_off[b] = acc;
     acc += ql[b];
   }
-  int64_t tiles = 0, row = 0, work = 0, max_nt = 0, total_tokens = 0;
+  int64_t tiles = 0, row = 0, work = 0, max_nt = 0, total_tokens = 0, vpairs = 0;
   int rows_max = 0;
+  bool split_rows = false;
   for (int k = 0; k < n_ent; ++k) {
     const int b = order[k];
     SeqInfo& s = P->seq[k];
     s.ctx_len = ctx[b];
     s.q_len = ql[b];
     s.q_off = q_off[b];
-    s.unit_start = 0;
+    const int hv = s.q_len * G > 64 ? 2 : 1;  // row halves: pairs of more than 64 rows are two virtual pairs
+    s.unit_start = static_cast<int32_t>(vpairs);
     s.row_start = static_cast<int32_t>(row);
     s.n_chunks = 0;
     s.b = b;
     s.tile_start = static_cast<int32_t>(std::min<int64_t>(tiles, INT32_MAX));
     s.n_tiles = (s.ctx_len + T - 1) / T;
-    s.pad = 0;
-    tiles += static_cast<int64_t>(s.n_tiles) * Hkv;
+    s.halves = hv;
+    tiles += static_cast<int64_t>(s.n_tiles) * Hkv * hv;
+    vpairs += static_cast<int64_t>(Hkv) * hv;
+    split_rows = split_rows || hv > 1;
     row += static_cast<int64_t>(s.q_len) * d.num_q_heads;
     work += static_cast<int64_t>(s.ctx_len) * Hkv;
     max_nt = std::max<int64_t>(max_nt, s.n_tiles);
@@ -409,12 +424,13 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
     std::vector<int64_t> nt, w;
     int64_t total = 0, w_max = 0;
     for (int k = 0; k < n_ent; ++k)
-      for (int g = 0; g < Hkv; ++g) {
-        nt.push_back(P->seq[k].n_tiles);
-        w.push_back(tile_cost(np, P->seq[k].q_len * G));
-        total += nt.back() * w.back();
-        w_max = std::max(w_max, w.back());
-      }
+      for (int g = 0; g < Hkv; ++g)
+        for (int h = 0; h < P->seq[k].halves; ++h) {
+          nt.push_back(P->seq[k].n_tiles);
+          w.push_back(tile_cost(np, std::min(64, P->seq[k].q_len * G - 64 * h)));
+          total += nt.back() * w.back();
+          w_max = std::max(w_max, w.back());
+        }
     // a bound of the whole cost always fits one CTA
     int64_t lo = std::max((total + sms - 1) / sms, w_max), hi = total + sw * static_cast<int64_t>(nt.size());
     while (lo < hi) {
@@ -437,17 +453,19 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
                                 P->cta_start) - 1;
   };
   int max_splits = 0;
-  std::vector<int32_t> pu0(static_cast<size_t>(n_ent) * Hkv), pn(pu0.size());
+  std::vector<int32_t> pu0(static_cast<size_t>(vpairs)), pn(pu0.size());
   for (int k = 0; k < n_ent; ++k)
-    for (int g = 0; g < Hkv; ++g) {
-      const int64_t t0 = P->seq[k].tile_start + static_cast<int64_t>(g) * P->seq[k].n_tiles;
-      const int64_t t1 = t0 + P->seq[k].n_tiles - 1;
-      const int pr = k * Hkv + g;
-      pn[pr] = static_cast<int32_t>(cta_of(t1) - cta_of(t0) + 1);
-      pu0[pr] = static_cast<int32_t>(cta_of(t0) + pr);  // CTA c writes pair p's partial at slot c + p
-      max_splits = std::max<int>(max_splits, pn[pr]);
-    }
-  list_split_pairs(P, Hkv, G, pu0, pn);
+    for (int g = 0; g < Hkv; ++g)
+      for (int h = 0; h < P->seq[k].halves; ++h) {
+        const int vp = g * P->seq[k].halves + h;  // virtual pair of the entry
+        const int64_t t0 = P->seq[k].tile_start + static_cast<int64_t>(vp) * P->seq[k].n_tiles;
+        const int64_t t1 = t0 + P->seq[k].n_tiles - 1;
+        const int pr = P->seq[k].unit_start + vp;
+        pn[pr] = static_cast<int32_t>(cta_of(t1) - cta_of(t0) + 1);
+        pu0[pr] = static_cast<int32_t>(cta_of(t0) + pr);  // CTA c writes pair p's partial at slot c + p
+        max_splits = std::max<int>(max_splits, pn[pr]);
+      }
+  list_split_pairs(P, Hkv, G, pu0, pn, true);
   P->kernel = PA_KERNEL_TCGEN05;
   P->flat = 1;
   P->tile = T;
@@ -461,14 +479,17 @@ int plan_flat(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t* ctx, 
   P->needs_combine = max_splits > 1 ? 1 : 0;
   P->num_tokens = static_cast<int32_t>(total_tokens);
   P->num_rows = static_cast<int32_t>(row);
-  P->part_units = n_cta + static_cast<int64_t>(n_ent) * Hkv;  // slot c + p < CTAs + pairs
+  P->part_units = n_cta + vpairs;  // slot c + p < CTAs + (virtual) pairs
+  P->rows_split = split_rows ? 1 : 0;
+  P->part_rows = split_rows ? 64 : 0;  // partials hold a virtual pair's rows
   P->kv_bytes = work * (fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim));
   size_t ws = kWsHeader;
   if (P->needs_combine) {
     P->off_part = ws;
-    ws += align_up(static_cast<size_t>(P->part_units) * rows_max * d.head_dim * 4, 256);
+    const int stride = split_rows ? 64 : rows_max;
+    ws += align_up(static_cast<size_t>(P->part_units) * stride * d.head_dim * 4, 256);
     P->off_lse = ws;
-    ws += align_up(static_cast<size_t>(P->part_units) * rows_max * 4, 256);
+    ws += align_up(static_cast<size_t>(P->part_units) * stride * 4, 256);
   }
   P->ws_bytes = ws;
   *plan_out = P;
@@ -518,7 +539,7 @@ int plan_two_launch(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t*
     S->d = dd;
     return plan_flat(S, d, ctx, ql, sms, plan_out, workspace_bytes_out);
   }
-  const int stride = std::max(P->rows_max, B->rows_max);
+  const int stride = std::max(P->part_rows > 0 ? P->part_rows : P->rows_max, B->part_rows > 0 ? B->part_rows : B->rows_max);
   B->slot_base = static_cast<int32_t>(P->part_units);
   const int64_t units_all = P->part_units + B->part_units;
   if (comb) {
@@ -549,7 +570,7 @@ int plan_two_launch(pa_verify_plan_s* P, const pa_verify_desc& d, const int32_t*
   P->num_tokens += B->num_tokens;
   P->num_rows += B->num_rows;
   P->kv_bytes += B->kv_bytes;
-  P->batch_rows = stride;
+  P->batch_rows = std::max(P->rows_max, B->rows_max);
   P->second = B;
   *plan_out = P;
   *workspace_bytes_out = ws;
@@ -681,15 +702,21 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
     *workspace_bytes_out = P->ws_bytes;
     return PA_OK;
   }
-  const bool tc_ok = d.head_dim >= 64 && rows_max <= 64;  // head_dim 64 (bf16), 128, 256 (FP8)
+  // Up to 64 rows a pair is one pass of the tcgen05 kernel; 65-128 rows are two row halves (virtual pairs), in
+  // static plans whose virtual pairs all fit the combine's table.
+  const bool halves_ok =
+      d.num_seqs <= kMaxSeqs && static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * 2 <= kMaxCombinePairs;
+  const bool tc_ok = d.head_dim >= 64 && (rows_max <= 64 || (rows_max <= 128 && halves_ok));
   if (d.kernel == PA_KERNEL_TCGEN05 && !tc_ok) {
     delete P;
-    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs q_len * group <= 64");
+    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs q_len * group <= 64, or <= 128 with at most 64 "
+                                    "sequences and 128 (sequence, KV head) pairs");
   }
   const bool use_tc = d.kernel == PA_KERNEL_TCGEN05 || (d.kernel == PA_KERNEL_AUTO && tc_ok);
   if (d.head_dim == 256 && !use_tc) {
     delete P;
-    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only (q_len * group <= 64)");
+    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only (q_len * group <= 64, or <= 128 "
+                                    "with at most 64 sequences and 128 (sequence, KV head) pairs)");
   }
   if (d.num_seqs > kMaxSeqs) {
     // the table is too large for the kernel parameters: the device planner builds it at each run
@@ -757,7 +784,7 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
     s.row_start = static_cast<int32_t>(row);
     s.n_chunks = static_cast<int32_t>((s.ctx_len + chunk - 1) / chunk);
     s.b = b;
-    s.pad = 0;
+    s.halves = 0;
     unit += static_cast<int64_t>(s.n_chunks) * d.num_kv_heads;
     row += static_cast<int64_t>(s.q_len) * d.num_q_heads;
     max_splits = std::max(max_splits, s.n_chunks);
@@ -1020,7 +1047,8 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
     return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs q_len * group <= 64");
   const bool use_tc = d.kernel == PA_KERNEL_TCGEN05 || (d.kernel == PA_KERNEL_AUTO && tc_ok);
   if (d.head_dim == 256 && !use_tc)
-    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only (q_len * group <= 64)");
+    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only (q_len * group <= 64, or <= 128 "
+                                    "with at most 64 sequences and 128 (sequence, KV head) pairs)");
   return build_capacity_plan(d, sms, max_context_len, max_query_len, use_tc, plan_out, workspace_bytes_out);
 }
 

@@ -103,12 +103,13 @@ __device__ __forceinline__ RowRef resolve_row(const CombineTable& t, int rho) {
     if (t.pair[mid].row_base <= rho) lo = mid; else hi = mid - 1;
   }
   const CombinePair cp = t.pair[lo];
-  const int r = rho - cp.row_base;
-  const int i = r / t.group;
+  const int r = rho - cp.row_base;          // row of the partials
+  const int R = cp.row0 + r;                // row of the pair's q_len * G rows
+  const int i = R / t.group;
   rr.n = cp.n;
   rr.r = r;
   rr.u0 = static_cast<size_t>(cp.u0);
-  rr.orow = static_cast<size_t>(cp.q_off + i) * t.num_q_heads + cp.head0 + (r - i * t.group);
+  rr.orow = static_cast<size_t>(cp.q_off + i) * t.num_q_heads + cp.head0 + (R - i * t.group);
   return rr;
 }
 

@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kPlanThreads) pa_dyn_plan_kernel(DynPlanArgs a
     si.b = src;
     si.tile_start = static_cast<int>(ts);
     si.n_tiles = n_tiles;
-    si.pad = 0;
+    si.halves = 0;
     dyn_seq(a.out)[r] = si;
   }
   if (b == 0) {

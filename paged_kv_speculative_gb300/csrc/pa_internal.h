@@ -47,13 +47,16 @@ struct SeqInfo {
   int32_t ctx_len;     // L_b
   int32_t q_len;       // q_b
   int32_t q_off;       // first row of sequence b in q / out (batch order)
-  int32_t unit_start;  // chunk plans: first work unit of this sequence (units: kv head major, then chunk)
+  int32_t unit_start;  // chunk plans: first work unit of this sequence (units: kv head major, then chunk);
+                       // flat plans with row halves: first virtual pair of this sequence
   int32_t row_start;   // first combine row of this sequence (q_len * Hq rows)
   int32_t n_chunks;    // chunk plans: ceil(L_b / chunk)
   int32_t b;           // index of the sequence in the caller's batch
-  int32_t tile_start;  // flat plans: first tile of head 0 (head g starts at tile_start + g * n_tiles)
+  int32_t tile_start;  // flat plans: first tile of head 0 (head g, row half h starts at
+                       // tile_start + (g * halves + h) * n_tiles)
   int32_t n_tiles;     // flat plans: ceil(L_b / tile) tiles per KV head (0 for a padded sequence)
-  int32_t pad;
+  int32_t halves;      // flat plans: row halves of each pair, 2 when q_len * G > 64 (rows 0-63, then the
+                       // rest: two virtual pairs, each a pass over the context); 0 or 1: one
 };
 
 // Work description written on the device by the planner kernel of a
@@ -95,6 +98,8 @@ struct SplitParams {
   int32_t num_units;
   int32_t rows_max;             // row stride of the partials
   int32_t slot_base;            // flat plans: first partial slot of this launch (CTA c, pair p: slot_base + c + p)
+  int32_t rows_split;           // flat plans: 1 when some entry has two row halves (pair p is then the entry's
+                                // unit_start + g * halves + h), else 0 (p = entry * Hkv + g)
   int32_t out_f32;
   int32_t num_rows;             // sum_b q_b * Hq (combine grid)
   int32_t flat;                 // 1: flat plan (tiles per CTA), 0: chunk plan
@@ -194,7 +199,8 @@ struct CombinePair {
   int32_t u0, n;      // first partial slot, partial count
   int32_t q_off;      // first token row of the sequence in q / out
   int32_t head0;      // first q head of the pair (kv head * G)
-  int32_t rows;       // q_len * G
+  int32_t rows;       // rows of the (virtual) pair: q_len * G, or one row half of it
+  int32_t row0;       // first row of the pair's q_len * G rows that it covers (64 for a second row half)
   int32_t row_base;   // combine rows of the pairs before this one
 };
 constexpr int kMaxCombinePairs = 256;  // split pairs a table can list (else every row is covered)

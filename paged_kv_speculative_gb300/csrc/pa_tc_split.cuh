@@ -144,9 +144,14 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 }
 
 // Position in a CTA's tile range: entry k of the work table (plan order), KV
-// head g, tile t of the pair, with the entry's figures.
+// head g, row half h, tile t of the (virtual) pair, with the entry's figures.
+// A pair of more than 64 rows is two virtual pairs, rows 0-63 and the rest,
+// each a pass over the context (the two run side by side in neighbouring
+// CTA ranges, so the second pass mostly finds the tiles in L2).
+// RH: the instance can meet row halves (the 64-row one); elsewhere h stays 0 and costs nothing.
+template <bool RH>
 struct TileCursor {
-  int k, g, t;
+  int k, g, h, t;
   int L, QL, q_off, b, n_t;
   __device__ __forceinline__ void load_seq(const WorkView& wv) {
     const SeqInfo& s = wv.seq[k];
@@ -156,23 +161,43 @@ struct TileCursor {
     b = s.b;
     n_t = s.n_tiles;
   }
+  // the entry's row halves (read from the table where needed: registers are scarce in these instances)
+  __device__ __forceinline__ int halves(const WorkView& wv) const { return RH ? max(1, wv.seq[k].halves) : 1; }
   __device__ __forceinline__ void seek(const WorkView& wv, int f) {
     k = flat_seq_of(wv, f);
     load_seq(wv);
     const int off = f - wv.seq[k].tile_start;
-    g = off / n_t;
-    t = off - g * n_t;
+    const int vp = off / n_t, nh = halves(wv);
+    g = vp / nh;
+    h = vp - g * nh;
+    t = off - vp * n_t;
   }
   // to the next tile; the caller guarantees the range has one
   __device__ __forceinline__ void advance(const WorkView& wv, int hkv) {
     if (++t < n_t) return;
     t = 0;
+    if constexpr (RH) {
+      if (++h < halves(wv)) return;
+      h = 0;
+    }
     if (++g < hkv) return;
     g = 0;
     ++k;
     load_seq(wv);
   }
-  __device__ __forceinline__ int pair(int hkv) const { return k * hkv + g; }
+  // index of the (virtual) pair: its partial slots and its place among the pairs
+  __device__ __forceinline__ int pair(const WorkView& wv, int hkv, bool split) const {
+    if constexpr (RH) {
+      if (split) return wv.seq[k].unit_start + g * halves(wv) + h;
+    }
+    return k * hkv + g;
+  }
+  // rows of this virtual pair, and the first of the pair's q_len * G rows it covers
+  __device__ __forceinline__ int rows(int G) const {
+    if constexpr (RH) return min(64, QL * G - 64 * h);
+    else return QL * G;
+  }
+  __device__ __forceinline__ int row0() const { return RH ? 64 * h : 0; }
 };
 
 template <int KV_FP8, int NP, int D, int SUB = 1>
@@ -180,6 +205,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
     pa_tc_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ SplitParams p) {
   using C = TcCfg<KV_FP8, NP, D, SUB>;
+  using Cursor = TileCursor<NP == 64>;  // row halves reach only the 64-row instances
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = sm + C::kOffK;
@@ -244,32 +270,32 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
   static_assert(kTilePages * kHalves <= 32, "one box per lane");
   const int jl = lane < kTilePages * kHalves ? lane / kHalves : kTilePages;
   constexpr int kSmArrive = 4 * C::NWG;         // softmax warps: arrivals on sfree, pfull and qready
-  auto npages = [&](const TileCursor& cq) {
+  auto npages = [&](const Cursor& cq) {
     return min(C::kTile / kPage, (cq.L - cq.t * C::kTile + kPage - 1) / kPage);
   };
   // this lane's raw page id for a tile (-1: no copy); checked against the pool when issued
-  auto fetch = [&](const TileCursor& cq) {
+  auto fetch = [&](const Cursor& cq) {
     return jl < npages(cq) ? __ldg(p.block_table + static_cast<size_t>(cq.b) * p.bt_stride + cq.t * (C::kTile / kPage) + jl)
                            : -1;
   };
   // a softmax warp's Q rows of a segment: column col0 + (warp - 2) % 4 + 4 m, D / 32 bf16 per lane
   using QV = typename std::conditional<(D > 128), uint4, typename std::conditional<(D == 128), uint2, uint32_t>::type>::type;
-  auto q_load = [&](const TileCursor& cq, QV (&wq)[kRowsPerWarp]) {
-    const int rows = cq.QL * G;
+  auto q_load = [&](const Cursor& cq, QV (&wq)[kRowsPerWarp]) {
+    const int rows = cq.rows(G);
 #pragma unroll
     for (int m = 0; m < kRowsPerWarp; ++m) {
       const int r = row_of_col(col0 + ((warp - 2) & 3) + 4 * m);
       wq[m] = QV{};
       if (r < rows) {
-        const int i = r / G;
+        const int R = cq.row0() + r, i = R / G;  // row of the pair: query i, head g G + R - i G
         wq[m] = *reinterpret_cast<const QV*>(
-            p.q + (static_cast<size_t>(cq.q_off + i) * p.num_q_heads + cq.g * G + (r - i * G)) * C::kD +
+            p.q + (static_cast<size_t>(cq.q_off + i) * p.num_q_heads + cq.g * G + (R - i * G)) * C::kD +
             (C::kD / 32) * lane);
       }
     }
   };
-  TileCursor cu0;  // producers: the first tile; softmax warps: the first segment
-  TileCursor cu1, cu2;  // producers: the next two tiles (their page ids are read ahead)
+  Cursor cu0;  // producers: the first tile; softmax warps: the first segment
+  Cursor cu1, cu2;  // producers: the next two tiles (their page ids are read ahead)
   int pg0 = -1, pg1 = -1, pg2 = -1;
   QV wq0[kRowsPerWarp];
   if (is_prod || is_sm) cu0.seek(wv, f_lo);
@@ -346,11 +372,11 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
     // Page ids are read three tiles ahead (cursors cu, c1, c2 for tiles k, k+1, k+2, rotated by value):
     // a tile's issue is much shorter than a load from the block table, so reading only the next tile's
     // ids would hold the ring to about one tile per memory latency.
-    TileCursor cu = cu0, c1 = cu1, c2 = cu2;
+    Cursor cu = cu0, c1 = cu1, c2 = cu2;
     int pg_raw = pg0, p1 = pg1, p2 = pg2;
     int issued = 0;
     for (int k = 0; k < n_tiles; ++k) {
-      TileCursor c3 = c2;
+      Cursor c3 = c2;
       int p3 = -1;
       if (k + 3 < n_tiles) {
         c3.advance(wv, Hkv);
@@ -456,7 +482,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
       // Each MMA's operand descriptors are its stage's base descriptor plus a constant (one add): the issue
       // cost of a thread per MMA is then close to the tensor core's own time for these small N.
       const uint64_t dQ = tc::sdesc(smem_addr(sQ), 16, 1024, tc::kSwizzle128B);
-      TileCursor cs, cv;  // the next S tile, the next PV tile
+      Cursor cs, cv;  // the next S tile, the next PV tile
       cs.seek(wv, f_lo);
       cv = cs;
       int seg_s = 0;      // segment of the next S tile
@@ -578,8 +604,8 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
 
     // ---- Q rows of columns [col0, col0 + NH) of a segment into the Q buffer (one warp a row), their
     // constants into slot `sl`; then this warp's arrival on qready
-    auto stage_q = [&](const TileCursor& cq, const QV (&wq)[kRowsPerWarp], int sl) {
-      const int rows = cq.QL * G;
+    auto stage_q = [&](const Cursor& cq, const QV (&wq)[kRowsPerWarp], int sl) {
+      const int rows = cq.rows(G);
 #pragma unroll
       for (int m = 0; m < kRowsPerWarp; ++m) {
         const int r = col0 + ((warp - 2) & 3) + 4 * m;  // column (the Q buffer's row)
@@ -637,7 +663,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
         }
         if (lane == 0) {
           rowC[sl * 64 + r] = cr;
-          rowLim[sl * 64 + r] = pr < rows ? cq.L - cq.QL + pr / G : -1;
+          rowLim[sl * 64 + r] = pr < rows ? cq.L - cq.QL + (cq.row0() + pr) / G : -1;
         }
       }
       fence_proxy_async();
@@ -645,7 +671,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
       if (lane == 0) mbar_arrive(qready);
     };
 
-    TileCursor cu = cu0;
+    Cursor cu = cu0;
     stage_q(cu, wq0, 0);
     named_sync(bar_sync, 128);  // the group's row constants are visible to the group
 
@@ -689,14 +715,14 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
         }
         // the next segment's Q rows (the pair after this one, if the range reaches it) into L2
         if (cu.n_t - cu.t < n_tiles - i && gt < NH) {
-          TileCursor nx = cu;
+          Cursor nx = cu;
           nx.t = cu.n_t - 1;
           nx.advance(wv, Hkv);
           const int r = row_of_col(col0 + gt);
-          if (r < nx.QL * G) {
-            const int qi = r / G;
+          if (r < nx.rows(G)) {
+            const int R = nx.row0() + r, qi = R / G;
             const uint16_t* qp =
-                p.q + (static_cast<size_t>(nx.q_off + qi) * p.num_q_heads + nx.g * G + (r - qi * G)) * C::kD;
+                p.q + (static_cast<size_t>(nx.q_off + qi) * p.num_q_heads + nx.g * G + (R - qi * G)) * C::kD;
 #pragma unroll
             for (int o = 0; o < C::kD; o += 64) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(qp + o));
           }
@@ -710,8 +736,8 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
       // columns that are never read, and their row sums stay zero. (Elsewhere the branch cost registers:
       // the 48-row FP8 instance spilled 116 bytes a thread with it, 64 without.)
       // row chunks of the pair dealt to this group: chunk c0 of the group is live iff c0 < act
-      const int act = NP != 64 ? min(NH, max(0, cu.QL * G - col0))
-                               : min(NH, 8 * max(0, ((cu.QL * G + 7) / 8 - wg + C::NWG - 1) / C::NWG));
+      const int act = NP != 64 ? min(NH, max(0, cu.rows(G) - col0))
+                               : min(NH, 8 * max(0, ((cu.rows(G) + 7) / 8 - wg + C::NWG - 1) / C::NWG));
       // Scores of the owned columns for this thread's token of every sub-tile, in pairs (packed f32x2
       // arithmetic).
       float2 y[SUB][NH / 2];
@@ -748,7 +774,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
       if (lane == 0) mbar_arrive(&sfree[sb]);
       if (seg_last && i + 1 < n_tiles) {
         // S(i), the last reader of this segment's Q, is done: stage the next segment's rows
-        TileCursor nx = cu;
+        Cursor nx = cu;
         nx.advance(wv, Hkv);
         QV wq[kRowsPerWarp];
         q_load(nx, wq);  // every row's load first: one memory latency for the warp's rows
@@ -998,9 +1024,9 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
           if ((lane & ((1 << kShift) - 1)) == 0 && col < NH) redl[(warp - 2) * 64 + col0 + col] = v[0];
         }
         named_sync(bar_sync, 128);
-        const int rows = cu.QL * G;
+        const int rows = cu.rows(G);
         const bool whole = seg_t0 == 0 && pair_last;  // the segment is the whole pair: no combine
-        const size_t u = static_cast<size_t>(p.slot_base) + cta + cu.pair(Hkv);
+        const size_t u = static_cast<size_t>(p.slot_base) + cta + cu.pair(wv, Hkv, p.rows_split != 0);
         float* rinv = red + 4 * C::NWG * 64;  // 1 / row total (0 for an empty row)
         if (gt < NH) {
           const int cc = col0 + gt;
@@ -1033,9 +1059,9 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
               if (!whole) {
                 p.part_o[(u * p.rows_max + r) * C::kD + d] = val;
               } else {
-                const int qi = r / G;
+                const int R = cu.row0() + r, qi = R / G;
                 const size_t o =
-                    (static_cast<size_t>(cu.q_off + qi) * p.num_q_heads + cu.g * G + (r - qi * G)) * C::kD + d;
+                    (static_cast<size_t>(cu.q_off + qi) * p.num_q_heads + cu.g * G + (R - qi * G)) * C::kD + d;
                 if (p.out_f32) reinterpret_cast<float*>(p.out)[o] = val;
                 else reinterpret_cast<uint16_t*>(p.out)[o] = static_cast<uint16_t>(pack_bf16(val, 0.f) & 0xFFFFu);
               }

@@ -91,12 +91,14 @@ def pack(nt, w, sw, tau):
 
 def flat_model(ctx, ql, hkv, sms, split_override=0, group=8, tile=128, kv=pv.KV_BF16, d=128):
     """Independent model of a flat plan: pairs (longest sequence first, then KV
-    head) end to end as `tile`-token tiles, cut into CTA ranges. Returns (CTA
-    starts, every pair's (first tile, tiles), the cost bound)."""
+    head; a pair of more than 64 rows as two row halves, rows 0-63 then the
+    rest) end to end as `tile`-token tiles, cut into CTA ranges. Returns (CTA
+    starts, every (virtual) pair's (first tile, tiles), the cost bound)."""
     order = sorted(range(len(ctx)), key=lambda b: -ctx[b])  # stable: ties keep batch order
-    nt = [-(-ctx[b] // tile) for b in order for _ in range(hkv)]
+    halves = lambda b: [ql[b] * group] if ql[b] * group <= 64 else [64, ql[b] * group - 64]
+    nt = [-(-ctx[b] // tile) for b in order for _ in range(hkv) for _ in halves(b)]
     rows_max = max(ql) * group
-    w = [costs(rows_max, ql[b] * group, kv, d)[0] for b in order for _ in range(hkv)]
+    w = [costs(rows_max, r, kv, d)[0] for b in order for _ in range(hkv) for r in halves(b)]
     sw = costs(rows_max, 0, kv, d)[1]
     total = sum(nt)
     pairs, t = [], 0
@@ -117,13 +119,13 @@ def flat_model(ctx, ql, hkv, sms, split_override=0, group=8, tile=128, kv=pv.KV_
     return pack(nt, w, sw, lo)[1], pairs, (lo, w, sw)
 
 
-def check_launch(starts, chunk_tokens, ctx, ql, hkv, split, sms, kv):
+def check_launch(starts, chunk_tokens, ctx, ql, hkv, split, sms, kv, group=8):
     """One launch's CTA ranges equal the model's and keep the invariants the kernels rely on; returns the
-    pairs' CTA spans."""
-    T = tc_tile(kv, 128, 8 * max(ql))
-    m_starts, pairs, bound = flat_model(ctx, ql, hkv, sms, split, tile=T, kv=kv)
+    (virtual) pairs' CTA spans."""
+    T = tc_tile(kv, 128, group * max(ql))
+    m_starts, pairs, bound = flat_model(ctx, ql, hkv, sms, split, group=group, tile=T, kv=kv)
     assert starts == m_starts
-    assert starts[-1] == hkv * sum(-(-c // T) for c in ctx)
+    assert starts[-1] == hkv * sum(-(-c // T) * (2 if q * group > 64 else 1) for c, q in zip(ctx, ql))
     # the ranges tile the flat space once, without empty CTAs
     assert starts[0] == 0 and all(a < b for a, b in zip(starts, starts[1:]))
     n = len(starts) - 1
@@ -142,13 +144,13 @@ def check_launch(starts, chunk_tokens, ctx, ql, hkv, split, sms, kv):
     return spans
 
 
-def check_flat_plan(ctx, ql, hkv, split, sms=152, kv=pv.KV_BF16):
+def check_flat_plan(ctx, ql, hkv, split, sms=152, kv=pv.KV_BF16, group=8):
     """The library's flat plan equals the model's ranges and keeps every invariant the kernels rely on. A batch
     of FP8 pairs with up to 48 rows and pairs with more is planned as two launches, one per class."""
-    p = mk(ctx, ql, hq=8 * hkv, hkv=hkv, split_override=split, sms=sms, kv=kv)
+    p = mk(ctx, ql, hq=group * hkv, hkv=hkv, split_override=split, sms=sms, kv=kv)
     i = p.info
     assert i.flat == 1 and i.kernel == pv.KERNEL_TCGEN05
-    lo = [b for b in range(len(ctx)) if 8 * ql[b] <= 48]
+    lo = [b for b in range(len(ctx)) if group * ql[b] <= 48]
     two = kv == pv.KV_FP8_E4M3 and split == 0 and 0 < len(lo) < len(ctx)
     assert i.launches == (2 if two else 1)
     parts = [(p, list(range(len(ctx))))] if not two else [(p, lo), (p.second(), [b for b in range(len(ctx)) if b not in lo])]
@@ -156,9 +158,9 @@ def check_flat_plan(ctx, ql, hkv, split, sms=152, kv=pv.KV_BF16):
     for part, mem in parts:
         c_ctx, c_ql = [ctx[b] for b in mem], [ql[b] for b in mem]
         starts = part.cta_starts()
-        T = tc_tile(kv, 128, 8 * max(c_ql))
+        T = tc_tile(kv, 128, group * max(c_ql))
         assert part.info.tile_tokens == T
-        spans = check_launch(starts, part.info.chunk_tokens, c_ctx, c_ql, hkv, split, sms, kv)
+        spans = check_launch(starts, part.info.chunk_tokens, c_ctx, c_ql, hkv, split, sms, kv, group)
         n = len(starts) - 1
         # slot base + c + pair of each CTA's piece of a pair: unique over both launches
         slots += [base + c + k for k, (a, b) in enumerate(spans) for c in range(a, b + 1)]
@@ -170,7 +172,7 @@ def check_flat_plan(ctx, ql, hkv, split, sms=152, kv=pv.KV_BF16):
     assert i.split_pairs == n_split  # the combine's table lists every split pair of both launches
     assert i.num_units == units and i.total_tiles == tiles
     assert i.max_splits == splits and i.needs_combine == (splits > 1)
-    assert i.rows_max == 8 * max(ql)
+    assert i.rows_max == group * max(ql)
     assert i.kv_bytes == sum(ctx) * hkv * (128 * 4 if kv == pv.KV_BF16 else 128 * 2 + 8)
     if two:
         q = p.second()
@@ -259,9 +261,9 @@ def test_empty_batch_plans():
     (dict(ctx=[100], ql=[2], stride=3), pv.ERR_INVALID),
     (dict(ctx=[10] * 1025, ql=[1] * 1025), pv.ERR_UNSUPPORTED),
     (dict(ctx=[100], ql=[6], d=256, kernel=pv.KERNEL_WARP_MMA), pv.ERR_UNSUPPORTED),  # 256: tcgen05 only
-    (dict(ctx=[100], ql=[8], hq=16, hkv=1, d=256), pv.ERR_UNSUPPORTED),  # bf16 256 with 128 rows
+    (dict(ctx=[100] * 65, ql=[8] * 65, hq=16, hkv=1, d=256), pv.ERR_UNSUPPORTED),  # 128 rows, 65 sequences
     (dict(ctx=[100], ql=[6], d=32), pv.ERR_UNSUPPORTED),
-    (dict(ctx=[100], ql=[8], hq=16, hkv=1, d=256, kv=pv.KV_FP8_E4M3), pv.ERR_UNSUPPORTED),  # 128 rows
+    (dict(ctx=[100] * 40, ql=[8] * 40, hq=64, hkv=4, d=256, kv=pv.KV_FP8_E4M3), pv.ERR_UNSUPPORTED),  # 320 pairs
     (dict(ctx=[100], ql=[6], d=256, kv=pv.KV_FP8_E4M3, kernel=pv.KERNEL_WARP_MMA), pv.ERR_UNSUPPORTED),
 ])
 def test_plan_refusals(kw, status):
@@ -382,3 +384,19 @@ def test_two_launch_plans_only_where_they_apply(kv, d, ql, split, launches):
         assert p.info.tile_tokens == 256 and q.info.tile_tokens == 128
         assert q.info.rows_max == 64 and p.info.rows_max == 64
         assert p.info.num_units == len(p.cta_starts()) - 1 + q.info.num_units
+
+
+@pytest.mark.parametrize("kv", [pv.KV_BF16, pv.KV_FP8_E4M3], ids=["bf16", "fp8"])
+@pytest.mark.parametrize("ctx,ql", [([30000, 5000, 9000], [8, 5, 2]), ([1 << 17], [7]), ([700, 64, 4000, 129], [6, 8, 3, 5])])
+@pytest.mark.parametrize("split", [0, 3])
+def test_flat_plan_row_halves(ctx, ql, kv, split):
+    """Group 16: pairs of 80-128 rows run as two row halves (virtual pairs) of the 64-row instance."""
+    check_flat_plan(ctx, ql, 1, split, kv=kv, group=16)
+    assert mk(ctx, ql, hq=16, hkv=1, kv=kv, split_override=split).info.kernel == pv.KERNEL_TCGEN05
+
+
+def test_row_halves_need_a_static_table():
+    # 65-128 rows: the tensor-core kernel in static plans of up to 128 virtual pairs, else the warp-MMA kernel
+    assert mk([5000] * 64, [8] * 64, hq=16, hkv=1).info.kernel == pv.KERNEL_TCGEN05
+    assert mk([5000] * 40, [8] * 40, hq=64, hkv=4).info.kernel == pv.KERNEL_WARP_MMA
+    assert mk([5000] * 65, [8] * 65, hq=16, hkv=1).info.kernel == pv.KERNEL_WARP_MMA

@@ -27,7 +27,10 @@ def built():
 
 
 def tc_applies(prob):
-    return int(prob.query_lens.max()) * prob.group <= 64  # every head_dim
+    # every head_dim; 65-128 rows as two row halves in static plans of up to 64 sequences and 128 virtual pairs
+    rows = int(prob.query_lens.max()) * prob.group
+    n = len(prob.query_lens)
+    return rows <= 64 or (rows <= 128 and n <= 64 and n * prob.num_kv_heads * 2 <= 256)
 
 
 def mma_applies(prob):
@@ -281,3 +284,34 @@ def test_two_launch_plan_static_entry_point_matches():
     torch.cuda.synchronize()
     assert pv.device_errors(None) == 0
     assert torch.equal(a, b)
+
+
+# --------------------------------------------------------------- 65-128 rows: row halves
+ROW_HALF_CASES = [
+    ("bf16_d128", synth.KV_BF16, 128, 16, 1, [3000, 130, 8000, 600], [8, 5, 1, 7]),
+    ("fp8_d128", synth.KV_FP8, 128, 16, 1, [3000, 130, 8000, 600], [8, 5, 1, 7]),
+    ("bf16_d64", synth.KV_BF16, 64, 16, 1, [2000, 257, 4100], [8, 6, 3]),
+    ("bf16_d256", synth.KV_BF16, 256, 16, 1, [2000, 257, 4100], [8, 6, 3]),
+    ("fp8_d256", synth.KV_FP8, 256, 16, 1, [2000, 257, 4100], [8, 6, 3]),
+    ("fp8_hkv2_group12", synth.KV_FP8, 128, 24, 2, [5000, 1000, 77], [7, 8, 2]),
+]
+
+
+@pytest.mark.parametrize("split", [0, 1, 4], ids=["planner", "one_segment", "four_way"])
+@pytest.mark.parametrize("name,kv,d,hq,hkv,ctx,ql", ROW_HALF_CASES, ids=[c[0] for c in ROW_HALF_CASES])
+def test_row_halves_against_oracle(name, kv, d, hq, hkv, ctx, ql, split):
+    """Pairs of 65-128 rows on the tcgen05 kernel: two virtual pairs of the 64-row instance, rows 0-63 and
+    the rest, each a pass over the context; every output row against the oracle."""
+    prob = synth.make_problem(ctx, ql, hq, hkv, d, kv_dtype=kv, seed=59)
+    ref = oracle.verify_attention(prob)
+    got, va = gpu_run(prob, split_override=split, kernel=pv.KERNEL_AUTO)
+    assert va.info["kernel"] == pv.KERNEL_TCGEN05 and va.info["rows_max"] > 64
+    assert max_err(got, ref) <= TOL[kv], name
+
+
+def test_row_halves_match_the_warp_mma_kernel():
+    prob = synth.make_problem([9000, 3100], [8, 8], 16, 1, 128, seed=60)
+    a, va = gpu_run(prob, kernel=pv.KERNEL_TCGEN05)
+    b, vb = gpu_run(prob, kernel=pv.KERNEL_WARP_MMA)
+    assert va.info["kernel"] == pv.KERNEL_TCGEN05 and vb.info["kernel"] == pv.KERNEL_WARP_MMA
+    assert max_err(a, b.astype(np.float64)) <= 1e-2
