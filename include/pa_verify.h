@@ -75,8 +75,8 @@ typedef struct {
   int32_t num_q_heads;        /* Hq >= 1 */
   int32_t num_kv_heads;       /* Hkv >= 1, Hq % Hkv == 0, group G = Hq / Hkv */
   int32_t head_dim;           /* D: 64, 128 or 256 (bf16 KV); 128 or 256 (FP8 KV). 256 runs on the
-                                 tcgen05 kernel only, q_b * G <= 64 (FP8: the aiter follow-up's
-                                 head-256 shape on the MTP-5 routing page) */
+                                 tcgen05 kernel only, within its envelope (see `kernel`; FP8: the
+                                 aiter follow-up's head-256 shape on the MTP-5 routing page) */
   int32_t page_size;          /* must be 16 */
   int32_t kv_dtype;           /* PA_KV_* */
   int32_t out_dtype;          /* PA_OUT_* */
@@ -87,8 +87,10 @@ typedef struct {
                                  (num_seqs <= 64 only) */
   int32_t sm_count;           /* 0: query the current device; > 0: plan for that many SMs */
   int32_t kernel;             /* PA_KERNEL_*: 0 picks the tensor-core (tcgen05) kernel where it
-                                 applies (q_b * G <= 64, every head_dim), else the warp-MMA kernel
-                                 (head_dim 64 or 128, up to 128 rows) */
+                                 applies (every head_dim; q_b * G <= 64, or up to 128 rows in a
+                                 static plan of at most 64 sequences and 128 (sequence, KV head)
+                                 pairs, such a pair running as two row halves), else the warp-MMA
+                                 kernel (head_dim 64 or 128, up to 128 rows) */
 } pa_verify_desc;
 
 enum { PA_KERNEL_AUTO = 0, PA_KERNEL_WARP_MMA = 1, PA_KERNEL_TCGEN05 = 2 };

@@ -1,7 +1,8 @@
 // Split-KV paged verify attention on 5th-generation tensor cores (tcgen05).
 //
-// Work. The (sequence, KV head) pairs are laid end to end as 128-token tiles
-// and CTA c takes a consecutive range of them (the host planner's cost-bounded
+// Work. The (sequence, KV head) pairs are laid end to end as K/V tiles of 128
+// tokens (256 in the FP8 head_dim-128 instances up to 48 rows: two MMA
+// sub-tiles) and CTA c takes a consecutive range of them (the host planner's cost-bounded
 // cut, or [c * per, (c + 1) * per)), so every SM gets about the same amount of
 // K/V whatever the length mix. A CTA walks its range
 // as segments, one per pair the range touches. A segment covering a whole
@@ -10,8 +11,9 @@
 // split decode: MTP-5 routing page, Motivation).
 //
 // A pair's q_b * G query rows ("rows = query length x GQA group", same page)
-// are the N dimension of the MMAs, padded to NP; the 128 tokens of a K/V
-// tile are the M dimension, so every K/V byte reaches the tensor core
+// are the N dimension of the MMAs, padded to NP (a pair of 65-128 rows runs
+// as two row halves, virtual pairs of the 64-row instance); the 128 tokens of
+// an MMA sub-tile are the M dimension, so every K/V byte reaches the tensor core
 // straight from the TMA-staged shared memory, once:
 //   S^T[tok, r]  = K[tok, :] . Q[r, :]           (A = K tile, K-major; B = Q, K-major)
 //   O^T[d, r]   += V[:, d]^T . P^T[:, r]          (A = V tile, MN-major; B = P, MN-major)
