@@ -327,7 +327,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=3.0, help="seconds of oracle time per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--also", default="mtp5_fp8,mixed_fp8,ctx1mi_bf16,d256_fp8_bs8",
+    ap.add_argument("--also", default="mtp5_fp8,mixed_fp8,ctx1mi_bf16,d256_fp8_bs8,d256_bf16_bs8",
                     help="comma-separated extra workloads to report under 'other_configs' ('' for none)")
     ap.add_argument("--also-cpu-budget", type=float, default=3.0,
                     help="seconds of oracle time for each extra workload's cpu_baseline")
