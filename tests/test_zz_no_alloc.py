@@ -91,8 +91,9 @@ def test_static_scratch_with_a_dynamic_plan():
 
 
 def test_static_scratch_error_word_reads_back():
-    """An out-of-range page id is flagged in the fixed scratch's error word; the
-    next clean call starts from a cleared word."""
+    """An out-of-range page id, then device lengths that differ from the plan's,
+    are flagged in the fixed scratch's error word; each call starts from a
+    cleared word."""
     _build.build()
     lib = pv.lib()
     prob = synth.make_problem([900, 400], [6, 3], 16, 2, 128, seed=94)
@@ -106,6 +107,13 @@ def test_static_scratch_error_word_reads_back():
     dev_bad = type(dev)(**{**dev.__dict__, "block_table": bad})
     assert _static_call(lib, va.plan, dev_bad, prob.softmax_scale, out) == pv.OK, pv.last_error()
     assert pv.device_errors(None) & pv.DEVERR_PAGE_RANGE
+    # device lengths that differ from the plan's: the kernel follows the plan and the word says so
+    ctx_bad = dev.context_lens.clone()
+    ctx_bad[1] += 5
+    dev_len = type(dev)(**{**dev.__dict__, "context_lens": ctx_bad})
+    assert _static_call(lib, va.plan, dev_len, prob.softmax_scale, out) == pv.OK, pv.last_error()
+    flags = pv.device_errors(None)
+    assert flags & pv.DEVERR_LENGTHS and not flags & pv.DEVERR_PAGE_RANGE
     assert _static_call(lib, va.plan, dev, prob.softmax_scale, out) == pv.OK, pv.last_error()
     assert pv.device_errors(None) == 0
     torch.cuda.synchronize()
