@@ -593,8 +593,12 @@ int build_capacity_plan(const pa_verify_desc& d, int sms, int max_len, int max_q
   const int64_t per_pair = (static_cast<int64_t>(max_context_len) + kMaxChunk - 1) / kMaxChunk;
   const int64_t units_cap =
       use_tc ? slots : std::max<int64_t>(slots, static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * per_pair);
-  // partial slots: a flat plan's CTA c writes pair p's partial at c + p
-  const int64_t part_cap = use_tc ? units_cap + static_cast<int64_t>(d.num_seqs) * d.num_kv_heads : units_cap;
+  // partial slots: a flat plan's CTA c writes pair p's partial at c + p (a pair of more than 64 rows is two
+  // virtual pairs, whose partials hold 64 rows each)
+  const bool halves = use_tc && rows_max > 64;
+  const int64_t part_cap =
+      use_tc ? units_cap + static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * (halves ? 2 : 1) : units_cap;
+  const int stride = halves ? 64 : rows_max;  // rows of a partial
   const int64_t rows_cap = static_cast<int64_t>(d.num_seqs) * max_query_len * d.num_q_heads;
   if (units_cap >= (int64_t(1) << 31) || rows_cap >= (int64_t(1) << 31))
     return fail(PA_ERR_UNSUPPORTED, "capacity too large for one call");
@@ -621,13 +625,15 @@ int build_capacity_plan(const pa_verify_desc& d, int sms, int max_len, int max_q
   const int64_t per_th = fp8 ? (2 * d.head_dim + 8) : (4 * d.head_dim);
   P->kv_bytes = static_cast<int64_t>(d.num_seqs) * max_context_len * d.num_kv_heads * per_th;  // at capacity
   P->part_units = part_cap;
+  P->rows_split = halves ? 1 : 0;
+  P->part_rows = halves ? 64 : 0;
   size_t ws = kWsHeader;
   P->off_dyn = ws;
   ws += align_up(dyn_work_bytes(d.num_seqs), 256);
   P->off_part = ws;
-  ws += align_up(static_cast<size_t>(part_cap) * rows_max * d.head_dim * 4, 256);
+  ws += align_up(static_cast<size_t>(part_cap) * stride * d.head_dim * 4, 256);
   P->off_lse = ws;
-  ws += align_up(static_cast<size_t>(part_cap) * rows_max * 4, 256);
+  ws += align_up(static_cast<size_t>(part_cap) * stride * 4, 256);
   P->ws_bytes = ws;
   *plan_out = P;
   *workspace_bytes_out = ws;
@@ -702,21 +708,16 @@ int pa_verify_plan(const pa_verify_desc* desc, const int32_t* context_lens_host,
     *workspace_bytes_out = P->ws_bytes;
     return PA_OK;
   }
-  // Up to 64 rows a pair is one pass of the tcgen05 kernel; 65-128 rows are two row halves (virtual pairs), in
-  // static plans whose virtual pairs all fit the combine's table.
-  const bool halves_ok =
-      d.num_seqs <= kMaxSeqs && static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * 2 <= kMaxCombinePairs;
-  const bool tc_ok = d.head_dim >= 64 && (rows_max <= 64 || (rows_max <= 128 && halves_ok));
+  // Up to 64 rows a pair is one pass of the tcgen05 kernel; 65-128 rows are two row halves (virtual pairs).
+  const bool tc_ok = d.head_dim >= 64 && rows_max <= 128;
   if (d.kernel == PA_KERNEL_TCGEN05 && !tc_ok) {
     delete P;
-    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs q_len * group <= 64, or <= 128 with at most 64 "
-                                    "sequences and 128 (sequence, KV head) pairs");
+    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs q_len * group <= 128");
   }
   const bool use_tc = d.kernel == PA_KERNEL_TCGEN05 || (d.kernel == PA_KERNEL_AUTO && tc_ok);
   if (d.head_dim == 256 && !use_tc) {
     delete P;
-    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only (q_len * group <= 64, or <= 128 "
-                                    "with at most 64 sequences and 128 (sequence, KV head) pairs)");
+    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only");
   }
   if (d.num_seqs > kMaxSeqs) {
     // the table is too large for the kernel parameters: the device planner builds it at each run
@@ -1042,13 +1043,12 @@ int pa_verify_plan_dynamic(const pa_verify_desc* desc, int32_t max_context_len, 
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("SM count query failed: ") + cudaGetErrorString(e));
   }
-  const bool tc_ok = d.head_dim >= 64 && rows_max <= 64;  // head_dim 64 (bf16), 128, 256 (FP8)
+  const bool tc_ok = d.head_dim >= 64 && rows_max <= 128;  // 65-128 rows: row halves (the device planner)
   if (d.kernel == PA_KERNEL_TCGEN05 && !tc_ok)
-    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs q_len * group <= 64");
+    return fail(PA_ERR_UNSUPPORTED, "the tcgen05 kernel needs q_len * group <= 128");
   const bool use_tc = d.kernel == PA_KERNEL_TCGEN05 || (d.kernel == PA_KERNEL_AUTO && tc_ok);
   if (d.head_dim == 256 && !use_tc)
-    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only (q_len * group <= 64, or <= 128 "
-                                    "with at most 64 sequences and 128 (sequence, KV head) pairs)");
+    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 runs on the tcgen05 kernel only");
   return build_capacity_plan(d, sms, max_context_len, max_query_len, use_tc, plan_out, workspace_bytes_out);
 }
 

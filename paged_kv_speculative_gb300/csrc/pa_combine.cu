@@ -80,12 +80,17 @@ __device__ __forceinline__ RowRef resolve_row(const SplitParams& p, int rho) {
   rr.r = i * G + (h - kvh * G);
   rr.orow = static_cast<size_t>(si.q_off + i) * p.num_q_heads + h;
   if (p.flat) {
-    // pair (lo, kvh) covers tiles [t0, t0 + n_tiles); CTA c wrote its piece at slot c + pair
-    const int pair = lo * p.num_kv_heads + kvh;
-    const int t0 = si.tile_start + kvh * si.n_tiles;
+    // (virtual) pair of this row: a pair of more than 64 rows is two, rows 0-63 and the rest, and the partials
+    // hold a virtual pair's rows; it covers tiles [t0, t0 + n_tiles) and CTA c wrote its piece at slot
+    // slot_base + c + pair
+    const int hv = max(1, si.halves), half = hv > 1 ? rr.r / 64 : 0;
+    const int vp = kvh * hv + half;
+    const int pair = p.rows_split ? si.unit_start + vp : lo * p.num_kv_heads + kvh;
+    const int t0 = si.tile_start + vp * si.n_tiles;
     const int c0 = flat_cta_of(wv, t0);
     rr.n = flat_cta_of(wv, t0 + si.n_tiles - 1) - c0 + 1;
-    rr.u0 = static_cast<size_t>(c0) + pair;
+    rr.u0 = static_cast<size_t>(p.slot_base) + c0 + pair;
+    rr.r -= 64 * half;
   } else {
     rr.n = si.n_chunks;
     rr.u0 = static_cast<size_t>(si.unit_start) + static_cast<size_t>(kvh) * rr.n;

@@ -7,7 +7,8 @@
 // of more than 64 sequences built from host lengths use it too: their table
 // is too large for the kernel parameters.
 //
-// Same rules as the host planner. Chunk plans: the chunk is the smallest
+// Same rules as the host planner (a pair of more than 64 rows is two virtual
+// pairs in flat plans). Chunk plans: the chunk is the smallest
 // multiple of the staging tile whose unit count fits `slots` (one wave),
 // capped at the page-id staging limit. Flat plans: the pairs' K/V tiles of the
 // tensor-core kernel end to end, ceil(tiles / slots) of them per CTA. Sequences are scheduled
@@ -144,25 +145,29 @@ __global__ void __launch_bounds__(kPlanThreads) pa_dyn_plan_kernel(DynPlanArgs a
   const int Ls = in ? s_len[src] : 0, qs = in ? s_q[src] : 0;
   const int n_chunks = a.flat ? 0 : (Ls > 0 ? (Ls + chunk - 1) / chunk : 0);
   const int n_tiles = (Ls + a.tile - 1) / a.tile;  // flat plans (the kernel's K/V tiles); 0 for padding
+  // flat plans: a pair of more than 64 rows is two virtual pairs (row halves), each a pass over the context
+  const int hv = a.flat && qs * (a.num_q_heads / a.num_kv_heads) > 64 ? 2 : 1;
   const long long units_r = static_cast<long long>(n_chunks) * a.num_kv_heads;
   const long long rows_r = static_cast<long long>(qs) * a.num_q_heads;
-  const long long tiles_r = static_cast<long long>(n_tiles) * a.num_kv_heads;
-  long long total_units, total_rows, total_tiles;
+  const long long tiles_r = static_cast<long long>(n_tiles) * a.num_kv_heads * hv;
+  const long long vps_r = static_cast<long long>(a.num_kv_heads) * hv;
+  long long total_units, total_rows, total_tiles, total_vps;
   const long long us = block_scan(units_r, s_red, &total_units) - units_r;
   const long long rs = block_scan(rows_r, s_red, &total_rows) - rows_r;
   const long long ts = block_scan(tiles_r, s_red, &total_tiles) - tiles_r;
+  const long long vs = block_scan(vps_r, s_red, &total_vps) - vps_r;
   if (in) {
     SeqInfo si;
     si.ctx_len = Ls;
     si.q_len = qs;
     si.q_off = s_qoff[src];
-    si.unit_start = static_cast<int>(us);
+    si.unit_start = static_cast<int>(a.flat ? vs : us);  // flat plans: the entry's first (virtual) pair
     si.row_start = static_cast<int>(rs);
     si.n_chunks = n_chunks;
     si.b = src;
     si.tile_start = static_cast<int>(ts);
     si.n_tiles = n_tiles;
-    si.halves = 0;
+    si.halves = hv;
     dyn_seq(a.out)[r] = si;
   }
   if (b == 0) {

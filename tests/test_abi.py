@@ -261,9 +261,9 @@ def test_empty_batch_plans():
     (dict(ctx=[100], ql=[2], stride=3), pv.ERR_INVALID),
     (dict(ctx=[10] * 1025, ql=[1] * 1025), pv.ERR_UNSUPPORTED),
     (dict(ctx=[100], ql=[6], d=256, kernel=pv.KERNEL_WARP_MMA), pv.ERR_UNSUPPORTED),  # 256: tcgen05 only
-    (dict(ctx=[100] * 65, ql=[8] * 65, hq=16, hkv=1, d=256), pv.ERR_UNSUPPORTED),  # 128 rows, 65 sequences
+    (dict(ctx=[100], ql=[8], hq=32, hkv=1, d=256), pv.ERR_UNSUPPORTED),  # 256 rows
     (dict(ctx=[100], ql=[6], d=32), pv.ERR_UNSUPPORTED),
-    (dict(ctx=[100] * 40, ql=[8] * 40, hq=64, hkv=4, d=256, kv=pv.KV_FP8_E4M3), pv.ERR_UNSUPPORTED),  # 320 pairs
+    (dict(ctx=[100], ql=[8], hq=32, hkv=1, d=256, kv=pv.KV_FP8_E4M3), pv.ERR_UNSUPPORTED),  # 256 rows
     (dict(ctx=[100], ql=[6], d=256, kv=pv.KV_FP8_E4M3, kernel=pv.KERNEL_WARP_MMA), pv.ERR_UNSUPPORTED),
 ])
 def test_plan_refusals(kw, status):
@@ -395,8 +395,14 @@ def test_flat_plan_row_halves(ctx, ql, kv, split):
     assert mk(ctx, ql, hq=16, hkv=1, kv=kv, split_override=split).info.kernel == pv.KERNEL_TCGEN05
 
 
-def test_row_halves_need_a_static_table():
-    # 65-128 rows: the tensor-core kernel in static plans of up to 128 virtual pairs, else the warp-MMA kernel
+def test_row_halves_everywhere():
+    # 65-128 rows run on the tensor-core kernel as row halves: static plans (with or without the combine's table)
+    # and device-built tables alike; the warp-MMA kernel only when asked for
     assert mk([5000] * 64, [8] * 64, hq=16, hkv=1).info.kernel == pv.KERNEL_TCGEN05
-    assert mk([5000] * 40, [8] * 40, hq=64, hkv=4).info.kernel == pv.KERNEL_WARP_MMA
-    assert mk([5000] * 65, [8] * 65, hq=16, hkv=1).info.kernel == pv.KERNEL_WARP_MMA
+    p = mk([5000] * 40, [8] * 40, hq=64, hkv=4, split_override=4)  # 320 split virtual pairs: no table, the
+    assert p.info.kernel == pv.KERNEL_TCGEN05 and p.info.split_pairs == -1  # combine resolves every row itself
+    q = mk([5000] * 65, [8] * 65, hq=16, hkv=1)
+    assert q.info.kernel == pv.KERNEL_TCGEN05 and q.info.device_table == 1
+    assert mk([5000] * 8, [8] * 8, hq=16, hkv=1, kernel=pv.KERNEL_WARP_MMA).info.kernel == pv.KERNEL_WARP_MMA
+    dyn = pv.plan_dynamic(16, 1, 128, pv.KV_BF16, pv.OUT_BF16, 20000, 9400, 4, 150000, 8, sm_count=152)
+    assert dyn.info.kernel == pv.KERNEL_TCGEN05 and dyn.info.rows_max == 128

@@ -178,3 +178,36 @@ def test_out_of_capacity_lengths_are_flagged_and_padded():
     ref = oracle.verify_attention(prob)
     assert float(np.abs(out[:6].cpu().numpy() - ref).max()) <= 1e-2
     assert bool((out[6:] == 7.0).all())
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kvd,d", [(synth.KV_BF16, 128), (synth.KV_FP8, 128), (synth.KV_FP8, 256)],
+                         ids=["bf16", "fp8", "fp8_d256"])
+def test_dynamic_row_halves_match_oracle(kvd, d):
+    """Capacity plans of up to 128 rows (group 16 x query 8) on the tcgen05 kernel: the device planner makes a
+    pair of more than 64 rows two virtual pairs, and the combine finds a row's half without a host table."""
+    base = synth.make_problem([4000] * 4, [8] * 4, 16, 1, d, kv_dtype=kvd, seed=65)
+    dev = to_device(base)
+    cap_rows = 4 * 8
+    plan = pv.plan_dynamic(16, 1, d, kvd, pv.OUT_F32, base.num_pages, base.block_table.shape[1], capacity=4,
+                           max_context_len=4000, max_query_len=8)
+    assert plan.info.kernel == pv.KERNEL_TCGEN05 and plan.info.rows_max == 128
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    q_buf = torch.zeros((cap_rows, 16, d), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((cap_rows, 16, d), dtype=torch.float32, device="cuda")
+    for k, (ctx, ql) in enumerate(SCENARIOS):
+        prob = _scenario(base, ctx, ql, seed=200 + k)
+        T = int(sum(ql))
+        q_buf[:T].copy_(torch.from_numpy(prob.q.view(np.int16)).view(torch.bfloat16))
+        out.fill_(7.0)
+        ctx_d = torch.tensor(ctx, dtype=torch.int32, device="cuda")
+        ql_d = torch.tensor(ql, dtype=torch.int32, device="cuda")
+        pv.run(plan, q_buf, dev.k_cache, dev.v_cache, dev.k_scale, dev.v_scale, dev.block_table, ctx_d, ql_d,
+               base.softmax_scale, out, ws)
+        torch.cuda.synchronize()
+        assert pv.device_errors(ws) == 0
+        ref = oracle.verify_attention(prob)
+        got = out[:T].cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all()
+        assert float(np.abs(got - ref).max()) <= TOL[kvd], (ctx, ql)
+        assert bool((out[T:] == 7.0).all())

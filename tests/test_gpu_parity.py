@@ -315,3 +315,14 @@ def test_row_halves_match_the_warp_mma_kernel():
     b, vb = gpu_run(prob, kernel=pv.KERNEL_WARP_MMA)
     assert va.info["kernel"] == pv.KERNEL_TCGEN05 and vb.info["kernel"] == pv.KERNEL_WARP_MMA
     assert max_err(a, b.astype(np.float64)) <= 1e-2
+
+
+def test_row_halves_without_the_combine_table():
+    """320 split virtual pairs: more than the combine's table holds, so the combine finds each row's half and
+    partials from the plan's work table."""
+    ctx = [2000 + 37 * i for i in range(40)]
+    ql = [8 - (i % 3) for i in range(40)]  # 128, 112 and 96 rows
+    prob = synth.make_problem(ctx, ql, 64, 4, 128, seed=61)
+    got, va = gpu_run(prob, split_override=4)
+    assert va.info["kernel"] == pv.KERNEL_TCGEN05 and va.info["split_pairs"] == -1
+    assert max_err(got, oracle.verify_attention(prob)) <= TOL[synth.KV_BF16]

@@ -45,15 +45,18 @@ def max_err(a, b):
     (synth.KV_BF16, 128, 16, 2, pv.KERNEL_AUTO),
     (synth.KV_FP8, 128, 16, 2, pv.KERNEL_AUTO),
     (synth.KV_FP8, 256, 8, 1, pv.KERNEL_AUTO),
-    (synth.KV_BF16, 128, 16, 1, pv.KERNEL_AUTO),   # up to 128 rows: the warp-MMA kernel
+    (synth.KV_BF16, 128, 16, 1, pv.KERNEL_AUTO),       # up to 128 rows: row halves on the tcgen05 kernel
+    (synth.KV_FP8, 128, 16, 1, pv.KERNEL_AUTO),
+    (synth.KV_BF16, 128, 16, 1, pv.KERNEL_WARP_MMA),   # the same on the warp-MMA kernel
     (synth.KV_BF16, 64, 8, 2, pv.KERNEL_AUTO),
-], ids=["bf16", "fp8", "fp8_d256", "bf16_rows128", "bf16_d64"])
+], ids=["bf16", "fp8", "fp8_d256", "bf16_rows128", "fp8_rows128", "bf16_rows128_mma", "bf16_d64"])
 def test_large_batch_every_row(B, kv, d, hq, hkv, kernel):
     ctx, ql = lengths(B, seed=B + d + hkv)
     prob = synth.make_problem(ctx, ql, hq, hkv, d, kv_dtype=kv, seed=70 + B)
     dev = to_device(prob)
     va = pv.VerifyAttention(hq, hkv, d, kv, prob.num_pages, prob.block_table.shape[1], ctx, ql, kernel=kernel)
     assert va.info["device_table"] == 1
+    assert va.info["kernel"] == (pv.KERNEL_WARP_MMA if kernel == pv.KERNEL_WARP_MMA else pv.KERNEL_TCGEN05)
     out = va(*dev.args(), prob.softmax_scale)
     torch.cuda.synchronize()
     assert va.device_errors() == 0
