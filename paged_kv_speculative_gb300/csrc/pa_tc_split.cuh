@@ -821,30 +821,33 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
       }
       // d = y - M (log2 units); with M = -inf a finite score gives +inf (and a masked one NaN, dropped
       // below). (Shared-memory way: a segment's first tile has no reference yet and d holds y itself.)
+      // The tile maximum runs as four independent chains (a single one is 2 x NH x SUB dependent steps).
       float2 dl[SUB][NH / 2];
       float dmax;
       if constexpr (kRegs) {
-        dmax = -INFINITY;
+        float dm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int h = 0; h < SUB; ++h)
 #pragma unroll
           for (int c = 0; c < NH / 2; ++c) {
             dl[h][c] = __fadd2_rn(y[h][c], negm[c % kRP]);
-            dmax = fmaxf(dmax, fmaxf(dl[h][c].x, dl[h][c].y));
+            dm4[(h * (NH / 2) + c) & 3] = fmaxf(dm4[(h * (NH / 2) + c) & 3], fmaxf(dl[h][c].x, dl[h][c].y));
           }
+        dmax = fmaxf(fmaxf(dm4[0], dm4[1]), fmaxf(dm4[2], dm4[3]));
       } else {
         dmax = INFINITY;
         if (!seg_first) {
-          dmax = -INFINITY;
+          float dm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int c = 0; c < NH / 2; ++c) {
             const float2 m = reinterpret_cast<const float2*>(mref)[c];
 #pragma unroll
             for (int h = 0; h < SUB; ++h) {
               dl[h][c] = __fadd2_rn(y[h][c], make_float2(-m.x, -m.y));
-              dmax = fmaxf(dmax, fmaxf(dl[h][c].x, dl[h][c].y));
+              dm4[(c * SUB + h) & 3] = fmaxf(dm4[(c * SUB + h) & 3], fmaxf(dl[h][c].x, dl[h][c].y));
             }
           }
+          dmax = fmaxf(fmaxf(dm4[0], dm4[1]), fmaxf(dm4[2], dm4[3]));
         } else {
 #pragma unroll
           for (int h = 0; h < SUB; ++h)
