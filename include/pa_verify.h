@@ -86,11 +86,10 @@ typedef struct {
                                  ceil(max_b L_b / k) rounded up to the staging tile
                                  (num_seqs <= 64 only) */
   int32_t sm_count;           /* 0: query the current device; > 0: plan for that many SMs */
-  int32_t kernel;             /* PA_KERNEL_*: 0 picks the tensor-core (tcgen05) kernel where it
-                                 applies (every head_dim; q_b * G <= 64, or up to 128 rows in a
-                                 static plan of at most 64 sequences and 128 (sequence, KV head)
-                                 pairs, such a pair running as two row halves), else the warp-MMA
-                                 kernel (head_dim 64 or 128, up to 128 rows) */
+  int32_t kernel;             /* PA_KERNEL_*: 0 picks the tensor-core (tcgen05) kernel, which takes
+                                 every head_dim and up to 128 rows (a pair of more than 64 rows runs
+                                 as two row halves); the warp-MMA kernel (head_dim 64 or 128, up to
+                                 128 rows) runs only when asked for */
 } pa_verify_desc;
 
 enum { PA_KERNEL_AUTO = 0, PA_KERNEL_WARP_MMA = 1, PA_KERNEL_TCGEN05 = 2 };
