@@ -1,7 +1,7 @@
 """The online softmax under scores that rise inside a segment, and the inputs
 that stress the FP8 arithmetic, against the fp64 oracle through the C ABI.
 
-With q, K, V ~ N(0, 1) a later 128-token tile never beats the first tile's
+With q, K, V ~ N(0, 1) a later K/V tile never beats the first tile's
 row maximum by 2^8 (the tensor-core kernel's lazy-reference threshold), so the
 kernel's in-segment rescale of the output accumulator in tensor memory would
 never run. Here the K rows grow along the context (2^(a t / L)) and the q rows

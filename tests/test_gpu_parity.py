@@ -27,10 +27,8 @@ def built():
 
 
 def tc_applies(prob):
-    # every head_dim; 65-128 rows as two row halves in static plans of up to 64 sequences and 128 virtual pairs
-    rows = int(prob.query_lens.max()) * prob.group
-    n = len(prob.query_lens)
-    return rows <= 64 or (rows <= 128 and n <= 64 and n * prob.num_kv_heads * 2 <= 256)
+    # every head_dim and up to 128 rows (65-128 rows as two row halves)
+    return int(prob.query_lens.max()) * prob.group <= 128
 
 
 def mma_applies(prob):
