@@ -411,7 +411,6 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
         atomicOr(p.err, 1u);
         pg = -1;
       }
-      // FP8 (K producer): one k and one v scale copy per page inside the pool (lanes 16-23 hold the ids)
       const int sslot = k % (C::SS > 0 ? C::SS : 1);  // scale slot (FP8)
       if (lane == 0) mbar_arrive_expect_tx(bar, npg * (kPage * C::kRowB));
       __syncwarp();
@@ -595,9 +594,10 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
     }
   } else if (is_sm) {
     // ============================================================ softmax warpgroups
-    // NWG warpgroups (warps 2-5, 6-9, 10-13). Each covers the 128 tokens of a tile
-    // (one per thread, = tensor-memory lane) for its own NH = NP / NWG columns
-    // (rows of the pair); the groups never wait on each other inside the loop.
+    // NWG warpgroups (warps 2-5, 6-9, 10-13). Each covers the 128 tokens of an MMA
+    // sub-tile (one per thread, = tensor-memory lane; a thread takes its token of
+    // every sub-tile of the tile) for its own NH = NP / NWG columns (rows of the
+    // pair); the groups never wait on each other inside the loop.
     const int gt = tid - 64 - wg * 128;           // 0..127 inside the group
     const int q4 = warp & 3;                      // tensor-memory lane quarter of this warp
     const int tok = q4 * 32 + lane;               // token of the tile this thread owns
@@ -1002,7 +1002,7 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
         // ---- segment epilogue: O / l for the owned columns (PV(i) done: O holds the segment)
         wait(&pfree[pb], static_cast<uint32_t>(i / C::PB) & 1u);
         tc::fence_after_sync();
-        // Row sums over the group's 128 tokens. Within a warp, a halving butterfly: at each step a lane
+        // Row sums over the group's 128 threads. Within a warp, a halving butterfly: at each step a lane
         // keeps half of its columns, sends the other half to its partner and adds what it receives, so
         // the NH columns cost about NH shuffles in all and lane L ends with column L >> (5 - log2 W).
         // Then the group's 4 warps meet in shared memory. (This code runs once per segment: it is kept
