@@ -678,11 +678,12 @@ __global__ void __launch_bounds__(TcCfg<KV_FP8, NP, D, SUB>::kThreads, 1)
     named_sync(bar_sync, 128);  // the group's row constants are visible to the group
 
     // Per owned column pair, this thread's row-sum partial l. The group-uniform per-column values (the
-    // reference maxima M_r, the FP8 score multiplier) are held one of two ways. Up to 24 columns a
-    // group, one token a thread, they sit in registers (as -M_r); at 32 columns, or two tokens a thread
-    // (256-token tiles), they would spill, and shared memory (broadcast reads) holds them instead. (Both
-    // ways measured: each is the faster one where it is used.)
-    constexpr bool kRegs = NH <= 24 && SUB == 1;
+    // reference maxima M_r, the FP8 score multiplier) are held one of two ways. With FP8 K/V, up to 24
+    // columns a group and one token a thread, they sit in registers (as -M_r); at 32 columns, or two
+    // tokens a thread (256-token tiles), they would spill, and shared memory (broadcast reads) holds them
+    // instead. bf16 reads them from shared memory too: its register way spilled 44-56 bytes a thread
+    // and measured 1-2 % slower. (Both ways measured: each is the faster one where it is used.)
+    constexpr bool kRegs = NH <= 24 && SUB == 1 && KV_FP8 != 0;
     constexpr int kRP = kRegs ? NH / 2 : 1;
     float2 l[NH / 2];
     float2 negm[kRP], crow2[kRP];
