@@ -175,6 +175,11 @@ class Plan:
             pass
 
 
+def _runnable(p: Plan):
+    if not p.owned:
+        raise ValueError("the second launch of a two-launch plan runs only as part of its plan")
+
+
 def plan(num_q_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: int, out_dtype: int, num_pages: int,
          block_table_stride: int, context_lens: Sequence[int], query_lens: Sequence[int],
          split_override: int = 0, sm_count: int = 0, page_size: int = 16, kernel: int = KERNEL_AUTO) -> Plan:
@@ -225,6 +230,7 @@ def run(p: Plan, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, 
         query_lens: torch.Tensor, softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
         stream: Optional[torch.cuda.Stream] = None):
     """pa_verify_run on device tensors (enqueued on ``stream`` or torch's current stream)."""
+    _runnable(p)
     _need(q, "q", torch.bfloat16)
     for t, nm in ((k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out"), (workspace, "workspace")):
         _need(t, nm)
@@ -246,6 +252,7 @@ def run_static(p: Plan, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
                stream: Optional[torch.cuda.Stream] = None):
     """pa_verify_run_static: like ``run`` but with the library's fixed device
     scratch instead of a workspace, for callers that cannot allocate."""
+    _runnable(p)
     _need(q, "q", torch.bfloat16)
     for t, nm in ((k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
         _need(t, nm)

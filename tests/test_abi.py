@@ -381,6 +381,11 @@ def test_two_launch_plans_only_where_they_apply(kv, d, ql, split, launches):
     assert (p.second() is not None) == (launches == 2)
     if launches == 2:
         q = p.second()
+        with pytest.raises(ValueError):  # a view: not runnable on its own, freed with its plan
+            pv.run(q, *([None] * 9), 1.0, None, None)
+        q.free()
+        assert q.handle is None and p.second() is not None
+        q = p.second()
         assert p.info.tile_tokens == 256 and q.info.tile_tokens == 128
         assert q.info.rows_max == 64 and p.info.rows_max == 64
         assert p.info.num_units == len(p.cta_starts()) - 1 + q.info.num_units
